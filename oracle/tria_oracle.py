@@ -1,0 +1,271 @@
+"""TriAttention eviction pass, restated step by step on the CPU (float64).
+
+TEST INFRASTRUCTURE, NOT PRODUCT CODE (see :mod:`oracle`).
+
+Sources - the two web pages this restates, cited by title and section:
+
+  [Worklog] "TriAttention Native C++ Worklog" (TensorRT-Model-Connect).
+            Sections used: "Phase 9: final root cause - native scorer used the
+            wrong formulation" (direct K_rot scorer), "2026-04-18: later-
+            compaction absolute-position bug isolated and fixed" (phases from
+            the absolute decode position), "Hypothesis: sampled-head mapping
+            ..." (query-to-KV head map), "K-cache repack correctness ..." and
+            "Later correction ..." (compaction = exact gather of kept rows).
+  [Doc]     "TriAttention KV-Cache Eviction (--triattention)" (llama.cpp fork
+            docs). Sections used: "At a glance" (NEOX-RoPE GQA models),
+            "§1 CLI flags" (budget %, window, sink, interval), "§2 Calibration
+            file (.tria)" (per-head RoPE-direction statistics), "§4 Backend and
+            model support" (GPU gate, q8_0 K), "§5 How it works - Phase B"
+            (score, protect, sort, compact in place) and "Phase C" (per-query-
+            head z-normalisation, max over the GQA group, omega / q_mean /
+            q_abs arrays).
+
+Readings where the pages are silent:
+
+* NEOX pairing: frequency pair f of a head_dim-hd vector is the complex number
+  x[f] + i x[f + hd/2]; omega_f = theta ** (-2 f / hd).
+* Score of cached row r for query head h at decode position p
+  ([Worklog] Phase 9: "Q_mean * conj(K_rot)", "only the query-side trig
+  term", "additive MLR term on |K_rot|")::
+
+      raw_h(r) = (1/|D|) sum_{d in D} sum_f Re( qbar_{h,f} e^{i w_f (p+d)} conj(k_{r,f}) )
+                 + sum_f M_{h,f} |k_{r,f}|
+
+  with M = q_abs - |qbar|: "MLR" read as the mean resultant length
+  R_f = |qbar_f| / q_abs_f, the norm term weighted by (1 - R_f) q_abs_f.
+  D (future query offsets) is a load-time parameter; default {1, 2, 4, ..., 2^16}.
+* z-normalisation: population mean/std over all n live rows of the segment,
+  z = (raw - mu) / (sigma + 1e-6); KV-head score s = max over its query heads.
+* Budget B = floor(budget_frac * n_ctx) survivors in total, sink and window
+  included; candidates are rows [sink, n - window); k = B - sink - window of
+  them are kept by (s descending, row ascending). n <= B is a no-op;
+  B < sink + window is an error.
+* Compaction writes kept row i (ascending original order) to row i of K, V,
+  the q8_0 scales and pos; rows at or past B keep their old contents.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+Z_EPS = 1e-6
+
+
+class BudgetError(ValueError):
+    """Budget smaller than the protected sink + window rows."""
+
+
+# ---------------------------------------------------------------------------
+# RoPE frequencies, future offsets, calibration weights
+# ---------------------------------------------------------------------------
+
+def rope_omega(head_dim: int, theta: float) -> np.ndarray:
+    """omega_f = theta^(-2f/hd), f = 0 .. hd/2 - 1 (NEOX pairs; [Doc] At a glance,
+    Phase C "calibration omega")."""
+    fc = head_dim // 2
+    return np.array([theta ** (-2.0 * f / head_dim) for f in range(fc)], dtype=np.float64)
+
+
+def default_future_offsets() -> np.ndarray:
+    """Future query offsets D = {2^0, ..., 2^16} (reading; the pages give none)."""
+    return np.array([2 ** j for j in range(17)], dtype=np.int64)
+
+
+def as_complex(q_mean: np.ndarray) -> np.ndarray:
+    """[..., fc, 2] (re, im) -> complex128 [..., fc]."""
+    q = np.asarray(q_mean, dtype=np.float64)
+    return q[..., 0] + 1j * q[..., 1]
+
+
+def mlr_weight(q_mean: np.ndarray, q_abs: np.ndarray | None) -> np.ndarray:
+    """M = q_abs - |qbar| per (head, pair) ([Worklog] Phase 9 "MLR term";
+    [Doc] §2 "per-frequency importance weights", Phase C "q_mean / q_abs").
+    ``q_abs`` None means M = 0."""
+    qc = as_complex(q_mean)
+    if q_abs is None:
+        return np.zeros(qc.shape, dtype=np.float64)
+    return np.asarray(q_abs, dtype=np.float64) - np.abs(qc)
+
+
+def heads_of_kv(n_q_heads: int, n_kv_heads: int, kv_of_q=None) -> list:
+    """Query heads of each KV head, ascending ([Worklog] "sampled-head mapping":
+    follow the given map; default contiguous groups h // G)."""
+    if kv_of_q is None:
+        g = n_q_heads // n_kv_heads
+        kv_of_q = [h // g for h in range(n_q_heads)]
+    return [[h for h in range(n_q_heads) if kv_of_q[h] == kv] for kv in range(n_kv_heads)]
+
+
+# ---------------------------------------------------------------------------
+# keys
+# ---------------------------------------------------------------------------
+
+def dequant_q8_0(qs: np.ndarray, d: np.ndarray) -> np.ndarray:
+    """Planar q8_0 rows -> float64: value = fp16 scale of the 32-wide block x code
+    ([Doc] §4 "--cache-type-k q8_0"; ggml Q8_0 block = 32 int8 codes + fp16 scale)."""
+    n, hd = qs.shape
+    scale = np.repeat(np.asarray(d, dtype=np.float16).astype(np.float64), 32, axis=1)
+    return qs.astype(np.float64) * scale[:, :hd]
+
+
+def keys_f64(k: np.ndarray, k_scale: np.ndarray | None = None) -> np.ndarray:
+    """Stored keys widened exactly to float64."""
+    if k.dtype == np.int8:
+        return dequant_q8_0(k, k_scale)
+    return np.asarray(k, dtype=np.float64)
+
+
+# ---------------------------------------------------------------------------
+# scoring ([Worklog] Phase 9; [Doc] Phase C)
+# ---------------------------------------------------------------------------
+
+def raw_scores(k_rot: np.ndarray, q_mean_c: np.ndarray, m_weight: np.ndarray,
+               omega: np.ndarray, p: int, offsets) -> np.ndarray:
+    """raw[r, j] for rows r of one segment and the segment's query heads j.
+
+    ``k_rot`` float64 [n, hd] stored (already rotated) keys; ``q_mean_c``
+    complex [G, fc]; ``m_weight`` [G, fc]; ``p`` absolute decode position
+    ([Worklog] 2026-04-18: phases from the absolute position, not the row count).
+    Loops over the offsets literally; each offset is one complex matmul.
+    """
+    k_rot = np.asarray(k_rot, dtype=np.float64)
+    n, hd = k_rot.shape
+    fc = hd // 2
+    kc = k_rot[:, :fc] + 1j * k_rot[:, fc:]
+    g = q_mean_c.shape[0]
+    trig = np.zeros((n, g), dtype=np.float64)
+    offsets = list(offsets)
+    for d in offsets:
+        ang = np.fmod(omega * float(p + int(d)), 2.0 * math.pi)
+        phase = np.cos(ang) + 1j * np.sin(ang)             # e^{i w_f (p + d)}
+        q_rot = q_mean_c * phase[None, :]                    # mean query at position p + d
+        trig += np.real(np.conj(kc) @ q_rot.T)              # sum_f Re(q_rot conj(k))
+    trig /= len(offsets)
+    norm = np.abs(kc) @ np.asarray(m_weight, dtype=np.float64).T   # sum_f M |k_f|
+    return trig + norm
+
+
+def znorm(raw: np.ndarray) -> np.ndarray:
+    """Per-query-head z-score over all live rows ([Doc] Phase C)."""
+    mu = raw.mean(axis=0)
+    sd = raw.std(axis=0)  # population
+    return (raw - mu[None, :]) / (sd[None, :] + Z_EPS)
+
+
+def gqa_max(z: np.ndarray) -> np.ndarray:
+    """KV-head score = max over the group's query heads ([Doc] Phase C)."""
+    return z.max(axis=1)
+
+
+def segment_scores(k_rot, q_mean_c, m_weight, omega, p, offsets):
+    """(raw [n, G], s [n]) of one segment."""
+    raw = raw_scores(k_rot, q_mean_c, m_weight, omega, p, offsets)
+    return raw, gqa_max(znorm(raw))
+
+
+# ---------------------------------------------------------------------------
+# selection ([Doc] §1, §5 Phase B)
+# ---------------------------------------------------------------------------
+
+def budget_rows(budget_frac: float, n_ctx: int) -> int:
+    """B = floor(budget_frac * n_ctx) ([Doc] §1 "--tri-budget": retain N % of n_ctx)."""
+    return int(math.floor(float(budget_frac) * int(n_ctx)))
+
+
+def select_keep(s: np.ndarray, n: int, budget: int, sink: int, window: int) -> np.ndarray:
+    """Kept rows of one segment, ascending ([Doc] Phase B steps 2-3).
+
+    Protect rows [0, sink) and [n - window, n); of the rest keep the
+    k = B - sink - window best by (s descending, row ascending), via a stable
+    sort of -s. NaN scores sort last.
+    """
+    if n <= budget:
+        return np.arange(n, dtype=np.int64)
+    if budget < sink + window:
+        raise BudgetError(f"budget {budget} < sink {sink} + window {window}")
+    cand = np.arange(sink, n - window, dtype=np.int64)
+    k = budget - sink - window
+    order = np.argsort(-np.asarray(s, dtype=np.float64)[cand], kind="stable")
+    chosen = cand[order[:k]]
+    keep = np.concatenate([np.arange(sink, dtype=np.int64), chosen,
+                           np.arange(n - window, n, dtype=np.int64)])
+    return np.sort(keep)
+
+
+# ---------------------------------------------------------------------------
+# compaction ([Doc] Phase B step 4; [Worklog] exact-gather checks)
+# ---------------------------------------------------------------------------
+
+def compact_rows(plane: np.ndarray, keep: np.ndarray) -> np.ndarray:
+    """Kept rows gathered to the front in order; rows >= len(keep) unchanged."""
+    out = plane.copy()
+    out[:len(keep)] = plane[keep]
+    return out
+
+
+# ---------------------------------------------------------------------------
+# one layer, global-row layout (the same layout the C ABI uses)
+# ---------------------------------------------------------------------------
+
+def evict_layer(layer_cache: dict, q_mean: np.ndarray, q_abs, *, layer: int, n_kv_heads: int,
+                head_dim: int, rope_theta: float, cur_pos, n_ctx, budget_frac: float,
+                window: int, sink: int, offsets=None, kv_of_q=None, omega=None,
+                budget_rows_override=None, segments=None):
+    """Run the pass on one layer's host cache.
+
+    ``layer_cache`` holds ``k`` (float or int8 codes), ``k_scale`` (or None),
+    ``v``, ``pos`` over global rows plus ``n_live``, ``seq_row0``,
+    ``capacity`` per sequence. ``q_mean`` [L][Hq][fc][2], ``q_abs`` [L][Hq][fc].
+    ``segments`` optionally restricts the work to a list of (seq, head).
+
+    Returns ``(new_cache, info)``: ``info[(s, g)]`` = dict(raw, s, keep, B, n).
+    """
+    omega = rope_omega(head_dim, rope_theta) if omega is None else np.asarray(omega, np.float64)
+    offsets = default_future_offsets() if offsets is None else np.asarray(offsets, np.int64)
+    n_q = q_mean.shape[1]
+    groups = heads_of_kv(n_q, n_kv_heads, kv_of_q)
+    qc_all = as_complex(q_mean[layer])
+    m_all = mlr_weight(q_mean[layer], None if q_abs is None else q_abs[layer])
+    out = {key: (None if val is None else np.array(val, copy=True))
+           for key, val in layer_cache.items()}
+    info = {}
+    n_seqs = len(layer_cache["n_live"])
+    for s in range(n_seqs):
+        n = int(layer_cache["n_live"][s])
+        cap = int(layer_cache["capacity"][s])
+        if budget_rows_override is not None:
+            b = int(budget_rows_override[s])
+        else:
+            b = budget_rows(budget_frac, n_ctx[s])
+        for g in range(n_kv_heads):
+            if segments is not None and (s, g) not in segments:
+                continue
+            r0 = int(layer_cache["seq_row0"][s]) + g * cap
+            ks = None if layer_cache.get("k_scale") is None else layer_cache["k_scale"][r0:r0 + n]
+            kf = keys_f64(layer_cache["k"][r0:r0 + n], ks)
+            hs = groups[g]
+            raw, sc = segment_scores(kf, qc_all[hs], m_all[hs], omega, int(cur_pos[s]), offsets)
+            keep = select_keep(sc, n, b, sink, window)
+            info[(s, g)] = {"raw": raw, "s": sc, "keep": keep, "B": b, "n": n, "row0": r0}
+            if n <= b:
+                continue
+            for name in ("k", "k_scale", "v", "pos"):
+                if out.get(name) is None:
+                    continue
+                seg = out[name][r0:r0 + cap]
+                out[name][r0:r0 + cap] = compact_rows(seg, keep)
+    for s in range(n_seqs):
+        n = int(layer_cache["n_live"][s])
+        b = (int(budget_rows_override[s]) if budget_rows_override is not None
+             else budget_rows(budget_frac, n_ctx[s]))
+        if n > b:
+            out["n_live"][s] = b
+    return out, info
+
+
+def should_evict(n_live: int, budget: int, interval: int) -> bool:
+    """Lifecycle trigger: compact once the live rows reach budget + interval
+    ([Worklog] "Final apples-to-apples check": trigger = kv_budget + divide_length;
+    [Doc] §1 "--tri-interval")."""
+    return n_live >= budget + interval
