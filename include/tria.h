@@ -1,0 +1,212 @@
+/*
+ * tria.h - TriAttention KV-cache eviction pass (score -> select -> compact) on
+ * one NVIDIA GB300 (sm_103a).
+ *
+ * Sources, cited by page title and section:
+ *   [Worklog] "TriAttention Native C++ Worklog" (TensorRT-Model-Connect).
+ *   [Doc]     "TriAttention KV-Cache Eviction (--triattention)" (llama.cpp fork
+ *             documentation).
+ *
+ * What one pass computes, for every segment = (sequence s, KV head g) of one
+ * layer with n live rows (rows ascend in token position):
+ *   1. score  - for each query head h of g's GQA group and each live row r
+ *        raw_h(r) = (1/|D|) sum_{d in D} sum_f Re( qbar_{h,f} e^{i w_f (p_s + d)} conj(k_{r,f}) )
+ *                   + sum_f (q_abs_{h,f} - |qbar_{h,f}|) |k_{r,f}|
+ *      on the stored RoPE-rotated key k_r (NEOX pairs k_{r,f} = K[r][f] + i K[r][f+hd/2]),
+ *      with p_s the absolute decode position ([Worklog] "Phase 9: final root
+ *      cause ...": direct K_rot scoring, query-side trig term only, additive
+ *      MLR term on |K_rot|; "2026-04-18: later-compaction absolute-position
+ *      bug ...": phases from the absolute position). Then per query head
+ *      z = (raw - mean) / (std + 1e-6) over the n live rows, and the row's
+ *      score s(r) = max over the group ([Doc] §5 Phase C).
+ *   2. select - with B = budget rows, keep rows [0, sink) and [n - window, n)
+ *      and the B - sink - window best of the rest by (s descending, row
+ *      ascending) ([Doc] §1 CLI flags, §5 Phase B steps 1-3).
+ *   3. compact - move kept row i (ascending) to row i of K, V, the q8_0 scale
+ *      planes and pos, in place; set n_live = B ([Doc] §5 Phase B step 4;
+ *      [Worklog] exact-gather checks of K and V after compaction).
+ *
+ * Conventions for every call:
+ *   - Pointers marked "device" are CUDA device pointers owned by the caller;
+ *     pointers marked "host" are read during the call only.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL = legacy default stream) unless stated otherwise. They return the
+ *     errors detected on the host. Errors found on the device (bad n_live, bad
+ *     keep list, a bounded wait that gave up) are recorded in the workspace
+ *     and read with tria_device_status().
+ *   - The library keeps no global mutable state; all per-call state lives in
+ *     the caller's workspace, which calls must not share while they overlap
+ *     on the GPU.
+ *   - Nothing here falls back to the CPU: without a usable GPU the calls fail.
+ */
+#ifndef TRIA_H
+#define TRIA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TRIA_VERSION 1
+#define TRIA_MAX_SEQS 128      /* sequences per call */
+#define TRIA_MAX_HEAD_DIM 256  /* [Doc] §4/§6: head_dim <= 256, freq_count <= 128 */
+#define TRIA_MAX_GROUP 8       /* query heads per KV head supported */
+
+typedef enum tria_status {
+  TRIA_OK = 0,
+  TRIA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, layout overlap */
+  TRIA_ERR_UNSUPPORTED = 2,   /* gate: head_dim > 256 or % 32, n_q % n_kv, group > 8, dtype */
+  TRIA_ERR_BUDGET = 3,        /* budget rows < sink + window */
+  TRIA_ERR_CUDA = 4,          /* a CUDA runtime call failed */
+  TRIA_ERR_WORKSPACE = 5,     /* workspace too small or not 256-byte aligned */
+  TRIA_ERR_TIMEOUT = 6,       /* device: a bounded wait gave up */
+  TRIA_ERR_DEVICE_ARG = 7,    /* device: n_live < 0 or > capacity (sequence skipped) */
+  TRIA_ERR_KEEP_LIST = 8      /* device: keep list not strictly ascending / out of range */
+} tria_status;
+
+typedef enum tria_dtype {
+  TRIA_F32 = 0,
+  TRIA_F16 = 1,
+  /* q8_0 (ggml Q8_0 values, stored planar): int8 codes [row][head_dim] in the
+   * data plane plus fp16 block scales [row][head_dim/32] in the scale plane;
+   * value = scale of its 32-wide block x code ([Doc] §4 "--cache-type-k q8_0"). */
+  TRIA_Q8_0 = 2
+} tria_dtype;
+
+/* Calibration statistics of one model ([Doc] §2 "Calibration file (.tria)":
+ * per-layer, per-head RoPE-direction statistics; §5 Phase C: omega and
+ * per-head q_mean / q_abs laid out [n_layers x n_heads x freq_count]).
+ * All arrays are host memory, copied by tria_load_stats. */
+typedef struct tria_stats_desc {
+  int32_t n_layers;
+  int32_t n_q_heads;
+  int32_t n_kv_heads;
+  int32_t head_dim;           /* uniform across layers ([Doc] §6) */
+  double rope_theta;          /* w_f = theta^(-2f/head_dim) when omega is NULL */
+  const double* omega;        /* [head_dim/2] optional RoPE angular frequencies */
+  const float* q_mean;        /* [n_layers][n_q_heads][head_dim/2][2] pre-RoPE mean query (re, im) */
+  const float* q_abs;         /* [n_layers][n_q_heads][head_dim/2] mean |q_f|; NULL: no norm term */
+  const int32_t* kv_of_q;     /* [n_q_heads] optional query->KV head map ([Worklog] "sampled-head
+                                 mapping"); NULL: h / (n_q_heads / n_kv_heads). Each KV head must
+                                 get the same number of query heads. */
+  const int64_t* offsets;     /* [n_offsets] future query offsets D; NULL: {1, 2, 4, ..., 65536} */
+  int32_t n_offsets;
+} tria_stats_desc;
+
+typedef struct tria_stats tria_stats;  /* opaque, device resident, immutable after load */
+
+/* One layer's cache for all sequences of the call.
+ * Rows: sequence s owns n_kv_heads * capacity[s] consecutive rows from row
+ * seq_row0[s]; KV head g of it (one segment) starts at row
+ * seq_row0[s] + g * capacity[s]. Row r of every plane is at byte offset
+ * r * (row bytes of that plane). Row bytes: f32 4*hd, f16 2*hd, q8_0 data hd,
+ * q8_0 scales hd/16; pos 4. Segments must not overlap. */
+typedef struct tria_layer_cache {
+  int32_t n_seqs;             /* 1 .. TRIA_MAX_SEQS */
+  int32_t n_kv_heads;
+  int32_t head_dim;
+  tria_dtype k_type;          /* F32, F16 or Q8_0 */
+  tria_dtype v_type;          /* F32, F16 or Q8_0 */
+  void* k;                    /* device, 16-byte aligned, rotated keys */
+  void* k_scale;              /* device, q8_0 keys only (else NULL) */
+  void* v;                    /* device, 16-byte aligned */
+  void* v_scale;              /* device, q8_0 values only (else NULL) */
+  int32_t* pos;               /* device [rows] absolute token positions (moved with the rows) */
+  int32_t* n_live;            /* device [n_seqs] live rows per sequence (all its KV heads);
+                                 read at the start, set to the budget by compaction */
+  const int64_t* seq_row0;    /* host [n_seqs] */
+  const int32_t* capacity;    /* host [n_seqs] physical rows per segment */
+} tria_layer_cache;
+
+/* Eviction policy ([Doc] §1 CLI flags: --tri-budget N % of n_ctx, --tri-window
+ * (default 512), --tri-interval (default 128), --tri-sink (default 0);
+ * [Worklog] absolute decode position). Host arrays, read during the call. */
+typedef struct tria_policy {
+  double budget_frac;         /* (0, 1]: budget rows B_s = floor(budget_frac * n_ctx[s]) */
+  const int32_t* n_ctx;       /* [n_seqs] context length the fraction refers to */
+  const int32_t* budget_rows; /* [n_seqs] optional absolute budget; overrides the fraction */
+  int32_t window;             /* most recent rows always kept */
+  int32_t sink;               /* first rows always kept */
+  int32_t interval;           /* decode steps between passes (used by tria_should_evict) */
+  const int64_t* cur_pos;     /* [n_seqs] absolute decode position p_s (not the row count) */
+} tria_policy;
+
+/* Host-only gate of [Doc] §4 "GPU scoring requirements" (n_q % n_kv == 0,
+ * head_dim <= 256 and % 32 == 0) plus this build's group <= 8. No GPU use. */
+tria_status tria_gate_check(int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim);
+
+/* Budget rows floor(budget_frac * n_ctx) computed in double ([Doc] §1). */
+int64_t tria_budget_rows(double budget_frac, int64_t n_ctx);
+
+/* Decode-loop trigger: 1 when n_live >= budget + interval ([Worklog] "Final
+ * apples-to-apples check": compaction starts at kv_budget + divide_length). */
+int32_t tria_should_evict(int64_t n_live, int64_t budget, int64_t interval);
+
+/* Copies the statistics to the device (allocates with cudaMalloc), folds the
+ * offset average and the norm weights (q_abs - |q_mean|) in a kernel, and
+ * synchronises `stream`. *out is NULL on error. */
+tria_status tria_load_stats(const tria_stats_desc* desc, tria_stats** out, void* stream);
+void tria_free_stats(tria_stats* stats);
+
+/* Workspace bytes for calls on `cache` with `group` query heads per KV head
+ * (0 when only tria_select / tria_compact are used). 0 on invalid input. */
+size_t tria_workspace_size(const tria_layer_cache* cache, int32_t group);
+
+/* Zeroes a workspace (required once after allocation and after any device
+ * error). Asynchronous. */
+tria_status tria_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* Step 1 only: writes s(r) to score_out[row] (device float, global row index)
+ * and, if raw_out is not NULL, raw_h(r) to raw_out[row * G + j] for the j-th
+ * query head of the segment's group (ascending head index). Rows at or past
+ * n_live are not written. The cache is not modified. */
+tria_status tria_score(const tria_stats* stats, int32_t layer, const tria_layer_cache* cache,
+                       const tria_policy* policy, float* score_out, float* raw_out,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* Step 2 only, on a caller-given score array (device float, global row
+ * index). Writes each segment's kept rows (segment-local indices, ascending)
+ * to keep_out[seg_row0 + i] (device int32): B entries when n_live > B, else
+ * the n_live identity entries. The cache is not modified. */
+tria_status tria_select(const float* score, const tria_layer_cache* cache, const tria_policy* policy,
+                        int32_t* keep_out, void* ws, size_t ws_bytes, void* stream);
+
+/* Step 3 only: compacts every segment with n_live > B using the caller's
+ * keep list (as tria_select writes it: B strictly ascending entries in
+ * [0, n_live) per segment), then sets n_live = B. Rows at or past B keep their
+ * old contents. A keep list that breaks the rules is reported as
+ * TRIA_ERR_KEEP_LIST and nothing is moved. */
+tria_status tria_compact(const tria_layer_cache* cache, const tria_policy* policy,
+                         const int32_t* keep, void* ws, size_t ws_bytes, void* stream);
+
+/* The whole pass (steps 1-3) for one layer and all sequences of the call. */
+tria_status tria_evict(const tria_stats* stats, int32_t layer, const tria_layer_cache* cache,
+                       const tria_policy* policy, void* ws, size_t ws_bytes, void* stream);
+
+/* tria_evict with CUDA events recorded on `stream` between its stages;
+ * synchronises `stream` and writes the stage times in milliseconds to
+ * stage_ms[5] = {raw scores, z-max scores, select, compact, whole pass} and the
+ * number of kernels launched to *launches. For benchmarks and tracing. */
+tria_status tria_evict_profiled(const tria_stats* stats, int32_t layer, const tria_layer_cache* cache,
+                                const tria_policy* policy, void* ws, size_t ws_bytes, void* stream,
+                                float* stage_ms, int32_t* launches);
+
+/* Synchronises `stream`, returns the first device-detected error of the
+ * calls since the last check (TRIA_OK if none) and clears it. */
+tria_status tria_device_status(void* ws, void* stream);
+
+/* Runs the bounded wait used by the compaction kernel on a flag that nothing
+ * sets, with `spin_limit` polls, and returns what the kernel reported
+ * (TRIA_ERR_TIMEOUT expected). Synchronises `stream`. For failure tests. */
+tria_status tria_selftest_bounded_wait(int32_t spin_limit, void* ws, size_t ws_bytes, void* stream);
+
+const char* tria_status_string(tria_status status);
+int32_t tria_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TRIA_H */

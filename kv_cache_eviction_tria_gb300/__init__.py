@@ -1,0 +1,335 @@
+"""Python binding of the TriAttention KV-cache eviction library (``libtria.so``).
+
+Argument marshalling only: every step of the pass runs in the CUDA kernels of
+``libtria.so``; the functions here turn tensors and Python values into the C
+structs of ``include/tria.h`` and call the entry point of the same name. There
+is no CPU fallback: if the library cannot be loaded, every call raises.
+
+PyTorch supplies device memory and streams. Device arguments are CUDA
+tensors; host arguments are sequences of ints / numpy arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtria.so")
+
+TRIA_MAX_SEQS = 128
+F32, F16, Q8_0 = 0, 1, 2
+DTYPES = {"f32": F32, "f16": F16, "q8_0": Q8_0}
+
+STATUS = {
+    0: "TRIA_OK", 1: "TRIA_ERR_INVALID_ARG", 2: "TRIA_ERR_UNSUPPORTED", 3: "TRIA_ERR_BUDGET",
+    4: "TRIA_ERR_CUDA", 5: "TRIA_ERR_WORKSPACE", 6: "TRIA_ERR_TIMEOUT", 7: "TRIA_ERR_DEVICE_ARG",
+    8: "TRIA_ERR_KEEP_LIST",
+}
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_BUDGET, ERR_CUDA, ERR_WORKSPACE, ERR_TIMEOUT, \
+    ERR_DEVICE_ARG, ERR_KEEP_LIST = range(9)
+
+EXPORTS = (
+    "tria_gate_check", "tria_budget_rows", "tria_should_evict", "tria_load_stats", "tria_free_stats",
+    "tria_workspace_size", "tria_workspace_init", "tria_score", "tria_select", "tria_compact",
+    "tria_evict", "tria_evict_profiled", "tria_device_status", "tria_selftest_bounded_wait", "tria_status_string",
+    "tria_version",
+)
+
+
+class TriaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+# --------------------------------------------------------------------------- C structs
+
+class _StatsDesc(ctypes.Structure):
+    _fields_ = [
+        ("n_layers", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("rope_theta", ctypes.c_double),
+        ("omega", ctypes.POINTER(ctypes.c_double)), ("q_mean", ctypes.POINTER(ctypes.c_float)),
+        ("q_abs", ctypes.POINTER(ctypes.c_float)), ("kv_of_q", ctypes.POINTER(ctypes.c_int32)),
+        ("offsets", ctypes.POINTER(ctypes.c_int64)), ("n_offsets", ctypes.c_int32),
+    ]
+
+
+class _LayerCache(ctypes.Structure):
+    _fields_ = [
+        ("n_seqs", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+        ("k_type", ctypes.c_int32), ("v_type", ctypes.c_int32),
+        ("k", ctypes.c_void_p), ("k_scale", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("v_scale", ctypes.c_void_p), ("pos", ctypes.c_void_p), ("n_live", ctypes.c_void_p),
+        ("seq_row0", ctypes.POINTER(ctypes.c_int64)), ("capacity", ctypes.POINTER(ctypes.c_int32)),
+    ]
+
+
+class _Policy(ctypes.Structure):
+    _fields_ = [
+        ("budget_frac", ctypes.c_double), ("n_ctx", ctypes.POINTER(ctypes.c_int32)),
+        ("budget_rows", ctypes.POINTER(ctypes.c_int32)), ("window", ctypes.c_int32),
+        ("sink", ctypes.c_int32), ("interval", ctypes.c_int32),
+        ("cur_pos", ctypes.POINTER(ctypes.c_int64)),
+    ]
+
+
+_lib = None
+
+
+def load_library(path: str | None = None):
+    """Load ``libtria.so`` (raises if it is missing: there is no fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} not found: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    lib.tria_gate_check.argtypes = [i32, i32, i32]
+    lib.tria_gate_check.restype = i32
+    lib.tria_budget_rows.argtypes = [ctypes.c_double, i64]
+    lib.tria_budget_rows.restype = i64
+    lib.tria_should_evict.argtypes = [i64, i64, i64]
+    lib.tria_should_evict.restype = i32
+    lib.tria_load_stats.argtypes = [ctypes.POINTER(_StatsDesc), ctypes.POINTER(vp), vp]
+    lib.tria_load_stats.restype = i32
+    lib.tria_free_stats.argtypes = [vp]
+    lib.tria_free_stats.restype = None
+    lib.tria_workspace_size.argtypes = [ctypes.POINTER(_LayerCache), i32]
+    lib.tria_workspace_size.restype = sz
+    lib.tria_workspace_init.argtypes = [vp, sz, vp]
+    lib.tria_workspace_init.restype = i32
+    lib.tria_score.argtypes = [vp, i32, ctypes.POINTER(_LayerCache), ctypes.POINTER(_Policy), vp, vp, vp, sz, vp]
+    lib.tria_score.restype = i32
+    lib.tria_select.argtypes = [vp, ctypes.POINTER(_LayerCache), ctypes.POINTER(_Policy), vp, vp, sz, vp]
+    lib.tria_select.restype = i32
+    lib.tria_compact.argtypes = [ctypes.POINTER(_LayerCache), ctypes.POINTER(_Policy), vp, vp, sz, vp]
+    lib.tria_compact.restype = i32
+    lib.tria_evict.argtypes = [vp, i32, ctypes.POINTER(_LayerCache), ctypes.POINTER(_Policy), vp, sz, vp]
+    lib.tria_evict.restype = i32
+    lib.tria_evict_profiled.argtypes = [vp, i32, ctypes.POINTER(_LayerCache), ctypes.POINTER(_Policy), vp, sz,
+                                        vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(i32)]
+    lib.tria_evict_profiled.restype = i32
+    lib.tria_device_status.argtypes = [vp, vp]
+    lib.tria_device_status.restype = i32
+    lib.tria_selftest_bounded_wait.argtypes = [i32, vp, sz, vp]
+    lib.tria_selftest_bounded_wait.restype = i32
+    lib.tria_status_string.argtypes = [i32]
+    lib.tria_status_string.restype = ctypes.c_char_p
+    lib.tria_version.argtypes = []
+    lib.tria_version.restype = i32
+    _lib = lib
+    return lib
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise TriaError(status, where)
+
+
+def _stream_handle(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return ctypes.c_void_p(t)
+    if not t.is_cuda:
+        raise ValueError("device argument must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("device argument must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _host_array(values, dtype, ctype):
+    if values is None:
+        return None, None
+    arr = np.ascontiguousarray(np.asarray(values, dtype=dtype))
+    return arr, arr.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+# --------------------------------------------------------------------------- host-only helpers
+
+def gate_check(n_q_heads: int, n_kv_heads: int, head_dim: int) -> int:
+    return load_library().tria_gate_check(n_q_heads, n_kv_heads, head_dim)
+
+
+def budget_rows(budget_frac: float, n_ctx: int) -> int:
+    return load_library().tria_budget_rows(budget_frac, n_ctx)
+
+
+def should_evict(n_live: int, budget: int, interval: int) -> bool:
+    return bool(load_library().tria_should_evict(n_live, budget, interval))
+
+
+def status_string(status: int) -> str:
+    return load_library().tria_status_string(status).decode()
+
+
+def version() -> int:
+    return load_library().tria_version()
+
+
+# --------------------------------------------------------------------------- stats
+
+class Stats:
+    """Device-resident calibration statistics (``tria_load_stats``)."""
+
+    def __init__(self, q_mean, q_abs, *, n_kv_heads: int, head_dim: int, rope_theta: float,
+                 omega=None, kv_of_q=None, offsets=None, stream=None):
+        lib = load_library()
+        q_mean = np.ascontiguousarray(np.asarray(q_mean, dtype=np.float32))
+        n_layers, n_q = q_mean.shape[0], q_mean.shape[1]
+        self._keep = []
+        qm_arr, qm_p = _host_array(q_mean, np.float32, ctypes.c_float)
+        qa_arr, qa_p = _host_array(q_abs, np.float32, ctypes.c_float)
+        om_arr, om_p = _host_array(omega, np.float64, ctypes.c_double)
+        kv_arr, kv_p = _host_array(kv_of_q, np.int32, ctypes.c_int32)
+        of_arr, of_p = _host_array(offsets, np.int64, ctypes.c_int64)
+        self._keep += [qm_arr, qa_arr, om_arr, kv_arr, of_arr]
+        desc = _StatsDesc(n_layers, n_q, n_kv_heads, head_dim, float(rope_theta), om_p, qm_p, qa_p,
+                          kv_p, of_p, 0 if of_arr is None else len(of_arr))
+        handle = ctypes.c_void_p()
+        _check(lib.tria_load_stats(ctypes.byref(desc), ctypes.byref(handle), _stream_handle(stream)),
+               "tria_load_stats")
+        self.handle = handle
+        self.n_layers, self.n_q_heads, self.n_kv_heads, self.head_dim = n_layers, n_q, n_kv_heads, head_dim
+        self.group = n_q // n_kv_heads
+
+    def close(self):
+        if self.handle:
+            load_library().tria_free_stats(self.handle)
+            self.handle = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def load_stats(q_mean, q_abs, **kw) -> Stats:
+    return Stats(q_mean, q_abs, **kw)
+
+
+# --------------------------------------------------------------------------- cache / policy
+
+class LayerCache:
+    """One layer's cache (``tria_layer_cache``): device tensors + host layout."""
+
+    def __init__(self, *, k, v, pos, n_live, seq_row0, capacity, head_dim: int, n_kv_heads: int,
+                 k_type: str = "f16", v_type: str = "f16", k_scale=None, v_scale=None):
+        self.k, self.v, self.pos, self.n_live = k, v, pos, n_live
+        self.k_scale, self.v_scale = k_scale, v_scale
+        self.head_dim, self.n_kv_heads = head_dim, n_kv_heads
+        self.k_type, self.v_type = DTYPES[k_type], DTYPES[v_type]
+        self.seq_row0 = np.ascontiguousarray(np.asarray(seq_row0, dtype=np.int64))
+        self.capacity = np.ascontiguousarray(np.asarray(capacity, dtype=np.int32))
+
+    def c_struct(self) -> _LayerCache:
+        return _LayerCache(
+            len(self.seq_row0), self.n_kv_heads, self.head_dim, self.k_type, self.v_type,
+            _ptr(self.k), _ptr(self.k_scale), _ptr(self.v), _ptr(self.v_scale), _ptr(self.pos),
+            _ptr(self.n_live), self.seq_row0.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+            self.capacity.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)))
+
+
+class Policy:
+    """Eviction policy (``tria_policy``)."""
+
+    def __init__(self, *, budget_frac: float = 0.0, n_ctx=None, budget_rows=None, window: int = 512,
+                 sink: int = 0, interval: int = 128, cur_pos=None):
+        self.budget_frac, self.window, self.sink, self.interval = budget_frac, window, sink, interval
+        self.n_ctx, self._n_ctx_p = _host_array(n_ctx, np.int32, ctypes.c_int32)
+        self.budget_rows, self._br_p = _host_array(budget_rows, np.int32, ctypes.c_int32)
+        self.cur_pos, self._cp_p = _host_array(cur_pos, np.int64, ctypes.c_int64)
+
+    def c_struct(self) -> _Policy:
+        return _Policy(float(self.budget_frac), self._n_ctx_p, self._br_p, self.window, self.sink,
+                       self.interval, self._cp_p)
+
+
+# --------------------------------------------------------------------------- the pass
+
+def workspace_size(cache: LayerCache, group: int) -> int:
+    c = cache.c_struct()
+    n = load_library().tria_workspace_size(ctypes.byref(c), group)
+    if n == 0:
+        raise TriaError(ERR_INVALID_ARG, "tria_workspace_size")
+    return n
+
+
+def workspace_init(ws, stream=None):
+    _check(load_library().tria_workspace_init(_ptr(ws), ws.numel() * ws.element_size(),
+                                              _stream_handle(stream)), "tria_workspace_init")
+
+
+def _ws(ws):
+    return _ptr(ws), ws.numel() * ws.element_size()
+
+
+def score(stats: Stats, layer: int, cache: LayerCache, policy: Policy, score_out, raw_out=None,
+          *, ws, stream=None):
+    c, p = cache.c_struct(), policy.c_struct()
+    wp, wb = _ws(ws)
+    _check(load_library().tria_score(stats.handle, layer, ctypes.byref(c), ctypes.byref(p),
+                                     _ptr(score_out), _ptr(raw_out), wp, wb, _stream_handle(stream)),
+           "tria_score")
+
+
+def select(score_in, cache: LayerCache, policy: Policy, keep_out, *, ws, stream=None):
+    c, p = cache.c_struct(), policy.c_struct()
+    wp, wb = _ws(ws)
+    _check(load_library().tria_select(_ptr(score_in), ctypes.byref(c), ctypes.byref(p), _ptr(keep_out),
+                                      wp, wb, _stream_handle(stream)), "tria_select")
+
+
+def compact(cache: LayerCache, policy: Policy, keep, *, ws, stream=None):
+    c, p = cache.c_struct(), policy.c_struct()
+    wp, wb = _ws(ws)
+    _check(load_library().tria_compact(ctypes.byref(c), ctypes.byref(p), _ptr(keep), wp, wb,
+                                       _stream_handle(stream)), "tria_compact")
+
+
+def evict(stats: Stats, layer: int, cache: LayerCache, policy: Policy, *, ws, stream=None):
+    c, p = cache.c_struct(), policy.c_struct()
+    wp, wb = _ws(ws)
+    _check(load_library().tria_evict(stats.handle, layer, ctypes.byref(c), ctypes.byref(p), wp, wb,
+                                     _stream_handle(stream)), "tria_evict")
+
+
+def evict_profiled(stats: Stats, layer: int, cache: LayerCache, policy: Policy, *, ws, stream=None):
+    """tria_evict_profiled: returns ({stage: ms}, kernels launched); synchronises."""
+    c, p = cache.c_struct(), policy.c_struct()
+    wp, wb = _ws(ws)
+    ms = (ctypes.c_float * 5)()
+    nl = ctypes.c_int32()
+    _check(load_library().tria_evict_profiled(stats.handle, layer, ctypes.byref(c), ctypes.byref(p), wp, wb,
+                                              _stream_handle(stream), ms, ctypes.byref(nl)),
+           "tria_evict_profiled")
+    names = ("score", "zscore", "select", "compact", "total")
+    return dict(zip(names, list(ms))), nl.value
+
+
+def device_status(ws, stream=None) -> int:
+    return load_library().tria_device_status(_ptr(ws), _stream_handle(stream))
+
+
+def selftest_bounded_wait(spin_limit: int, ws, stream=None) -> int:
+    wp, wb = _ws(ws)
+    return load_library().tria_selftest_bounded_wait(spin_limit, wp, wb, _stream_handle(stream))
+
+
+def raw_call(name: str, *args):
+    """Call an entry point by name with ctypes arguments (used by the host tests)."""
+    return getattr(load_library(), name)(*args)

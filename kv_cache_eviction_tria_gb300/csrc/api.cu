@@ -1,0 +1,396 @@
+// C ABI of the eviction pass: argument checks, workspace layout, launches.
+//
+// Sources cited by page title and section:
+//   [Worklog] "TriAttention Native C++ Worklog"
+//   [Doc]     "TriAttention KV-Cache Eviction (--triattention)"
+#include <math.h>
+#include <string.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "tria_internal.cuh"
+
+using namespace tria;
+
+namespace {
+
+int row_bytes(tria_dtype t, int hd) {
+  switch (t) {
+    case TRIA_F32: return 4 * hd;
+    case TRIA_F16: return 2 * hd;
+    case TRIA_Q8_0: return hd;
+  }
+  return 0;
+}
+
+int scale_row_bytes(tria_dtype t, int hd) { return t == TRIA_Q8_0 ? hd / 16 : 0; }
+
+bool dtype_ok(int t) { return t == TRIA_F32 || t == TRIA_F16 || t == TRIA_Q8_0; }
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+struct Layout {
+  size_t ctrl, seg, schunk, chunk, prefix, hist, flags, score, keep, raw, total;
+  int cs_rows, cs_max, c_max, n_seg;
+  int64_t total_rows;
+};
+
+size_t up(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Everything but `raw` is independent of the group size, and `raw` comes last,
+// so one workspace serves every entry point on the same cache.
+Layout make_layout(const tria_layer_cache* c, int G) {
+  Layout L{};
+  const int hd = c->head_dim;
+  const int k_rb = row_bytes(c->k_type, hd);
+  int piece_rows = 8192 / k_rb;
+  piece_rows = std::min(64, std::max(1, piece_rows));
+  L.cs_rows = 8 * piece_rows;
+  int cap_max = 0;
+  int64_t total_rows = 0;
+  for (int s = 0; s < c->n_seqs; ++s) {
+    cap_max = std::max(cap_max, c->capacity[s]);
+    total_rows = std::max(total_rows, c->seq_row0[s] + (int64_t)c->n_kv_heads * c->capacity[s]);
+  }
+  cap_max = std::max(cap_max, 1);
+  L.total_rows = total_rows;
+  L.n_seg = c->n_seqs * c->n_kv_heads;
+  L.cs_max = (cap_max + L.cs_rows - 1) / L.cs_rows;
+  L.c_max = (cap_max + kChunk - 1) / kChunk;
+  size_t off = 0;
+  L.ctrl = off;
+  off = up(off + sizeof(Ctrl));
+  L.seg = off;
+  off = up(off + (size_t)L.n_seg * sizeof(SegState));
+  L.schunk = off;
+  off = up(off + (size_t)L.n_seg * L.cs_max * sizeof(ScoreChunk));
+  L.chunk = off;
+  off = up(off + (size_t)L.n_seg * L.c_max * sizeof(SelChunk));
+  L.prefix = off;
+  off = up(off + (size_t)L.n_seg * (L.c_max + 1) * sizeof(int32_t));
+  L.hist = off;
+  off = up(off + (size_t)L.n_seg * kHistBins * sizeof(uint32_t));
+  L.flags = off;
+  off = up(off + (size_t)L.n_seg * L.c_max * sizeof(uint32_t));
+  L.score = off;
+  off = up(off + (size_t)total_rows * sizeof(float));
+  L.keep = off;
+  off = up(off + (size_t)total_rows * sizeof(int32_t));
+  L.raw = off;
+  off = up(off + (size_t)total_rows * std::max(G, 0) * sizeof(float));
+  L.total = off;
+  return L;
+}
+
+tria_status check_cache(const tria_layer_cache* c) {
+  if (!c) return TRIA_ERR_INVALID_ARG;
+  if (c->n_seqs < 1 || c->n_seqs > kMaxSeqs || c->n_kv_heads < 1) return TRIA_ERR_INVALID_ARG;
+  const int hd = c->head_dim;
+  if (hd <= 0 || hd > TRIA_MAX_HEAD_DIM || hd % 32 != 0) return TRIA_ERR_UNSUPPORTED;
+  if (!dtype_ok(c->k_type) || !dtype_ok(c->v_type)) return TRIA_ERR_UNSUPPORTED;
+  if (!c->k || !c->v || !c->pos || !c->n_live || !c->seq_row0 || !c->capacity) return TRIA_ERR_INVALID_ARG;
+  if (!aligned(c->k, 16) || !aligned(c->v, 16) || !aligned(c->pos, 4) || !aligned(c->n_live, 4))
+    return TRIA_ERR_INVALID_ARG;
+  if ((c->k_type == TRIA_Q8_0) != (c->k_scale != nullptr)) return TRIA_ERR_INVALID_ARG;
+  if ((c->v_type == TRIA_Q8_0) != (c->v_scale != nullptr)) return TRIA_ERR_INVALID_ARG;
+  if (c->k_scale && !aligned(c->k_scale, 16)) return TRIA_ERR_INVALID_ARG;
+  if (c->v_scale && !aligned(c->v_scale, 16)) return TRIA_ERR_INVALID_ARG;
+  // segments of different sequences must not overlap
+  std::vector<std::pair<int64_t, int64_t>> spans;
+  for (int s = 0; s < c->n_seqs; ++s) {
+    if (c->capacity[s] < 0 || c->seq_row0[s] < 0) return TRIA_ERR_INVALID_ARG;
+    spans.push_back({c->seq_row0[s], c->seq_row0[s] + (int64_t)c->n_kv_heads * c->capacity[s]});
+  }
+  std::sort(spans.begin(), spans.end());
+  for (size_t i = 1; i < spans.size(); ++i)
+    if (spans[i].first < spans[i - 1].second) return TRIA_ERR_INVALID_ARG;
+  return TRIA_OK;
+}
+
+tria_status check_policy(const tria_layer_cache* c, const tria_policy* p, bool need_pos, std::vector<int>& budget) {
+  if (!p) return TRIA_ERR_INVALID_ARG;
+  if (p->window < 0 || p->sink < 0) return TRIA_ERR_INVALID_ARG;
+  if (need_pos && !p->cur_pos) return TRIA_ERR_INVALID_ARG;
+  if (!p->budget_rows && (!p->n_ctx || !(p->budget_frac > 0.0) || p->budget_frac > 1.0))
+    return TRIA_ERR_INVALID_ARG;
+  budget.assign(c->n_seqs, 0);
+  for (int s = 0; s < c->n_seqs; ++s) {
+    int64_t b;
+    if (p->budget_rows) {
+      b = p->budget_rows[s];
+    } else {
+      if (p->n_ctx[s] < 0) return TRIA_ERR_INVALID_ARG;
+      b = tria_budget_rows(p->budget_frac, p->n_ctx[s]);
+    }
+    if (b < 0 || b > INT32_MAX) return TRIA_ERR_INVALID_ARG;
+    if (b < (int64_t)p->sink + p->window) return TRIA_ERR_BUDGET;
+    if (need_pos && p->cur_pos[s] < 0) return TRIA_ERR_INVALID_ARG;
+    budget[s] = (int)b;
+  }
+  return TRIA_OK;
+}
+
+tria_status check_ws(void* ws, size_t ws_bytes, const Layout& L) {
+  if (!ws || !aligned(ws, 256)) return TRIA_ERR_WORKSPACE;
+  if (ws_bytes < L.total) return TRIA_ERR_WORKSPACE;
+  return TRIA_OK;
+}
+
+void fill_pass(Pass& P, const tria_layer_cache* c, const tria_policy* p, const std::vector<int>& budget,
+               const Layout& L, void* ws, int G) {
+  memset(&P, 0, sizeof(P));
+  P.n_seqs = c->n_seqs;
+  P.n_kv = c->n_kv_heads;
+  P.n_seg = L.n_seg;
+  P.G = G;
+  P.hd = c->head_dim;
+  P.fc = c->head_dim / 2;
+  P.sink = p ? p->sink : 0;
+  P.window = p ? p->window : 0;
+  P.k_type = c->k_type;
+  P.v_type = c->v_type;
+  P.k_rb = row_bytes(c->k_type, c->head_dim);
+  P.ks_rb = scale_row_bytes(c->k_type, c->head_dim);
+  P.v_rb = row_bytes(c->v_type, c->head_dim);
+  P.vs_rb = scale_row_bytes(c->v_type, c->head_dim);
+  P.spin_limit = kDefaultSpinLimit;
+  P.k = (uint8_t*)c->k;
+  P.ks = (uint8_t*)c->k_scale;
+  P.v = (uint8_t*)c->v;
+  P.vs = (uint8_t*)c->v_scale;
+  P.pos = c->pos;
+  P.n_live = c->n_live;
+  uint8_t* w = (uint8_t*)ws;
+  P.ctrl = (Ctrl*)(w + L.ctrl);
+  P.seg = (SegState*)(w + L.seg);
+  P.schunk = (ScoreChunk*)(w + L.schunk);
+  P.chunk = (SelChunk*)(w + L.chunk);
+  P.prefix = (int32_t*)(w + L.prefix);
+  P.hist = (uint32_t*)(w + L.hist);
+  P.flags = (uint32_t*)(w + L.flags);
+  P.cs_rows = L.cs_rows;
+  P.cs_max = L.cs_max;
+  P.c_max = L.c_max;
+  for (int s = 0; s < c->n_seqs; ++s) {
+    P.seq[s].row0 = c->seq_row0[s];
+    P.seq[s].cap = c->capacity[s];
+    P.seq[s].budget = budget.empty() ? 0 : budget[s];
+    P.seq[s].cur_pos = (p && p->cur_pos) ? p->cur_pos[s] : 0;
+  }
+}
+
+tria_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TRIA_OK : TRIA_ERR_CUDA; }
+
+tria_status check_stats(const tria_stats* st, int layer, const tria_layer_cache* c) {
+  if (!st) return TRIA_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= st->n_layers) return TRIA_ERR_INVALID_ARG;
+  if (st->n_kv_heads != c->n_kv_heads || st->head_dim != c->head_dim) return TRIA_ERR_INVALID_ARG;
+  return TRIA_OK;
+}
+
+void set_stats(Pass& P, const tria_stats* st, int layer) {
+  const size_t per_layer = (size_t)st->n_kv_heads * st->group * (st->head_dim / 2);
+  P.qe = st->qe + per_layer * layer;
+  P.mw = st->mw + per_layer * layer;
+  P.turns = st->turns;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+
+extern "C" tria_status tria_gate_check(int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim) {
+  if (n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0) return TRIA_ERR_INVALID_ARG;
+  if (n_q_heads % n_kv_heads != 0) return TRIA_ERR_UNSUPPORTED;          // [Doc] §4: nh % nkv == 0
+  if (head_dim > TRIA_MAX_HEAD_DIM || head_dim % 32 != 0) return TRIA_ERR_UNSUPPORTED;  // hd <= 256, % 32
+  const int G = n_q_heads / n_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return TRIA_ERR_UNSUPPORTED;
+  return TRIA_OK;
+}
+
+extern "C" int64_t tria_budget_rows(double budget_frac, int64_t n_ctx) {
+  return (int64_t)floor(budget_frac * (double)n_ctx);
+}
+
+extern "C" int32_t tria_should_evict(int64_t n_live, int64_t budget, int64_t interval) {
+  return n_live >= budget + interval ? 1 : 0;
+}
+
+extern "C" size_t tria_workspace_size(const tria_layer_cache* cache, int32_t group) {
+  if (check_cache(cache) != TRIA_OK || group < 0 || group > kMaxG) return 0;
+  return make_layout(cache, group).total;
+}
+
+extern "C" tria_status tria_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || !aligned(ws, 256) || ws_bytes < sizeof(Ctrl)) return TRIA_ERR_WORKSPACE;
+  return cuda_status(cudaMemsetAsync(ws, 0, ws_bytes, (cudaStream_t)stream));
+}
+
+extern "C" tria_status tria_score(const tria_stats* stats, int32_t layer, const tria_layer_cache* cache,
+                                  const tria_policy* policy, float* score_out, float* raw_out, void* ws,
+                                  size_t ws_bytes, void* stream) {
+  tria_status r;
+  if ((r = check_cache(cache)) != TRIA_OK) return r;
+  if ((r = check_stats(stats, layer, cache)) != TRIA_OK) return r;
+  if (!score_out || !aligned(score_out, 4) || (raw_out && !aligned(raw_out, 4))) return TRIA_ERR_INVALID_ARG;
+  std::vector<int> budget;
+  if ((r = check_policy(cache, policy, true, budget)) != TRIA_OK) return r;
+  const Layout L = make_layout(cache, stats->group);
+  if ((r = check_ws(ws, ws_bytes, L)) != TRIA_OK) return r;
+  Pass P;
+  fill_pass(P, cache, policy, budget, L, ws, stats->group);
+  set_stats(P, stats, layer);
+  P.only_active = 0;
+  P.raw = raw_out ? raw_out : (float*)((uint8_t*)ws + L.raw);
+  P.score = score_out;
+  cudaStream_t st = (cudaStream_t)stream;
+  if ((r = cuda_status(launch_score(P, st))) != TRIA_OK) return r;
+  return cuda_status(launch_zscore(P, st));
+}
+
+extern "C" tria_status tria_select(const float* score, const tria_layer_cache* cache, const tria_policy* policy,
+                                   int32_t* keep_out, void* ws, size_t ws_bytes, void* stream) {
+  tria_status r;
+  if ((r = check_cache(cache)) != TRIA_OK) return r;
+  if (!score || !keep_out || !aligned(score, 4) || !aligned(keep_out, 4)) return TRIA_ERR_INVALID_ARG;
+  std::vector<int> budget;
+  if ((r = check_policy(cache, policy, false, budget)) != TRIA_OK) return r;
+  const Layout L = make_layout(cache, 0);
+  if ((r = check_ws(ws, ws_bytes, L)) != TRIA_OK) return r;
+  Pass P;
+  fill_pass(P, cache, policy, budget, L, ws, 0);
+  P.only_active = 0;
+  P.score_in = score;
+  P.keep = keep_out;
+  return cuda_status(launch_select(P, true, (cudaStream_t)stream));
+}
+
+extern "C" tria_status tria_compact(const tria_layer_cache* cache, const tria_policy* policy, const int32_t* keep,
+                                    void* ws, size_t ws_bytes, void* stream) {
+  tria_status r;
+  if ((r = check_cache(cache)) != TRIA_OK) return r;
+  if (!keep || !aligned(keep, 4)) return TRIA_ERR_INVALID_ARG;
+  std::vector<int> budget;
+  if ((r = check_policy(cache, policy, false, budget)) != TRIA_OK) return r;
+  const Layout L = make_layout(cache, 0);
+  if ((r = check_ws(ws, ws_bytes, L)) != TRIA_OK) return r;
+  Pass P;
+  fill_pass(P, cache, policy, budget, L, ws, 0);
+  P.only_active = 1;
+  P.keep = const_cast<int32_t*>(keep);
+  cudaStream_t st = (cudaStream_t)stream;
+  if ((r = cuda_status(launch_keep_prepass(P, st))) != TRIA_OK) return r;
+  return cuda_status(launch_move(P, st));
+}
+
+extern "C" tria_status tria_evict(const tria_stats* stats, int32_t layer, const tria_layer_cache* cache,
+                                  const tria_policy* policy, void* ws, size_t ws_bytes, void* stream) {
+  tria_status r;
+  if ((r = check_cache(cache)) != TRIA_OK) return r;
+  if ((r = check_stats(stats, layer, cache)) != TRIA_OK) return r;
+  std::vector<int> budget;
+  if ((r = check_policy(cache, policy, true, budget)) != TRIA_OK) return r;
+  const Layout L = make_layout(cache, stats->group);
+  if ((r = check_ws(ws, ws_bytes, L)) != TRIA_OK) return r;
+  Pass P;
+  fill_pass(P, cache, policy, budget, L, ws, stats->group);
+  set_stats(P, stats, layer);
+  P.only_active = 1;
+  P.raw = (float*)((uint8_t*)ws + L.raw);
+  P.score = (float*)((uint8_t*)ws + L.score);
+  P.score_in = P.score;
+  P.keep = (int32_t*)((uint8_t*)ws + L.keep);
+  cudaStream_t st = (cudaStream_t)stream;
+  if ((r = cuda_status(launch_score(P, st))) != TRIA_OK) return r;
+  if ((r = cuda_status(launch_zscore(P, st))) != TRIA_OK) return r;
+  if ((r = cuda_status(launch_select(P, true, st))) != TRIA_OK) return r;
+  return cuda_status(launch_move(P, st));
+}
+
+extern "C" tria_status tria_evict_profiled(const tria_stats* stats, int32_t layer, const tria_layer_cache* cache,
+                                           const tria_policy* policy, void* ws, size_t ws_bytes, void* stream,
+                                           float* stage_ms, int32_t* launches) {
+  tria_status r;
+  if (!stage_ms || !launches) return TRIA_ERR_INVALID_ARG;
+  if ((r = check_cache(cache)) != TRIA_OK) return r;
+  if ((r = check_stats(stats, layer, cache)) != TRIA_OK) return r;
+  std::vector<int> budget;
+  if ((r = check_policy(cache, policy, true, budget)) != TRIA_OK) return r;
+  const Layout L = make_layout(cache, stats->group);
+  if ((r = check_ws(ws, ws_bytes, L)) != TRIA_OK) return r;
+  Pass P;
+  fill_pass(P, cache, policy, budget, L, ws, stats->group);
+  set_stats(P, stats, layer);
+  P.only_active = 1;
+  P.raw = (float*)((uint8_t*)ws + L.raw);
+  P.score = (float*)((uint8_t*)ws + L.score);
+  P.score_in = P.score;
+  P.keep = (int32_t*)((uint8_t*)ws + L.keep);
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaEvent_t ev[5] = {};
+  for (int i = 0; i < 5; ++i)
+    if (cudaEventCreate(&ev[i]) != cudaSuccess) {
+      for (int j = 0; j < i; ++j) cudaEventDestroy(ev[j]);
+      return TRIA_ERR_CUDA;
+    }
+  cudaError_t e = cudaEventRecord(ev[0], st);
+  if (e == cudaSuccess) e = launch_score(P, st);
+  if (e == cudaSuccess) e = cudaEventRecord(ev[1], st);
+  if (e == cudaSuccess) e = launch_zscore(P, st);
+  if (e == cudaSuccess) e = cudaEventRecord(ev[2], st);
+  if (e == cudaSuccess) e = launch_select(P, true, st);
+  if (e == cudaSuccess) e = cudaEventRecord(ev[3], st);
+  if (e == cudaSuccess) e = launch_move(P, st);
+  if (e == cudaSuccess) e = cudaEventRecord(ev[4], st);
+  if (e == cudaSuccess) e = cudaEventSynchronize(ev[4]);
+  if (e == cudaSuccess) {
+    for (int i = 0; i < 4; ++i) cudaEventElapsedTime(&stage_ms[i], ev[i], ev[i + 1]);
+    cudaEventElapsedTime(&stage_ms[4], ev[0], ev[4]);
+    *launches = 8;
+  }
+  for (int i = 0; i < 5; ++i) cudaEventDestroy(ev[i]);
+  return cuda_status(e);
+}
+
+extern "C" tria_status tria_device_status(void* ws, void* stream) {
+  if (!ws || !aligned(ws, 256)) return TRIA_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  uint32_t words[2] = {0, 0};
+  if (cudaMemcpyAsync(words, ws, sizeof(words), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return TRIA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return TRIA_ERR_CUDA;
+  if (words[0] != 0) {
+    if (cudaMemsetAsync(ws, 0, sizeof(words), st) != cudaSuccess) return TRIA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return TRIA_ERR_CUDA;
+  }
+  return (tria_status)words[0];
+}
+
+extern "C" tria_status tria_selftest_bounded_wait(int32_t spin_limit, void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || !aligned(ws, 256) || ws_bytes < sizeof(Ctrl) || spin_limit < 1) return TRIA_ERR_WORKSPACE;
+  Pass P;
+  memset(&P, 0, sizeof(P));
+  P.ctrl = (Ctrl*)ws;
+  P.spin_limit = spin_limit;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (launch_wait_selftest(P, st) != cudaSuccess) return TRIA_ERR_CUDA;
+  return tria_device_status(ws, stream);
+}
+
+extern "C" const char* tria_status_string(tria_status s) {
+  switch (s) {
+    case TRIA_OK: return "ok";
+    case TRIA_ERR_INVALID_ARG: return "invalid argument";
+    case TRIA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case TRIA_ERR_BUDGET: return "budget smaller than sink + window";
+    case TRIA_ERR_CUDA: return "CUDA error";
+    case TRIA_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case TRIA_ERR_TIMEOUT: return "device wait timed out";
+    case TRIA_ERR_DEVICE_ARG: return "n_live out of range";
+    case TRIA_ERR_KEEP_LIST: return "invalid keep list";
+  }
+  return "unknown status";
+}
+
+extern "C" int32_t tria_version(void) { return TRIA_VERSION; }

@@ -1,0 +1,174 @@
+// Calibration statistics: upload and load-time folding.
+//
+// [Doc] "TriAttention KV-Cache Eviction (--triattention)", §2 Calibration file
+// (per-layer, per-head RoPE-direction statistics: mean query directions and
+// per-frequency importance weights) and §5 Phase C (omega and per-head
+// q_mean / q_abs arrays laid out [n_layers x n_heads x freq_count]).
+//
+// What is folded once at load, per (layer, KV head, group member j, pair f):
+//   qe = qbar * E_f,  E_f = (1/|D|) sum_{d in D} e^{i w_f d}
+//   mw = q_abs - |qbar|
+// so that a pass needs only one phase e^{i w_f p} per pair:
+//   mean_d Re(qbar e^{i w (p + d)} conj(k)) = Re(qe e^{i w p} conj(k)).
+//
+// Phase arithmetic: w_f / (2 pi) is stored as a 64-bit fixed-point fraction of
+// a turn ("turns"). For an integer position x, turns * x mod 2^64 is the exact
+// fractional turn of w_f * x (up to the rounding of w_f / 2pi itself), so no
+// floating-point range reduction is needed at any context length.
+#include <math.h>
+
+#include <vector>
+
+#include "tria_internal.cuh"
+
+namespace tria {
+
+__global__ void k_stats_freq(int fc, int hd, double theta, const double* __restrict__ omega_in,
+                             const long long* __restrict__ offsets, int n_off,
+                             unsigned long long* __restrict__ turns, double2* __restrict__ efold) {
+  const int f = blockIdx.x * blockDim.x + threadIdx.x;
+  if (f >= fc) return;
+  const double w = omega_in ? omega_in[f] : pow(theta, -2.0 * (double)f / (double)hd);
+  double t = w / (2.0 * 3.14159265358979323846);
+  t -= floor(t);                                   // fraction of a turn in [0, 1)
+  double scaled = ldexp(t, 64);
+  unsigned long long tu = scaled >= 18446744073709551615.0 ? 0ull : (unsigned long long)scaled;
+  turns[f] = tu;
+  double re = 0.0, im = 0.0;
+  for (int i = 0; i < n_off; ++i) {
+    const unsigned long long x = tu * (unsigned long long)offsets[i];   // mod 2^64
+    const double ang = ldexp((double)(long long)x, -64) * (2.0 * 3.14159265358979323846);
+    double s, c;
+    sincos(ang, &s, &c);
+    re += c;
+    im += s;
+  }
+  efold[f] = make_double2(re / n_off, im / n_off);
+}
+
+__global__ void k_stats_heads(int L, int n_q, int n_kv, int G, int fc, const float* __restrict__ q_mean,
+                              const float* __restrict__ q_abs, const int* __restrict__ head_order,
+                              const double2* __restrict__ efold, float2* __restrict__ qe,
+                              float* __restrict__ mw) {
+  const long long total = (long long)L * n_kv * G * fc;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int f = (int)(i % fc);
+    const long long t = i / fc;
+    const int slot = (int)(t % (n_kv * G));       // g * G + j
+    const int l = (int)(t / (n_kv * G));
+    const int h = head_order[slot];
+    const long long src = ((long long)l * n_q + h) * fc + f;
+    const double a = q_mean[2 * src], b = q_mean[2 * src + 1];
+    const double2 e = efold[f];
+    qe[i] = make_float2((float)(a * e.x - b * e.y), (float)(a * e.y + b * e.x));
+    const double mag = sqrt(a * a + b * b);
+    mw[i] = q_abs ? (float)((double)q_abs[src] - mag) : 0.0f;
+  }
+}
+
+}  // namespace tria
+
+using namespace tria;
+
+namespace {
+
+template <typename T>
+cudaError_t upload(T** dst, const T* src, size_t count) {
+  *dst = nullptr;
+  if (count == 0) return cudaSuccess;
+  cudaError_t e = cudaMalloc((void**)dst, count * sizeof(T));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpy(*dst, src, count * sizeof(T), cudaMemcpyHostToDevice);
+}
+
+}  // namespace
+
+extern "C" tria_status tria_load_stats(const tria_stats_desc* d, tria_stats** out, void* stream) {
+  if (!out) return TRIA_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!d || !d->q_mean || d->n_layers <= 0) return TRIA_ERR_INVALID_ARG;
+  tria_status gate = tria_gate_check(d->n_q_heads, d->n_kv_heads, d->head_dim);
+  if (gate != TRIA_OK) return gate;
+  const int L = d->n_layers, nq = d->n_q_heads, nkv = d->n_kv_heads, hd = d->head_dim;
+  const int fc = hd / 2, G = nq / nkv;
+  if (!d->omega && !(d->rope_theta > 1.0)) return TRIA_ERR_INVALID_ARG;
+  if (d->offsets && d->n_offsets <= 0) return TRIA_ERR_INVALID_ARG;
+
+  // query heads of each KV head, ascending ([Worklog] "sampled-head mapping")
+  std::vector<int> order;
+  order.reserve(nq);
+  for (int g = 0; g < nkv; ++g) {
+    int cnt = 0;
+    for (int h = 0; h < nq; ++h) {
+      const int kv = d->kv_of_q ? d->kv_of_q[h] : h / G;
+      if (kv < 0 || kv >= nkv) return TRIA_ERR_INVALID_ARG;
+      if (kv == g) {
+        order.push_back(h);
+        ++cnt;
+      }
+    }
+    if (cnt != G) return TRIA_ERR_INVALID_ARG;
+  }
+  std::vector<long long> offs;
+  if (d->offsets) {
+    offs.assign(d->offsets, d->offsets + d->n_offsets);
+  } else {
+    for (int j = 0; j <= 16; ++j) offs.push_back(1ll << j);
+  }
+
+  cudaStream_t st = (cudaStream_t)stream;
+  tria_stats* s = new tria_stats();
+  s->n_layers = L;
+  s->n_q_heads = nq;
+  s->n_kv_heads = nkv;
+  s->head_dim = hd;
+  s->group = G;
+  float* qm_d = nullptr;
+  float* qa_d = nullptr;
+  double* om_d = nullptr;
+  long long* off_d = nullptr;
+  int* order_d = nullptr;
+  double2* ef_d = nullptr;
+  const size_t nqm = (size_t)L * nq * fc;
+  cudaError_t e = cudaSuccess;
+  auto fail = [&]() {
+    cudaFree(qm_d); cudaFree(qa_d); cudaFree(om_d); cudaFree(off_d); cudaFree(order_d); cudaFree(ef_d);
+    cudaFree(s->qe); cudaFree(s->mw); cudaFree(s->turns);
+    delete s;
+    return TRIA_ERR_CUDA;
+  };
+  if ((e = upload(&qm_d, d->q_mean, 2 * nqm)) != cudaSuccess) return fail();
+  if (d->q_abs && (e = upload(&qa_d, d->q_abs, nqm)) != cudaSuccess) return fail();
+  if (d->omega && (e = upload(&om_d, d->omega, (size_t)fc)) != cudaSuccess) return fail();
+  if ((e = upload(&off_d, offs.data(), offs.size())) != cudaSuccess) return fail();
+  if ((e = upload(&order_d, order.data(), order.size())) != cudaSuccess) return fail();
+  if ((e = cudaMalloc((void**)&ef_d, fc * sizeof(double2))) != cudaSuccess) return fail();
+  if ((e = cudaMalloc((void**)&s->turns, fc * sizeof(unsigned long long))) != cudaSuccess) return fail();
+  const size_t nfold = (size_t)L * nkv * G * fc;
+  if ((e = cudaMalloc((void**)&s->qe, nfold * sizeof(float2))) != cudaSuccess) return fail();
+  if ((e = cudaMalloc((void**)&s->mw, nfold * sizeof(float))) != cudaSuccess) return fail();
+
+  k_stats_freq<<<(fc + 127) / 128, 128, 0, st>>>(fc, hd, d->rope_theta, om_d, off_d, (int)offs.size(),
+                                                s->turns, ef_d);
+  const int blocks = (int)((nfold + 255) / 256 < 4096 ? (nfold + 255) / 256 : 4096);
+  k_stats_heads<<<blocks, 256, 0, st>>>(L, nq, nkv, G, fc, qm_d, qa_d, order_d, ef_d, s->qe, s->mw);
+  if ((e = cudaGetLastError()) != cudaSuccess) return fail();
+  if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return fail();
+  cudaFree(qm_d);
+  cudaFree(qa_d);
+  cudaFree(om_d);
+  cudaFree(off_d);
+  cudaFree(order_d);
+  cudaFree(ef_d);
+  *out = s;
+  return TRIA_OK;
+}
+
+extern "C" void tria_free_stats(tria_stats* s) {
+  if (!s) return;
+  cudaFree(s->qe);
+  cudaFree(s->mw);
+  cudaFree(s->turns);
+  delete s;
+}

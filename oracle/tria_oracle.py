@@ -250,7 +250,7 @@ def evict_layer(layer_cache: dict, q_mean: np.ndarray, q_abs, *, layer: int, n_k
             info[(s, g)] = {"raw": raw, "s": sc, "keep": keep, "B": b, "n": n, "row0": r0}
             if n <= b:
                 continue
-            for name in ("k", "k_scale", "v", "pos"):
+            for name in ("k", "k_scale", "v", "v_scale", "pos"):
                 if out.get(name) is None:
                     continue
                 seg = out[name][r0:r0 + cap]

@@ -1,0 +1,134 @@
+"""Host-side checks of the C ABI: the library loads, exports what the header
+declares, and rejects bad arguments before touching a GPU (no compute calls)."""
+import ctypes
+import json
+import os
+import re
+
+import numpy as np
+import pytest
+
+import kv_cache_eviction_tria_gb300 as tria
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tria.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(tria.LIB_PATH):
+        from kv_cache_eviction_tria_gb300 import _build
+        _build.build()
+    return tria.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\S[^;(]*?\b(tria_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_pass_entry_points():
+    names = declared_functions()
+    for n in ("tria_load_stats", "tria_score", "tria_select", "tria_compact", "tria_evict"):
+        assert n in names
+
+
+def test_library_exports_every_declared_function(lib):
+    names = declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in tria.h but not exported"
+    assert set(tria.EXPORTS) <= set(names)
+
+
+def test_version_and_status_strings(lib):
+    assert tria.version() == 1
+    for code in range(9):
+        assert tria.status_string(code) not in ("", "unknown status")
+    assert tria.status_string(99) == "unknown status"
+
+
+def test_gate_matches_the_documented_gate(lib):
+    with open(os.path.join(ROOT, "tests", "golden", "doc_gpu_gate.json")) as fh:
+        gold = json.load(fh)
+    for row in gold["eligible"]:
+        assert tria.gate_check(row["nh"], row["nkv"], row["hd"]) == tria.OK, row
+    for row in gold["ineligible"]:
+        assert tria.gate_check(row["nh"], row["nkv"], row["hd"]) == tria.ERR_UNSUPPORTED, row
+    assert tria.gate_check(48, 3, 128) == tria.ERR_UNSUPPORTED   # group 16 > 8
+    assert tria.gate_check(0, 8, 128) == tria.ERR_INVALID_ARG
+
+
+def test_budget_rows_and_trigger(lib):
+    assert tria.budget_rows(0.5, 512) == 256
+    assert tria.budget_rows(0.25, 98710) == 24677
+    assert tria.budget_rows(0.3, 10) == 3
+    gold = json.load(open(os.path.join(ROOT, "tests", "golden", "worklog_compaction_schedule.json")))
+    assert tria.should_evict(gold["trigger"], gold["kv_budget"], gold["divide_length"])
+    assert not tria.should_evict(gold["trigger"] - 1, gold["kv_budget"], gold["divide_length"])
+
+
+def _fake_cache(n_seqs=2, cap=(1000, 900), k=0x10000, v=0x20000, k_type="f16", hd=128, n_kv=8,
+                k_scale=None):
+    """A cache struct with fake (never dereferenced) device addresses."""
+    return tria.LayerCache(k=k, v=v, pos=0x30000, n_live=0x40000,
+                           seq_row0=[0, n_kv * cap[0]][:n_seqs], capacity=list(cap)[:n_seqs],
+                           head_dim=hd, n_kv_heads=n_kv, k_type=k_type, v_type="f16", k_scale=k_scale)
+
+
+def test_workspace_size_layout_rules(lib):
+    c = _fake_cache()
+    n4 = tria.workspace_size(c, 4)
+    n0 = tria.workspace_size(c, 0)
+    rows = 8 * 1900
+    assert n4 - n0 >= rows * 4 * 4          # raw scores for G = 4
+    assert n0 >= rows * 8                   # score + keep per row
+    with pytest.raises(tria.TriaError):
+        tria.workspace_size(_fake_cache(k=0x10008), 4)            # k not 16-byte aligned
+    with pytest.raises(tria.TriaError):
+        tria.workspace_size(_fake_cache(hd=80), 4)                # head_dim % 32
+    with pytest.raises(tria.TriaError):
+        tria.workspace_size(_fake_cache(k_type="q8_0"), 4)        # q8_0 without scales
+    overlap = tria.LayerCache(k=0x10000, v=0x20000, pos=0x30000, n_live=0x40000, seq_row0=[0, 100],
+                              capacity=[64, 64], head_dim=64, n_kv_heads=2)
+    with pytest.raises(tria.TriaError):
+        tria.workspace_size(overlap, 4)                           # sequences overlap
+
+
+def _call_select(c, pol, ws=0x100000, nbytes=1 << 30, score=0x50000, keep=0x60000):
+    cs, ps = c.c_struct(), pol.c_struct()
+    return tria.raw_call("tria_select", ctypes.c_void_p(score), ctypes.byref(cs), ctypes.byref(ps),
+                         ctypes.c_void_p(keep), ctypes.c_void_p(ws), nbytes, None)
+
+
+def test_host_validation_rejects_before_any_launch(lib):
+    c = _fake_cache()
+    good = tria.Policy(budget_frac=0.5, n_ctx=[1000, 900], window=64, sink=4, cur_pos=[1000, 900])
+    assert _call_select(c, tria.Policy(budget_frac=0.05, n_ctx=[1000, 900], window=64, sink=4)) \
+        == tria.ERR_BUDGET
+    assert _call_select(c, good, ws=0x100010) == tria.ERR_WORKSPACE          # misaligned ws
+    assert _call_select(c, good, nbytes=1024) == tria.ERR_WORKSPACE          # too small
+    assert _call_select(c, good, score=0) == tria.ERR_INVALID_ARG
+    assert _call_select(c, tria.Policy(budget_frac=1.5, n_ctx=[1, 1])) == tria.ERR_INVALID_ARG
+    assert _call_select(c, tria.Policy(budget_rows=[100, -1], window=0, sink=0)) == tria.ERR_INVALID_ARG
+    cs, ps = c.c_struct(), good.c_struct()
+    # evict / score with no stats handle
+    assert tria.raw_call("tria_evict", None, 0, ctypes.byref(cs), ctypes.byref(ps),
+                         ctypes.c_void_p(0x100000), 1 << 30, None) == tria.ERR_INVALID_ARG
+    assert tria.raw_call("tria_workspace_init", ctypes.c_void_p(0x100010), 4096, None) \
+        == tria.ERR_WORKSPACE
+
+
+def test_load_stats_rejects_ineligible_shapes(lib):
+    qm = np.zeros((1, 30, 64, 2), np.float32)
+    with pytest.raises(tria.TriaError) as e:
+        tria.Stats(qm, None, n_kv_heads=8, head_dim=128, rope_theta=1e6, stream=0)
+    assert e.value.status == tria.ERR_UNSUPPORTED
+    qm = np.zeros((1, 32, 40, 2), np.float32)
+    with pytest.raises(tria.TriaError) as e:
+        tria.Stats(qm, None, n_kv_heads=8, head_dim=80, rope_theta=1e6, stream=0)
+    assert e.value.status == tria.ERR_UNSUPPORTED
+    qm = np.zeros((1, 32, 64, 2), np.float32)
+    with pytest.raises(tria.TriaError) as e:    # uneven head map
+        tria.Stats(qm, None, n_kv_heads=8, head_dim=128, rope_theta=1e6, kv_of_q=[0] * 32, stream=0)
+    assert e.value.status == tria.ERR_INVALID_ARG
