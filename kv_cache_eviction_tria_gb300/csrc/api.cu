@@ -108,10 +108,18 @@ tria_status check_cache(const tria_layer_cache* c) {
   return TRIA_OK;
 }
 
-tria_status check_policy(const tria_layer_cache* c, const tria_policy* p, bool need_pos, std::vector<int>& budget) {
+// need_budget = false (scoring only): the budget is not used and not checked.
+tria_status check_policy(const tria_layer_cache* c, const tria_policy* p, bool need_pos, std::vector<int>& budget,
+                         bool need_budget = true) {
   if (!p) return TRIA_ERR_INVALID_ARG;
   if (p->window < 0 || p->sink < 0) return TRIA_ERR_INVALID_ARG;
   if (need_pos && !p->cur_pos) return TRIA_ERR_INVALID_ARG;
+  if (!need_budget) {
+    budget.assign(c->n_seqs, 0);
+    for (int s = 0; s < c->n_seqs; ++s)
+      if (need_pos && p->cur_pos[s] < 0) return TRIA_ERR_INVALID_ARG;
+    return TRIA_OK;
+  }
   if (!p->budget_rows && (!p->n_ctx || !(p->budget_frac > 0.0) || p->budget_frac > 1.0))
     return TRIA_ERR_INVALID_ARG;
   budget.assign(c->n_seqs, 0);
@@ -235,7 +243,7 @@ extern "C" tria_status tria_score(const tria_stats* stats, int32_t layer, const 
   if ((r = check_stats(stats, layer, cache)) != TRIA_OK) return r;
   if (!score_out || !aligned(score_out, 4) || (raw_out && !aligned(raw_out, 4))) return TRIA_ERR_INVALID_ARG;
   std::vector<int> budget;
-  if ((r = check_policy(cache, policy, true, budget)) != TRIA_OK) return r;
+  if ((r = check_policy(cache, policy, true, budget, false)) != TRIA_OK) return r;
   const Layout L = make_layout(cache, stats->group);
   if ((r = check_ws(ws, ws_bytes, L)) != TRIA_OK) return r;
   Pass P;

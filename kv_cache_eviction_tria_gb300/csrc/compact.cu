@@ -255,8 +255,10 @@ cudaError_t launch_keep_prepass(const Pass& P, cudaStream_t st) {
 
 cudaError_t launch_move(const Pass& P, cudaStream_t st) {
   const MoveSmem L = move_smem_layout(P.k_rb, P.ks_rb, P.v_rb, P.vs_rb);
-  cudaError_t e = cudaFuncSetAttribute(k_move, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
-  if (e != cudaSuccess) return e;
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(k_move, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  if (attr != cudaSuccess) return attr;
+  if (L.total > 200 * 1024) return cudaErrorInvalidValue;
   const int grid = P.n_seg * P.c_max;
   k_move<<<grid, kThreads, L.total, st>>>(P);
   return cudaGetLastError();

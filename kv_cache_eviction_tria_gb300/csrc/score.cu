@@ -230,12 +230,11 @@ __global__ void __launch_bounds__(kThreads, 2) k_score(const __grid_constant__ P
         for (int o = TPR / 2; o > 0; o >>= 1)
 #pragma unroll
           for (int h = 0; h < G; ++h) acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], o);
-        if (row_on && q < G) {
-          float val = acc[0];
+        // every lane holds all G sums; lane q writes the heads h with h % TPR == q
+        if (row_on) {
 #pragma unroll
-          for (int h = 1; h < G; ++h)
-            if (q == h) val = acc[h];
-          sraw[(pr0 + rr) * G + q] = val;
+          for (int h = 0; h < G; ++h)
+            if ((h % TPR) == q) sraw[(pr0 + rr) * G + h] = acc[h];
         }
       }
     }
@@ -343,8 +342,12 @@ template <int KT, int G, int TPR, int PPT>
 cudaError_t launch_score_t(const Pass& P, cudaStream_t st) {
   const size_t smem = score_smem_bytes(P);
   auto kern = k_score<KT, G, TPR, PPT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
+  // the largest dynamic shared memory any layout of this instantiation needs;
+  // set once per process (the attribute is per function, not per call)
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  if (attr != cudaSuccess) return attr;
+  if (smem > 200 * 1024) return cudaErrorInvalidValue;
   dim3 grid(P.cs_max, P.n_seg);
   kern<<<grid, kThreads, smem, st>>>(P);
   return cudaGetLastError();
