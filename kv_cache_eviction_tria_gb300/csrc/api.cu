@@ -44,9 +44,7 @@ Layout make_layout(const tria_layer_cache* c, int G) {
   Layout L{};
   const int hd = c->head_dim;
   const int k_rb = row_bytes(c->k_type, hd);
-  int piece_rows = 8192 / k_rb;
-  piece_rows = std::min(64, std::max(1, piece_rows));
-  L.cs_rows = 8 * piece_rows;
+  L.cs_rows = 0;
   int cap_max = 0;
   int64_t total_rows = 0;
   for (int s = 0; s < c->n_seqs; ++s) {
@@ -56,7 +54,7 @@ Layout make_layout(const tria_layer_cache* c, int G) {
   cap_max = std::max(cap_max, 1);
   L.total_rows = total_rows;
   L.n_seg = c->n_seqs * c->n_kv_heads;
-  L.cs_max = (cap_max + L.cs_rows - 1) / L.cs_rows;
+  L.cs_max = score_pieces_max(k_rb, cap_max);
   L.c_max = (cap_max + kChunk - 1) / kChunk;
   size_t off = 0;
   L.ctrl = off;
@@ -86,6 +84,7 @@ Layout make_layout(const tria_layer_cache* c, int G) {
 tria_status check_cache(const tria_layer_cache* c) {
   if (!c) return TRIA_ERR_INVALID_ARG;
   if (c->n_seqs < 1 || c->n_seqs > kMaxSeqs || c->n_kv_heads < 1) return TRIA_ERR_INVALID_ARG;
+  if (c->n_seqs * c->n_kv_heads > kMaxSegments) return TRIA_ERR_UNSUPPORTED;
   const int hd = c->head_dim;
   if (hd <= 0 || hd > TRIA_MAX_HEAD_DIM || hd % 32 != 0) return TRIA_ERR_UNSUPPORTED;
   if (!dtype_ok(c->k_type) || !dtype_ok(c->v_type)) return TRIA_ERR_UNSUPPORTED;

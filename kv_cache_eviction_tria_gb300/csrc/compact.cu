@@ -8,32 +8,54 @@
 // GPU work on GPU" (one gather kernel instead of thousands of small copies).
 //
 // Kept row i of a segment moves to row i, and i <= keep[i], so data only moves
-// towards lower rows. The CTA that owns source chunk c (64 rows) moves its kept
-// rows to the contiguous destination range [prefix[c], prefix[c+1]). Those
-// destination rows can belong only to chunks <= c. The CTA therefore
-//   1. copies its moving rows (all planes) into shared memory,
+// towards lower rows. The warp that owns source chunk c (32 rows) moves its
+// kept rows to the contiguous destination range [prefix[c], prefix[c+1]),
+// which can only cover rows of chunks <= c. It therefore
+//   1. copies its moving rows (all planes) into its own shared-memory stage,
 //   2. publishes "chunk c read" (flag = epoch + 1, release),
 //   3. waits (bounded) for the flags of the lower chunks whose rows it will
-//      overwrite - at most two, since 64 destination rows span at most two
-//      64-row source chunks - and
-//   4. writes the rows out.
-// CTAs take tickets in the order they start, and chunk c only waits on chunks
-// with smaller tickets, which are already running or done: no deadlock. Each
-// byte moved is read once and written once.
+//      overwrite - at most two, since 32 destination rows span at most two
+//      32-row source chunks - and
+//   4. writes the stage out.
+// Warps take chunks in increasing order and every warp of the cooperative
+// grid is resident, so the lowest unpublished chunk can always proceed: no
+// deadlock. Each byte moved is read once and written once.
 #include "tria_internal.cuh"
 
 namespace tria {
 
-struct MoveSmem {
-  int k, ks, v, vs, pos, src, total;
+// ---------------------------------------------------------------------------
+// async-copy helpers (cp.async: per-thread global -> shared copies that need
+// no registers; completion per thread group, then a block barrier)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// One staging buffer: the moving rows of one chunk, every plane packed
+// in destination order.
+struct MoveStage {
+  int k, ks, v, vs, pos, bytes;
 };
 
-__host__ __device__ inline MoveSmem move_smem_layout(int k_rb, int ks_rb, int v_rb, int vs_rb) {
-  MoveSmem L;
+__host__ __device__ inline MoveStage move_stage_layout(int k_rb, int ks_rb, int v_rb, int vs_rb) {
+  MoveStage L;
   int off = 0;
-  auto take = [&](int bytes) {
-    int at = off;
-    off = (off + bytes + 15) & ~15;
+  auto take = [&](int b) {
+    const int at = off;
+    off = (off + b + 15) & ~15;
     return at;
   };
   L.k = take(kChunk * k_rb);
@@ -41,148 +63,181 @@ __host__ __device__ inline MoveSmem move_smem_layout(int k_rb, int ks_rb, int v_
   L.v = take(kChunk * v_rb);
   L.vs = take(kChunk * vs_rb);
   L.pos = take(kChunk * 4);
-  L.src = take(kChunk * 4);
-  L.total = off;
+  L.bytes = off;
   return L;
 }
 
-// Copy `rows` rows of `rb` bytes from scattered source rows into packed shared
-// memory (gather) or from packed shared memory to consecutive rows (scatter),
-// with the widest unit that divides the row size.
-template <bool kGather>
-__device__ __forceinline__ void copy_rows(uint8_t* plane, int64_t row0, int rb, uint8_t* stage,
-                                          const int* src_rows, int dst_row, int rows) {
-  if (rb == 0 || rows == 0) return;
-  if ((rb & 15) == 0) {
-    const int per = rb >> 4;
-    const int units = rows * per;
-    for (int u = threadIdx.x; u < units; u += blockDim.x) {
-      const int j = u / per, w = u - j * per;
-      uint4* sp = reinterpret_cast<uint4*>(stage + (size_t)j * rb) + w;
-      if (kGather) {
-        const uint4* gp = reinterpret_cast<const uint4*>(plane + (size_t)(row0 + src_rows[j]) * rb) + w;
-        *sp = __ldcg(gp);
-      } else {
-        uint4* gp = reinterpret_cast<uint4*>(plane + (size_t)(row0 + dst_row + j) * rb) + w;
-        *gp = *sp;
-      }
-    }
-  } else if ((rb & 3) == 0) {
-    const int per = rb >> 2;
-    const int units = rows * per;
-    for (int u = threadIdx.x; u < units; u += blockDim.x) {
-      const int j = u / per, w = u - j * per;
-      uint32_t* sp = reinterpret_cast<uint32_t*>(stage + (size_t)j * rb) + w;
-      if (kGather) {
-        const uint32_t* gp = reinterpret_cast<const uint32_t*>(plane + (size_t)(row0 + src_rows[j]) * rb) + w;
-        *sp = __ldcg(gp);
-      } else {
-        uint32_t* gp = reinterpret_cast<uint32_t*>(plane + (size_t)(row0 + dst_row + j) * rb) + w;
-        *gp = *sp;
-      }
-    }
+constexpr int kMoveSmemLimit = 200 * 1024;
+constexpr int kMoveMaxWarps = 16;
+
+__host__ __device__ inline int move_warps(const MoveStage& L) {
+  int w = kMoveSmemLimit / L.bytes;
+  return w > kMoveMaxWarps ? kMoveMaxWarps : w;
+}
+
+// Lane -> (row, unit) mapping of one plane for the warp-wide row copies: a
+// row of `rb` bytes is `per` units of `unit` bytes; when per <= 32 a warp
+// instruction covers `rpi` rows, else a row takes several instructions.
+struct PlaneMap {
+  int rb, unit, per, rpi, lr, lu;
+};
+
+__device__ __forceinline__ PlaneMap plane_map(int rb, int lane) {
+  PlaneMap m;
+  m.rb = rb;
+  m.unit = (rb & 15) == 0 ? 16 : ((rb & 7) == 0 ? 8 : ((rb & 3) == 0 ? 4 : 2));
+  m.per = rb > 0 ? rb / m.unit : 1;
+  m.rpi = m.per <= 32 ? 32 / m.per : 1;
+  m.lr = m.per <= 32 ? lane / m.per : 0;
+  m.lu = m.per <= 32 ? lane - m.lr * m.per : lane;
+  return m;
+}
+
+__device__ __forceinline__ void copy_unit_async(uint8_t* d, const uint8_t* g, int unit) {
+  if (unit == 16) cp_async16(d, g);
+  else if (unit == 8) cp_async8(d, g);
+  else if (unit == 4) cp_async4(d, g);
+  else *reinterpret_cast<uint16_t*>(d) = *reinterpret_cast<const uint16_t*>(g);
+}
+
+// gather rows src[0 .. rows) of one plane into packed staging (cp.async)
+__device__ __forceinline__ void warp_gather(const uint8_t* plane, int64_t row0, const PlaneMap& m,
+                                            uint8_t* stage, const int* src, int rows) {
+  if (m.rb == 0 || rows == 0) return;
+  if (m.per <= 32) {
+    if (m.lr >= m.rpi) return;
+    for (int j = m.lr; j < rows; j += m.rpi)
+      copy_unit_async(stage + (size_t)j * m.rb + m.lu * m.unit,
+                      plane + (size_t)(row0 + src[j]) * m.rb + m.lu * m.unit, m.unit);
   } else {
-    const int per = rb >> 1;
-    const int units = rows * per;
-    for (int u = threadIdx.x; u < units; u += blockDim.x) {
-      const int j = u / per, w = u - j * per;
-      uint16_t* sp = reinterpret_cast<uint16_t*>(stage + (size_t)j * rb) + w;
-      if (kGather) {
-        const uint16_t* gp = reinterpret_cast<const uint16_t*>(plane + (size_t)(row0 + src_rows[j]) * rb) + w;
-        *sp = __ldcg(gp);
-      } else {
-        uint16_t* gp = reinterpret_cast<uint16_t*>(plane + (size_t)(row0 + dst_row + j) * rb) + w;
-        *gp = *sp;
-      }
+    for (int j = 0; j < rows; ++j) {
+      const uint8_t* g = plane + (size_t)(row0 + src[j]) * m.rb;
+      for (int u = m.lu; u < m.per; u += 32)
+        copy_unit_async(stage + (size_t)j * m.rb + u * m.unit, g + u * m.unit, m.unit);
     }
   }
 }
 
-__global__ void __launch_bounds__(kThreads) k_move(const __grid_constant__ Pass P) {
+// write `rows` packed staged rows of one plane to consecutive rows from dst
+__device__ __forceinline__ void warp_scatter(uint8_t* plane, int64_t row0, int rb, const uint8_t* stage, int dst,
+                                             int rows, int lane) {
+  if (rb == 0 || rows == 0) return;
+  const size_t bytes = (size_t)rows * rb;
+  uint8_t* out = plane + (size_t)(row0 + dst) * rb;
+  if ((rb & 15) == 0) {
+    for (size_t u = lane; u < bytes / 16; u += 32)
+      reinterpret_cast<uint4*>(out)[u] = reinterpret_cast<const uint4*>(stage)[u];
+  } else if ((rb & 3) == 0) {
+    for (size_t u = lane; u < bytes / 4; u += 32)
+      reinterpret_cast<uint32_t*>(out)[u] = reinterpret_cast<const uint32_t*>(stage)[u];
+  } else {
+    for (size_t u = lane; u < bytes / 2; u += 32)
+      reinterpret_cast<uint16_t*>(out)[u] = reinterpret_cast<const uint16_t*>(stage)[u];
+  }
+}
+
+// Persistent compaction, one chunk per warp at a time. Work items are the
+// 32-row source chunks of all segments, enumerated segment-major; warp w of
+// the grid takes items w, w + W, w + 2W, ... in order. For its chunk a warp
+//   1. reads the chunk's kept-row list and the destination range,
+//   2. gathers the moving rows of every plane into its own shared-memory
+//      stage with cp.async, waits for them,
+//   3. publishes "chunk read" (flag = epoch + 1, release),
+//   4. waits (bounded) for the lower chunks whose rows its destination range
+//      covers, and
+//   5. writes the stage out to the contiguous destination rows.
+// Chunks only wait on lower chunks, which are taken earlier by resident warps
+// (cooperative launch): the lowest unpublished chunk can always proceed.
+__global__ void k_move(const __grid_constant__ Pass P) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ uint32_t s_ticket, s_epoch, s_bad;
-  __shared__ int s_first, s_timeout;
+  __shared__ uint32_t s_epoch, s_bad;
+  __shared__ int s_n[kMaxSegments];   // live rows of active segments, 0 otherwise
+  __shared__ int s_src[kMoveMaxWarps][kChunk];   // moving source rows of each warp's chunk
+  const MoveStage L = move_stage_layout(P.k_rb, P.ks_rb, P.v_rb, P.vs_rb);
   if (threadIdx.x == 0) {
-    s_ticket = atomicAdd(&P.ctrl->move_ticket, 1u);
     s_epoch = ld_acquire_u32(&P.ctrl->epoch);
     s_bad = ld_acquire_u32(&P.ctrl->bad_keep);
-    s_first = kChunk;
-    s_timeout = 0;
+  }
+  for (int sg = threadIdx.x; sg < P.n_seg; sg += blockDim.x) {
+    const SegView v = seg_view(P, sg);
+    s_n[sg] = v.active ? v.n : 0;
   }
   __syncthreads();
-  const int seg = (int)(s_ticket / (uint32_t)P.c_max);
-  const int c = (int)(s_ticket % (uint32_t)P.c_max);
-  bool work = seg < P.n_seg && s_bad == 0;
-  SegView sv;
-  if (work) {
-    sv = seg_view(P, seg);
-    work = sv.active && c * kChunk < sv.n;
-  }
-  if (work) {
-    const MoveSmem L = move_smem_layout(P.k_rb, P.ks_rb, P.v_rb, P.vs_rb);
-    int* ssrc = reinterpret_cast<int*>(smem + L.src);
-    const int* pre = P.prefix + (size_t)seg * (P.c_max + 1);
-    const int i0 = __ldcg(&pre[c]), i1 = __ldcg(&pre[c + 1]);
-    const int nk = i1 - i0;
-    // a chunk keeps at most its 64 rows, inside [0, B)
-    const bool sane = i0 >= 0 && nk >= 0 && nk <= kChunk && i1 <= min(sv.B, sv.n);
-    if (!sane && threadIdx.x == 0) {
-      s_timeout = 1;
-      report(P.ctrl, TRIA_ERR_INVALID_ARG, 0x10000000u | (uint32_t)seg);
-    }
-    // kept rows of this chunk and the first one that changes row
-    for (int j = threadIdx.x; sane && j < nk; j += blockDim.x) {
-      const int src = __ldcg(&P.keep[sv.row0 + i0 + j]);
-      ssrc[j] = src;
-      if (src < c * kChunk || src >= min(sv.n, (c + 1) * kChunk)) {
-        s_timeout = 1;
-        report(P.ctrl, TRIA_ERR_INVALID_ARG, 0x08000000u | (uint32_t)seg);
-      }
-      if (src != i0 + j) atomicMin(&s_first, j);
-    }
-    __syncthreads();
-    if (s_timeout) {
-      // inconsistent kept-row list: move nothing for this chunk, but still
-      // publish the flag so that no other chunk waits on it
-      if (threadIdx.x == 0) st_release_u32(&P.flags[(size_t)seg * P.c_max + c], s_epoch + 1u);
-      goto done;
-    }
-    {
-    const int first = min(s_first, nk);
-    const int nmove = nk - first;
-    const int dst0 = i0 + first;
-    const int* msrc = ssrc + first;
-    copy_rows<true>(P.k, sv.row0, P.k_rb, smem + L.k, msrc, 0, nmove);
-    copy_rows<true>(P.ks, sv.row0, P.ks_rb, smem + L.ks, msrc, 0, nmove);
-    copy_rows<true>(P.v, sv.row0, P.v_rb, smem + L.v, msrc, 0, nmove);
-    copy_rows<true>(P.vs, sv.row0, P.vs_rb, smem + L.vs, msrc, 0, nmove);
-    copy_rows<true>(reinterpret_cast<uint8_t*>(P.pos), sv.row0, 4, smem + L.pos, msrc, 0, nmove);
-    __syncthreads();
-    uint32_t* flags = P.flags + (size_t)seg * P.c_max;
-    if (threadIdx.x == 0) {
-      __threadfence();
-      st_release_u32(&flags[c], s_epoch + 1u);
+  const uint32_t tag = s_epoch + 1u;
+  const int total = P.n_seg * P.c_max;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps_cta = blockDim.x >> 5;
+  const int W = gridDim.x * nwarps_cta;
+  uint8_t* stg = smem + (size_t)warp * L.bytes;
+  int* msrc = s_src[warp];
+  const PlaneMap mk = plane_map(P.k_rb, lane), mks = plane_map(P.ks_rb, lane), mv = plane_map(P.v_rb, lane),
+                 mvs = plane_map(P.vs_rb, lane), mp = plane_map(4, lane);
+
+  if (s_bad == 0) {
+    for (int t = blockIdx.x * nwarps_cta + warp; t < total; t += W) {
+      const int sg = t / P.c_max, c = t - sg * P.c_max;
+      const int n = s_n[sg];
+      if (c * kChunk >= n) continue;
+      const int sq = sg / P.n_kv;
+      const int64_t row0 = P.seq[sq].row0 + (int64_t)(sg - sq * P.n_kv) * P.seq[sq].cap;
+      const int B = P.seq[sq].budget;
+      const int* pre = P.prefix + (size_t)sg * (P.c_max + 1);
+      const int i0 = __ldcg(&pre[c]), i1 = __ldcg(&pre[c + 1]);
+      const int nk = i1 - i0;
+      bool ok = i0 >= 0 && nk >= 0 && nk <= kChunk && i1 <= min(B, n);
+      // kept rows of the chunk: entry q in lane q
+      int a = -1;
+      if (ok && lane < nk) a = __ldcg(&P.keep[row0 + i0 + lane]);
+      const int lo_row = c * kChunk, hi_row = min(n, lo_row + kChunk);
+      ok = ok && !__any_sync(0xffffffffu, lane < nk && (a < lo_row || a >= hi_row));
+      if (!ok && lane == 0) report(P.ctrl, TRIA_ERR_INVALID_ARG, 0x10000000u | (uint32_t)sg);
+      // first kept entry whose row changes (all later ones change too)
+      const unsigned ma = __ballot_sync(0xffffffffu, ok && lane < nk && a != i0 + lane);
+      const int first = !ok ? 0 : (ma ? __ffs(ma) - 1 : nk);
+      const int nmove = ok ? nk - first : 0;
+      if (lane >= first && lane < nk) msrc[lane - first] = a;
+      __syncwarp();
       if (nmove > 0) {
-        const int lo = dst0 / kChunk, hi = min((i1 - 1) / kChunk, c - 1);
-        for (int cc = lo; cc <= hi; ++cc)
-          if (!wait_flag_bounded(&flags[cc], s_epoch + 1u, P.spin_limit)) {
-            s_timeout = 1;
-            report(P.ctrl, TRIA_ERR_TIMEOUT, (uint32_t)seg);
-            break;
-          }
+        warp_gather(P.k, row0, mk, stg + L.k, msrc, nmove);
+        warp_gather(P.ks, row0, mks, stg + L.ks, msrc, nmove);
+        warp_gather(P.v, row0, mv, stg + L.v, msrc, nmove);
+        warp_gather(P.vs, row0, mvs, stg + L.vs, msrc, nmove);
+        warp_gather(reinterpret_cast<const uint8_t*>(P.pos), row0, mp, stg + L.pos, msrc, nmove);
       }
-    }
-    __syncthreads();
-    if (!s_timeout && nmove > 0) {
-      copy_rows<false>(P.k, sv.row0, P.k_rb, smem + L.k, nullptr, dst0, nmove);
-      copy_rows<false>(P.ks, sv.row0, P.ks_rb, smem + L.ks, nullptr, dst0, nmove);
-      copy_rows<false>(P.v, sv.row0, P.v_rb, smem + L.v, nullptr, dst0, nmove);
-      copy_rows<false>(P.vs, sv.row0, P.vs_rb, smem + L.vs, nullptr, dst0, nmove);
-      copy_rows<false>(reinterpret_cast<uint8_t*>(P.pos), sv.row0, 4, smem + L.pos, nullptr, dst0, nmove);
-    }
+      cp_async_commit();
+      cp_async_wait<0>();
+      __syncwarp();
+      // publish "read"; then wait for the lower chunks the destination range covers
+      uint32_t* flags = P.flags + (size_t)sg * P.c_max;
+      int go = 0;
+      if (lane == 0) {
+        __threadfence();
+        st_release_u32(&flags[c], tag);
+        go = ok;
+        if (go && nmove > 0) {
+          const int dst0 = i0 + first;
+          const int lo = dst0 / kChunk, hi = min((i1 - 1) / kChunk, c - 1);
+          for (int cc = lo; cc <= hi; ++cc)
+            if (!wait_flag_bounded(&flags[cc], tag, P.spin_limit)) {
+              go = 0;
+              report(P.ctrl, TRIA_ERR_TIMEOUT, (uint32_t)sg);
+              break;
+            }
+        }
+      }
+      go = __shfl_sync(0xffffffffu, go, 0);
+      if (go && nmove > 0) {
+        const int dst0 = i0 + first;
+        warp_scatter(P.k, row0, P.k_rb, stg + L.k, dst0, nmove, lane);
+        warp_scatter(P.ks, row0, P.ks_rb, stg + L.ks, dst0, nmove, lane);
+        warp_scatter(P.v, row0, P.v_rb, stg + L.v, dst0, nmove, lane);
+        warp_scatter(P.vs, row0, P.vs_rb, stg + L.vs, dst0, nmove, lane);
+        warp_scatter(reinterpret_cast<uint8_t*>(P.pos), row0, 4, stg + L.pos, dst0, nmove, lane);
+      }
+      __syncwarp();
     }
   }
-done:
+
   // the last CTA to finish sets n_live and resets the call's counters
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -206,7 +261,7 @@ done:
 }
 
 // Caller-given keep lists: check them and derive the kept-row prefix of every
-// 64-row source chunk (the entries of chunk c are keep[prefix[c] .. prefix[c+1])).
+// source chunk (the entries of chunk c are keep[prefix[c] .. prefix[c+1])).
 __global__ void __launch_bounds__(kThreads) k_keep_prepass(const __grid_constant__ Pass P) {
   const int seg = blockIdx.y;
   const SegView sv = seg_view(P, seg);
@@ -254,14 +309,27 @@ cudaError_t launch_keep_prepass(const Pass& P, cudaStream_t st) {
 }
 
 cudaError_t launch_move(const Pass& P, cudaStream_t st) {
-  const MoveSmem L = move_smem_layout(P.k_rb, P.ks_rb, P.v_rb, P.vs_rb);
+  const MoveStage L = move_stage_layout(P.k_rb, P.ks_rb, P.v_rb, P.vs_rb);
+  const int warps = move_warps(L);
+  if (warps < 1) return cudaErrorInvalidValue;
+  const int threads = warps * 32;
+  const int smem = warps * L.bytes;
   static const cudaError_t attr =
-      cudaFuncSetAttribute(k_move, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+      cudaFuncSetAttribute(k_move, cudaFuncAttributeMaxDynamicSharedMemorySize, kMoveSmemLimit);
   if (attr != cudaSuccess) return attr;
-  if (L.total > 200 * 1024) return cudaErrorInvalidValue;
-  const int grid = P.n_seg * P.c_max;
-  k_move<<<grid, kThreads, L.total, st>>>(P);
-  return cudaGetLastError();
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_move, threads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  int grid = sms * per_sm;
+  const int items = P.n_seg * P.c_max;
+  const int need = (items + warps - 1) / warps;
+  if (grid > need) grid = need;
+  if (grid < 1) grid = 1;
+  void* args[] = {const_cast<Pass*>(&P)};
+  return cudaLaunchCooperativeKernel((const void*)k_move, dim3(grid), dim3(threads), args, (size_t)smem, st);
 }
 
 cudaError_t launch_wait_selftest(const Pass& P, cudaStream_t st) {

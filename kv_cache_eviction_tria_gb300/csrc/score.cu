@@ -8,319 +8,533 @@
 //
 // Per row r and query head h of the segment's group:
 //   raw_h(r) = sum_f  Wr_{h,f} K[r][f] + Wi_{h,f} K[r][f+fc] + M_{h,f} |k_f|
-// with W = qbar E_f e^{i w_f p} (built once per CTA) and M = q_abs - |qbar|.
+// with W = qbar E_f e^{i w_f p} and M = q_abs - |qbar|.
 //
-// Layout of the work: one CTA = one chunk of rows of one segment; each of its
-// 8 warps owns a contiguous piece of the chunk, which one lane brings into
-// shared memory with a single bulk async copy (TMA, non-tensor form) completed
-// on the warp's own mbarrier. A row is handled by TPR lanes; lane q holds the
-// PPT frequency pairs [q*PPT, q*PPT+PPT) of every head in registers, reads the
-// matching 2*PPT elements (both NEOX halves) of the row from shared memory,
-// and the TPR partial sums are combined with warp shuffles.
+// Work layout (persistent, one CTA per SM): the live rows of all segments are
+// cut into pieces of at most 8 KB of keys; the pieces, in segment order, are
+// split into equal contiguous runs, one per warp. Each warp streams its run
+// through a private two-stage ring in shared memory: lane 0 starts the bulk
+// async copy (TMA, non-tensor form, completion on an mbarrier) of piece i+1
+// before the warp computes piece i. A row is handled by TPR lanes; lane q owns
+// the PPT frequency pairs [q*PPT, q*PPT+PPT) of every head of the group, with
+// its slice of W and M in registers, and works on pairs of consecutive
+// frequencies with packed fp32x2 FMAs. The TPR partial sums are combined with a
+// transposed shuffle reduction (each step halves the heads a lane carries).
+//
+// Moments: each lane keeps shifted sums of the heads it ends up owning; a warp
+// merges them (Chan et al. pairwise update) into one partial per contiguous
+// run of a segment, stored at the run's first piece. The last warp to finish
+// a segment merges its runs in order (deterministic) into mean and
+// 1 / (std + 1e-6).
 #include "tria_internal.cuh"
 
 namespace tria {
 
+constexpr int kScoreWarps = 12;
+constexpr int kScoreThreads = kScoreWarps * 32;
+constexpr int kPieceBytes = 8192;
+constexpr int kMaxSegs = 1024;
+constexpr int kMomTable = kScoreWarps * 32 * 2 * (12 + 4);   // per-warp [lane][slot] moments + head
+constexpr int kScoreSmemMax = kScoreWarps * 2 * kPieceBytes + kScoreWarps * 2 * 8 + 2 * (kMaxSegs + 1) * 4 + kMomTable + 16;
+
+__device__ __forceinline__ float sqrt_approx(float x) {
+  float y;
+  asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Loads PPT consecutive elements of one NEOX half as PPT/2 float2 (consecutive pairs).
 template <int KT, int PPT>
 struct Loader;
 
 template <int PPT>
 struct Loader<TRIA_F16, PPT> {
-  static __device__ __forceinline__ void half(const uint8_t* row, int e0, float* x) {
-    const __half2* p = reinterpret_cast<const __half2*>(row + 2 * e0);
+  static __device__ __forceinline__ void half(const uint8_t* row, int e0, float2* x) {
     if constexpr (PPT == 8) {
-      uint4 u = *reinterpret_cast<const uint4*>(p);
+      const uint4 u = *reinterpret_cast<const uint4*>(row + 2 * e0);
       const __half2* h = reinterpret_cast<const __half2*>(&u);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float2 f = __half22float2(h[i]);
-        x[2 * i] = f.x;
-        x[2 * i + 1] = f.y;
-      }
+      for (int i = 0; i < 4; ++i) x[i] = __half22float2(h[i]);
     } else {
-      uint2 u = *reinterpret_cast<const uint2*>(p);
+      const uint2 u = *reinterpret_cast<const uint2*>(row + 2 * e0);
       const __half2* h = reinterpret_cast<const __half2*>(&u);
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        float2 f = __half22float2(h[i]);
-        x[2 * i] = f.x;
-        x[2 * i + 1] = f.y;
-      }
+      for (int i = 0; i < 2; ++i) x[i] = __half22float2(h[i]);
     }
   }
 };
 
 template <int PPT>
 struct Loader<TRIA_F32, PPT> {
-  static __device__ __forceinline__ void half(const uint8_t* row, int e0, float* x) {
+  static __device__ __forceinline__ void half(const uint8_t* row, int e0, float2* x) {
     const float4* p = reinterpret_cast<const float4*>(row + 4 * e0);
 #pragma unroll
     for (int i = 0; i < PPT / 4; ++i) {
-      float4 v = p[i];
-      x[4 * i] = v.x;
-      x[4 * i + 1] = v.y;
-      x[4 * i + 2] = v.z;
-      x[4 * i + 3] = v.w;
+      const float4 v = p[i];
+      x[2 * i] = make_float2(v.x, v.y);
+      x[2 * i + 1] = make_float2(v.z, v.w);
     }
   }
 };
 
 template <int PPT>
 struct Loader<TRIA_Q8_0, PPT> {
-  static __device__ __forceinline__ void half(const uint8_t* row, int e0, float* x) {
+  static __device__ __forceinline__ void half(const uint8_t* row, int e0, float2* x) {
     if constexpr (PPT == 8) {
-      uint2 u = *reinterpret_cast<const uint2*>(row + e0);
+      const uint2 u = *reinterpret_cast<const uint2*>(row + e0);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) x[i] = (float)(int)(int8_t)(u.x >> (8 * i));
-#pragma unroll
-      for (int i = 0; i < 4; ++i) x[4 + i] = (float)(int)(int8_t)(u.y >> (8 * i));
+      for (int i = 0; i < 2; ++i) {
+        x[i] = make_float2((float)(int8_t)(u.x >> (16 * i)), (float)(int8_t)(u.x >> (16 * i + 8)));
+        x[2 + i] = make_float2((float)(int8_t)(u.y >> (16 * i)), (float)(int8_t)(u.y >> (16 * i + 8)));
+      }
     } else {
-      uint32_t u = *reinterpret_cast<const uint32_t*>(row + e0);
+      const uint32_t u = *reinterpret_cast<const uint32_t*>(row + e0);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) x[i] = (float)(int)(int8_t)(u >> (8 * i));
+      for (int i = 0; i < 2; ++i)
+        x[i] = make_float2((float)(int8_t)(u >> (16 * i)), (float)(int8_t)(u >> (16 * i + 8)));
     }
   }
 };
 
-struct ScoreSmem {
-  // byte offsets inside dynamic shared memory
-  int data, w, m, raw, bar, total;
+// Transposed reduction of NV partial sums over the TPR lanes of a row group:
+// each step with more than one value left sends half of them to the partner
+// lane and keeps the other half; once a lane carries one value the rest is a
+// butterfly. Afterwards the lane holds the full sums of the flattened values
+// [base, base + kOut) in v[0 .. kOut); `writer` is false on butterfly duplicates.
+template <int NV, int TPR>
+struct HeadReduce {
+  static constexpr int kOut = NV >= TPR ? NV / TPR : 1;
+  static __device__ __forceinline__ int run(float (&v)[NV], int q, bool& writer) {
+    int base = 0;
+    writer = true;
+    int m = NV;
+#pragma unroll
+    for (int span = TPR / 2; span >= 1; span >>= 1) {
+      if (m > 1) {
+        const int half = m / 2;
+        const bool upper = (q & span) != 0;
+#pragma unroll
+        for (int i = 0; i < (NV > 1 ? NV / 2 : 1); ++i) {
+          if (i < half) {
+            const float send = upper ? v[i] : v[i + half];
+            const float keep = upper ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, span);
+          }
+        }
+        if (upper) base += half;
+        m = half;
+      } else {
+        v[0] += __shfl_xor_sync(0xffffffffu, v[0], span);
+        if (q & span) writer = false;
+      }
+    }
+    return base;
+  }
 };
 
-__host__ __device__ inline ScoreSmem score_smem_layout(int cs_rows, int k_rb, int G, int fc) {
-  ScoreSmem L;
-  int off = 0;
-  L.data = off;
-  off += cs_rows * k_rb;
-  off = (off + 15) & ~15;
-  L.w = off;
-  off += G * fc * 8;
-  L.m = off;
-  off += G * fc * 4;
-  off = (off + 15) & ~15;
-  L.raw = off;
-  off += cs_rows * G * 4;
-  off = (off + 15) & ~15;
-  L.bar = off;
-  off += 8 * 8;
-  L.total = off;
-  return L;
+// Compile-time shape of the row batch a lane accumulates before one reduction.
+template <int KT, int G, int TPR, int PPT>
+struct Batch {
+  static constexpr int kElem = KT == TRIA_F32 ? 4 : (KT == TRIA_F16 ? 2 : 1);
+  static constexpr int kRowsPerStep = 32 / TPR;
+  static constexpr int kRbMax = kElem * 2 * TPR * PPT;   // key bytes of the widest row
+  static constexpr int kPieceRows = (kPieceBytes / kRbMax) > 64 ? 64 : (kPieceBytes / kRbMax);
+  static constexpr int kSteps = (kPieceRows / kRowsPerStep) > 0 ? (kPieceRows / kRowsPerStep) : 1;
+  static constexpr int kTarget = TPR / G > 0 ? TPR / G : 1;   // NV = TPR: no butterfly duplicates
+  static constexpr int kRowsB = kTarget < kSteps ? kTarget : kSteps;   // rows per lane per batch
+  static constexpr int kNV = kRowsB * G;
+};
+
+// running (count, mean, M2) of one head
+struct Mom {
+  float n, mean, m2;
+};
+
+__device__ __forceinline__ Mom mom_merge(Mom a, Mom b) {
+  const float n = a.n + b.n;
+  if (n == 0.f) return a;
+  const float d = b.mean - a.mean;
+  const float fb = b.n / n;
+  Mom r;
+  r.n = n;
+  r.mean = a.mean + d * fb;
+  r.m2 = a.m2 + b.m2 + d * d * a.n * fb;
+  return r;
+}
+
+__device__ __forceinline__ Mom mom_shfl(Mom a, int mask) {
+  Mom b;
+  b.n = __shfl_xor_sync(0xffffffffu, a.n, mask);
+  b.mean = __shfl_xor_sync(0xffffffffu, a.mean, mask);
+  b.m2 = __shfl_xor_sync(0xffffffffu, a.m2, mask);
+  return b;
+}
+
+struct ScoreGeom {
+  int R;       // rows per piece
+  int stage;   // bytes per ring stage
+};
+
+__host__ __device__ inline ScoreGeom score_geom(int k_rb) {
+  ScoreGeom g;
+  g.R = kPieceBytes / k_rb;
+  if (g.R > 64) g.R = 64;
+  if (g.R < 1) g.R = 1;
+  g.stage = (g.R * k_rb + 15) & ~15;
+  return g;
+}
+
+__host__ __device__ inline int score_smem_bytes_for(int k_rb) {
+  const ScoreGeom g = score_geom(k_rb);
+  return kScoreWarps * 2 * g.stage + kScoreWarps * 2 * 8 + 2 * (kMaxSegs + 1) * 4 + kMomTable + 16;
 }
 
 template <int KT, int G, int TPR, int PPT>
-__global__ void __launch_bounds__(kThreads, 2) k_score(const __grid_constant__ Pass P) {
-  const int seg = blockIdx.y;
-  const SegView sv = seg_view(P, seg);
-  if (!sv.valid) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) report(P.ctrl, TRIA_ERR_DEVICE_ARG, (uint32_t)sv.s);
-    return;
-  }
-  if (P.only_active && !sv.active) return;
-  const int n = sv.n;
-  const int c0 = blockIdx.x * P.cs_rows;
-  if (c0 >= n) return;
-  const int rows = min(P.cs_rows, n - c0);
-  const int nchunks = (n + P.cs_rows - 1) / P.cs_rows;
-  const int fc = P.fc;
-  const int k_rb = P.k_rb;
+__global__ void __launch_bounds__(kScoreThreads, 1) k_score(const __grid_constant__ Pass P) {
+  static_assert(PPT % 2 == 0, "pairs of frequencies");
+  static_assert(HeadReduce<Batch<KT, G, TPR, PPT>::kNV, TPR>::kOut <= 2, "moment table holds 2 slots");
+  using BT = Batch<KT, G, TPR, PPT>;
+  constexpr int kRowsPerStep = BT::kRowsPerStep;
+  constexpr int kRowsB = BT::kRowsB;
+  constexpr int kNV = BT::kNV;
+  using Red = HeadReduce<kNV, TPR>;
+  constexpr int kOut = Red::kOut;
 
   extern __shared__ __align__(128) uint8_t smem[];
-  const ScoreSmem L = score_smem_layout(P.cs_rows, k_rb, G, fc);
-  uint8_t* sdata = smem + L.data;
-  float2* sW = reinterpret_cast<float2*>(smem + L.w);
-  float* sM = reinterpret_cast<float*>(smem + L.m);
-  float* sraw = reinterpret_cast<float*>(smem + L.raw);
-  uint64_t* sbar = reinterpret_cast<uint64_t*>(smem + L.bar);
-  __shared__ int s_last;
-
+  const ScoreGeom geo = score_geom(P.k_rb);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int piece_rows = P.cs_rows >> 3;
-  const int pr0 = warp * piece_rows;
-  const int prows = max(0, min(piece_rows, rows - pr0));
+  uint8_t* ring = smem + (size_t)warp * 2 * geo.stage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kScoreWarps * 2 * geo.stage) + warp * 2;
+  int* seg_first = reinterpret_cast<int*>(smem + (size_t)kScoreWarps * 2 * geo.stage + kScoreWarps * 2 * 8);
+  int* seg_rows = seg_first + (kMaxSegs + 1);   // live rows of each scored segment
 
-  // 1. each warp starts the bulk copy of its piece
+  // pieces of every segment, in segment order (skipped segments have none):
+  // thread t counts segments [t*per_t, t*per_t + per_t), then a block scan
+  {
+    __shared__ int sbuf[40];
+    const int per_t = (P.n_seg + kScoreThreads - 1) / kScoreThreads;
+    const int sb = min(P.n_seg, (int)threadIdx.x * per_t), se = min(P.n_seg, sb + per_t);
+    int cnt[(kMaxSegs + kScoreThreads - 1) / kScoreThreads];
+    int local = 0;
+#pragma unroll
+    for (int i = 0; i < (kMaxSegs + kScoreThreads - 1) / kScoreThreads; ++i) {
+      cnt[i] = 0;
+      const int s = sb + i;
+      if (s < se) {
+        const SegView v = seg_view(P, s);
+        if (!v.valid) {
+          if (blockIdx.x == 0 && v.g == 0) report(P.ctrl, TRIA_ERR_DEVICE_ARG, (uint32_t)v.s);
+        } else if (!P.only_active || v.active) {
+          cnt[i] = (v.n + geo.R - 1) / geo.R;
+        }
+        seg_rows[s] = cnt[i] ? v.n : 0;
+        local += cnt[i];
+      }
+    }
+    int tot;
+    int before = block_exclusive_scan(local, &tot, sbuf);
+#pragma unroll
+    for (int i = 0; i < (kMaxSegs + kScoreThreads - 1) / kScoreThreads; ++i) {
+      const int s = sb + i;
+      if (s < se) {
+        seg_first[s] = before;
+        before += cnt[i];
+      }
+    }
+    if (threadIdx.x == 0) seg_first[P.n_seg] = tot;
+  }
+  __syncthreads();
+  // the consumer of the moment partials needs the piece layout
+  if (blockIdx.x == 0) {
+    const int nw = gridDim.x * kScoreWarps;
+    for (int s = threadIdx.x; s < P.n_seg; s += blockDim.x) {
+      P.seg[s].piece_first = seg_first[s];
+      P.seg[s].piece_end = seg_first[s + 1];
+      P.seg[s].piece_per = (seg_first[P.n_seg] + nw - 1) / nw;
+    }
+  }
   if (lane == 0) {
-    mbar_init(&sbar[warp], 1);
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
     fence_mbar_init();
-  }
-  __syncwarp();
-  if (lane == 0 && prows > 0) {
-    const uint32_t bytes = (uint32_t)(prows * k_rb);
-    mbar_arrive_expect_tx(&sbar[warp], bytes);
-    bulk_g2s(sdata + (size_t)pr0 * k_rb, P.k + (size_t)(sv.row0 + c0 + pr0) * k_rb, bytes, &sbar[warp]);
-  }
-
-  // 2. folded weights of this segment at the current position:
-  //    W = qe * e^{i w_f p}, phase from the exact fixed-point turn count
-  const unsigned long long p = (unsigned long long)P.seq[sv.s].cur_pos;
-  const float2* qe = P.qe + (size_t)sv.g * G * fc;
-  const float* mw = P.mw + (size_t)sv.g * G * fc;
-  for (int i = threadIdx.x; i < G * fc; i += blockDim.x) {
-    const int f = i % fc;
-    const unsigned long long x = P.turns[f] * p;
-    const float half_turns = (float)(int)(x >> 32) * 0x1p-31f;   // [-1, 1) half turns
-    float sn, cs;
-    sincospif(half_turns, &sn, &cs);
-    const float2 q = qe[i];
-    sW[i] = make_float2(q.x * cs - q.y * sn, q.x * sn + q.y * cs);
-    sM[i] = mw[i];
   }
   __syncthreads();
 
-  // 3. this lane's pairs of every head into registers
+  const int total = seg_first[P.n_seg];
+  const int nwarps = gridDim.x * kScoreWarps;
+  const int per = (total + nwarps - 1) / nwarps;
+  const int gw = blockIdx.x * kScoreWarps + warp;
+  const int p_beg = min(total, gw * per), p_end = min(total, p_beg + per);
+  if (p_beg >= p_end) return;
+
+  auto seg_of = [&](int p, int from) {
+    int s = from;
+    while (seg_first[s + 1] <= p) ++s;
+    return s;
+  };
+  // lane 0: start the bulk copy of piece p (segment sg) into ring stage `stage_i`
+  auto seg_row0 = [&](int sg) {
+    const int sq = sg / P.n_kv;
+    return P.seq[sq].row0 + (int64_t)(sg - sq * P.n_kv) * P.seq[sq].cap;
+  };
+  auto issue = [&](int p, int sg, int stage_i) {
+    const int r = (p - seg_first[sg]) * geo.R;
+    const int rows = min(geo.R, seg_rows[sg] - r);
+    const uint32_t bytes = (uint32_t)(rows * P.k_rb);
+    mbar_arrive_expect_tx(&bars[stage_i], bytes);
+    bulk_g2s(ring + stage_i * geo.stage, P.k + (size_t)(seg_row0(sg) + r) * P.k_rb, bytes, &bars[stage_i]);
+  };
+
   const int q = lane % TPR;
   const int f0 = q * PPT;
+  const int fc = P.fc;
   const bool lane_on = f0 < fc;
-  float wr[G][PPT], wi[G][PPT], wm[G][PPT];
-#pragma unroll
-  for (int h = 0; h < G; ++h)
+
+  // this lane's slice of W (real / imaginary) and M for the current segment,
+  // on pairs of consecutive frequencies
+  float2 wr[G][PPT / 2], wi[G][PPT / 2], wm[G][PPT / 2];
+  auto load_consts = [&](const SegView& v) {
+    const unsigned long long p = (unsigned long long)P.seq[v.s].cur_pos;
+    float cs[PPT], sn[PPT];
 #pragma unroll
     for (int j = 0; j < PPT; ++j) {
-      const int idx = h * fc + f0 + j;
-      const bool on = lane_on;
-      const float2 w2 = on ? sW[idx] : make_float2(0.f, 0.f);
-      wr[h][j] = w2.x;
-      wi[h][j] = w2.y;
-      wm[h][j] = on ? sM[idx] : 0.f;
+      if (lane_on) {
+        const unsigned long long x = P.turns[f0 + j] * p;   // exact turn fraction of w_f * p
+        sincospif((float)(int)(x >> 32) * 0x1p-31f, &sn[j], &cs[j]);
+      } else {
+        sn[j] = 0.f;
+        cs[j] = 0.f;
+      }
     }
+    const float2* qe = P.qe + (size_t)v.g * G * fc;
+    const float* mw = P.mw + (size_t)v.g * G * fc;
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int j = 0; j < PPT; j += 2) {
+        float2 a = make_float2(0.f, 0.f), b = make_float2(0.f, 0.f), m = make_float2(0.f, 0.f);
+        if (lane_on) {
+          a = qe[h * fc + f0 + j];
+          b = qe[h * fc + f0 + j + 1];
+          m = make_float2(mw[h * fc + f0 + j], mw[h * fc + f0 + j + 1]);
+        }
+        wr[h][j / 2] = make_float2(a.x * cs[j] - a.y * sn[j], b.x * cs[j + 1] - b.y * sn[j + 1]);
+        wi[h][j / 2] = make_float2(a.x * sn[j] + a.y * cs[j], b.x * sn[j + 1] + b.y * cs[j + 1]);
+        wm[h][j / 2] = m;
+      }
+  };
 
-  // 4. rows of my piece
-  if (prows > 0) {
-    if (!mbar_wait_bounded(&sbar[warp], 0, P.spin_limit)) {
+  int seg = seg_of(p_beg, 0);
+  if (lane == 0) issue(p_beg, seg, 0);
+  SegView sv = seg_view(P, seg);
+  load_consts(sv);
+
+  // flattened (row, head) values this lane owns after the reduction: constant
+  // per lane, so slot o always carries head (vbase + o) % G
+  bool writer = true;
+  int vbase = 0;
+  {
+    float dummy[kNV];
+#pragma unroll
+    for (int i = 0; i < kNV; ++i) dummy[i] = 0.f;
+    vbase = Red::run(dummy, q, writer);
+  }
+  Mom* mtab = reinterpret_cast<Mom*>(seg_rows + (kMaxSegs + 1)) + warp * 32 * 2;
+  int* mhead = reinterpret_cast<int*>(reinterpret_cast<Mom*>(seg_rows + (kMaxSegs + 1)) + kScoreWarps * 32 * 2) +
+               warp * 32 * 2;
+
+  Mom run_m[kOut];
+#pragma unroll
+  for (int o = 0; o < kOut; ++o) run_m[o] = Mom{0.f, 0.f, 0.f};
+  int run_first = p_beg;   // global index of the run's first piece
+
+  auto flush_run = [&]() {
+    // every lane lists its slots (head, moments); lane h < G merges the
+    // entries of head h in lane-major order
+#pragma unroll
+    for (int o = 0; o < kOut; ++o) {
+      mtab[lane * kOut + o] = writer ? run_m[o] : Mom{0.f, 0.f, 0.f};
+      mhead[lane * kOut + o] = (vbase + o) % G;
+    }
+    __syncwarp();
+    if (lane < G) {
+      Mom a{0.f, 0.f, 0.f};
+      for (int e = 0; e < 32 * kOut; ++e)
+        if (mhead[e] == lane) a = mom_merge(a, mtab[e]);
+      ScoreChunk* part = P.schunk + run_first;
+      part->mean[lane] = a.mean;
+      part->m2[lane] = a.m2;
+      if (lane == 0) part->n = (int)a.n;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int o = 0; o < kOut; ++o) run_m[o] = Mom{0.f, 0.f, 0.f};
+  };
+
+  for (int p = p_beg; p < p_end; ++p) {
+    const int k = p - p_beg;
+    const int st = k & 1;
+    // next piece into the other stage (its previous contents were consumed)
+    if (p + 1 < p_end && lane == 0) issue(p + 1, seg_of(p + 1, seg), st ^ 1);
+    if (seg_first[seg + 1] <= p) {
+      flush_run();
+      seg = seg_of(p, seg);
+      sv = seg_view(P, seg);
+      load_consts(sv);
+      run_first = p;
+    }
+    const int r0 = (p - seg_first[seg]) * geo.R;
+    const int rows = min(geo.R, seg_rows[seg] - r0);
+    const int64_t grow = seg_row0(seg) + r0;
+    if (!mbar_wait_bounded(&bars[st], (uint32_t)((k >> 1) & 1), P.spin_limit)) {
       if (lane == 0) report(P.ctrl, TRIA_ERR_TIMEOUT, (uint32_t)seg);
-    } else {
-      constexpr int kRowsPerStep = 32 / TPR;
-      const int steps = (prows + kRowsPerStep - 1) / kRowsPerStep;
-      for (int stp = 0; stp < steps; ++stp) {
-        const int rr = stp * kRowsPerStep + lane / TPR;
-        const bool row_on = rr < prows;
-        float kr[PPT], ki[PPT];
-        if (row_on && lane_on) {
-          const uint8_t* row = sdata + (size_t)(pr0 + rr) * k_rb;
+      return;
+    }
+    const uint8_t* buf = ring + st * geo.stage;
+    // lane-local shifted sums of this piece for my value slots
+    float shift[kOut], s1[kOut], s2[kOut], cnt[kOut];
+#pragma unroll
+    for (int o = 0; o < kOut; ++o) shift[o] = s1[o] = s2[o] = cnt[o] = 0.f;
+    const int steps = (rows + kRowsPerStep - 1) / kRowsPerStep;
+    const int gi = lane / TPR;   // row group of this lane
+    for (int b0 = 0; b0 < steps; b0 += kRowsB) {
+      float v[kNV];
+#pragma unroll
+      for (int rb = 0; rb < kRowsB; ++rb) {
+        const int rr = (b0 + rb) * kRowsPerStep + gi;
+        float2 kr[PPT / 2], ki[PPT / 2];
+        if (rr < rows && lane_on) {
+          const uint8_t* row = buf + (size_t)rr * P.k_rb;
           Loader<KT, PPT>::half(row, f0, kr);
           Loader<KT, PPT>::half(row, fc + f0, ki);
           if constexpr (KT == TRIA_Q8_0) {
-            const __half* sc = reinterpret_cast<const __half*>(P.ks + (size_t)(sv.row0 + c0 + pr0 + rr) * P.ks_rb);
+            const __half* sc = reinterpret_cast<const __half*>(P.ks + (size_t)(grow + rr) * P.ks_rb);
             const float d1 = __half2float(sc[f0 >> 5]);
             const float d2 = __half2float(sc[(fc + f0) >> 5]);
 #pragma unroll
-            for (int j = 0; j < PPT; ++j) {
-              kr[j] *= d1;
-              ki[j] *= d2;
+            for (int j = 0; j < PPT / 2; ++j) {
+              kr[j] = __fmul2_rn(kr[j], make_float2(d1, d1));
+              ki[j] = __fmul2_rn(ki[j], make_float2(d2, d2));
             }
           }
         } else {
 #pragma unroll
-          for (int j = 0; j < PPT; ++j) kr[j] = ki[j] = 0.f;
+          for (int j = 0; j < PPT / 2; ++j) kr[j] = ki[j] = make_float2(0.f, 0.f);
         }
-        float acc[G];
+        float2 mag[PPT / 2];
 #pragma unroll
-        for (int h = 0; h < G; ++h) acc[h] = 0.f;
+        for (int j = 0; j < PPT / 2; ++j) {
+          const float2 sq = __ffma2_rn(ki[j], ki[j], __fmul2_rn(kr[j], kr[j]));
+          mag[j] = make_float2(sqrt_approx(sq.x), sqrt_approx(sq.y));
+        }
 #pragma unroll
-        for (int j = 0; j < PPT; ++j) {
-          const float mag = sqrtf(fmaf(kr[j], kr[j], ki[j] * ki[j]));
+        for (int h = 0; h < G; ++h) {
+          // two independent accumulation chains per head
+          float2 a0 = __fmul2_rn(wr[h][0], kr[0]);
+          float2 a1 = __fmul2_rn(wi[h][0], ki[0]);
+          a0 = __ffma2_rn(wm[h][0], mag[0], a0);
 #pragma unroll
-          for (int h = 0; h < G; ++h) {
-            acc[h] = fmaf(wr[h][j], kr[j], acc[h]);
-            acc[h] = fmaf(wi[h][j], ki[j], acc[h]);
-            acc[h] = fmaf(wm[h][j], mag, acc[h]);
+          for (int j = 1; j < PPT / 2; ++j) {
+            a0 = __ffma2_rn(wr[h][j], kr[j], a0);
+            a1 = __ffma2_rn(wi[h][j], ki[j], a1);
+            if (j & 1)
+              a1 = __ffma2_rn(wm[h][j], mag[j], a1);
+            else
+              a0 = __ffma2_rn(wm[h][j], mag[j], a0);
+          }
+          v[rb * G + h] = (a0.x + a1.x) + (a0.y + a1.y);
+        }
+      }
+      bool wr_lane;
+      Red::run(v, q, wr_lane);
+      if (wr_lane) {
+#pragma unroll
+        for (int o = 0; o < kOut; ++o) {
+          const int idx = vbase + o;
+          const int rr = (b0 + idx / G) * kRowsPerStep + gi;
+          if (rr < rows) {
+            P.raw[(size_t)(grow + rr) * G + (idx % G)] = v[o];
+            if (cnt[o] == 0.f) shift[o] = v[o];
+            const float d = v[o] - shift[o];
+            s1[o] += d;
+            s2[o] = fmaf(d, d, s2[o]);
+            cnt[o] += 1.f;
           }
         }
-#pragma unroll
-        for (int o = TPR / 2; o > 0; o >>= 1)
-#pragma unroll
-          for (int h = 0; h < G; ++h) acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], o);
-        // every lane holds all G sums; lane q writes the heads h with h % TPR == q
-        if (row_on) {
-#pragma unroll
-          for (int h = 0; h < G; ++h)
-            if ((h % TPR) == q) sraw[(pr0 + rr) * G + h] = acc[h];
-        }
       }
     }
-  }
-  __syncthreads();
-
-  // 5. raw scores out (coalesced) and the chunk's moments (two passes in fp32)
-  float* graw = P.raw + (size_t)(sv.row0 + c0) * G;
-  for (int i = threadIdx.x; i < rows * G; i += blockDim.x) graw[i] = sraw[i];
-  if (warp < G) {
-    float sum = 0.f;
-    for (int r = lane; r < rows; r += 32) sum += sraw[r * G + warp];
+    // this piece's moments (lane-local) -> the run's moments
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    const float mean = sum / (float)rows;
-    float m2 = 0.f;
-    for (int r = lane; r < rows; r += 32) {
-      const float dlt = sraw[r * G + warp] - mean;
-      m2 = fmaf(dlt, dlt, m2);
+    for (int o = 0; o < kOut; ++o) {
+      Mom b;
+      b.n = cnt[o];
+      const float mean_d = cnt[o] > 0.f ? s1[o] / cnt[o] : 0.f;
+      b.mean = shift[o] + mean_d;
+      b.m2 = fmaxf(s2[o] - s1[o] * mean_d, 0.f);
+      run_m[o] = mom_merge(run_m[o], b);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m2 += __shfl_xor_sync(0xffffffffu, m2, o);
-    if (lane == 0) {
-      ScoreChunk* sc = P.schunk + (size_t)seg * P.cs_max + blockIdx.x;
-      sc->mean[warp] = mean;
-      sc->m2[warp] = m2;
-      if (warp == 0) sc->n = rows;
-    }
+    __syncwarp();
   }
-
-  // 6. the last chunk of the segment merges the moments (Chan et al. pairwise
-  //    update, fp64, fixed order) into mean and 1 / (std + 1e-6)
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_last = (atomicAdd(&P.seg[seg].cnt, 1) == nchunks - 1);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  if (warp < G) {
-    double cn = 0.0, cmean = 0.0, cm2 = 0.0;
-    for (int ci = lane; ci < nchunks; ci += 32) {
-      const ScoreChunk* sc = P.schunk + (size_t)seg * P.cs_max + ci;
-      const double bn = (double)__ldcg(&sc->n);
-      const double bmean = (double)__ldcg(&sc->mean[warp]);
-      const double bm2 = (double)__ldcg(&sc->m2[warp]);
-      const double tn = cn + bn;
-      const double dlt = bmean - cmean;
-      cmean += dlt * bn / tn;
-      cm2 += bm2 + dlt * dlt * cn * bn / tn;
-      cn = tn;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const double bn = __shfl_xor_sync(0xffffffffu, cn, o);
-      const double bmean = __shfl_xor_sync(0xffffffffu, cmean, o);
-      const double bm2 = __shfl_xor_sync(0xffffffffu, cm2, o);
-      const double tn = cn + bn;
-      if (tn > 0.0) {
-        const double dlt = bmean - cmean;
-        const double nmean = cmean + dlt * bn / tn;
-        const double nm2 = cm2 + bm2 + dlt * dlt * cn * bn / tn;
-        cmean = nmean;
-        cm2 = nm2;
-      }
-      cn = tn;
-    }
-    if (lane == 0) {
-      const double sd = sqrt(cm2 / cn);
-      P.seg[seg].mu[warp] = (float)cmean;
-      P.seg[seg].inv[warp] = (float)(1.0 / (sd + (double)kZEps));
-    }
-  }
-  if (threadIdx.x == 0) P.seg[seg].cnt = 0;
+  flush_run();
 }
 
-// z-max score per live row: s = max_h (raw_h - mu_h) * inv_h
+// Merge of a segment's run partials (written by k_score) into mean and
+// 1 / (std + 1e-6), by one CTA: thread t merges runs t, t + blockDim, ...
+// (Chan et al. pairwise update, fp32), then a fixed shuffle / shared-memory
+// tree. Runs start at the segment's first piece and at each multiple of the
+// per-warp piece count after it. Deterministic for a given layout.
+template <int G>
+__device__ void merge_segment_moments(const Pass& P, int seg, float* mu, float* inv) {
+  __shared__ Mom red[kThreads / 32][G];
+  const int s0 = __ldcg(&P.seg[seg].piece_first), s1 = __ldcg(&P.seg[seg].piece_end);
+  const int per = max(1, __ldcg(&P.seg[seg].piece_per));
+  const int first_mult = (s0 / per + 1) * per;
+  const int nruns = s1 > s0 ? 1 + (s1 > first_mult ? (s1 - first_mult + per - 1) / per : 0) : 0;
+  Mom acc[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) acc[h] = Mom{0.f, 0.f, 0.f};
+  for (int i = threadIdx.x; i < nruns; i += blockDim.x) {
+    const int j = i == 0 ? s0 : first_mult + (i - 1) * per;
+    const ScoreChunk* pp = P.schunk + j;
+    const float n = (float)__ldcg(&pp->n);
+#pragma unroll
+    for (int h = 0; h < G; ++h) acc[h] = mom_merge(acc[h], Mom{n, __ldcg(&pp->mean[h]), __ldcg(&pp->m2[h])});
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+#pragma unroll
+    for (int mask = 1; mask < 32; mask <<= 1) acc[h] = mom_merge(acc[h], mom_shfl(acc[h], mask));
+    if (lane == 0) red[warp][h] = acc[h];
+  }
+  __syncthreads();
+  if (threadIdx.x < G) {
+    Mom a = red[0][threadIdx.x];
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) a = mom_merge(a, red[w][threadIdx.x]);
+    red[0][threadIdx.x] = a;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const Mom a = red[0][h];
+    mu[h] = a.mean;
+    inv[h] = 1.0f / (sqrtf(a.m2 / fmaxf(a.n, 1.f)) + kZEps);
+  }
+}
+
+// z-max score per live row: s = max_h (raw_h - mu_h) * inv_h. The CTA with
+// blockIdx.x == 0 of each segment also records mean / inv in the segment state.
 template <int G>
 __global__ void __launch_bounds__(kThreads) k_zscore(const __grid_constant__ Pass P) {
   const int seg = blockIdx.y;
   const SegView sv = seg_view(P, seg);
   if (!sv.valid || (P.only_active && !sv.active)) return;
+  if ((int)blockIdx.x * 1024 >= sv.n) return;
   float mu[G], inv[G];
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    mu[h] = P.seg[seg].mu[h];
-    inv[h] = P.seg[seg].inv[h];
+  merge_segment_moments<G>(P, seg, mu, inv);
+  if (blockIdx.x == 0 && threadIdx.x < G) {
+    P.seg[seg].mu[threadIdx.x] = mu[threadIdx.x];
+    P.seg[seg].inv[threadIdx.x] = inv[threadIdx.x];
   }
   const int r_end = min(sv.n, (int)(blockIdx.x + 1) * 1024);
   for (int r = blockIdx.x * 1024 + threadIdx.x; r < r_end; r += blockDim.x) {
@@ -332,24 +546,32 @@ __global__ void __launch_bounds__(kThreads) k_zscore(const __grid_constant__ Pas
   }
 }
 
-size_t score_smem_bytes(const Pass& P) {
-  return (size_t)score_smem_layout(P.cs_rows, P.k_rb, P.G, P.fc).total;
+size_t score_smem_bytes(const Pass& P) { return (size_t)score_smem_bytes_for(P.k_rb); }
+
+int score_pieces_max(int k_rb, int cap) {
+  const ScoreGeom g = score_geom(k_rb);
+  return (cap + g.R - 1) / g.R;
 }
 
 namespace {
+
+int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
 
 template <int KT, int G, int TPR, int PPT>
 cudaError_t launch_score_t(const Pass& P, cudaStream_t st) {
   const size_t smem = score_smem_bytes(P);
   auto kern = k_score<KT, G, TPR, PPT>;
-  // the largest dynamic shared memory any layout of this instantiation needs;
-  // set once per process (the attribute is per function, not per call)
+  // the attribute is per function: set the largest size any layout needs, once
   static const cudaError_t attr =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmemMax);
   if (attr != cudaSuccess) return attr;
-  if (smem > 200 * 1024) return cudaErrorInvalidValue;
-  dim3 grid(P.cs_max, P.n_seg);
-  kern<<<grid, kThreads, smem, st>>>(P);
+  static const int sms = sm_count();
+  kern<<<sms, kScoreThreads, smem, st>>>(P);
   return cudaGetLastError();
 }
 
@@ -390,6 +612,7 @@ cudaError_t launch_score_k(const Pass& P, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_score(const Pass& P, cudaStream_t st) {
+  if (P.n_seg > kMaxSegs) return cudaErrorInvalidValue;
   switch (P.k_type) {
     case TRIA_F32: return launch_score_k<TRIA_F32>(P, st);
     case TRIA_F16: return launch_score_k<TRIA_F16>(P, st);

@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kThreads) k_hist(const __grid_constant__ Pass 
   if (threadIdx.x == 0) P.seg[seg].cnt = 0;
 }
 
-// Per 64-row chunk: candidates above T, ties at T, protected rows. The last CTA
+// Per chunk: candidates above T, ties at T, protected rows. The last CTA
 // of the segment places the tie cut and writes the kept-row prefix per chunk.
 __global__ void __launch_bounds__(kThreads) k_count(const __grid_constant__ Pass P) {
   const int seg = blockIdx.y;
@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kThreads) k_count(const __grid_constant__ Pass
     if (c >= nch) break;
     int gt = 0, tie = 0, prot = 0;
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
+    for (int half = 0; half < kChunk / 32; ++half) {
       const int r = c * kChunk + half * 32 + lane;
       const bool in = r < n;
       const bool pr = in && is_protected(r, n, P.sink, P.window);
@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(kThreads) k_count(const __grid_constant__ Pass
   // 2. the row of that tie
   if (cstar >= 0 && warp == 0) {
     int seen = 0;
-    for (int half = 0; half < 2; ++half) {
+    for (int half = 0; half < kChunk / 32; ++half) {
       const int r = cstar * kChunk + half * 32 + lane;
       const bool in = r < n;
       const bool cand = in && !is_protected(r, n, P.sink, P.window);
@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(kThreads) k_keeplist(const __grid_constant__ P
     if (c >= nch) break;
     int base = __ldcg(&pre[c]);
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
+    for (int half = 0; half < kChunk / 32; ++half) {
       const int r = c * kChunk + half * 32 + lane;
       const bool in = r < n;
       const bool pr = in && is_protected(r, n, P.sink, P.window);

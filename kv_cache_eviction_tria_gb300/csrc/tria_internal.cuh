@@ -9,19 +9,20 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/tria.h"
+#include "tria.h"
 
 namespace tria {
 
 constexpr int kMaxSeqs = TRIA_MAX_SEQS;
 constexpr int kMaxG = TRIA_MAX_GROUP;
-constexpr int kChunk = 64;            // rows per select / compaction chunk
+constexpr int kChunk = 32;            // rows per select / compaction chunk (one warp lane per row)
 constexpr int kHistRowsPerCta = 2048; // rows per CTA in the radix-histogram passes
-constexpr int kCountChunksPerCta = 16;// 64-row chunks per CTA in the count / keep-list passes
+constexpr int kCountChunksPerCta = 16;// chunks per CTA in the count / keep-list passes (2 per warp)
 constexpr int kHistBins = 2048;       // 11-bit digits (last pass: 10 bits)
 constexpr float kZEps = 1e-6f;        // z = (raw - mean) / (std + 1e-6)
 constexpr int kThreads = 256;
 constexpr int kDefaultSpinLimit = 1 << 22;
+constexpr int kMaxSegments = 1024;    // sequences x KV heads per call
 
 // ---------------------------------------------------------------------------
 // workspace
@@ -49,18 +50,21 @@ struct SegState {
   uint32_t T;            // key of the last kept candidate (after three passes)
   int32_t tie_row;       // last kept row among those with key == T (-1: none)
   int32_t cnt;           // last-arriver counter of the current kernel
-  int32_t pad[11];
+  int32_t piece_first;   // score pieces of the segment: [piece_first, piece_end)
+  int32_t piece_end;
+  int32_t piece_per;     // score pieces per warp (runs start at its multiples)
+  int32_t pad[8];
 };
 static_assert(sizeof(SegState) == 128, "SegState layout");
 
-struct ScoreChunk {      // moments of one score chunk (two-pass within the chunk)
+struct ScoreChunk {      // moments of one contiguous run of score pieces
   float mean[kMaxG];
   float m2[kMaxG];
   int32_t n;
   int32_t pad[3];
 };
 
-struct SelChunk {        // counts of one 64-row chunk
+struct SelChunk {        // counts of one chunk
   int32_t n_gt;          // candidates with key > T
   int32_t n_tie;         // candidates with key == T
   int32_t n_prot;        // protected rows (sink / window)
@@ -102,14 +106,14 @@ struct Pass {
   // workspace
   Ctrl* ctrl;
   SegState* seg;
-  ScoreChunk* schunk;                  // [n_seg][cs_max]
+  ScoreChunk* schunk;                  // [n_seg * cs_max] indexed by global score piece
   SelChunk* chunk;                     // [n_seg][c_max]
   int32_t* prefix;                     // [n_seg][c_max + 1] kept rows before each chunk
   uint32_t* hist;                      // [n_seg][kHistBins]
   uint32_t* flags;                     // [n_seg][c_max] compaction read-done flags
-  int32_t cs_rows;                     // rows per score chunk
-  int32_t cs_max;                      // score chunks per segment (max)
-  int32_t c_max;                       // 64-row chunks per segment (max)
+  int32_t cs_rows;                     // unused (layout compatibility)
+  int32_t cs_max;                      // score pieces per segment (max)
+  int32_t c_max;                       // chunks per segment (max)
   int32_t pad0;
   SeqInfo seq[kMaxSeqs];
 };
@@ -263,6 +267,7 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int* total, int* sbuf
 cudaError_t launch_score(const Pass& P, cudaStream_t st);
 cudaError_t launch_zscore(const Pass& P, cudaStream_t st);
 size_t score_smem_bytes(const Pass& P);
+int score_pieces_max(int k_rb, int cap);   // score pieces of a segment of `cap` rows
 // select.cu
 cudaError_t launch_select(const Pass& P, bool write_keep, cudaStream_t st);
 // compact.cu
