@@ -173,6 +173,28 @@ tria_status tria_score(const tria_stats* stats, int32_t layer, const tria_layer_
 tria_status tria_select(const float* score, const tria_layer_cache* cache, const tria_policy* policy,
                         int32_t* keep_out, void* ws, size_t ws_bytes, void* stream);
 
+/* tria_select without a workspace argument. The paper has no counterpart to
+ * this entry point: it exists for callers that cannot allocate device memory
+ * where they select (an allocator-free decode step, a runtime that owns every
+ * allocation and forbids cudaMalloc after start-up). It allocates nothing and
+ * calls no allocating routine; its scratch is a fixed 4 MiB array compiled
+ * into the library, which every GPU that loads the library holds until the
+ * process exits. Same inputs, outputs and results as tria_select.
+ *  - Limit: control words + per-segment state and 8 KiB histogram + 20 bytes
+ *    per 32-row chunk of the largest capacity, for all n_seqs * n_kv_heads
+ *    segments, must fit in 4 MiB (e.g. 32 segments of 131072 rows do);
+ *    larger calls return TRIA_ERR_WORKSPACE.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - All calls share the one array, which keeps the previous call's contents;
+ *    each call clears what must start at zero. Calls that overlap on the GPU
+ *    (different streams, no ordering) race and give undefined results.
+ *  - Device-detected errors are not reported (only host-side checks return
+ *    an error). Asynchronous on `stream`. */
+tria_status tria_select_noalloc(const float* score, const tria_layer_cache* cache, const tria_policy* policy,
+                                int32_t* keep_out, void* stream);
+
 /* Step 3 only: compacts every segment with n_live > B using the caller's
  * keep list (as tria_select writes it: B strictly ascending entries in
  * [0, n_live) per segment), then sets n_live = B. Rows at or past B keep their

@@ -33,7 +33,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_BUDGET, ERR_CUDA, ERR_WORKSPACE, ERR_T
 EXPORTS = (
     "tria_gate_check", "tria_budget_rows", "tria_should_evict", "tria_load_stats", "tria_free_stats",
     "tria_workspace_size", "tria_workspace_init", "tria_score", "tria_select", "tria_compact",
-    "tria_evict", "tria_evict_profiled", "tria_device_status", "tria_selftest_bounded_wait", "tria_status_string",
+    "tria_evict", "tria_evict_profiled", "tria_select_noalloc", "tria_device_status", "tria_selftest_bounded_wait", "tria_status_string",
     "tria_version",
 )
 
@@ -106,6 +106,8 @@ def load_library(path: str | None = None):
     lib.tria_score.restype = i32
     lib.tria_select.argtypes = [vp, ctypes.POINTER(_LayerCache), ctypes.POINTER(_Policy), vp, vp, sz, vp]
     lib.tria_select.restype = i32
+    lib.tria_select_noalloc.argtypes = [vp, ctypes.POINTER(_LayerCache), ctypes.POINTER(_Policy), vp, vp]
+    lib.tria_select_noalloc.restype = i32
     lib.tria_compact.argtypes = [ctypes.POINTER(_LayerCache), ctypes.POINTER(_Policy), vp, vp, sz, vp]
     lib.tria_compact.restype = i32
     lib.tria_evict.argtypes = [vp, i32, ctypes.POINTER(_LayerCache), ctypes.POINTER(_Policy), vp, sz, vp]
@@ -292,6 +294,14 @@ def select(score_in, cache: LayerCache, policy: Policy, keep_out, *, ws, stream=
     wp, wb = _ws(ws)
     _check(load_library().tria_select(_ptr(score_in), ctypes.byref(c), ctypes.byref(p), _ptr(keep_out),
                                       wp, wb, _stream_handle(stream)), "tria_select")
+
+
+def select_noalloc(score_in, cache: LayerCache, policy: Policy, keep_out, *, stream=None):
+    """tria_select_noalloc: tria_select with the library's fixed scratch array
+    instead of a workspace (for callers that cannot allocate)."""
+    c, p = cache.c_struct(), policy.c_struct()
+    _check(load_library().tria_select_noalloc(_ptr(score_in), ctypes.byref(c), ctypes.byref(p), _ptr(keep_out),
+                                              _stream_handle(stream)), "tria_select_noalloc")
 
 
 def compact(cache: LayerCache, policy: Policy, keep, *, ws, stream=None):
