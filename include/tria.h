@@ -209,7 +209,8 @@ tria_status tria_evict(const tria_stats* stats, int32_t layer, const tria_layer_
 
 /* tria_evict with CUDA events recorded on `stream` between its stages;
  * synchronises `stream` and writes the stage times in milliseconds to
- * stage_ms[5] = {raw scores, z-max scores, select, compact, whole pass} and the
+ * stage_ms[5] = {raw scores, z-max scores (0: computed inside select), select,
+ * compact, whole pass} and the
  * number of kernels launched to *launches. For benchmarks and tracing. */
 tria_status tria_evict_profiled(const tria_stats* stats, int32_t layer, const tria_layer_cache* cache,
                                 const tria_policy* policy, void* ws, size_t ws_bytes, void* stream,

@@ -310,8 +310,7 @@ extern "C" tria_status tria_evict(const tria_stats* stats, int32_t layer, const 
   P.keep = (int32_t*)((uint8_t*)ws + L.keep);
   cudaStream_t st = (cudaStream_t)stream;
   if ((r = cuda_status(launch_score(P, st))) != TRIA_OK) return r;
-  if ((r = cuda_status(launch_zscore(P, st))) != TRIA_OK) return r;
-  if ((r = cuda_status(launch_select(P, true, st))) != TRIA_OK) return r;
+  if ((r = cuda_status(launch_select(P, true, st, stats->group))) != TRIA_OK) return r;
   return cuda_status(launch_move(P, st));
 }
 
@@ -341,12 +340,12 @@ extern "C" tria_status tria_evict_profiled(const tria_stats* stats, int32_t laye
       for (int j = 0; j < i; ++j) cudaEventDestroy(ev[j]);
       return TRIA_ERR_CUDA;
     }
+  // the z-max score is computed inside the select kernel: its stage time is 0
   cudaError_t e = cudaEventRecord(ev[0], st);
   if (e == cudaSuccess) e = launch_score(P, st);
   if (e == cudaSuccess) e = cudaEventRecord(ev[1], st);
-  if (e == cudaSuccess) e = launch_zscore(P, st);
   if (e == cudaSuccess) e = cudaEventRecord(ev[2], st);
-  if (e == cudaSuccess) e = launch_select(P, true, st);
+  if (e == cudaSuccess) e = launch_select(P, true, st, stats->group);
   if (e == cudaSuccess) e = cudaEventRecord(ev[3], st);
   if (e == cudaSuccess) e = launch_move(P, st);
   if (e == cudaSuccess) e = cudaEventRecord(ev[4], st);
@@ -354,7 +353,7 @@ extern "C" tria_status tria_evict_profiled(const tria_stats* stats, int32_t laye
   if (e == cudaSuccess) {
     for (int i = 0; i < 4; ++i) cudaEventElapsedTime(&stage_ms[i], ev[i], ev[i + 1]);
     cudaEventElapsedTime(&stage_ms[4], ev[0], ev[4]);
-    *launches = 8;
+    *launches = 3;
   }
   for (int i = 0; i < 5; ++i) cudaEventDestroy(ev[i]);
   return cuda_status(e);

@@ -145,31 +145,6 @@ struct Batch {
   static constexpr int kNV = kRowsB * G;
 };
 
-// running (count, mean, M2) of one head
-struct Mom {
-  float n, mean, m2;
-};
-
-__device__ __forceinline__ Mom mom_merge(Mom a, Mom b) {
-  const float n = a.n + b.n;
-  if (n == 0.f) return a;
-  const float d = b.mean - a.mean;
-  const float fb = b.n / n;
-  Mom r;
-  r.n = n;
-  r.mean = a.mean + d * fb;
-  r.m2 = a.m2 + b.m2 + d * d * a.n * fb;
-  return r;
-}
-
-__device__ __forceinline__ Mom mom_shfl(Mom a, int mask) {
-  Mom b;
-  b.n = __shfl_xor_sync(0xffffffffu, a.n, mask);
-  b.mean = __shfl_xor_sync(0xffffffffu, a.mean, mask);
-  b.m2 = __shfl_xor_sync(0xffffffffu, a.m2, mask);
-  return b;
-}
-
 struct ScoreGeom {
   int R;       // rows per piece
   int stage;   // bytes per ring stage
@@ -476,50 +451,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1) k_score(const __grid_constan
     __syncwarp();
   }
   flush_run();
-}
-
-// Merge of a segment's run partials (written by k_score) into mean and
-// 1 / (std + 1e-6), by one CTA: thread t merges runs t, t + blockDim, ...
-// (Chan et al. pairwise update, fp32), then a fixed shuffle / shared-memory
-// tree. Runs start at the segment's first piece and at each multiple of the
-// per-warp piece count after it. Deterministic for a given layout.
-template <int G>
-__device__ void merge_segment_moments(const Pass& P, int seg, float* mu, float* inv) {
-  __shared__ Mom red[kThreads / 32][G];
-  const int s0 = __ldcg(&P.seg[seg].piece_first), s1 = __ldcg(&P.seg[seg].piece_end);
-  const int per = max(1, __ldcg(&P.seg[seg].piece_per));
-  const int first_mult = (s0 / per + 1) * per;
-  const int nruns = s1 > s0 ? 1 + (s1 > first_mult ? (s1 - first_mult + per - 1) / per : 0) : 0;
-  Mom acc[G];
-#pragma unroll
-  for (int h = 0; h < G; ++h) acc[h] = Mom{0.f, 0.f, 0.f};
-  for (int i = threadIdx.x; i < nruns; i += blockDim.x) {
-    const int j = i == 0 ? s0 : first_mult + (i - 1) * per;
-    const ScoreChunk* pp = P.schunk + j;
-    const float n = (float)__ldcg(&pp->n);
-#pragma unroll
-    for (int h = 0; h < G; ++h) acc[h] = mom_merge(acc[h], Mom{n, __ldcg(&pp->mean[h]), __ldcg(&pp->m2[h])});
-  }
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-#pragma unroll
-    for (int mask = 1; mask < 32; mask <<= 1) acc[h] = mom_merge(acc[h], mom_shfl(acc[h], mask));
-    if (lane == 0) red[warp][h] = acc[h];
-  }
-  __syncthreads();
-  if (threadIdx.x < G) {
-    Mom a = red[0][threadIdx.x];
-    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) a = mom_merge(a, red[w][threadIdx.x]);
-    red[0][threadIdx.x] = a;
-  }
-  __syncthreads();
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    const Mom a = red[0][h];
-    mu[h] = a.mean;
-    inv[h] = 1.0f / (sqrtf(a.m2 / fmaxf(a.n, 1.f)) + kZEps);
-  }
 }
 
 // z-max score per live row: s = max_h (raw_h - mu_h) * inv_h. The CTA with

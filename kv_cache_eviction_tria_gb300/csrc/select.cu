@@ -3,7 +3,8 @@
 // [Doc] "TriAttention KV-Cache Eviction (--triattention)", §1 CLI flags
 // (--tri-budget, --tri-window, --tri-sink) and §5 Phase B steps 2-3 (protect
 // the first sink and last window tokens, sort the rest by score, evict the
-// lowest down to the budget).
+// lowest down to the budget); §5 Phase C (z-normalise per query head, then max
+// over the GQA group) for the score this stage starts from on the evict path.
 //
 // Exact top-k by radix select on an order-preserving 32-bit key of the score:
 //   pass 0: histogram of key bits [31:21] over the candidates
@@ -13,11 +14,21 @@
 // no spinning) locates the bin holding the k-th largest key, so that T = the
 // k-th largest key and kr = how many rows with key == T are kept. The count
 // pass then finds the row of the kr-th tie (lowest row indices win ties) and
-// the number of kept rows before every 64-row chunk; the keep-list pass writes
-// the kept row indices in ascending order.
+// the number of kept rows before every chunk; the keep-list pass writes the
+// kept row indices in ascending order.
+//
+// All passes run in one cooperative kernel (every CTA resident), separated by
+// bounded grid barriers; work items of a pass are (segment, row block) pairs
+// dealt round-robin to the CTAs.
+#include <cooperative_groups.h>
+
 #include "tria_internal.cuh"
 
+namespace cg = cooperative_groups;
+
 namespace tria {
+
+namespace {
 
 __device__ __forceinline__ SelChunk load_chunk(const SelChunk* p) {
   const int4 v = __ldcg(reinterpret_cast<const int4*>(p));
@@ -29,50 +40,61 @@ __device__ __forceinline__ SelChunk load_chunk(const SelChunk* p) {
   return c;
 }
 
-__device__ __forceinline__ const float* score_base(const Pass& P, const SegView& sv) {
-  return P.score_in + sv.row0;
-}
+struct SelShared {
+  uint32_t h[kHistBins];
+  int sbuf[40];
+  int last, cstar, need, tie_row;
+};
 
-template <int PASS>
-__global__ void __launch_bounds__(kThreads) k_hist(const __grid_constant__ Pass P) {
+// One row block of one radix pass. PASS 0 on the evict path (G > 0) first
+// turns the raw scores into the z-max score and stores it.
+template <int PASS, int G>
+__device__ void hist_block(const Pass& P, int seg, int blk, const SegView& sv, SelShared& sh) {
   constexpr int NB = PASS == 2 ? 1024 : 2048;
   constexpr int PER = NB / kThreads;
-  const int seg = blockIdx.y;
-  const SegView sv = seg_view(P, seg);
-  if (!sv.active || sv.k <= 0) return;
   const int n = sv.n;
   const int nblk = (n + kHistRowsPerCta - 1) / kHistRowsPerCta;
-  if ((int)blockIdx.x >= nblk) return;
-
-  __shared__ uint32_t h[NB];
-  __shared__ int sbuf[40];
-  __shared__ int s_last;
-  for (int i = threadIdx.x; i < NB; i += blockDim.x) h[i] = 0;
+  for (int i = threadIdx.x; i < NB; i += blockDim.x) sh.h[i] = 0;
+  float mu[G > 0 ? G : 1], inv[G > 0 ? G : 1];
+  if constexpr (PASS == 0 && G > 0) merge_segment_moments<G>(P, seg, mu, inv);
   __syncthreads();
 
   const uint32_t prefix = PASS > 0 ? __ldcg(&P.seg[seg].prefix) : 0u;
-  const int lo = max(P.sink, (int)blockIdx.x * kHistRowsPerCta);
-  const int hi = min(n - P.window, ((int)blockIdx.x + 1) * kHistRowsPerCta);
-  const float* s = score_base(P, sv);
-  for (int r = lo + threadIdx.x; r < hi; r += blockDim.x) {
-    const uint32_t key = score_key(s[r]);
-    if (PASS == 0) {
-      atomicAdd(&h[key >> 21], 1u);
-    } else if (PASS == 1) {
-      if ((key >> 21) == prefix) atomicAdd(&h[(key >> 10) & 0x7FFu], 1u);
+  const int r_beg = blk * kHistRowsPerCta, r_end = min(n, r_beg + kHistRowsPerCta);
+  const int lo = P.sink, hi = n - P.window;
+  const bool do_hist = sv.k > 0;
+  for (int r = r_beg + threadIdx.x; r < r_end; r += blockDim.x) {
+    float s;
+    if constexpr (PASS == 0 && G > 0) {
+      const float* rp = P.raw + (size_t)(sv.row0 + r) * G;
+      s = (rp[0] - mu[0]) * inv[0];
+#pragma unroll
+      for (int h = 1; h < G; ++h) s = fmaxf(s, (rp[h] - mu[h]) * inv[h]);
+      P.score[sv.row0 + r] = s;
     } else {
-      if ((key >> 10) == prefix) atomicAdd(&h[key & 0x3FFu], 1u);
+      if (!do_hist || r < lo || r >= hi) continue;
+      s = __ldcg(&P.score_in[sv.row0 + r]);
+    }
+    if (!do_hist || r < lo || r >= hi) continue;
+    const uint32_t key = score_key(s);
+    if (PASS == 0) {
+      atomicAdd(&sh.h[key >> 21], 1u);
+    } else if (PASS == 1) {
+      if ((key >> 21) == prefix) atomicAdd(&sh.h[(key >> 10) & 0x7FFu], 1u);
+    } else {
+      if ((key >> 10) == prefix) atomicAdd(&sh.h[key & 0x3FFu], 1u);
     }
   }
   __syncthreads();
+  if (!do_hist) return;
   uint32_t* gh = P.hist + (size_t)seg * kHistBins;
   for (int i = threadIdx.x; i < NB; i += blockDim.x)
-    if (h[i]) atomicAdd(&gh[i], h[i]);
+    if (sh.h[i]) atomicAdd(&gh[i], sh.h[i]);
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) s_last = (atomicAdd(&P.seg[seg].cnt, 1) == nblk - 1);
+  if (threadIdx.x == 0) sh.last = (atomicAdd(&P.seg[seg].cnt, 1) == nblk - 1);
   __syncthreads();
-  if (!s_last) return;
+  if (!sh.last) return;
   __threadfence();
 
   // bins scanned from the top: thread t owns bins NB-1-(PER*t) .. NB-PER*(t+1)
@@ -85,7 +107,7 @@ __global__ void __launch_bounds__(kThreads) k_hist(const __grid_constant__ Pass 
     local += (int)cnt[j];
   }
   int total;
-  const int before = block_exclusive_scan(local, &total, sbuf);
+  const int before = block_exclusive_scan(local, &total, sh.sbuf);
   if (before < kr && kr <= before + local) {
     int cum = before;
 #pragma unroll
@@ -108,27 +130,21 @@ __global__ void __launch_bounds__(kThreads) k_hist(const __grid_constant__ Pass 
   if (threadIdx.x == 0) P.seg[seg].cnt = 0;
 }
 
-// Per chunk: candidates above T, ties at T, protected rows. The last CTA
-// of the segment places the tie cut and writes the kept-row prefix per chunk.
-__global__ void __launch_bounds__(kThreads) k_count(const __grid_constant__ Pass P) {
-  const int seg = blockIdx.y;
-  const SegView sv = seg_view(P, seg);
-  if (!sv.active) return;
+// One block of kCountChunksPerCta chunks: candidates above T, ties at T,
+// protected rows. The last block of the segment places the tie cut and writes
+// the kept-row prefix of every chunk.
+__device__ void count_block(const Pass& P, int seg, int blk, const SegView& sv, SelShared& sh) {
   const int n = sv.n;
   const int nch = (n + kChunk - 1) / kChunk;
   const int nblk = (nch + kCountChunksPerCta - 1) / kCountChunksPerCta;
-  if ((int)blockIdx.x >= nblk) return;
   const bool none = sv.k <= 0;
   const uint32_t T = none ? 0xFFFFFFFFu : __ldcg(&P.seg[seg].T);
-  const float* s = score_base(P, sv);
+  const float* s = P.score_in + sv.row0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   SelChunk* ch = P.chunk + (size_t)seg * P.c_max;
 
-  __shared__ int sbuf[40];
-  __shared__ int s_last, s_cstar, s_need, s_tie_row;
-
   for (int cc = 0; cc < kCountChunksPerCta / 8; ++cc) {
-    const int c = blockIdx.x * kCountChunksPerCta + warp * (kCountChunksPerCta / 8) + cc;
+    const int c = blk * kCountChunksPerCta + warp * (kCountChunksPerCta / 8) + cc;
     if (c >= nch) break;
     int gt = 0, tie = 0, prot = 0;
 #pragma unroll
@@ -137,7 +153,7 @@ __global__ void __launch_bounds__(kThreads) k_count(const __grid_constant__ Pass
       const bool in = r < n;
       const bool pr = in && is_protected(r, n, P.sink, P.window);
       const bool cand = in && !pr && !none;
-      const uint32_t key = cand ? score_key(s[r]) : 0u;
+      const uint32_t key = cand ? score_key(__ldcg(&s[r])) : 0u;
       gt += __popc(__ballot_sync(0xffffffffu, cand && key > T));
       tie += __popc(__ballot_sync(0xffffffffu, cand && key == T));
       prot += __popc(__ballot_sync(0xffffffffu, pr));
@@ -153,9 +169,9 @@ __global__ void __launch_bounds__(kThreads) k_count(const __grid_constant__ Pass
   }
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) s_last = (atomicAdd(&P.seg[seg].cnt, 1) == nblk - 1);
+  if (threadIdx.x == 0) sh.last = (atomicAdd(&P.seg[seg].cnt, 1) == nblk - 1);
   __syncthreads();
-  if (!s_last) return;
+  if (!sh.last) return;
   __threadfence();
 
   // 1. the chunk holding the kr-th tie (kr ties at T are kept, lowest rows first)
@@ -165,11 +181,11 @@ __global__ void __launch_bounds__(kThreads) k_count(const __grid_constant__ Pass
   int local = 0;
   for (int c = cbeg; c < cend; ++c) local += __ldcg(&ch[c].n_tie);
   int total;
-  int before = block_exclusive_scan(local, &total, sbuf);
+  const int before = block_exclusive_scan(local, &total, sh.sbuf);
   if (threadIdx.x == 0) {
-    s_cstar = -1;
-    s_need = 0;
-    s_tie_row = -1;
+    sh.cstar = -1;
+    sh.need = 0;
+    sh.tie_row = -1;
   }
   __syncthreads();
   if (kr > 0 && before < kr && kr <= before + local) {
@@ -177,15 +193,15 @@ __global__ void __launch_bounds__(kThreads) k_count(const __grid_constant__ Pass
     for (int c = cbeg; c < cend; ++c) {
       const int t = __ldcg(&ch[c].n_tie);
       if (cum + t >= kr) {
-        s_cstar = c;
-        s_need = kr - cum;
+        sh.cstar = c;
+        sh.need = kr - cum;
         break;
       }
       cum += t;
     }
   }
   __syncthreads();
-  const int cstar = s_cstar, need = s_need;
+  const int cstar = sh.cstar, need = sh.need;
   // 2. the row of that tie
   if (cstar >= 0 && warp == 0) {
     int seen = 0;
@@ -193,21 +209,19 @@ __global__ void __launch_bounds__(kThreads) k_count(const __grid_constant__ Pass
       const int r = cstar * kChunk + half * 32 + lane;
       const bool in = r < n;
       const bool cand = in && !is_protected(r, n, P.sink, P.window);
-      const bool t = cand && score_key(s[r]) == T;
+      const bool t = cand && score_key(__ldcg(&s[r])) == T;
       const uint32_t b = __ballot_sync(0xffffffffu, t);
       const int cnt = __popc(b);
       if (seen + cnt >= need) {
-        // the (need - seen)-th set bit of b
-        int want = need - seen;
+        const int want = need - seen;
         const int rank = __popc(b & ((1u << lane) - 1u));
-        if (t && rank == want - 1) s_tie_row = r;
+        if (t && rank == want - 1) sh.tie_row = r;
         break;
       }
       seen += cnt;
     }
   }
-  if (kr > 0 && threadIdx.x == 0 && total < kr)
-    report(P.ctrl, TRIA_ERR_INVALID_ARG, 0x40000000u | (uint32_t)seg);
+  if (kr > 0 && threadIdx.x == 0 && total < kr) report(P.ctrl, TRIA_ERR_INVALID_ARG, 0x40000000u | (uint32_t)seg);
   __syncthreads();
 
   // 3. kept rows per chunk -> exclusive prefix
@@ -217,7 +231,7 @@ __global__ void __launch_bounds__(kThreads) k_count(const __grid_constant__ Pass
     keep_local += v.n_prot + v.n_gt + (c < cstar ? v.n_tie : (c == cstar ? need : 0));
   }
   int keep_total;
-  const int kbefore = block_exclusive_scan(keep_local, &keep_total, sbuf);
+  const int kbefore = block_exclusive_scan(keep_local, &keep_total, sh.sbuf);
   int* pre = P.prefix + (size_t)seg * (P.c_max + 1);
   int cum = kbefore;
   for (int c = cbeg; c < cend; ++c) {
@@ -228,21 +242,18 @@ __global__ void __launch_bounds__(kThreads) k_count(const __grid_constant__ Pass
   if (threadIdx.x == 0) {
     pre[nch] = keep_total;
     if (keep_total != sv.B) report(P.ctrl, TRIA_ERR_INVALID_ARG, 0x20000000u | (uint32_t)seg);
-    P.seg[seg].tie_row = s_tie_row;
+    P.seg[seg].tie_row = sh.tie_row;
     P.seg[seg].cnt = 0;
   }
 }
 
-// Kept row indices of every segment, ascending, at keep[seg_row0 + i].
-__global__ void __launch_bounds__(kThreads) k_keeplist(const __grid_constant__ Pass P) {
-  const int seg = blockIdx.y;
-  const SegView sv = seg_view(P, seg);
-  if (!sv.valid) return;
+// Kept row indices of one block of chunks, ascending, at keep[seg_row0 + i];
+// segments at or below budget get the identity list.
+__device__ void keeplist_block(const Pass& P, int seg, int blk, const SegView& sv) {
   const int n = sv.n;
   int32_t* keep = P.keep + sv.row0;
-  const int r_beg = blockIdx.x * kCountChunksPerCta * kChunk;
+  const int r_beg = blk * kCountChunksPerCta * kChunk;
   if (!sv.active) {
-    if (P.only_active) return;
     const int r_end = min(n, r_beg + kCountChunksPerCta * kChunk);
     for (int r = r_beg + threadIdx.x; r < r_end; r += blockDim.x) keep[r] = r;
     return;
@@ -251,11 +262,11 @@ __global__ void __launch_bounds__(kThreads) k_keeplist(const __grid_constant__ P
   const bool none = sv.k <= 0;
   const uint32_t T = none ? 0xFFFFFFFFu : __ldcg(&P.seg[seg].T);
   const int tie_row = none ? -1 : __ldcg(&P.seg[seg].tie_row);
-  const float* s = score_base(P, sv);
+  const float* s = P.score_in + sv.row0;
   const int* pre = P.prefix + (size_t)seg * (P.c_max + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int cc = 0; cc < kCountChunksPerCta / 8; ++cc) {
-    const int c = blockIdx.x * kCountChunksPerCta + warp * (kCountChunksPerCta / 8) + cc;
+    const int c = blk * kCountChunksPerCta + warp * (kCountChunksPerCta / 8) + cc;
     if (c >= nch) break;
     int base = __ldcg(&pre[c]);
 #pragma unroll
@@ -265,7 +276,7 @@ __global__ void __launch_bounds__(kThreads) k_keeplist(const __grid_constant__ P
       const bool pr = in && is_protected(r, n, P.sink, P.window);
       bool kp = pr;
       if (in && !pr && !none) {
-        const uint32_t key = score_key(s[r]);
+        const uint32_t key = score_key(__ldcg(&s[r]));
         kp = key > T || (key == T && r <= tie_row);
       }
       const uint32_t b = __ballot_sync(0xffffffffu, kp);
@@ -275,16 +286,332 @@ __global__ void __launch_bounds__(kThreads) k_keeplist(const __grid_constant__ P
   }
 }
 
-cudaError_t launch_select(const Pass& P, bool write_keep, cudaStream_t st) {
-  const int cap_rows = P.c_max * kChunk;
-  dim3 gh((cap_rows + kHistRowsPerCta - 1) / kHistRowsPerCta, P.n_seg);
-  k_hist<0><<<gh, kThreads, 0, st>>>(P);
-  k_hist<1><<<gh, kThreads, 0, st>>>(P);
-  k_hist<2><<<gh, kThreads, 0, st>>>(P);
-  dim3 gc((P.c_max + kCountChunksPerCta - 1) / kCountChunksPerCta, P.n_seg);
-  k_count<<<gc, kThreads, 0, st>>>(P);
-  if (write_keep) k_keeplist<<<gc, kThreads, 0, st>>>(P);
-  return cudaGetLastError();
+// The whole select stage (and, with G > 0, the z-max score) in one
+// cooperative launch.
+template <int G>
+__global__ void __launch_bounds__(kThreads) k_select(const __grid_constant__ Pass P, int write_keep) {
+  __shared__ SelShared sh;
+  const int hist_blocks = (P.c_max * kChunk + kHistRowsPerCta - 1) / kHistRowsPerCta;
+  const int hist_items = P.n_seg * hist_blocks;
+  const int count_blocks = (P.c_max + kCountChunksPerCta - 1) / kCountChunksPerCta;
+  const int count_items = P.n_seg * count_blocks;
+
+  // pass 0 (+ z-max score): every active segment
+  for (int it = blockIdx.x; it < hist_items; it += gridDim.x) {
+    const int seg = it / hist_blocks, blk = it - seg * hist_blocks;
+    const SegView sv = seg_view(P, seg);
+    if (!sv.valid) {
+      if (blk == 0 && threadIdx.x == 0) report(P.ctrl, TRIA_ERR_DEVICE_ARG, (uint32_t)sv.s);
+      continue;
+    }
+    if (!sv.active || blk * kHistRowsPerCta >= sv.n) continue;
+    hist_block<0, G>(P, seg, blk, sv, sh);
+  }
+  grid_barrier(P);
+  for (int it = blockIdx.x; it < hist_items; it += gridDim.x) {
+    const int seg = it / hist_blocks, blk = it - seg * hist_blocks;
+    const SegView sv = seg_view(P, seg);
+    if (!sv.active || sv.k <= 0 || blk * kHistRowsPerCta >= sv.n) continue;
+    hist_block<1, 0>(P, seg, blk, sv, sh);
+  }
+  grid_barrier(P);
+  for (int it = blockIdx.x; it < hist_items; it += gridDim.x) {
+    const int seg = it / hist_blocks, blk = it - seg * hist_blocks;
+    const SegView sv = seg_view(P, seg);
+    if (!sv.active || sv.k <= 0 || blk * kHistRowsPerCta >= sv.n) continue;
+    hist_block<2, 0>(P, seg, blk, sv, sh);
+  }
+  grid_barrier(P);
+  for (int it = blockIdx.x; it < count_items; it += gridDim.x) {
+    const int seg = it / count_blocks, blk = it - seg * count_blocks;
+    const SegView sv = seg_view(P, seg);
+    if (!sv.active || blk * kCountChunksPerCta * kChunk >= sv.n) continue;
+    count_block(P, seg, blk, sv, sh);
+  }
+  if (!write_keep) return;
+  grid_barrier(P);
+  for (int it = blockIdx.x; it < count_items; it += gridDim.x) {
+    const int seg = it / count_blocks, blk = it - seg * count_blocks;
+    const SegView sv = seg_view(P, seg);
+    if (!sv.valid || blk * kCountChunksPerCta * kChunk >= sv.n) continue;
+    if (!sv.active && P.only_active) continue;
+    keeplist_block(P, seg, blk, sv);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Cluster path: one thread-block cluster of kClusterCtas CTAs per segment. CTA
+// `rank` owns the contiguous, chunk-aligned row range [rank*RPC, rank*RPC+RPC)
+// and keeps the 32-bit keys of its rows in shared memory for all passes.
+// Radix histograms are combined through distributed shared memory after a
+// cluster barrier (every CTA sums all ranks' histograms for itself, so no
+// broadcast step); tie counts and kept counts are exchanged the same way.
+// ---------------------------------------------------------------------------
+
+constexpr int kClusterCtas = 8;
+constexpr int kClThreads = 512;
+constexpr int kClMaxRowsPerCta = 32768;   // 128 KiB of keys
+
+struct ClShared {
+  uint32_t h[2][kHistBins];     // this CTA's histogram, double-buffered by pass
+  int sbuf[40];
+  int info[4];                  // prefix, kr after the current pass
+  int cnt[2];                   // ties, strict keeps (gt + protected) of this CTA
+  int warp_tie[kClThreads / 32], warp_keep[kClThreads / 32];
+};
+
+template <int G>
+__global__ void __launch_bounds__(kClThreads) k_select_cl(const __grid_constant__ Pass P, int write_keep) {
+  extern __shared__ __align__(16) uint32_t keys[];
+  __shared__ ClShared sh;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int seg = blockIdx.y;
+  const SegView sv = seg_view(P, seg);
+  if (!sv.valid) {
+    if (rank == 0 && threadIdx.x == 0) report(P.ctrl, TRIA_ERR_DEVICE_ARG, (uint32_t)sv.s);
+    return;   // the whole cluster leaves (same segment)
+  }
+  const int n = sv.n;
+  const int rpc = (((n + kClusterCtas - 1) / kClusterCtas) + kChunk - 1) / kChunk * kChunk;
+  const int r0 = min(n, rank * rpc), r1 = min(n, r0 + rpc);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int32_t* keep = P.keep + sv.row0;
+  if (!sv.active) {
+    if (write_keep && !P.only_active)
+      for (int r = r0 + threadIdx.x; r < r1; r += blockDim.x) keep[r] = r;
+    return;
+  }
+  const int lo = P.sink, hi = n - P.window;
+  const bool none = sv.k <= 0;
+
+  // keys of my rows (the evict path turns raw scores into the z-max score here)
+  {
+    float mu[G > 0 ? G : 1], inv[G > 0 ? G : 1];
+    if constexpr (G > 0) merge_segment_moments<G>(P, seg, mu, inv);
+    for (int r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
+      float s;
+      if constexpr (G > 0) {
+        const float* rp = P.raw + (size_t)(sv.row0 + r) * G;
+        s = (rp[0] - mu[0]) * inv[0];
+#pragma unroll
+        for (int h = 1; h < G; ++h) s = fmaxf(s, (rp[h] - mu[h]) * inv[h]);
+      } else {
+        s = __ldcg(&P.score_in[sv.row0 + r]);
+      }
+      keys[r - r0] = score_key(s);
+    }
+  }
+
+  // three radix passes over the candidates [lo, hi)
+  uint32_t prefix = 0, T = 0xFFFFFFFFu;
+  int kr = sv.k;
+  if (!none) {
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+      const int NB = pass == 2 ? 1024 : 2048;
+      uint32_t* hb = sh.h[pass & 1];
+      for (int i = threadIdx.x; i < NB; i += blockDim.x) hb[i] = 0;
+      __syncthreads();
+      for (int r = max(r0, lo) + threadIdx.x; r < min(r1, hi); r += blockDim.x) {
+        const uint32_t key = keys[r - r0];
+        if (pass == 0) atomicAdd(&hb[key >> 21], 1u);
+        else if (pass == 1) { if ((key >> 21) == prefix) atomicAdd(&hb[(key >> 10) & 0x7FFu], 1u); }
+        else if ((key >> 10) == prefix) atomicAdd(&hb[key & 0x3FFu], 1u);
+      }
+      cluster.sync();
+      // every CTA sums all ranks' bins and finds the bin of the kr-th largest
+      const int per = NB / kClThreads;   // 4 or 2 bins per thread, scanned from the top
+      uint32_t tot[4];
+      int local = 0;
+      for (int j = 0; j < per; ++j) {
+        const int b = NB - 1 - (per * threadIdx.x + j);
+        uint32_t acc = 0;
+        for (int q = 0; q < kClusterCtas; ++q) acc += cluster.map_shared_rank(hb, q)[b];
+        tot[j] = acc;
+        local += (int)acc;
+      }
+      int total;
+      const int before = block_exclusive_scan(local, &total, sh.sbuf);
+      if (before < kr && kr <= before + local) {
+        int cum = before;
+        for (int j = 0; j < per; ++j) {
+          const int b = NB - 1 - (per * threadIdx.x + j);
+          if (cum + (int)tot[j] >= kr) {
+            sh.info[0] = (int)(pass == 0 ? (uint32_t)b : pass == 1 ? ((prefix << 11) | (uint32_t)b)
+                                                                     : ((prefix << 10) | (uint32_t)b));
+            sh.info[1] = kr - cum;
+            break;
+          }
+          cum += (int)tot[j];
+        }
+      }
+      if (threadIdx.x == 0 && total < kr && rank == 0)
+        report(P.ctrl, TRIA_ERR_INVALID_ARG, 0x80000000u | (uint32_t)seg);
+      __syncthreads();
+      prefix = (uint32_t)sh.info[0];
+      kr = sh.info[1];
+    }
+    T = prefix;
+  }
+
+  // counts of my rows; ties at T are kept lowest rows first across the cluster
+  const int nch_mine = (r1 - r0 + kChunk - 1) / kChunk;
+  const int cpw = (nch_mine + (kClThreads / 32) - 1) / (kClThreads / 32);   // chunks per warp
+  int w_tie = 0, w_keep = 0;
+  for (int ci = warp * cpw; ci < min(nch_mine, (warp + 1) * cpw); ++ci) {
+    const int r = r0 + ci * kChunk + lane;
+    const bool in = r < r1;
+    const bool pr = in && is_protected(r, n, lo, P.window);
+    const bool cand = in && !pr && !none;
+    const uint32_t key = in ? keys[r - r0] : 0u;
+    w_tie += __popc(__ballot_sync(0xffffffffu, cand && key == T));
+    w_keep += __popc(__ballot_sync(0xffffffffu, pr || (cand && key > T)));
+  }
+  if (lane == 0) {
+    sh.warp_tie[warp] = w_tie;
+    sh.warp_keep[warp] = w_keep;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int a = 0, b = 0;
+    for (int w = 0; w < kClThreads / 32; ++w) {
+      a += sh.warp_tie[w];
+      b += sh.warp_keep[w];
+    }
+    sh.cnt[0] = a;
+    sh.cnt[1] = b;
+  }
+  cluster.sync();
+  // ties and kept rows of the lower ranks
+  __shared__ int s_off[3];
+  if (threadIdx.x == 0) {
+    int tie_before = 0, keep_before = 0;
+    for (int q = 0; q < rank; ++q) {
+      const int* c = cluster.map_shared_rank(sh.cnt, q);
+      const int tq = c[0];
+      const int kept_ties = max(0, min(tq, kr - tie_before));
+      keep_before += c[1] + kept_ties;
+      tie_before += tq;
+    }
+    s_off[0] = keep_before;
+    s_off[1] = max(0, min(sh.cnt[0], kr - tie_before));   // my ties that are kept
+    s_off[2] = 0;
+  }
+  __syncthreads();
+  const int keep_base = s_off[0], my_ties = s_off[1];
+  // per-warp offsets (ties and kept rows of the lower warps of this CTA)
+  int tie_off = 0, keep_off = 0;
+  for (int w = 0; w < warp; ++w) {
+    const int tw = sh.warp_tie[w];
+    tie_off += tw;
+  }
+  {
+    // kept rows of lower warps = strict keeps + their kept ties
+    int t_run = 0;
+    for (int w = 0; w < warp; ++w) {
+      const int tw = sh.warp_tie[w];
+      keep_off += sh.warp_keep[w] + max(0, min(tw, my_ties - t_run));
+      t_run += tw;
+    }
+  }
+  int* pre = P.prefix + (size_t)seg * (P.c_max + 1);
+  const int chunk0 = r0 / kChunk;
+  int tie_run = tie_off, keep_run = keep_base + keep_off;
+  for (int ci = warp * cpw; ci < min(nch_mine, (warp + 1) * cpw); ++ci) {
+    const int r = r0 + ci * kChunk + lane;
+    const bool in = r < r1;
+    const bool pr = in && is_protected(r, n, lo, P.window);
+    const bool cand = in && !pr && !none;
+    const uint32_t key = in ? keys[r - r0] : 0u;
+    const bool is_tie = cand && key == T;
+    const uint32_t bt = __ballot_sync(0xffffffffu, is_tie);
+    const int trank = tie_run + __popc(bt & ((1u << lane) - 1u));
+    const bool kp = pr || (cand && key > T) || (is_tie && trank < my_ties);
+    const uint32_t bk = __ballot_sync(0xffffffffu, kp);
+    if (lane == 0) pre[chunk0 + ci] = keep_run;
+    if (write_keep && kp) keep[keep_run + __popc(bk & ((1u << lane) - 1u))] = r;
+    tie_run += __popc(bt);
+    keep_run += __popc(bk);
+  }
+  if (rank == 0 && threadIdx.x == 0) {
+    pre[(n + kChunk - 1) / kChunk] = sv.B;
+    if (sv.B > n) report(P.ctrl, TRIA_ERR_INVALID_ARG, 0x20000000u | (uint32_t)seg);
+  }
+  cluster.sync();   // no CTA leaves while another may still read its shared memory
+}
+
+template <int G>
+cudaError_t launch_select_cl(const Pass& P, bool write_keep, cudaStream_t st, int cap_max) {
+  const int rpc_max = (((cap_max + kClusterCtas - 1) / kClusterCtas) + kChunk - 1) / kChunk * kChunk;
+  const size_t smem = (size_t)rpc_max * 4;
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(k_select_cl<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kClMaxRowsPerCta * 4);
+  if (attr != cudaSuccess) return attr;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kClusterCtas, P.n_seg, 1);
+  cfg.blockDim = dim3(kClThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = kClusterCtas;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_select_cl<G>, P, write_keep ? 1 : 0);
+}
+
+template <int G>
+cudaError_t launch_select_g(const Pass& P, bool write_keep, cudaStream_t st) {
+  static int per_sm = -1;
+  if (per_sm < 0) {
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_select<G>, kThreads, 0);
+    if (e != cudaSuccess) {
+      per_sm = -1;
+      return e;
+    }
+  }
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int hist_blocks = (P.c_max * kChunk + kHistRowsPerCta - 1) / kHistRowsPerCta;
+  const int count_blocks = (P.c_max + kCountChunksPerCta - 1) / kCountChunksPerCta;
+  const int items = P.n_seg * (hist_blocks > count_blocks ? hist_blocks : count_blocks);
+  int grid = sms * (per_sm < 2 ? per_sm : 2);
+  if (grid > items) grid = items;
+  if (grid < 1) grid = 1;
+  int wk = write_keep ? 1 : 0;
+  void* args[] = {const_cast<Pass*>(&P), &wk};
+  return cudaLaunchCooperativeKernel((const void*)k_select<G>, dim3(grid), dim3(kThreads), args, 0, st);
+}
+
+}  // namespace
+
+cudaError_t launch_select(const Pass& P, bool write_keep, cudaStream_t st, int score_group) {
+  // segments up to kClusterCtas * kClMaxRowsPerCta rows: one cluster per
+  // segment; longer ones: the cooperative grid path
+  const int cap_max = P.c_max * kChunk;
+  if (cap_max <= kClusterCtas * kClMaxRowsPerCta) {
+    switch (score_group) {
+      case 0: return launch_select_cl<0>(P, write_keep, st, cap_max);
+      case 1: return launch_select_cl<1>(P, write_keep, st, cap_max);
+      case 2: return launch_select_cl<2>(P, write_keep, st, cap_max);
+      case 4: return launch_select_cl<4>(P, write_keep, st, cap_max);
+      case 8: return launch_select_cl<8>(P, write_keep, st, cap_max);
+    }
+    return cudaErrorInvalidValue;
+  }
+  switch (score_group) {
+    case 0: return launch_select_g<0>(P, write_keep, st);
+    case 1: return launch_select_g<1>(P, write_keep, st);
+    case 2: return launch_select_g<2>(P, write_keep, st);
+    case 4: return launch_select_g<4>(P, write_keep, st);
+    case 8: return launch_select_g<8>(P, write_keep, st);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace tria

@@ -38,7 +38,9 @@ struct Ctrl {
   uint32_t epoch;        // compaction flags carry epoch + 1 of their call
   uint32_t bad_keep;     // keep-list entries rejected by the validation pass
   uint32_t wait_flag;    // never set: target of the bounded-wait self-test
-  uint32_t pad[57];
+  uint32_t bar_count;    // grid barrier: CTAs arrived (reset by the last one)
+  uint32_t bar_gen;      // grid barrier: generation, bumped when all arrived
+  uint32_t pad[55];
 };
 
 // Per-segment state (one segment = one sequence x KV head of the layer).
@@ -227,6 +229,15 @@ __device__ __forceinline__ bool wait_flag_bounded(const uint32_t* flag, uint32_t
   return false;
 }
 
+// Bounded poll until a word differs from `old`; false when the limit ran out.
+__device__ __forceinline__ bool wait_flag_bounded_ne(const uint32_t* flag, uint32_t old, int limit) {
+  for (int it = 0; it < limit; ++it) {
+    if (ld_acquire_u32(flag) != old) return true;
+    __nanosleep(it < 64 ? 32 : 256);
+  }
+  return false;
+}
+
 // ---------------------------------------------------------------------------
 // block-wide helpers
 // ---------------------------------------------------------------------------
@@ -260,6 +271,105 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int* total, int* sbuf
 }
 
 // ---------------------------------------------------------------------------
+// moments (Chan et al. pairwise update) and the per-segment merge
+// ---------------------------------------------------------------------------
+
+// running (count, mean, M2) of one head
+struct Mom {
+  float n, mean, m2;
+};
+
+__device__ __forceinline__ Mom mom_merge(Mom a, Mom b) {
+  const float n = a.n + b.n;
+  if (n == 0.f) return a;
+  const float d = b.mean - a.mean;
+  const float fb = b.n / n;
+  Mom r;
+  r.n = n;
+  r.mean = a.mean + d * fb;
+  r.m2 = a.m2 + b.m2 + d * d * a.n * fb;
+  return r;
+}
+
+__device__ __forceinline__ Mom mom_shfl(Mom a, int mask) {
+  Mom b;
+  b.n = __shfl_xor_sync(0xffffffffu, a.n, mask);
+  b.mean = __shfl_xor_sync(0xffffffffu, a.mean, mask);
+  b.m2 = __shfl_xor_sync(0xffffffffu, a.m2, mask);
+  return b;
+}
+
+// Merge of a segment's run partials (written by k_score) into mean and
+// 1 / (std + 1e-6), by one CTA: thread t merges runs t, t + blockDim, ...
+// (Chan et al. pairwise update, fp32), then a fixed shuffle / shared-memory
+// tree. Runs start at the segment's first piece and at each multiple of the
+// per-warp piece count after it. Deterministic for a given layout.
+template <int G>
+__device__ void merge_segment_moments(const Pass& P, int seg, float* mu, float* inv) {
+  __shared__ Mom red[32][G];   // up to 32 warps
+  const int s0 = __ldcg(&P.seg[seg].piece_first), s1 = __ldcg(&P.seg[seg].piece_end);
+  const int per = max(1, __ldcg(&P.seg[seg].piece_per));
+  const int first_mult = (s0 / per + 1) * per;
+  const int nruns = s1 > s0 ? 1 + (s1 > first_mult ? (s1 - first_mult + per - 1) / per : 0) : 0;
+  Mom acc[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) acc[h] = Mom{0.f, 0.f, 0.f};
+  for (int i = threadIdx.x; i < nruns; i += blockDim.x) {
+    const int j = i == 0 ? s0 : first_mult + (i - 1) * per;
+    const ScoreChunk* pp = P.schunk + j;
+    const float n = (float)__ldcg(&pp->n);
+#pragma unroll
+    for (int h = 0; h < G; ++h) acc[h] = mom_merge(acc[h], Mom{n, __ldcg(&pp->mean[h]), __ldcg(&pp->m2[h])});
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+#pragma unroll
+    for (int mask = 1; mask < 32; mask <<= 1) acc[h] = mom_merge(acc[h], mom_shfl(acc[h], mask));
+    if (lane == 0) red[warp][h] = acc[h];
+  }
+  __syncthreads();
+  if (threadIdx.x < G) {
+    Mom a = red[0][threadIdx.x];
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) a = mom_merge(a, red[w][threadIdx.x]);
+    red[0][threadIdx.x] = a;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const Mom a = red[0][h];
+    mu[h] = a.mean;
+    inv[h] = 1.0f / (sqrtf(a.m2 / fmaxf(a.n, 1.f)) + kZEps);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// grid barrier of a cooperative launch (all CTAs resident), bounded: after the
+// spin limit it records TRIA_ERR_TIMEOUT and lets the CTA go on (no hang)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ bool grid_barrier(const Pass& P) {
+  __shared__ int s_timeout;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    s_timeout = 0;
+    const uint32_t gen = ld_acquire_u32(&P.ctrl->bar_gen);
+    __threadfence();
+    if (atomicAdd(&P.ctrl->bar_count, 1u) == gridDim.x - 1) {
+      atomicExch(&P.ctrl->bar_count, 0u);
+      __threadfence();
+      atomicAdd(&P.ctrl->bar_gen, 1u);
+    } else if (!wait_flag_bounded_ne(&P.ctrl->bar_gen, gen, P.spin_limit)) {
+      s_timeout = 1;
+      report(P.ctrl, TRIA_ERR_TIMEOUT, 0xB0000000u);
+    }
+    __threadfence();
+  }
+  __syncthreads();
+  return s_timeout == 0;
+}
+
+// ---------------------------------------------------------------------------
 // launchers (one per translation unit)
 // ---------------------------------------------------------------------------
 
@@ -268,8 +378,9 @@ cudaError_t launch_score(const Pass& P, cudaStream_t st);
 cudaError_t launch_zscore(const Pass& P, cudaStream_t st);
 size_t score_smem_bytes(const Pass& P);
 int score_pieces_max(int k_rb, int cap);   // score pieces of a segment of `cap` rows
-// select.cu
-cudaError_t launch_select(const Pass& P, bool write_keep, cudaStream_t st);
+// select.cu: score_group > 0 computes the z-max score from the raw scores of
+// the score stage (evict path) and writes it to P.score; 0 reads P.score_in
+cudaError_t launch_select(const Pass& P, bool write_keep, cudaStream_t st, int score_group = 0);
 // compact.cu
 cudaError_t launch_keep_prepass(const Pass& P, cudaStream_t st);
 cudaError_t launch_move(const Pass& P, cudaStream_t st);
