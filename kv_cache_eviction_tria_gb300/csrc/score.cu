@@ -443,7 +443,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) k_score(const __grid_constan
     for (int o = 0; o < kOut; ++o) {
       Mom b;
       b.n = cnt[o];
-      const float mean_d = cnt[o] > 0.f ? s1[o] / cnt[o] : 0.f;
+      const float mean_d = cnt[o] > 0.f ? __fdividef(s1[o], cnt[o]) : 0.f;
       b.mean = shift[o] + mean_d;
       b.m2 = fmaxf(s2[o] - s1[o] * mean_d, 0.f);
       run_m[o] = mom_merge(run_m[o], b);

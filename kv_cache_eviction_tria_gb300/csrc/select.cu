@@ -353,12 +353,71 @@ constexpr int kClThreads = 512;
 constexpr int kClMaxRowsPerCta = 32768;   // 128 KiB of keys
 
 struct ClShared {
-  uint32_t h[2][kHistBins];     // this CTA's histogram, double-buffered by pass
+  alignas(16) uint32_t h[2][kHistBins];   // this CTA's histogram, double-buffered by pass
   int sbuf[40];
   int info[4];                  // prefix, kr after the current pass
   int cnt[2];                   // ties, strict keeps (gt + protected) of this CTA
   int warp_tie[kClThreads / 32], warp_keep[kClThreads / 32];
 };
+
+// the G raw scores of one row (vector loads; rows are G consecutive floats,
+// so 16-byte aligned for G = 4 and 8)
+template <int G>
+__device__ __forceinline__ void load_raw_row(const float* rp, float* x) {
+  if constexpr (G % 4 == 0) {
+#pragma unroll
+    for (int h = 0; h < G; h += 4) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(rp + h));
+      x[h] = v.x;
+      x[h + 1] = v.y;
+      x[h + 2] = v.z;
+      x[h + 3] = v.w;
+    }
+  } else if constexpr (G == 2) {
+    const float2 v = __ldcg(reinterpret_cast<const float2*>(rp));
+    x[0] = v.x;
+    x[1] = v.y;
+  } else {
+#pragma unroll
+    for (int h = 0; h < G; ++h) x[h] = __ldcg(rp + h);
+  }
+}
+
+// Sum of the NB-bin histograms of all cluster ranks for the PER consecutive
+// bins of this thread, read as one PER-word vector per rank. Thread t holds
+// bins NB-1-PER*t-j, j = 0..PER-1 (descending), in tot[j]; returns their sum.
+template <int PER>
+__device__ __forceinline__ int cluster_bins(cg::cluster_group& cluster, uint32_t* hb, int NB, uint32_t* tot) {
+  const int v = NB / PER - 1 - (int)threadIdx.x;   // vector index of this thread's bins
+#pragma unroll
+  for (int j = 0; j < PER; ++j) tot[j] = 0;
+  if (v < 0) return 0;
+  if constexpr (PER == 4) {
+    uint4 r[kClusterCtas];
+#pragma unroll
+    for (int q = 0; q < kClusterCtas; ++q) r[q] = reinterpret_cast<const uint4*>(cluster.map_shared_rank(hb, q))[v];
+#pragma unroll
+    for (int q = 0; q < kClusterCtas; ++q) {
+      tot[0] += r[q].w;
+      tot[1] += r[q].z;
+      tot[2] += r[q].y;
+      tot[3] += r[q].x;
+    }
+  } else {
+    uint2 r[kClusterCtas];
+#pragma unroll
+    for (int q = 0; q < kClusterCtas; ++q) r[q] = reinterpret_cast<const uint2*>(cluster.map_shared_rank(hb, q))[v];
+#pragma unroll
+    for (int q = 0; q < kClusterCtas; ++q) {
+      tot[0] += r[q].y;
+      tot[1] += r[q].x;
+    }
+  }
+  int local = 0;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) local += (int)tot[j];
+  return local;
+}
 
 template <int G>
 __global__ void __launch_bounds__(kClThreads) k_select_cl(const __grid_constant__ Pass P, int write_keep) {
@@ -385,21 +444,42 @@ __global__ void __launch_bounds__(kClThreads) k_select_cl(const __grid_constant_
   const int lo = P.sink, hi = n - P.window;
   const bool none = sv.k <= 0;
 
-  // keys of my rows (the evict path turns raw scores into the z-max score here)
+  // keys of my rows (the evict path turns raw scores into the z-max score
+  // here); loads are batched U rows per thread so that they are in flight
+  // together, and the first batch is loaded before the moment merge so that
+  // its latency overlaps the merge's
   {
-    float mu[G > 0 ? G : 1], inv[G > 0 ? G : 1];
-    if constexpr (G > 0) merge_segment_moments<G>(P, seg, mu, inv);
-    for (int r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
-      float s;
-      if constexpr (G > 0) {
-        const float* rp = P.raw + (size_t)(sv.row0 + r) * G;
-        s = (rp[0] - mu[0]) * inv[0];
+    constexpr int GG = G > 0 ? G : 1;
+    constexpr int U = G > 4 ? 4 : 8;
+    float x[U][GG];
+    auto load_batch = [&](int base) {
 #pragma unroll
-        for (int h = 1; h < G; ++h) s = fmaxf(s, (rp[h] - mu[h]) * inv[h]);
-      } else {
-        s = __ldcg(&P.score_in[sv.row0 + r]);
+      for (int u = 0; u < U; ++u) {
+        const int r = base + u * kClThreads;
+        if (r < r1) {
+          if constexpr (G > 0) load_raw_row<G>(P.raw + (size_t)(sv.row0 + r) * G, x[u]);
+          else x[u][0] = __ldcg(&P.score_in[sv.row0 + r]);
+        }
       }
-      keys[r - r0] = score_key(s);
+    };
+    float mu[GG], inv[GG];
+    load_batch(r0 + threadIdx.x);
+    if constexpr (G > 0) merge_segment_moments<G>(P, seg, mu, inv);
+    for (int base = r0 + threadIdx.x; base < r1; base += U * kClThreads) {
+      if (base != r0 + (int)threadIdx.x) load_batch(base);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int r = base + u * kClThreads;
+        if (r < r1) {
+          float s = x[u][0];
+          if constexpr (G > 0) {
+            s = (x[u][0] - mu[0]) * inv[0];
+#pragma unroll
+            for (int h = 1; h < G; ++h) s = fmaxf(s, (x[u][h] - mu[h]) * inv[h]);
+          }
+          keys[r - r0] = score_key(s);
+        }
+      }
     }
   }
 
@@ -423,14 +503,7 @@ __global__ void __launch_bounds__(kClThreads) k_select_cl(const __grid_constant_
       // every CTA sums all ranks' bins and finds the bin of the kr-th largest
       const int per = NB / kClThreads;   // 4 or 2 bins per thread, scanned from the top
       uint32_t tot[4];
-      int local = 0;
-      for (int j = 0; j < per; ++j) {
-        const int b = NB - 1 - (per * threadIdx.x + j);
-        uint32_t acc = 0;
-        for (int q = 0; q < kClusterCtas; ++q) acc += cluster.map_shared_rank(hb, q)[b];
-        tot[j] = acc;
-        local += (int)acc;
-      }
+      const int local = pass == 2 ? cluster_bins<2>(cluster, hb, NB, tot) : cluster_bins<4>(cluster, hb, NB, tot);
       int total;
       const int before = block_exclusive_scan(local, &total, sh.sbuf);
       if (before < kr && kr <= before + local) {

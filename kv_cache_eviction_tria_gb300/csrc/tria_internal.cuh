@@ -283,7 +283,7 @@ __device__ __forceinline__ Mom mom_merge(Mom a, Mom b) {
   const float n = a.n + b.n;
   if (n == 0.f) return a;
   const float d = b.mean - a.mean;
-  const float fb = b.n / n;
+  const float fb = __fdividef(b.n, n);   // counts: n well inside the fast divide's range
   Mom r;
   r.n = n;
   r.mean = a.mean + d * fb;
@@ -301,9 +301,11 @@ __device__ __forceinline__ Mom mom_shfl(Mom a, int mask) {
 
 // Merge of a segment's run partials (written by k_score) into mean and
 // 1 / (std + 1e-6), by one CTA: thread t merges runs t, t + blockDim, ...
-// (Chan et al. pairwise update, fp32), then a fixed shuffle / shared-memory
-// tree. Runs start at the segment's first piece and at each multiple of the
-// per-warp piece count after it. Deterministic for a given layout.
+// (Chan et al. pairwise update, fp32), then a butterfly over the lanes of each
+// warp and a second butterfly over the warp results, which every warp
+// computes identically (lane 0's result is broadcast), so no serial chain and
+// one barrier. Runs start at the segment's first piece and at each multiple
+// of the per-warp piece count after it. Deterministic for a given layout.
 template <int G>
 __device__ void merge_segment_moments(const Pass& P, int seg, float* mu, float* inv) {
   __shared__ Mom red[32][G];   // up to 32 warps
@@ -323,23 +325,27 @@ __device__ void merge_segment_moments(const Pass& P, int seg, float* mu, float* 
   }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
+  for (int mask = 1; mask < 32; mask <<= 1)
 #pragma unroll
-    for (int mask = 1; mask < 32; mask <<= 1) acc[h] = mom_merge(acc[h], mom_shfl(acc[h], mask));
-    if (lane == 0) red[warp][h] = acc[h];
-  }
+    for (int h = 0; h < G; ++h) acc[h] = mom_merge(acc[h], mom_shfl(acc[h], mask));
+  if (lane == 0)
+#pragma unroll
+    for (int h = 0; h < G; ++h) red[warp][h] = acc[h];
   __syncthreads();
-  if (threadIdx.x < G) {
-    Mom a = red[0][threadIdx.x];
-    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) a = mom_merge(a, red[w][threadIdx.x]);
-    red[0][threadIdx.x] = a;
-  }
-  __syncthreads();
+  const int nw = (int)(blockDim.x >> 5);
+#pragma unroll
+  for (int h = 0; h < G; ++h) acc[h] = lane < nw ? red[lane][h] : Mom{0.f, 0.f, 0.f};
+#pragma unroll
+  for (int mask = 1; mask < 32; mask <<= 1)
+#pragma unroll
+    for (int h = 0; h < G; ++h) acc[h] = mom_merge(acc[h], mom_shfl(acc[h], mask));
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-    const Mom a = red[0][h];
-    mu[h] = a.mean;
-    inv[h] = 1.0f / (sqrtf(a.m2 / fmaxf(a.n, 1.f)) + kZEps);
+    const float n = __shfl_sync(0xffffffffu, acc[h].n, 0);
+    const float m = __shfl_sync(0xffffffffu, acc[h].mean, 0);
+    const float m2 = __shfl_sync(0xffffffffu, acc[h].m2, 0);
+    mu[h] = m;
+    inv[h] = 1.0f / (sqrtf(m2 / fmaxf(n, 1.f)) + kZEps);
   }
 }
 
