@@ -8,17 +8,18 @@
 // GPU work on GPU" (one gather kernel instead of thousands of small copies).
 //
 // Kept row i of a segment moves to row i, and i <= keep[i], so data only moves
-// towards lower rows. The warp that owns source chunk c (32 rows) moves its
-// kept rows to the contiguous destination range [prefix[c], prefix[c+1]),
-// which can only cover rows of chunks <= c. It therefore
+// towards lower rows. Work is split by 32-row DESTINATION block: block j
+// gathers rows keep[32j .. 32j+32) and writes them to rows [32j, 32j+32), so
+// every block but a segment's last moves a full stage. Block j overwrites
+// source rows [32j, 32j+32), which are read by the blocks that own keep
+// entries [prefix[j], prefix[j+1]) (prefix[c] = kept rows before source chunk
+// c) - blocks <= j, at most two of them lower than j. So block j
 //   1. copies its moving rows (all planes) into its own shared-memory stage,
-//   2. publishes "chunk c read" (flag = epoch + 1, release),
-//   3. waits (bounded) for the flags of the lower chunks whose rows it will
-//      overwrite - at most two, since 32 destination rows span at most two
-//      32-row source chunks - and
+//   2. publishes "block j read" (flag = epoch + 1),
+//   3. waits (bounded) for the flags of those lower blocks, and
 //   4. writes the stage out.
-// Warps take chunks in increasing order and every warp of the cooperative
-// grid is resident, so the lowest unpublished chunk can always proceed: no
+// Warps take blocks in increasing order and every warp of the cooperative
+// grid is resident, so the lowest unpublished block can always proceed: no
 // deadlock. Each byte moved is read once and written once.
 #include "tria_internal.cuh"
 
@@ -136,35 +137,54 @@ __device__ __forceinline__ void warp_scatter(uint8_t* plane, int64_t row0, int r
   }
 }
 
-// Persistent compaction, one chunk per warp at a time. Work items are the
-// 32-row source chunks of all segments, enumerated segment-major; warp w of
-// the grid takes items w, w + W, w + 2W, ... in order. For its chunk a warp
-//   1. reads the chunk's kept-row list and the destination range,
-//   2. gathers the moving rows of every plane into its own shared-memory
-//      stage with cp.async, waits for them,
-//   3. publishes "chunk read" (flag = epoch + 1, release),
-//   4. waits (bounded) for the lower chunks whose rows its destination range
-//      covers, and
-//   5. writes the stage out to the contiguous destination rows.
-// Chunks only wait on lower chunks, which are taken earlier by resident warps
-// (cooperative launch): the lowest unpublished chunk can always proceed.
+// One work item: destination block j of segment sg, with this lane's keep
+// entry and the keep-index range [p0, p1) that reads the block's source rows.
+struct MoveItem {
+  int t, sg, j, a, p0, p1, n;
+};
+
+// Persistent compaction, one destination block per warp at a time. Items are
+// the destination blocks of all active segments, enumerated segment-major;
+// warp w of the grid takes items w, w + W, w + 2W, ... in order and loads the
+// next item's keep entries while it moves the current one. For its block a
+// warp
+//   1. gathers the moving rows of every plane into its own shared-memory
+//      stage with cp.async and waits for them,
+//   2. publishes "block read" (flag = epoch + 1; the reads are complete, so
+//      no fence is needed before the flag),
+//   3. waits (bounded) for the lower blocks that read its destination rows,
+//   4. writes the stage out to the contiguous destination rows.
 __global__ void k_move(const __grid_constant__ Pass P) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint32_t s_epoch, s_bad;
-  __shared__ int s_n[kMaxSegments];   // live rows of active segments, 0 otherwise
-  __shared__ int s_src[kMoveMaxWarps][kChunk];   // moving source rows of each warp's chunk
+  __shared__ int s_off[kMaxSegments + 1];   // first item of every segment
+  __shared__ int s_scan[40];
+  __shared__ int s_src[kMoveMaxWarps][kChunk];   // moving source rows of each warp's block
   const MoveStage L = move_stage_layout(P.k_rb, P.ks_rb, P.v_rb, P.vs_rb);
   if (threadIdx.x == 0) {
     s_epoch = ld_acquire_u32(&P.ctrl->epoch);
     s_bad = ld_acquire_u32(&P.ctrl->bad_keep);
   }
-  for (int sg = threadIdx.x; sg < P.n_seg; sg += blockDim.x) {
-    const SegView v = seg_view(P, sg);
-    s_n[sg] = v.active ? v.n : 0;
+  // destination blocks of the active segments, prefix-summed over segments
+  {
+    int carry = 0;
+    for (int base = 0; base < P.n_seg; base += blockDim.x) {
+      const int sg = base + threadIdx.x;
+      int nb = 0;
+      if (sg < P.n_seg) {
+        const SegView v = seg_view(P, sg);
+        nb = v.active ? (v.B + kChunk - 1) / kChunk : 0;
+      }
+      int tot;
+      const int before = block_exclusive_scan(nb, &tot, s_scan);
+      if (sg < P.n_seg) s_off[sg] = carry + before;
+      carry += tot;
+    }
+    if (threadIdx.x == 0) s_off[P.n_seg] = carry;
   }
   __syncthreads();
   const uint32_t tag = s_epoch + 1u;
-  const int total = P.n_seg * P.c_max;
+  const int total = s_off[P.n_seg];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nwarps_cta = blockDim.x >> 5;
   const int W = gridDim.x * nwarps_cta;
@@ -173,30 +193,51 @@ __global__ void k_move(const __grid_constant__ Pass P) {
   const PlaneMap mk = plane_map(P.k_rb, lane), mks = plane_map(P.ks_rb, lane), mv = plane_map(P.v_rb, lane),
                  mvs = plane_map(P.vs_rb, lane), mp = plane_map(4, lane);
 
+  int cur_sg = 0;
+  auto row0_of = [&](int sg) {
+    const int sq = sg / P.n_kv;
+    return P.seq[sq].row0 + (int64_t)(sg - sq * P.n_kv) * P.seq[sq].cap;
+  };
+  auto fetch = [&](int t, MoveItem& m) {
+    m.t = t;
+    if (t >= total) return;
+    while (s_off[cur_sg + 1] <= t) ++cur_sg;   // items are taken in increasing order
+    m.sg = cur_sg;
+    m.j = t - s_off[cur_sg];
+    const int B = P.seq[cur_sg / P.n_kv].budget;
+    const int i = m.j * kChunk + lane;
+    m.a = i < B ? __ldcg(&P.keep[row0_of(cur_sg) + i]) : -1;
+    const int* pre = P.prefix + (size_t)cur_sg * (P.c_max + 1);
+    m.p0 = __ldcg(&pre[m.j]);
+    m.p1 = __ldcg(&pre[m.j + 1]);
+    m.n = *((volatile const int32_t*)(P.n_live + cur_sg / P.n_kv));
+  };
+
   if (s_bad == 0) {
-    for (int t = blockIdx.x * nwarps_cta + warp; t < total; t += W) {
-      const int sg = t / P.c_max, c = t - sg * P.c_max;
-      const int n = s_n[sg];
-      if (c * kChunk >= n) continue;
+    MoveItem m;
+    fetch(blockIdx.x * nwarps_cta + warp, m);
+    while (m.t < total) {
+      const int sg = m.sg, j = m.j;
       const int sq = sg / P.n_kv;
-      const int64_t row0 = P.seq[sq].row0 + (int64_t)(sg - sq * P.n_kv) * P.seq[sq].cap;
+      const int64_t row0 = row0_of(sg);
       const int B = P.seq[sq].budget;
-      const int* pre = P.prefix + (size_t)sg * (P.c_max + 1);
-      const int i0 = __ldcg(&pre[c]), i1 = __ldcg(&pre[c + 1]);
-      const int nk = i1 - i0;
-      bool ok = i0 >= 0 && nk >= 0 && nk <= kChunk && i1 <= min(B, n);
-      // kept rows of the chunk: entry q in lane q
-      int a = -1;
-      if (ok && lane < nk) a = __ldcg(&P.keep[row0 + i0 + lane]);
-      const int lo_row = c * kChunk, hi_row = min(n, lo_row + kChunk);
-      ok = ok && !__any_sync(0xffffffffu, lane < nk && (a < lo_row || a >= hi_row));
+      const int n = m.n;
+      const int i0 = j * kChunk, cnt = min(kChunk, B - i0);
+      // every entry reads a row at or above its destination, inside the
+      // segment; the readers of this block's rows are at most 32 entries
+      // ending at or before the budget
+      const bool bad_entry = lane < cnt && (m.a < i0 + lane || m.a >= n);
+      const bool ok = !__any_sync(0xffffffffu, bad_entry) && m.p0 >= 0 && m.p0 <= m.p1 &&
+                      m.p1 - m.p0 <= kChunk && m.p1 <= B;
       if (!ok && lane == 0) report(P.ctrl, TRIA_ERR_INVALID_ARG, 0x10000000u | (uint32_t)sg);
-      // first kept entry whose row changes (all later ones change too)
-      const unsigned ma = __ballot_sync(0xffffffffu, ok && lane < nk && a != i0 + lane);
-      const int first = !ok ? 0 : (ma ? __ffs(ma) - 1 : nk);
-      const int nmove = ok ? nk - first : 0;
-      if (lane >= first && lane < nk) msrc[lane - first] = a;
+      // moving entries (keep[i] != i) are a suffix of the block
+      const unsigned mvm = __ballot_sync(0xffffffffu, ok && lane < cnt && m.a != i0 + lane);
+      const int first = mvm ? __ffs(mvm) - 1 : cnt;
+      const int nmove = ok ? cnt - first : 0;
+      if (lane >= first && lane < cnt) msrc[lane - first] = m.a;
       __syncwarp();
+      MoveItem nx;
+      fetch(m.t + W, nx);   // next item's keep entries load while this one moves
       if (nmove > 0) {
         warp_gather(P.k, row0, mk, stg + L.k, msrc, nmove);
         warp_gather(P.ks, row0, mks, stg + L.ks, msrc, nmove);
@@ -207,16 +248,14 @@ __global__ void k_move(const __grid_constant__ Pass P) {
       cp_async_commit();
       cp_async_wait<0>();
       __syncwarp();
-      // publish "read"; then wait for the lower chunks the destination range covers
+      // publish "read"; then wait for the lower blocks that read my destination rows
       uint32_t* flags = P.flags + (size_t)sg * P.c_max;
       int go = 0;
       if (lane == 0) {
-        __threadfence();
-        st_release_u32(&flags[c], tag);
+        st_relaxed_u32(&flags[j], tag);
         go = ok;
-        if (go && nmove > 0) {
-          const int dst0 = i0 + first;
-          const int lo = dst0 / kChunk, hi = min((i1 - 1) / kChunk, c - 1);
+        if (go && nmove > 0 && m.p1 > m.p0) {
+          const int lo = m.p0 / kChunk, hi = min((m.p1 - 1) / kChunk, j - 1);
           for (int cc = lo; cc <= hi; ++cc)
             if (!wait_flag_bounded(&flags[cc], tag, P.spin_limit)) {
               go = 0;
@@ -235,6 +274,7 @@ __global__ void k_move(const __grid_constant__ Pass P) {
         warp_scatter(reinterpret_cast<uint8_t*>(P.pos), row0, 4, stg + L.pos, dst0, nmove, lane);
       }
       __syncwarp();
+      m = nx;
     }
   }
 
@@ -324,9 +364,14 @@ cudaError_t launch_move(const Pass& P, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   int grid = sms * per_sm;
-  const int items = P.n_seg * P.c_max;
-  const int need = (items + warps - 1) / warps;
-  if (grid > need) grid = need;
+  // at most ceil(min(budget, capacity) / 32) destination blocks per segment
+  int64_t items = 0;
+  for (int s = 0; s < P.n_seqs; ++s) {
+    const int b = P.seq[s].budget < P.seq[s].cap ? P.seq[s].budget : P.seq[s].cap;
+    items += (int64_t)P.n_kv * ((b + kChunk - 1) / kChunk);
+  }
+  const int64_t need = (items + warps - 1) / warps;
+  if (grid > need) grid = (int)need;
   if (grid < 1) grid = 1;
   void* args[] = {const_cast<Pass*>(&P)};
   return cudaLaunchCooperativeKernel((const void*)k_move, dim3(grid), dim3(threads), args, (size_t)smem, st);

@@ -220,6 +220,10 @@ __device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+__device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // Bounded poll of a flag written by another CTA; false when the limit ran out.
 __device__ __forceinline__ bool wait_flag_bounded(const uint32_t* flag, uint32_t target, int limit) {
   for (int it = 0; it < limit; ++it) {
