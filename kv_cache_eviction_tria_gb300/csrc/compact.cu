@@ -355,7 +355,7 @@ cudaError_t launch_move(const Pass& P, cudaStream_t st) {
   const int threads = warps * 32;
   const int smem = warps * L.bytes;
   static const cudaError_t attr =
-      cudaFuncSetAttribute(k_move, cudaFuncAttributeMaxDynamicSharedMemorySize, kMoveSmemLimit);
+      set_smem_attrs(k_move, kMoveSmemLimit);
   if (attr != cudaSuccess) return attr;
   int dev = 0, sms = 0, per_sm = 0;
   cudaGetDevice(&dev);

@@ -154,6 +154,7 @@ __host__ __device__ inline ScoreGeom score_geom(int k_rb) {
   ScoreGeom g;
   g.R = kPieceBytes / k_rb;
   if (g.R > 64) g.R = 64;
+  if (g.R >= 16) g.R &= ~15;   // whole 16-row tiles for the tensor-core body
   if (g.R < 1) g.R = 1;
   g.stage = (g.R * k_rb + 15) & ~15;
   return g;
@@ -164,26 +165,12 @@ __host__ __device__ inline int score_smem_bytes_for(int k_rb) {
   return kScoreWarps * 2 * g.stage + kScoreWarps * 2 * 8 + 2 * (kMaxSegs + 1) * 4 + kMomTable + 16;
 }
 
-template <int KT, int G, int TPR, int PPT>
-__global__ void __launch_bounds__(kScoreThreads, 1) k_score(const __grid_constant__ Pass P) {
-  static_assert(PPT % 2 == 0, "pairs of frequencies");
-  static_assert(HeadReduce<Batch<KT, G, TPR, PPT>::kNV, TPR>::kOut <= 2, "moment table holds 2 slots");
-  using BT = Batch<KT, G, TPR, PPT>;
-  constexpr int kRowsPerStep = BT::kRowsPerStep;
-  constexpr int kRowsB = BT::kRowsB;
-  constexpr int kNV = BT::kNV;
-  using Red = HeadReduce<kNV, TPR>;
-  constexpr int kOut = Red::kOut;
-
-  extern __shared__ __align__(128) uint8_t smem[];
-  const ScoreGeom geo = score_geom(P.k_rb);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint8_t* ring = smem + (size_t)warp * 2 * geo.stage;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kScoreWarps * 2 * geo.stage) + warp * 2;
-  int* seg_first = reinterpret_cast<int*>(smem + (size_t)kScoreWarps * 2 * geo.stage + kScoreWarps * 2 * 8);
-  int* seg_rows = seg_first + (kMaxSegs + 1);   // live rows of each scored segment
-
-  // pieces of every segment, in segment order (skipped segments have none):
+// Segment tables (first piece and live rows of every scored segment, pieces
+// in segment order, skipped segments have none), the piece layout that the
+// consumer of the moment partials needs (CTA 0), and this warp's two ring
+// barriers. Called by every thread of the CTA.
+__device__ __forceinline__ void score_prologue(const Pass& P, const ScoreGeom& geo, int* seg_first, int* seg_rows,
+                                               uint64_t* bars, int lane) {
   // thread t counts segments [t*per_t, t*per_t + per_t), then a block scan
   {
     __shared__ int sbuf[40];
@@ -234,6 +221,28 @@ __global__ void __launch_bounds__(kScoreThreads, 1) k_score(const __grid_constan
     fence_mbar_init();
   }
   __syncthreads();
+}
+
+template <int KT, int G, int TPR, int PPT>
+__global__ void __launch_bounds__(kScoreThreads, 1) k_score(const __grid_constant__ Pass P) {
+  static_assert(PPT % 2 == 0, "pairs of frequencies");
+  static_assert(HeadReduce<Batch<KT, G, TPR, PPT>::kNV, TPR>::kOut <= 2, "moment table holds 2 slots");
+  using BT = Batch<KT, G, TPR, PPT>;
+  constexpr int kRowsPerStep = BT::kRowsPerStep;
+  constexpr int kRowsB = BT::kRowsB;
+  constexpr int kNV = BT::kNV;
+  using Red = HeadReduce<kNV, TPR>;
+  constexpr int kOut = Red::kOut;
+
+  extern __shared__ __align__(128) uint8_t smem[];
+  const ScoreGeom geo = score_geom(P.k_rb);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* ring = smem + (size_t)warp * 2 * geo.stage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kScoreWarps * 2 * geo.stage) + warp * 2;
+  int* seg_first = reinterpret_cast<int*>(smem + (size_t)kScoreWarps * 2 * geo.stage + kScoreWarps * 2 * 8);
+  int* seg_rows = seg_first + (kMaxSegs + 1);   // live rows of each scored segment
+
+  score_prologue(P, geo, seg_first, seg_rows, bars, lane);
 
   const int total = seg_first[P.n_seg];
   const int nwarps = gridDim.x * kScoreWarps;
@@ -477,6 +486,374 @@ __global__ void __launch_bounds__(kThreads) k_zscore(const __grid_constant__ Pas
   }
 }
 
+// ---------------------------------------------------------------------------
+// Tensor-core body (fp16 keys, head_dim a multiple of 64).
+//
+// The phase term sum_f Wr K[f] + Wi K[f+fc] is a contraction of the key rows
+// with a [head_dim x heads] weight matrix, and the keys are exact in fp16: it
+// runs as m16n8k16 MMAs (fp32 accumulation) against W split into an fp16 high
+// part and an fp16 remainder, scaled per head by a power of two so that both
+// parts are normal. The magnitude term sum_f M |k_f| is formed in fp32 from
+// the same key fragments and contracted with M by m16n8k8 tf32 MMAs, again on
+// a high part and its remainder. The columns of one n-tile are [high parts of
+// the G heads, remainders of the G heads], so a head's score is the sum of two
+// accumulator columns: fp32-level accuracy from half-precision operands.
+//
+// A warp computes 16 rows (one m-tile) at a time. Lane (g, q) = (lane / 4,
+// lane % 4) reads 16-byte granule q of the 64-byte step s of rows g and g + 8;
+// the MMA k-slots are mapped to the granule's elements (the same map in A and
+// B, which a contraction is free to permute), so no transposing load is
+// needed. Real and imaginary parts of a frequency sit in steps s and
+// s + S/2 at the same lane and register position.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t y;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// |k| of the 8 frequencies of one granule: real parts r, imaginary parts i
+__device__ __forceinline__ void granule_mag(const uint4& r, const uint4& i, float* m) {
+  const uint32_t rr[4] = {r.x, r.y, r.z, r.w}, ii[4] = {i.x, i.y, i.z, i.w};
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&rr[t]));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&ii[t]));
+    const float2 sq = __ffma2_rn(b, b, __fmul2_rn(a, a));
+    m[2 * t] = sqrt_approx(sq.x);
+    m[2 * t + 1] = sqrt_approx(sq.y);
+  }
+}
+
+template <int G, int S>
+struct TcShape {
+  static constexpr int NT = (2 * G + 7) / 8;   // n-tiles: G high-part columns, then G remainder columns
+  static constexpr bool kOk = S % 2 == 0 && NT * S <= 8;
+};
+
+template <int G, int S>
+__global__ void __launch_bounds__(kScoreThreads, 1) k_score_tc(const __grid_constant__ Pass P) {
+  using SH = TcShape<G, S>;
+  constexpr int NT = SH::NT;
+  constexpr int FC = 16 * S;   // frequency pairs (head_dim / 2)
+  static_assert(SH::kOk, "tensor-core body shape");
+
+  extern __shared__ __align__(128) uint8_t smem[];
+  const ScoreGeom geo = score_geom(P.k_rb);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* ring = smem + (size_t)warp * 2 * geo.stage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kScoreWarps * 2 * geo.stage) + warp * 2;
+  int* seg_first = reinterpret_cast<int*>(smem + (size_t)kScoreWarps * 2 * geo.stage + kScoreWarps * 2 * 8);
+  int* seg_rows = seg_first + (kMaxSegs + 1);
+
+  score_prologue(P, geo, seg_first, seg_rows, bars, lane);
+  // turn factors of the frequencies in shared memory (the moment-table area,
+  // which this body does not use)
+  unsigned long long* s_turns = reinterpret_cast<unsigned long long*>(seg_rows + (kMaxSegs + 1));
+  for (int i = threadIdx.x; i < FC; i += blockDim.x) s_turns[i] = P.turns[i];
+  __syncthreads();
+
+  const int total = seg_first[P.n_seg];
+  const int nwarps = gridDim.x * kScoreWarps;
+  const int per = (total + nwarps - 1) / nwarps;
+  const int gw = blockIdx.x * kScoreWarps + warp;
+  const int p_beg = min(total, gw * per), p_end = min(total, p_beg + per);
+  if (p_beg >= p_end) return;
+
+  auto seg_of = [&](int p, int from) {
+    int sg = from;
+    while (seg_first[sg + 1] <= p) ++sg;
+    return sg;
+  };
+  auto seg_row0 = [&](int sg) {
+    const int sq = sg / P.n_kv;
+    return P.seq[sq].row0 + (int64_t)(sg - sq * P.n_kv) * P.seq[sq].cap;
+  };
+  auto issue = [&](int p, int sg, int stage_i) {
+    const int r = (p - seg_first[sg]) * geo.R;
+    const int rows = min(geo.R, seg_rows[sg] - r);
+    const uint32_t bytes = (uint32_t)(rows * P.k_rb);
+    mbar_arrive_expect_tx(&bars[stage_i], bytes);
+    bulk_g2s(ring + stage_i * geo.stage, P.k + (size_t)(seg_row0(sg) + r) * P.k_rb, bytes, &bars[stage_i]);
+  };
+
+  const int g = lane >> 2, q = lane & 3;
+  // this lane's output: heads (oh, oh + 1) (one head when G == 1) of one row
+  // per m-tile (two rows when G == 8); with G <= 2 only lanes q < 2 write
+  constexpr int kHeads = G >= 2 ? 2 : 1;
+  const int oh = G == 8 ? 2 * q : (G == 4 ? 2 * (q & 1) : 0);
+  const bool owriter = G >= 4 || q < 2;
+
+  // B fragments of the current segment and the per-head unscaling factors.
+  // Lane (g, q) builds column g of every n-tile, which belongs to head hl.
+  const int hl = g < 2 * G ? g % G : 0;
+  uint32_t bp[S][NT][4];            // phase weights, fp16 pairs
+  uint32_t bm[S / 2][NT][4][2];     // magnitude weights, tf32
+  float unscale[kHeads];
+  auto load_consts = [&](const SegView& v) {
+    const unsigned long long pos = (unsigned long long)P.seq[v.s].cur_pos;
+    const float2* qe = P.qe + ((size_t)v.g * G + hl) * FC;
+    const float* mw = P.mw + ((size_t)v.g * G + hl) * FC;
+    // inputs of this lane's frequencies f = 32 s + 8 q + j (s < S / 2) of head
+    // hl, all loaded up front
+    float2 a[S / 2][8];
+    float m[S / 2][8];
+#pragma unroll
+    for (int s2 = 0; s2 < S / 2; ++s2)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int f = 32 * s2 + 8 * q + j;
+        a[s2][j] = qe[f];
+        m[s2][j] = mw[f];
+      }
+    // scale 2^e with max(|qbar E|, |M|) of the head (a bound of every weight,
+    // since |Wr|, |Wi| <= |qbar E|) in [2^14, 2^15): both fp16 parts stay
+    // normal; the four lanes of a column cover all frequencies
+    float amax = 0.f;
+#pragma unroll
+    for (int s2 = 0; s2 < S / 2; ++s2)
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(a[s2][j].x), fabsf(a[s2][j].y)), fabsf(m[s2][j])));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    int e = 0;
+    if (amax > 0.f && amax < INFINITY) e = 14 - ilogbf(amax);
+    e = max(-120, min(120, e));
+    const float scale = __int_as_float((127 + e) << 23);
+#pragma unroll
+    for (int s2 = 0; s2 < S / 2; ++s2) {
+      float wre_hi[8], wre_lo[8], wim_hi[8], wim_lo[8], wm_hi[8], wm_lo[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const unsigned long long x = s_turns[32 * s2 + 8 * q + j] * pos;   // exact turn fraction of w_f * p
+        float sn, cs;
+        sincospif((float)(int)(x >> 32) * 0x1p-31f, &sn, &cs);
+        const float wr = (a[s2][j].x * cs - a[s2][j].y * sn) * scale;
+        const float wi = (a[s2][j].x * sn + a[s2][j].y * cs) * scale;
+        const float ms = m[s2][j] * scale;
+        wre_hi[j] = __half2float(__float2half_rn(wr));
+        wre_lo[j] = wr - wre_hi[j];
+        wim_hi[j] = __half2float(__float2half_rn(wi));
+        wim_lo[j] = wi - wim_hi[j];
+        wm_hi[j] = __uint_as_float(to_tf32(ms));
+        wm_lo[j] = ms - wm_hi[j];
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int c = 8 * nt + g;
+        const bool live = c < 2 * G, rem = c >= G;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float r0 = !live ? 0.f : (rem ? wre_lo[2 * t] : wre_hi[2 * t]);
+          const float r1 = !live ? 0.f : (rem ? wre_lo[2 * t + 1] : wre_hi[2 * t + 1]);
+          const float i0 = !live ? 0.f : (rem ? wim_lo[2 * t] : wim_hi[2 * t]);
+          const float i1 = !live ? 0.f : (rem ? wim_lo[2 * t + 1] : wim_hi[2 * t + 1]);
+          const float m0 = !live ? 0.f : (rem ? wm_lo[2 * t] : wm_hi[2 * t]);
+          const float m1 = !live ? 0.f : (rem ? wm_lo[2 * t + 1] : wm_hi[2 * t + 1]);
+          bp[s2][nt][t] = pack_f16x2(r0, r1);
+          bp[s2 + S / 2][nt][t] = pack_f16x2(i0, i1);
+          bm[s2][nt][t][0] = __float_as_uint(m0);
+          bm[s2][nt][t][1] = __float_as_uint(m1);
+        }
+      }
+    }
+    // unscaling factors of the heads this lane writes: lane 4 h holds the
+    // exponent of head h (column h of n-tile 0)
+#pragma unroll
+    for (int k = 0; k < kHeads; ++k) {
+      const int eh = __shfl_sync(0xffffffffu, e, 4 * (oh + k));
+      unscale[k] = __int_as_float((127 - eh) << 23);
+    }
+  };
+
+  int seg = seg_of(p_beg, 0);
+  if (lane == 0) issue(p_beg, seg, 0);
+  SegView sv = seg_view(P, seg);
+  load_consts(sv);
+
+  Mom run_m[kHeads];
+#pragma unroll
+  for (int k = 0; k < kHeads; ++k) run_m[k] = Mom{0.f, 0.f, 0.f};
+  int run_first = p_beg;
+
+  auto flush_run = [&]() {
+    // butterfly over the lanes that carry the same heads (lanes without
+    // output carry zero counts), fixed order: deterministic. Afterwards the
+    // lanes with g == 0 and q < kWriters hold the run's moments of heads
+    // (oh, oh + 1).
+#pragma unroll
+    for (int k = 0; k < kHeads; ++k) {
+      if (!owriter) run_m[k] = Mom{0.f, 0.f, 0.f};
+#pragma unroll
+      for (int mask = 1; mask < 32; mask <<= 1) {
+        const bool same_heads = G == 8 ? mask >= 4 : (G == 4 ? mask >= 2 : true);
+        if (same_heads) run_m[k] = mom_merge(run_m[k], mom_shfl(run_m[k], mask));
+      }
+    }
+    constexpr int kWriters = G == 8 ? 4 : (G == 4 ? 2 : 1);
+    if (g == 0 && q < kWriters) {
+      ScoreChunk* part = P.schunk + run_first;
+#pragma unroll
+      for (int k = 0; k < kHeads; ++k) {
+        part->mean[oh + k] = run_m[k].mean;
+        part->m2[oh + k] = run_m[k].m2;
+      }
+      if (q == 0) part->n = (int)run_m[0].n;
+    }
+#pragma unroll
+    for (int k = 0; k < kHeads; ++k) run_m[k] = Mom{0.f, 0.f, 0.f};
+  };
+
+  for (int p = p_beg; p < p_end; ++p) {
+    const int kp = p - p_beg;
+    const int st = kp & 1;
+    // next piece into the other stage (its previous contents were consumed)
+    if (p + 1 < p_end && lane == 0) issue(p + 1, seg_of(p + 1, seg), st ^ 1);
+    if (seg_first[seg + 1] <= p) {
+      flush_run();
+      seg = seg_of(p, seg);
+      sv = seg_view(P, seg);
+      load_consts(sv);
+      run_first = p;
+    }
+    const int r0 = (p - seg_first[seg]) * geo.R;
+    const int rows = min(geo.R, seg_rows[seg] - r0);
+    const int64_t grow = seg_row0(seg) + r0;
+    if (!mbar_wait_bounded(&bars[st], (uint32_t)((kp >> 1) & 1), P.spin_limit)) {
+      if (lane == 0) report(P.ctrl, TRIA_ERR_TIMEOUT, (uint32_t)seg);
+      return;
+    }
+    const uint8_t* buf = ring + st * geo.stage;
+    // shifted sums of this piece for my output heads
+    float shift[kHeads], m1[kHeads], m2[kHeads], cnt[kHeads];
+#pragma unroll
+    for (int k = 0; k < kHeads; ++k) shift[k] = m1[k] = m2[k] = cnt[k] = 0.f;
+    auto emit = [&](int rr, const float (&x)[kHeads]) {
+      if (rr >= rows) return;
+      float y[kHeads];
+#pragma unroll
+      for (int k = 0; k < kHeads; ++k) y[k] = x[k] * unscale[k];
+      float* dst = P.raw + (size_t)(grow + rr) * G + oh;
+      if constexpr (kHeads == 2) *reinterpret_cast<float2*>(dst) = make_float2(y[0], y[1]);
+      else *dst = y[0];
+#pragma unroll
+      for (int k = 0; k < kHeads; ++k) {
+        if (cnt[k] == 0.f) shift[k] = y[k];
+        const float d = y[k] - shift[k];
+        m1[k] += d;
+        m2[k] = fmaf(d, d, m2[k]);
+        cnt[k] += 1.f;
+      }
+    };
+    for (int mt = 0; 16 * mt < rows; ++mt) {
+      // independent accumulator chains, summed at the end: real, imaginary,
+      // |k| high part, |k| remainder (two chains for head_dim > 128, where
+      // registers are short and the chains are long enough anyway)
+      constexpr bool kFour = S <= 4;
+      float acc[NT][4], acc_i[NT][4], acc_mh[NT][4], acc_ml[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int t = 0; t < 4; ++t) acc[nt][t] = acc_i[nt][t] = acc_mh[nt][t] = acc_ml[nt][t] = 0.f;
+      const uint8_t* rg = buf + (size_t)(16 * mt + g) * P.k_rb + 16 * q;
+      const uint8_t* rg8 = rg + (size_t)8 * P.k_rb;
+#pragma unroll
+      for (int s2 = 0; s2 < S / 2; ++s2) {
+        const uint4 kr0 = *reinterpret_cast<const uint4*>(rg + 64 * s2);
+        const uint4 kr8 = *reinterpret_cast<const uint4*>(rg8 + 64 * s2);
+        const uint4 ki0 = *reinterpret_cast<const uint4*>(rg + 64 * (s2 + S / 2));
+        const uint4 ki8 = *reinterpret_cast<const uint4*>(rg8 + 64 * (s2 + S / 2));
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          mma_f16(acc[nt], kr0.x, kr8.x, kr0.y, kr8.y, bp[s2][nt][0], bp[s2][nt][1]);
+          float(&di)[4] = kFour ? acc_i[nt] : acc[nt];
+          mma_f16(di, ki0.x, ki8.x, ki0.y, ki8.y, bp[s2 + S / 2][nt][0], bp[s2 + S / 2][nt][1]);
+          mma_f16(acc[nt], kr0.z, kr8.z, kr0.w, kr8.w, bp[s2][nt][2], bp[s2][nt][3]);
+          mma_f16(di, ki0.z, ki8.z, ki0.w, ki8.w, bp[s2 + S / 2][nt][2], bp[s2 + S / 2][nt][3]);
+        }
+        float mg0[8], mg8[8];
+        granule_mag(kr0, ki0, mg0);
+        granule_mag(kr8, ki8, mg8);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t h0 = to_tf32(mg0[2 * u]), h1 = to_tf32(mg8[2 * u]);
+          const uint32_t h2 = to_tf32(mg0[2 * u + 1]), h3 = to_tf32(mg8[2 * u + 1]);
+          const uint32_t l0 = __float_as_uint(mg0[2 * u] - __uint_as_float(h0));
+          const uint32_t l1 = __float_as_uint(mg8[2 * u] - __uint_as_float(h1));
+          const uint32_t l2 = __float_as_uint(mg0[2 * u + 1] - __uint_as_float(h2));
+          const uint32_t l3 = __float_as_uint(mg8[2 * u + 1] - __uint_as_float(h3));
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            mma_tf32(acc_mh[nt], h0, h1, h2, h3, bm[s2][nt][u][0], bm[s2][nt][u][1]);
+            float(&dl)[4] = kFour ? acc_ml[nt] : acc_mh[nt];
+            mma_tf32(dl, l0, l1, l2, l3, bm[s2][nt][u][0], bm[s2][nt][u][1]);
+          }
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          acc[nt][t] = kFour ? (acc[nt][t] + acc_i[nt][t]) + (acc_mh[nt][t] + acc_ml[nt][t]) : acc[nt][t] + acc_mh[nt][t];
+      // column pairs (high part, remainder) -> head scores
+      if constexpr (G == 8) {
+        emit(16 * mt + g, {acc[0][0] + acc[1][0], acc[0][1] + acc[1][1]});
+        emit(16 * mt + g + 8, {acc[0][2] + acc[1][2], acc[0][3] + acc[1][3]});
+      } else if constexpr (G == 4) {
+        float v[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) v[t] = acc[0][t] + __shfl_xor_sync(0xffffffffu, acc[0][t], 2);
+        if (q & 2) emit(16 * mt + g + 8, {v[2], v[3]});
+        else emit(16 * mt + g, {v[0], v[1]});
+      } else if constexpr (G == 2) {
+        float v[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) v[t] = acc[0][t] + __shfl_xor_sync(0xffffffffu, acc[0][t], 1);
+        if (q == 0) emit(16 * mt + g, {v[0], v[1]});
+        else if (q == 1) emit(16 * mt + g + 8, {v[2], v[3]});
+      } else {
+        const float a = acc[0][0] + acc[0][1], b = acc[0][2] + acc[0][3];
+        const float b_from0 = __shfl_xor_sync(0xffffffffu, b, 1);
+        if (q == 0) emit(16 * mt + g, {a});
+        else if (q == 1) emit(16 * mt + g + 8, {b_from0});
+      }
+    }
+    // this piece's moments -> the run's moments
+#pragma unroll
+    for (int k = 0; k < kHeads; ++k) {
+      Mom b;
+      b.n = cnt[k];
+      const float mean_d = cnt[k] > 0.f ? __fdividef(m1[k], cnt[k]) : 0.f;
+      b.mean = shift[k] + mean_d;
+      b.m2 = fmaxf(m2[k] - m1[k] * mean_d, 0.f);
+      run_m[k] = mom_merge(run_m[k], b);
+    }
+    __syncwarp();
+  }
+  flush_run();
+}
+
 size_t score_smem_bytes(const Pass& P) { return (size_t)score_smem_bytes_for(P.k_rb); }
 
 int score_pieces_max(int k_rb, int cap) {
@@ -499,7 +876,7 @@ cudaError_t launch_score_t(const Pass& P, cudaStream_t st) {
   auto kern = k_score<KT, G, TPR, PPT>;
   // the attribute is per function: set the largest size any layout needs, once
   static const cudaError_t attr =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmemMax);
+      set_smem_attrs(kern, kScoreSmemMax);
   if (attr != cudaSuccess) return attr;
   static const int sms = sm_count();
   kern<<<sms, kScoreThreads, smem, st>>>(P);
@@ -529,6 +906,52 @@ cudaError_t launch_score_g(const Pass& P, cudaStream_t st) {
   return cudaErrorInvalidValue;
 }
 
+template <int G, int S>
+cudaError_t launch_score_tc_t(const Pass& P, cudaStream_t st) {
+  const size_t smem = score_smem_bytes(P);
+  auto kern = k_score_tc<G, S>;
+  static const cudaError_t attr =
+      set_smem_attrs(kern, kScoreSmemMax);
+  if (attr != cudaSuccess) return attr;
+  static const int sms = sm_count();
+  kern<<<sms, kScoreThreads, smem, st>>>(P);
+  return cudaGetLastError();
+}
+
+// fp16 keys with head_dim a multiple of 64 and the B fragments in registers
+// (n-tiles x steps <= 8): the tensor-core body; false when it does not apply
+template <int G>
+bool launch_score_tc_g(const Pass& P, cudaStream_t st, cudaError_t* err) {
+  switch (P.hd) {
+    case 64: *err = launch_score_tc_t<G, 2>(P, st); return true;
+    case 128: *err = launch_score_tc_t<G, 4>(P, st); return true;
+    case 192:
+      if constexpr (TcShape<G, 6>::kOk) {
+        *err = launch_score_tc_t<G, 6>(P, st);
+        return true;
+      }
+      return false;
+    case 256:
+      if constexpr (TcShape<G, 8>::kOk) {
+        *err = launch_score_tc_t<G, 8>(P, st);
+        return true;
+      }
+      return false;
+  }
+  return false;
+}
+
+bool launch_score_tc(const Pass& P, cudaStream_t st, cudaError_t* err) {
+  if (P.k_type != TRIA_F16) return false;
+  switch (P.G) {
+    case 1: return launch_score_tc_g<1>(P, st, err);
+    case 2: return launch_score_tc_g<2>(P, st, err);
+    case 4: return launch_score_tc_g<4>(P, st, err);
+    case 8: return launch_score_tc_g<8>(P, st, err);
+  }
+  return false;
+}
+
 template <int KT>
 cudaError_t launch_score_k(const Pass& P, cudaStream_t st) {
   switch (P.G) {
@@ -544,6 +967,8 @@ cudaError_t launch_score_k(const Pass& P, cudaStream_t st) {
 
 cudaError_t launch_score(const Pass& P, cudaStream_t st) {
   if (P.n_seg > kMaxSegs) return cudaErrorInvalidValue;
+  cudaError_t e = cudaSuccess;
+  if (launch_score_tc(P, st, &e)) return e;
   switch (P.k_type) {
     case TRIA_F32: return launch_score_k<TRIA_F32>(P, st);
     case TRIA_F16: return launch_score_k<TRIA_F16>(P, st);

@@ -619,7 +619,7 @@ cudaError_t launch_select_cl(const Pass& P, bool write_keep, cudaStream_t st, in
   const int rpc_max = (((cap_max + kClusterCtas - 1) / kClusterCtas) + kChunk - 1) / kChunk * kChunk;
   const size_t smem = (size_t)rpc_max * 4;
   static const cudaError_t attr =
-      cudaFuncSetAttribute(k_select_cl<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kClMaxRowsPerCta * 4);
+      set_smem_attrs(k_select_cl<G>, kClMaxRowsPerCta * 4);
   if (attr != cudaSuccess) return attr;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(kClusterCtas, P.n_seg, 1);

@@ -353,6 +353,16 @@ __device__ void merge_segment_moments(const Pass& P, int seg, float* mu, float* 
   }
 }
 
+// Dynamic shared-memory limit and the largest shared-memory carveout of a
+// kernel: the stages of a pass then keep one L1 / shared split, and the SMs
+// need not switch it between them.
+template <typename Kernel>
+cudaError_t set_smem_attrs(Kernel* kern, int dyn_bytes) {
+  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_bytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+}
+
 // ---------------------------------------------------------------------------
 // grid barrier of a cooperative launch (all CTAs resident), bounded: after the
 // spin limit it records TRIA_ERR_TIMEOUT and lets the CTA go on (no hang)

@@ -48,6 +48,14 @@ SCORE_CASES = [
     dict(n_kv=2, group=4, hd=32, k_type="q8_0", v_type="q8_0", n_live=[100], capacity=[128], cur_pos=[77]),
     dict(n_kv=2, group=8, hd=128, k_type="f16", v_type="f16", n_live=[700], capacity=[700], cur_pos=[1 << 20],
          offsets=[1, 2, 3, 1000, -5]),
+    # fp16 shapes of the tensor-core body: one / two heads per group, head_dim
+    # 64 / 192 / 256, ragged 16-row tiles; hd 96 takes the fp32 body
+    dict(n_kv=3, group=1, hd=64, k_type="f16", v_type="f16", n_live=[37, 1, 16], capacity=[40, 8, 16],
+         cur_pos=[100, 3, 1 << 30]),
+    dict(n_kv=2, group=2, hd=192, k_type="f16", v_type="f32", n_live=[333], capacity=[350], cur_pos=[123457]),
+    dict(n_kv=1, group=4, hd=256, k_type="f16", v_type="f16", n_live=[1000, 17], capacity=[1024, 32],
+         cur_pos=[98765, 40]),
+    dict(n_kv=2, group=2, hd=96, k_type="f16", v_type="f16", n_live=[150], capacity=[160], cur_pos=[50]),
 ]
 
 
