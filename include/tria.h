@@ -217,7 +217,9 @@ tria_status tria_evict_profiled(const tria_stats* stats, int32_t layer, const tr
                                 float* stage_ms, int32_t* launches);
 
 /* Synchronises `stream`, returns the first device-detected error of the
- * calls since the last check (TRIA_OK if none) and clears it. */
+ * calls since the last check (TRIA_OK if none) and clears it. After
+ * TRIA_ERR_TIMEOUT a call may have stopped with its counters mid-way:
+ * re-initialise the workspace (tria_workspace_init) before the next call. */
 tria_status tria_device_status(void* ws, void* stream);
 
 /* Runs the bounded wait used by the compaction kernel on a flag that nothing

@@ -31,7 +31,7 @@ bool dtype_ok(int t) { return t == TRIA_F32 || t == TRIA_F16 || t == TRIA_Q8_0; 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 struct Layout {
-  size_t ctrl, seg, schunk, chunk, prefix, hist, flags, score, keep, raw, total;
+  size_t ctrl, seg, runs, chunk, prefix, hist, flags, score, keep, raw, total;
   int cs_rows, cs_max, c_max, n_seg;
   int64_t total_rows;
 };
@@ -61,8 +61,8 @@ Layout make_layout(const tria_layer_cache* c, int G) {
   off = up(off + sizeof(Ctrl));
   L.seg = off;
   off = up(off + (size_t)L.n_seg * sizeof(SegState));
-  L.schunk = off;
-  off = up(off + (size_t)L.n_seg * L.cs_max * sizeof(ScoreChunk));
+  L.runs = off;
+  off = up(off + (size_t)L.n_seg * kRunCols * L.cs_max * sizeof(float));
   L.chunk = off;
   off = up(off + (size_t)L.n_seg * L.c_max * sizeof(SelChunk));
   L.prefix = off;
@@ -171,7 +171,7 @@ void fill_pass(Pass& P, const tria_layer_cache* c, const tria_policy* p, const s
   uint8_t* w = (uint8_t*)ws;
   P.ctrl = (Ctrl*)(w + L.ctrl);
   P.seg = (SegState*)(w + L.seg);
-  P.schunk = (ScoreChunk*)(w + L.schunk);
+  P.runs = (float*)(w + L.runs);
   P.chunk = (SelChunk*)(w + L.chunk);
   P.prefix = (int32_t*)(w + L.prefix);
   P.hist = (uint32_t*)(w + L.hist);

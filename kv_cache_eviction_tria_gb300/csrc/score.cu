@@ -23,9 +23,8 @@
 //
 // Moments: each lane keeps shifted sums of the heads it ends up owning; a warp
 // merges them (Chan et al. pairwise update) into one partial per contiguous
-// run of a segment, stored at the run's first piece. The last warp to finish
-// a segment merges its runs in order (deterministic) into mean and
-// 1 / (std + 1e-6).
+// run of a segment, stored in the segment's run table (row = run index); the
+// consumer merges the runs into mean and 1 / (std + 1e-6).
 #include "tria_internal.cuh"
 
 namespace tria {
@@ -345,12 +344,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1) k_score(const __grid_constan
       Mom a{0.f, 0.f, 0.f};
       for (int e = 0; e < 32 * kOut; ++e)
         if (mhead[e] == lane) a = mom_merge(a, mtab[e]);
-      ScoreChunk* part = P.schunk + run_first;
-      part->mean[lane] = a.mean;
-      part->m2[lane] = a.m2;
-      if (lane == 0) part->n = (int)a.n;
+      float* tab = run_table(P, seg);
+      const int r = run_index(run_first, seg_first[seg], per);
+      tab[(1 + lane) * P.cs_max + r] = a.mean;
+      tab[(1 + kMaxG + lane) * P.cs_max + r] = a.m2;
+      if (lane == 0) tab[r] = a.n;
     }
-    __syncwarp();
 #pragma unroll
     for (int o = 0; o < kOut; ++o) run_m[o] = Mom{0.f, 0.f, 0.f};
   };
@@ -462,8 +461,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1) k_score(const __grid_constan
   flush_run();
 }
 
-// z-max score per live row: s = max_h (raw_h - mu_h) * inv_h. The CTA with
-// blockIdx.x == 0 of each segment also records mean / inv in the segment state.
+// z-max score per live row: s = max_h (raw_h - mu_h) * inv_h, with the
+// segment's moments merged from the run partials by each block.
 template <int G>
 __global__ void __launch_bounds__(kThreads) k_zscore(const __grid_constant__ Pass P) {
   const int seg = blockIdx.y;
@@ -471,11 +470,7 @@ __global__ void __launch_bounds__(kThreads) k_zscore(const __grid_constant__ Pas
   if (!sv.valid || (P.only_active && !sv.active)) return;
   if ((int)blockIdx.x * 1024 >= sv.n) return;
   float mu[G], inv[G];
-  merge_segment_moments<G>(P, seg, mu, inv);
-  if (blockIdx.x == 0 && threadIdx.x < G) {
-    P.seg[seg].mu[threadIdx.x] = mu[threadIdx.x];
-    P.seg[seg].inv[threadIdx.x] = inv[threadIdx.x];
-  }
+  block_segment_moments<G>(P, seg, mu, inv);
   const int r_end = min(sv.n, (int)(blockIdx.x + 1) * 1024);
   for (int r = blockIdx.x * 1024 + threadIdx.x; r < r_end; r += blockDim.x) {
     const float* rp = P.raw + (size_t)(sv.row0 + r) * G;
@@ -713,13 +708,14 @@ __global__ void __launch_bounds__(kScoreThreads, 1) k_score_tc(const __grid_cons
     }
     constexpr int kWriters = G == 8 ? 4 : (G == 4 ? 2 : 1);
     if (g == 0 && q < kWriters) {
-      ScoreChunk* part = P.schunk + run_first;
+      float* tab = run_table(P, seg);
+      const int r = run_index(run_first, seg_first[seg], per);
 #pragma unroll
       for (int k = 0; k < kHeads; ++k) {
-        part->mean[oh + k] = run_m[k].mean;
-        part->m2[oh + k] = run_m[k].m2;
+        tab[(1 + oh + k) * P.cs_max + r] = run_m[k].mean;
+        tab[(1 + kMaxG + oh + k) * P.cs_max + r] = run_m[k].m2;
       }
-      if (q == 0) part->n = (int)run_m[0].n;
+      if (q == 0) tab[r] = run_m[0].n;
     }
 #pragma unroll
     for (int k = 0; k < kHeads; ++k) run_m[k] = Mom{0.f, 0.f, 0.f};

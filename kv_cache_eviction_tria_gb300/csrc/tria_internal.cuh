@@ -59,12 +59,11 @@ struct SegState {
 };
 static_assert(sizeof(SegState) == 128, "SegState layout");
 
-struct ScoreChunk {      // moments of one contiguous run of score pieces
-  float mean[kMaxG];
-  float m2[kMaxG];
-  int32_t n;
-  int32_t pad[3];
-};
+// Moment partials of the score runs: per segment, columns of cs_max floats
+// (count, then the mean of head 0 .. kMaxG-1, then the sum of squared
+// deviations of head 0 .. kMaxG-1), run r of the segment in row r, so that a
+// warp reads them with coalesced loads.
+constexpr int kRunCols = 1 + 2 * kMaxG;
 
 struct SelChunk {        // counts of one chunk
   int32_t n_gt;          // candidates with key > T
@@ -108,7 +107,7 @@ struct Pass {
   // workspace
   Ctrl* ctrl;
   SegState* seg;
-  ScoreChunk* schunk;                  // [n_seg * cs_max] indexed by global score piece
+  float* runs;                         // [n_seg][kRunCols][cs_max] score-run moment partials
   SelChunk* chunk;                     // [n_seg][c_max]
   int32_t* prefix;                     // [n_seg][c_max + 1] kept rows before each chunk
   uint32_t* hist;                      // [n_seg][kHistBins]
@@ -303,54 +302,104 @@ __device__ __forceinline__ Mom mom_shfl(Mom a, int mask) {
   return b;
 }
 
-// Merge of a segment's run partials (written by k_score) into mean and
-// 1 / (std + 1e-6), by one CTA: thread t merges runs t, t + blockDim, ...
-// (Chan et al. pairwise update, fp32), then a butterfly over the lanes of each
-// warp and a second butterfly over the warp results, which every warp
-// computes identically (lane 0's result is broadcast), so no serial chain and
-// one barrier. Runs start at the segment's first piece and at each multiple
-// of the per-warp piece count after it. Deterministic for a given layout.
-template <int G>
-__device__ void merge_segment_moments(const Pass& P, int seg, float* mu, float* inv) {
-  __shared__ Mom red[32][G];   // up to 32 warps
-  const int s0 = __ldcg(&P.seg[seg].piece_first), s1 = __ldcg(&P.seg[seg].piece_end);
-  const int per = max(1, __ldcg(&P.seg[seg].piece_per));
+__device__ __forceinline__ float* run_table(const Pass& P, int seg) {
+  return P.runs + (size_t)seg * kRunCols * P.cs_max;
+}
+
+// index, within its segment, of the score run that starts at piece p
+__device__ __forceinline__ int run_index(int p, int s0, int per) {
+  return p == s0 ? 0 : (p - (s0 / per + 1) * per) / per + 1;
+}
+
+// Number of score runs of a segment whose pieces are [s0, s1) when every warp
+// takes `per` consecutive pieces: runs start at s0 and at each multiple of
+// per after it.
+__device__ __forceinline__ int segment_runs(int s0, int s1, int per) {
+  if (s1 <= s0) return 0;
   const int first_mult = (s0 / per + 1) * per;
-  const int nruns = s1 > s0 ? 1 + (s1 > first_mult ? (s1 - first_mult + per - 1) / per : 0) : 0;
-  Mom acc[G];
+  return 1 + (s1 > first_mult ? (s1 - first_mult + per - 1) / per : 0);
+}
+
+// Segment moments from the score-run partials (count n_i, mean m_i, sum of
+// squared deviations M2_i), by exact identities with a shift c (run 0's mean):
+// with d_i = m_i - c,
+//   N = sum n_i,  mean = c + (sum n_i d_i) / N,
+//   N var = sum (M2_i + n_i d_i^2) - (sum n_i d_i)^2 / N,
+// so partial sums over any split of the runs add up (no division per run),
+// and the shifted sums stay small (fp32).
+//
+// block_run_sums: the sums over runs [r_lo, r_hi) of one segment by a whole
+// block: thread t adds runs r_lo + t, r_lo + t + blockDim, ... in order, then
+// fixed butterflies over lanes and warps (deterministic). out (shared, 1 + 2G
+// floats) = {N, sum n d_h, sum (M2 + n d^2)_h}. All threads of the block call it.
+template <int G>
+__device__ void block_run_sums(const Pass& P, int seg, int r_lo, int r_hi, const float* c, float* out) {
+  __shared__ float red[32][1 + 2 * G];
+  const float* tab = run_table(P, seg);
+  const int cs = P.cs_max;
+  float v[1 + 2 * G];
 #pragma unroll
-  for (int h = 0; h < G; ++h) acc[h] = Mom{0.f, 0.f, 0.f};
-  for (int i = threadIdx.x; i < nruns; i += blockDim.x) {
-    const int j = i == 0 ? s0 : first_mult + (i - 1) * per;
-    const ScoreChunk* pp = P.schunk + j;
-    const float n = (float)__ldcg(&pp->n);
+  for (int k = 0; k < 1 + 2 * G; ++k) v[k] = 0.f;
+  for (int r = r_lo + threadIdx.x; r < r_hi; r += blockDim.x) {
+    const float n = __ldcg(&tab[r]);
+    v[0] += n;
 #pragma unroll
-    for (int h = 0; h < G; ++h) acc[h] = mom_merge(acc[h], Mom{n, __ldcg(&pp->mean[h]), __ldcg(&pp->m2[h])});
+    for (int h = 0; h < G; ++h) {
+      const float d = n > 0.f ? __ldcg(&tab[(1 + h) * cs + r]) - c[h] : 0.f;
+      const float nd = n * d;
+      v[1 + h] += nd;
+      v[1 + G + h] += fmaf(nd, d, __ldcg(&tab[(1 + kMaxG + h) * cs + r]));
+    }
   }
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (int)(blockDim.x >> 5);
 #pragma unroll
   for (int mask = 1; mask < 32; mask <<= 1)
 #pragma unroll
-    for (int h = 0; h < G; ++h) acc[h] = mom_merge(acc[h], mom_shfl(acc[h], mask));
+    for (int k = 0; k < 1 + 2 * G; ++k) v[k] += __shfl_xor_sync(0xffffffffu, v[k], mask);
   if (lane == 0)
 #pragma unroll
-    for (int h = 0; h < G; ++h) red[warp][h] = acc[h];
+    for (int k = 0; k < 1 + 2 * G; ++k) red[warp][k] = v[k];
   __syncthreads();
-  const int nw = (int)(blockDim.x >> 5);
-#pragma unroll
-  for (int h = 0; h < G; ++h) acc[h] = lane < nw ? red[lane][h] : Mom{0.f, 0.f, 0.f};
-#pragma unroll
-  for (int mask = 1; mask < 32; mask <<= 1)
-#pragma unroll
-    for (int h = 0; h < G; ++h) acc[h] = mom_merge(acc[h], mom_shfl(acc[h], mask));
+  if (threadIdx.x < 1 + 2 * G) {
+    float a = 0.f;
+    for (int w = 0; w < nw; ++w) a += red[w][threadIdx.x];
+    out[threadIdx.x] = a;
+  }
+  __syncthreads();
+}
+
+// mean and 1 / (std + 1e-6) of each head from the sums of all runs
+template <int G>
+__device__ __forceinline__ void moments_from_sums(const float* c, const float* sums, float* mu, float* inv) {
+  const float n = fmaxf(sums[0], 1.f);
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-    const float n = __shfl_sync(0xffffffffu, acc[h].n, 0);
-    const float m = __shfl_sync(0xffffffffu, acc[h].mean, 0);
-    const float m2 = __shfl_sync(0xffffffffu, acc[h].m2, 0);
-    mu[h] = m;
-    inv[h] = 1.0f / (sqrtf(m2 / fmaxf(n, 1.f)) + kZEps);
+    const float md = sums[1 + h] / n;
+    const float var = fmaxf(sums[1 + G + h] / n - md * md, 0.f);
+    mu[h] = c[h] + md;
+    inv[h] = 1.0f / (sqrtf(var) + kZEps);
   }
+}
+
+// the shift of the segment's sums (run 0's mean) and its run count
+template <int G>
+__device__ __forceinline__ int segment_shift(const Pass& P, int seg, float* c) {
+  const int s0 = __ldcg(&P.seg[seg].piece_first), s1 = __ldcg(&P.seg[seg].piece_end);
+  const int per = max(1, __ldcg(&P.seg[seg].piece_per));
+  const float* tab = run_table(P, seg);
+#pragma unroll
+  for (int h = 0; h < G; ++h) c[h] = __ldcg(&tab[(1 + h) * P.cs_max]);
+  return segment_runs(s0, s1, per);
+}
+
+// mean and 1 / (std + 1e-6) of the segment's heads, merged by one block
+template <int G>
+__device__ void block_segment_moments(const Pass& P, int seg, float* mu, float* inv) {
+  __shared__ float sums[1 + 2 * G];
+  float c[G];
+  const int nr = segment_shift<G>(P, seg, c);
+  block_run_sums<G>(P, seg, 0, nr, c, sums);
+  moments_from_sums<G>(c, sums, mu, inv);
 }
 
 // Dynamic shared-memory limit and the largest shared-memory carveout of a
