@@ -34,7 +34,11 @@ constexpr int kScoreThreads = kScoreWarps * 32;
 constexpr int kPieceBytes = 8192;
 constexpr int kMaxSegs = 1024;
 constexpr int kMomTable = kScoreWarps * 32 * 2 * (12 + 4);   // per-warp [lane][slot] moments + head
-constexpr int kScoreSmemMax = kScoreWarps * 2 * kPieceBytes + kScoreWarps * 2 * 8 + 2 * (kMaxSegs + 1) * 4 + kMomTable + 16;
+// q8_0 block scales of a piece (rows x head_dim / 16 bytes <= piece bytes / 16)
+constexpr int kScaleStage = kPieceBytes / 16;
+constexpr int kScaleRing = kScoreWarps * 2 * kScaleStage;
+constexpr int kScoreSmemMax =
+    kScoreWarps * 2 * kPieceBytes + kScoreWarps * 2 * 8 + 2 * (kMaxSegs + 1) * 4 + kMomTable + kScaleRing + 16;
 
 __device__ __forceinline__ float sqrt_approx(float x) {
   float y;
@@ -161,7 +165,7 @@ __host__ __device__ inline ScoreGeom score_geom(int k_rb) {
 
 __host__ __device__ inline int score_smem_bytes_for(int k_rb) {
   const ScoreGeom g = score_geom(k_rb);
-  return kScoreWarps * 2 * g.stage + kScoreWarps * 2 * 8 + 2 * (kMaxSegs + 1) * 4 + kMomTable + 16;
+  return kScoreWarps * 2 * g.stage + kScoreWarps * 2 * 8 + 2 * (kMaxSegs + 1) * 4 + kMomTable + kScaleRing + 16;
 }
 
 // Segment tables (first piece and live rows of every scored segment, pieces
@@ -527,6 +531,33 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// Four signed 8-bit values (one 32-bit word) as two fp16 pairs, exactly: with
+// u = x + 128 in a byte, the fp16 bit pattern 0x6400 | u is 1024 + u, and
+// subtracting 1152 leaves x (both steps exact in fp16).
+__device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140u);
+  const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342u);
+  const __half2 bias = __halves2half2(__ushort_as_half((unsigned short)0x6480u), __ushort_as_half((unsigned short)0x6480u));
+  const __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+  const __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+  lo = *reinterpret_cast<const uint32_t*>(&ha);
+  hi = *reinterpret_cast<const uint32_t*>(&hb);
+}
+
+// |k| of 8 frequencies from fp16 pairs of block values times their scales:
+// real parts r * dr, imaginary parts i * di
+__device__ __forceinline__ void q8_mag(const uint32_t* r, const uint32_t* i, float dr, float di, float* m) {
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const float2 a = __fmul2_rn(__half22float2(*reinterpret_cast<const __half2*>(&r[t])), make_float2(dr, dr));
+    const float2 b = __fmul2_rn(__half22float2(*reinterpret_cast<const __half2*>(&i[t])), make_float2(di, di));
+    const float2 sq = __ffma2_rn(b, b, __fmul2_rn(a, a));
+    m[2 * t] = sqrt_approx(sq.x);
+    m[2 * t + 1] = sqrt_approx(sq.y);
+  }
+}
+
 // |k| of the 8 frequencies of one granule: real parts r, imaginary parts i
 __device__ __forceinline__ void granule_mag(const uint4& r, const uint4& i, float* m) {
   const uint32_t rr[4] = {r.x, r.y, r.z, r.w}, ii[4] = {i.x, i.y, i.z, i.w};
@@ -546,8 +577,10 @@ struct TcShape {
   static constexpr bool kOk = S % 2 == 0 && NT * S <= 8;
 };
 
-template <int G, int S>
+template <int KT, int G, int S>
 __global__ void __launch_bounds__(kScoreThreads, 1) k_score_tc(const __grid_constant__ Pass P) {
+  static_assert(KT == TRIA_F16 || KT == TRIA_Q8_0, "fp16 or q8_0 keys");
+  constexpr bool kQ8 = KT == TRIA_Q8_0;
   using SH = TcShape<G, S>;
   constexpr int NT = SH::NT;
   constexpr int FC = 16 * S;   // frequency pairs (head_dim / 2)
@@ -560,6 +593,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1) k_score_tc(const __grid_cons
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kScoreWarps * 2 * geo.stage) + warp * 2;
   int* seg_first = reinterpret_cast<int*>(smem + (size_t)kScoreWarps * 2 * geo.stage + kScoreWarps * 2 * 8);
   int* seg_rows = seg_first + (kMaxSegs + 1);
+
+  // q8_0: this warp's two stages of block scales, after the moment table
+  uint8_t* sc_ring = smem + (size_t)kScoreWarps * 2 * geo.stage + kScoreWarps * 2 * 8 + 2 * (kMaxSegs + 1) * 4 +
+                     kMomTable + (size_t)warp * 2 * kScaleStage;
 
   score_prologue(P, geo, seg_first, seg_rows, bars, lane);
   // turn factors of the frequencies in shared memory (the moment-table area,
@@ -590,6 +627,16 @@ __global__ void __launch_bounds__(kScoreThreads, 1) k_score_tc(const __grid_cons
     const uint32_t bytes = (uint32_t)(rows * P.k_rb);
     mbar_arrive_expect_tx(&bars[stage_i], bytes);
     bulk_g2s(ring + stage_i * geo.stage, P.k + (size_t)(seg_row0(sg) + r) * P.k_rb, bytes, &bars[stage_i]);
+  };
+  // q8_0, all lanes: the block scales of piece p (rows x head_dim / 16 bytes,
+  // 4-byte async copies), one commit group per piece
+  auto issue_scales = [&](int p, int sg, int stage_i) {
+    const int r = (p - seg_first[sg]) * geo.R;
+    const int rows = min(geo.R, seg_rows[sg] - r);
+    const uint8_t* src = P.ks + (size_t)(seg_row0(sg) + r) * P.ks_rb;
+    uint8_t* dst = sc_ring + stage_i * kScaleStage;
+    for (int u = lane; u < rows * P.ks_rb / 4; u += 32) cp_async4(dst + 4 * u, src + 4 * u);
+    cp_async_commit();
   };
 
   const int g = lane >> 2, q = lane & 3;
@@ -684,6 +731,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) k_score_tc(const __grid_cons
 
   int seg = seg_of(p_beg, 0);
   if (lane == 0) issue(p_beg, seg, 0);
+  if constexpr (kQ8) issue_scales(p_beg, seg, 0);
   SegView sv = seg_view(P, seg);
   load_consts(sv);
 
@@ -726,6 +774,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1) k_score_tc(const __grid_cons
     const int st = kp & 1;
     // next piece into the other stage (its previous contents were consumed)
     if (p + 1 < p_end && lane == 0) issue(p + 1, seg_of(p + 1, seg), st ^ 1);
+    if constexpr (kQ8) {
+      if (p + 1 < p_end) issue_scales(p + 1, seg_of(p + 1, seg), st ^ 1);
+      else cp_async_commit();   // keep one group per piece
+    }
     if (seg_first[seg + 1] <= p) {
       flush_run();
       seg = seg_of(p, seg);
@@ -741,6 +793,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1) k_score_tc(const __grid_cons
       return;
     }
     const uint8_t* buf = ring + st * geo.stage;
+    const uint8_t* scb = sc_ring + st * kScaleStage;
+    if constexpr (kQ8) {
+      cp_async_wait<1>();   // this piece's scales (the next piece's may still be in flight)
+      __syncwarp();
+    }
     // shifted sums of this piece for my output heads
     float shift[kHeads], m1[kHeads], m2[kHeads], cnt[kHeads];
 #pragma unroll
@@ -772,38 +829,96 @@ __global__ void __launch_bounds__(kScoreThreads, 1) k_score_tc(const __grid_cons
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int t = 0; t < 4; ++t) acc[nt][t] = acc_i[nt][t] = acc_mh[nt][t] = acc_ml[nt][t] = 0.f;
-      const uint8_t* rg = buf + (size_t)(16 * mt + g) * P.k_rb + 16 * q;
-      const uint8_t* rg8 = rg + (size_t)8 * P.k_rb;
-#pragma unroll
-      for (int s2 = 0; s2 < S / 2; ++s2) {
-        const uint4 kr0 = *reinterpret_cast<const uint4*>(rg + 64 * s2);
-        const uint4 kr8 = *reinterpret_cast<const uint4*>(rg8 + 64 * s2);
-        const uint4 ki0 = *reinterpret_cast<const uint4*>(rg + 64 * (s2 + S / 2));
-        const uint4 ki8 = *reinterpret_cast<const uint4*>(rg8 + 64 * (s2 + S / 2));
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          mma_f16(acc[nt], kr0.x, kr8.x, kr0.y, kr8.y, bp[s2][nt][0], bp[s2][nt][1]);
-          float(&di)[4] = kFour ? acc_i[nt] : acc[nt];
-          mma_f16(di, ki0.x, ki8.x, ki0.y, ki8.y, bp[s2 + S / 2][nt][0], bp[s2 + S / 2][nt][1]);
-          mma_f16(acc[nt], kr0.z, kr8.z, kr0.w, kr8.w, bp[s2][nt][2], bp[s2][nt][3]);
-          mma_f16(di, ki0.z, ki8.z, ki0.w, ki8.w, bp[s2 + S / 2][nt][2], bp[s2 + S / 2][nt][3]);
+      if constexpr (!kQ8) {
+        const uint8_t* rg = buf + (size_t)(16 * mt + g) * P.k_rb + 16 * q;
+        const uint8_t* rg8 = rg + (size_t)8 * P.k_rb;
+  #pragma unroll
+        for (int s2 = 0; s2 < S / 2; ++s2) {
+          const uint4 kr0 = *reinterpret_cast<const uint4*>(rg + 64 * s2);
+          const uint4 kr8 = *reinterpret_cast<const uint4*>(rg8 + 64 * s2);
+          const uint4 ki0 = *reinterpret_cast<const uint4*>(rg + 64 * (s2 + S / 2));
+          const uint4 ki8 = *reinterpret_cast<const uint4*>(rg8 + 64 * (s2 + S / 2));
+  #pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            mma_f16(acc[nt], kr0.x, kr8.x, kr0.y, kr8.y, bp[s2][nt][0], bp[s2][nt][1]);
+            float(&di)[4] = kFour ? acc_i[nt] : acc[nt];
+            mma_f16(di, ki0.x, ki8.x, ki0.y, ki8.y, bp[s2 + S / 2][nt][0], bp[s2 + S / 2][nt][1]);
+            mma_f16(acc[nt], kr0.z, kr8.z, kr0.w, kr8.w, bp[s2][nt][2], bp[s2][nt][3]);
+            mma_f16(di, ki0.z, ki8.z, ki0.w, ki8.w, bp[s2 + S / 2][nt][2], bp[s2 + S / 2][nt][3]);
+          }
+          float mg0[8], mg8[8];
+          granule_mag(kr0, ki0, mg0);
+          granule_mag(kr8, ki8, mg8);
+  #pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t h0 = to_tf32(mg0[2 * u]), h1 = to_tf32(mg8[2 * u]);
+            const uint32_t h2 = to_tf32(mg0[2 * u + 1]), h3 = to_tf32(mg8[2 * u + 1]);
+            const uint32_t l0 = __float_as_uint(mg0[2 * u] - __uint_as_float(h0));
+            const uint32_t l1 = __float_as_uint(mg8[2 * u] - __uint_as_float(h1));
+            const uint32_t l2 = __float_as_uint(mg0[2 * u + 1] - __uint_as_float(h2));
+            const uint32_t l3 = __float_as_uint(mg8[2 * u + 1] - __uint_as_float(h3));
+  #pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              mma_tf32(acc_mh[nt], h0, h1, h2, h3, bm[s2][nt][u][0], bm[s2][nt][u][1]);
+              float(&dl)[4] = kFour ? acc_ml[nt] : acc_mh[nt];
+              mma_tf32(dl, l0, l1, l2, l3, bm[s2][nt][u][0], bm[s2][nt][u][1]);
+            }
+          }
         }
-        float mg0[8], mg8[8];
-        granule_mag(kr0, ki0, mg0);
-        granule_mag(kr8, ki8, mg8);
+      } else {
+        // q8_0: a 32-value block is one step s (bytes 32 s .. 32 s + 32 of the
+        // row); its two MMAs go to a fresh accumulator scaled by the block's
+        // scale of each row, and |k| uses the scaled values
+        const uint8_t* rg = buf + (size_t)(16 * mt + g) * P.k_rb + 8 * q;
+        const uint8_t* rg8 = rg + (size_t)8 * P.k_rb;
+        const __half* sg0 = reinterpret_cast<const __half*>(scb + (size_t)(16 * mt + g) * P.ks_rb);
+        const __half* sg8 = reinterpret_cast<const __half*>(scb + (size_t)(16 * mt + g + 8) * P.ks_rb);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t h0 = to_tf32(mg0[2 * u]), h1 = to_tf32(mg8[2 * u]);
-          const uint32_t h2 = to_tf32(mg0[2 * u + 1]), h3 = to_tf32(mg8[2 * u + 1]);
-          const uint32_t l0 = __float_as_uint(mg0[2 * u] - __uint_as_float(h0));
-          const uint32_t l1 = __float_as_uint(mg8[2 * u] - __uint_as_float(h1));
-          const uint32_t l2 = __float_as_uint(mg0[2 * u + 1] - __uint_as_float(h2));
-          const uint32_t l3 = __float_as_uint(mg8[2 * u + 1] - __uint_as_float(h3));
+        for (int s2 = 0; s2 < S / 2; ++s2) {
+          const uint2 wr0 = *reinterpret_cast<const uint2*>(rg + 32 * s2);
+          const uint2 wr8 = *reinterpret_cast<const uint2*>(rg8 + 32 * s2);
+          const uint2 wi0 = *reinterpret_cast<const uint2*>(rg + 32 * (s2 + S / 2));
+          const uint2 wi8 = *reinterpret_cast<const uint2*>(rg8 + 32 * (s2 + S / 2));
+          const float dr0 = __half2float(sg0[s2]), dr8 = __half2float(sg8[s2]);
+          const float di0 = __half2float(sg0[s2 + S / 2]), di8 = __half2float(sg8[s2 + S / 2]);
+          uint32_t ar0[4], ar8[4], ai0[4], ai8[4];
+          i8x4_to_h2x2(wr0.x, ar0[0], ar0[1]);
+          i8x4_to_h2x2(wr0.y, ar0[2], ar0[3]);
+          i8x4_to_h2x2(wr8.x, ar8[0], ar8[1]);
+          i8x4_to_h2x2(wr8.y, ar8[2], ar8[3]);
+          i8x4_to_h2x2(wi0.x, ai0[0], ai0[1]);
+          i8x4_to_h2x2(wi0.y, ai0[2], ai0[3]);
+          i8x4_to_h2x2(wi8.x, ai8[0], ai8[1]);
+          i8x4_to_h2x2(wi8.y, ai8[2], ai8[3]);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            mma_tf32(acc_mh[nt], h0, h1, h2, h3, bm[s2][nt][u][0], bm[s2][nt][u][1]);
-            float(&dl)[4] = kFour ? acc_ml[nt] : acc_mh[nt];
-            mma_tf32(dl, l0, l1, l2, l3, bm[s2][nt][u][0], bm[s2][nt][u][1]);
+            float tr[4] = {0.f, 0.f, 0.f, 0.f}, ti[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_f16(tr, ar0[0], ar8[0], ar0[1], ar8[1], bp[s2][nt][0], bp[s2][nt][1]);
+            mma_f16(ti, ai0[0], ai8[0], ai0[1], ai8[1], bp[s2 + S / 2][nt][0], bp[s2 + S / 2][nt][1]);
+            mma_f16(tr, ar0[2], ar8[2], ar0[3], ar8[3], bp[s2][nt][2], bp[s2][nt][3]);
+            mma_f16(ti, ai0[2], ai8[2], ai0[3], ai8[3], bp[s2 + S / 2][nt][2], bp[s2 + S / 2][nt][3]);
+            acc[nt][0] = fmaf(tr[0], dr0, fmaf(ti[0], di0, acc[nt][0]));
+            acc[nt][1] = fmaf(tr[1], dr0, fmaf(ti[1], di0, acc[nt][1]));
+            acc[nt][2] = fmaf(tr[2], dr8, fmaf(ti[2], di8, acc[nt][2]));
+            acc[nt][3] = fmaf(tr[3], dr8, fmaf(ti[3], di8, acc[nt][3]));
+          }
+          float mg0[8], mg8[8];
+          q8_mag(ar0, ai0, dr0, di0, mg0);
+          q8_mag(ar8, ai8, dr8, di8, mg8);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t h0 = to_tf32(mg0[2 * u]), h1 = to_tf32(mg8[2 * u]);
+            const uint32_t h2 = to_tf32(mg0[2 * u + 1]), h3 = to_tf32(mg8[2 * u + 1]);
+            const uint32_t l0 = __float_as_uint(mg0[2 * u] - __uint_as_float(h0));
+            const uint32_t l1 = __float_as_uint(mg8[2 * u] - __uint_as_float(h1));
+            const uint32_t l2 = __float_as_uint(mg0[2 * u + 1] - __uint_as_float(h2));
+            const uint32_t l3 = __float_as_uint(mg8[2 * u + 1] - __uint_as_float(h3));
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              mma_tf32(acc_mh[nt], h0, h1, h2, h3, bm[s2][nt][u][0], bm[s2][nt][u][1]);
+              float(&dl)[4] = kFour ? acc_ml[nt] : acc_mh[nt];
+              mma_tf32(dl, l0, l1, l2, l3, bm[s2][nt][u][0], bm[s2][nt][u][1]);
+            }
           }
         }
       }
@@ -902,10 +1017,10 @@ cudaError_t launch_score_g(const Pass& P, cudaStream_t st) {
   return cudaErrorInvalidValue;
 }
 
-template <int G, int S>
+template <int KT, int G, int S>
 cudaError_t launch_score_tc_t(const Pass& P, cudaStream_t st) {
   const size_t smem = score_smem_bytes(P);
-  auto kern = k_score_tc<G, S>;
+  auto kern = k_score_tc<KT, G, S>;
   static const cudaError_t attr =
       set_smem_attrs(kern, kScoreSmemMax);
   if (attr != cudaSuccess) return attr;
@@ -914,22 +1029,23 @@ cudaError_t launch_score_tc_t(const Pass& P, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// fp16 keys with head_dim a multiple of 64 and the B fragments in registers
-// (n-tiles x steps <= 8): the tensor-core body; false when it does not apply
-template <int G>
+// fp16 or q8_0 keys with head_dim a multiple of 64 and the B fragments in
+// registers (n-tiles x steps <= 8): the tensor-core body; false when it does
+// not apply
+template <int KT, int G>
 bool launch_score_tc_g(const Pass& P, cudaStream_t st, cudaError_t* err) {
   switch (P.hd) {
-    case 64: *err = launch_score_tc_t<G, 2>(P, st); return true;
-    case 128: *err = launch_score_tc_t<G, 4>(P, st); return true;
+    case 64: *err = launch_score_tc_t<KT, G, 2>(P, st); return true;
+    case 128: *err = launch_score_tc_t<KT, G, 4>(P, st); return true;
     case 192:
       if constexpr (TcShape<G, 6>::kOk) {
-        *err = launch_score_tc_t<G, 6>(P, st);
+        *err = launch_score_tc_t<KT, G, 6>(P, st);
         return true;
       }
       return false;
     case 256:
       if constexpr (TcShape<G, 8>::kOk) {
-        *err = launch_score_tc_t<G, 8>(P, st);
+        *err = launch_score_tc_t<KT, G, 8>(P, st);
         return true;
       }
       return false;
@@ -937,14 +1053,20 @@ bool launch_score_tc_g(const Pass& P, cudaStream_t st, cudaError_t* err) {
   return false;
 }
 
-bool launch_score_tc(const Pass& P, cudaStream_t st, cudaError_t* err) {
-  if (P.k_type != TRIA_F16) return false;
+template <int KT>
+bool launch_score_tc_k(const Pass& P, cudaStream_t st, cudaError_t* err) {
   switch (P.G) {
-    case 1: return launch_score_tc_g<1>(P, st, err);
-    case 2: return launch_score_tc_g<2>(P, st, err);
-    case 4: return launch_score_tc_g<4>(P, st, err);
-    case 8: return launch_score_tc_g<8>(P, st, err);
+    case 1: return launch_score_tc_g<KT, 1>(P, st, err);
+    case 2: return launch_score_tc_g<KT, 2>(P, st, err);
+    case 4: return launch_score_tc_g<KT, 4>(P, st, err);
+    case 8: return launch_score_tc_g<KT, 8>(P, st, err);
   }
+  return false;
+}
+
+bool launch_score_tc(const Pass& P, cudaStream_t st, cudaError_t* err) {
+  if (P.k_type == TRIA_F16) return launch_score_tc_k<TRIA_F16>(P, st, err);
+  if (P.k_type == TRIA_Q8_0) return launch_score_tc_k<TRIA_Q8_0>(P, st, err);
   return false;
 }
 

@@ -56,6 +56,10 @@ SCORE_CASES = [
     dict(n_kv=1, group=4, hd=256, k_type="f16", v_type="f16", n_live=[1000, 17], capacity=[1024, 32],
          cur_pos=[98765, 40]),
     dict(n_kv=2, group=2, hd=96, k_type="f16", v_type="f16", n_live=[150], capacity=[160], cur_pos=[50]),
+    # q8_0 keys on the tensor-core body: block scales per 32 values, ragged tiles
+    dict(n_kv=1, group=8, hd=64, k_type="q8_0", v_type="f16", n_live=[77, 300], capacity=[80, 320],
+         cur_pos=[123, 99999]),
+    dict(n_kv=2, group=1, hd=256, k_type="q8_0", v_type="q8_0", n_live=[333], capacity=[340], cur_pos=[7777]),
 ]
 
 
