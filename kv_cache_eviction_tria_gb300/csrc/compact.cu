@@ -218,6 +218,9 @@ __global__ void k_move(const __grid_constant__ Pass P) {
       __syncwarp();
       MoveItem nx;
       fetch(m.t + W, nx);   // next item's keep entries load while this one moves
+      // the previous item's bulk stores must have read the stage
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
       if (nmove > 0) {
         warp_gather(P.k, row0, mk, stg + L.k, msrc, nmove);
         warp_gather(P.ks, row0, mks, stg + L.ks, msrc, nmove);
@@ -247,9 +250,16 @@ __global__ void k_move(const __grid_constant__ Pass P) {
       go = __shfl_sync(0xffffffffu, go, 0);
       if (go && nmove > 0) {
         const int dst0 = i0 + first;
-        warp_scatter(P.k, row0, P.k_rb, stg + L.k, dst0, nmove, lane);
+        // key and value rows: one TMA bulk store per plane of the contiguous
+        // destination rows (off the L1 path the gathers use); the small
+        // planes with plain stores
+        if (lane == 0) {
+          fence_proxy_async_smem();
+          bulk_s2g(P.k + (size_t)(row0 + dst0) * P.k_rb, stg + L.k, (uint32_t)(nmove * P.k_rb));
+          bulk_s2g(P.v + (size_t)(row0 + dst0) * P.v_rb, stg + L.v, (uint32_t)(nmove * P.v_rb));
+          bulk_commit();
+        }
         warp_scatter(P.ks, row0, P.ks_rb, stg + L.ks, dst0, nmove, lane);
-        warp_scatter(P.v, row0, P.v_rb, stg + L.v, dst0, nmove, lane);
         warp_scatter(P.vs, row0, P.vs_rb, stg + L.vs, dst0, nmove, lane);
         warp_scatter(reinterpret_cast<uint8_t*>(P.pos), row0, 4, stg + L.pos, dst0, nmove, lane);
       }
@@ -258,6 +268,7 @@ __global__ void k_move(const __grid_constant__ Pass P) {
     }
   }
 
+  if (lane == 0) bulk_wait_all();   // this warp's bulk stores are complete
   // the last CTA to finish sets n_live and resets the call's counters
   __syncthreads();
   if (threadIdx.x == 0) {
