@@ -121,50 +121,46 @@ __device__ __forceinline__ void warp_scatter(uint8_t* plane, int64_t row0, int r
 // entry and the keep-index range [p0, p1) that reads the block's source rows.
 struct MoveItem {
   int t, sg, j, a, p0, p1, n;
+  bool valid;   // block j exists in segment sg (an active segment with j < its block count)
 };
 
-// Persistent compaction, one destination block per warp at a time. Items are
-// the destination blocks of all active segments, enumerated segment-major;
-// warp w of the grid takes items w, w + W, w + 2W, ... in order and loads the
-// next item's keep entries while it moves the current one. For its block a
-// warp
+// Persistent compaction, one destination block per warp at a time. Item t is
+// block t / n_seg of segment t % n_seg (block-major; items past a segment's
+// block count are empty); warp w of the grid takes items w, w + W, w + 2W, ...
+// in order and loads the next item's keep entries while it moves the current
+// one. For its block a warp
 //   1. gathers the moving rows of every plane into its own shared-memory
 //      stage with cp.async and waits for them,
 //   2. publishes "block read" (flag = epoch + 1; the reads are complete, so
 //      no fence is needed before the flag),
 //   3. waits (bounded) for the lower blocks that read its destination rows,
-//   4. writes the stage out to the contiguous destination rows.
+//   4. writes the stage out to the contiguous destination rows (TMA bulk
+//      stores for key and value rows).
 __global__ void k_move(const __grid_constant__ Pass P) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint32_t s_epoch, s_bad;
-  __shared__ int s_off[kMaxSegments + 1];   // first item of every segment
-  __shared__ int s_scan[40];
+  __shared__ int s_nb[kMaxSegments];   // destination blocks of every segment (0: inactive)
+  __shared__ int s_nbmax;
   __shared__ int s_src[kMoveMaxWarps][kChunk];   // moving source rows of each warp's block
   const MoveStage L = move_stage_layout(P.k_rb, P.ks_rb, P.v_rb, P.vs_rb);
   if (threadIdx.x == 0) {
     s_epoch = ld_acquire_u32(&P.ctrl->epoch);
     s_bad = ld_acquire_u32(&P.ctrl->bad_keep);
   }
-  // destination blocks of the active segments, prefix-summed over segments
-  {
-    int carry = 0;
-    for (int base = 0; base < P.n_seg; base += blockDim.x) {
-      const int sg = base + threadIdx.x;
-      int nb = 0;
-      if (sg < P.n_seg) {
-        const SegView v = seg_view(P, sg);
-        nb = v.active ? (v.B + kChunk - 1) / kChunk : 0;
-      }
-      int tot;
-      const int before = block_exclusive_scan(nb, &tot, s_scan);
-      if (sg < P.n_seg) s_off[sg] = carry + before;
-      carry += tot;
-    }
-    if (threadIdx.x == 0) s_off[P.n_seg] = carry;
+  // destination blocks of the active segments; items are enumerated
+  // block-major (block j of every segment before block j + 1 of any), so a
+  // block's readers - blocks near j * B / n of the same segment - come in
+  // earlier rounds of the grid, not beside it
+  if (threadIdx.x == 0) s_nbmax = 0;
+  __syncthreads();
+  for (int sg = threadIdx.x; sg < P.n_seg; sg += blockDim.x) {
+    const SegView v = seg_view(P, sg);
+    s_nb[sg] = v.active ? (v.B + kChunk - 1) / kChunk : 0;
+    atomicMax(&s_nbmax, s_nb[sg]);
   }
   __syncthreads();
   const uint32_t tag = s_epoch + 1u;
-  const int total = s_off[P.n_seg];
+  const int total = P.n_seg * s_nbmax;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nwarps_cta = blockDim.x >> 5;
   const int W = gridDim.x * nwarps_cta;
@@ -173,30 +169,37 @@ __global__ void k_move(const __grid_constant__ Pass P) {
   const PlaneMap mk = plane_map(P.k_rb, lane), mks = plane_map(P.ks_rb, lane), mv = plane_map(P.v_rb, lane),
                  mvs = plane_map(P.vs_rb, lane), mp = plane_map(4, lane);
 
-  int cur_sg = 0;
   auto row0_of = [&](int sg) {
     const int sq = sg / P.n_kv;
     return P.seq[sq].row0 + (int64_t)(sg - sq * P.n_kv) * P.seq[sq].cap;
   };
   auto fetch = [&](int t, MoveItem& m) {
     m.t = t;
+    m.valid = false;
     if (t >= total) return;
-    while (s_off[cur_sg + 1] <= t) ++cur_sg;   // items are taken in increasing order
-    m.sg = cur_sg;
-    m.j = t - s_off[cur_sg];
-    const int B = P.seq[cur_sg / P.n_kv].budget;
+    m.sg = t % P.n_seg;
+    m.j = t / P.n_seg;
+    if (m.j >= s_nb[m.sg]) return;
+    m.valid = true;
+    const int B = P.seq[m.sg / P.n_kv].budget;
     const int i = m.j * kChunk + lane;
-    m.a = i < B ? __ldcg(&P.keep[row0_of(cur_sg) + i]) : -1;
-    const int* pre = P.prefix + (size_t)cur_sg * (P.c_max + 1);
+    m.a = i < B ? __ldcg(&P.keep[row0_of(m.sg) + i]) : -1;
+    const int* pre = P.prefix + (size_t)m.sg * (P.c_max + 1);
     m.p0 = __ldcg(&pre[m.j]);
     m.p1 = __ldcg(&pre[m.j + 1]);
-    m.n = *((volatile const int32_t*)(P.n_live + cur_sg / P.n_kv));
+    m.n = *((volatile const int32_t*)(P.n_live + m.sg / P.n_kv));
   };
 
   if (s_bad == 0) {
     MoveItem m;
     fetch(blockIdx.x * nwarps_cta + warp, m);
     while (m.t < total) {
+      if (!m.valid) {   // no such block in this segment
+        MoveItem nx;
+        fetch(m.t + W, nx);
+        m = nx;
+        continue;
+      }
       const int sg = m.sg, j = m.j;
       const int sq = sg / P.n_kv;
       const int64_t row0 = row0_of(sg);
