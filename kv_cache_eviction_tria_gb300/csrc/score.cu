@@ -168,6 +168,23 @@ __host__ __device__ inline int score_smem_bytes_for(int k_rb) {
   return kScoreWarps * 2 * g.stage + kScoreWarps * 2 * 8 + 2 * (kMaxSegs + 1) * 4 + kMomTable + kScaleRing + 16;
 }
 
+// Ask L2 for this layer's weight inputs (qbar E, M, turn factors: a few tens
+// of KB) before the key stream starts, so that the warps' weight loads hit L2
+// instead of queueing in DRAM behind the first pieces. Lines are dealt over
+// all threads of the grid.
+__device__ __forceinline__ void prefetch_layer_stats(const Pass& P) {
+  const size_t n = (size_t)P.n_kv * P.G * P.fc;
+  const size_t lines_qe = (n * sizeof(float2) + 127) / 128, lines_mw = (n * sizeof(float) + 127) / 128,
+               lines_t = ((size_t)P.fc * 8 + 127) / 128;
+  const size_t total = lines_qe + lines_mw + lines_t;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const char* a = i < lines_qe ? reinterpret_cast<const char*>(P.qe) + 128 * i
+                    : i < lines_qe + lines_mw ? reinterpret_cast<const char*>(P.mw) + 128 * (i - lines_qe)
+                                              : reinterpret_cast<const char*>(P.turns) + 128 * (i - lines_qe - lines_mw);
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+  }
+}
+
 // Segment tables (first piece and live rows of every scored segment, pieces
 // in segment order, skipped segments have none), the piece layout that the
 // consumer of the moment partials needs (CTA 0), and this warp's two ring
@@ -245,6 +262,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) k_score(const __grid_constan
   int* seg_first = reinterpret_cast<int*>(smem + (size_t)kScoreWarps * 2 * geo.stage + kScoreWarps * 2 * 8);
   int* seg_rows = seg_first + (kMaxSegs + 1);   // live rows of each scored segment
 
+  prefetch_layer_stats(P);
   score_prologue(P, geo, seg_first, seg_rows, bars, lane);
 
   const int total = seg_first[P.n_seg];
@@ -598,6 +616,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) k_score_tc(const __grid_cons
   uint8_t* sc_ring = smem + (size_t)kScoreWarps * 2 * geo.stage + kScoreWarps * 2 * 8 + 2 * (kMaxSegs + 1) * 4 +
                      kMomTable + (size_t)warp * 2 * kScaleStage;
 
+  prefetch_layer_stats(P);
   score_prologue(P, geo, seg_first, seg_rows, bars, lane);
   // turn factors of the frequencies in shared memory (the moment-table area,
   // which this body does not use)
