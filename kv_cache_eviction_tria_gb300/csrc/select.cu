@@ -358,8 +358,6 @@ struct ClShared {
   int info[4];                  // prefix, kr after the current pass
   int cnt[2];                   // ties, strict keeps (gt + protected) of this CTA
   int warp_tie[kClThreads / 32], warp_keep[kClThreads / 32];
-  float msum[1 + 2 * kMaxG];    // this CTA's sums of the segment's score runs
-  float mtot[1 + 2 * kMaxG];    // the cluster's sums
 };
 
 // the G raw scores of one row (vector loads; rows are G consecutive floats,
@@ -466,22 +464,10 @@ __global__ void __launch_bounds__(kClThreads) k_select_cl(const __grid_constant_
     };
     float mu[GG], inv[GG];
     load_batch(r0 + threadIdx.x);
-    if constexpr (G > 0) {
-      // segment moments: CTA `rank` sums 1/8 of the score runs, the eight
-      // partial sums are added in rank order through distributed shared memory
-      float c[G];
-      const int nr = segment_shift<G>(P, seg, c);
-      const int per_rank = (nr + kClusterCtas - 1) / kClusterCtas;
-      block_run_sums<G>(P, seg, min(nr, rank * per_rank), min(nr, (rank + 1) * per_rank), c, sh.msum);
-      cluster.sync();
-      if (threadIdx.x < 1 + 2 * G) {
-        float a = 0.f;
-        for (int q = 0; q < kClusterCtas; ++q) a += cluster.map_shared_rank(sh.msum, q)[threadIdx.x];
-        sh.mtot[threadIdx.x] = a;
-      }
-      __syncthreads();
-      moments_from_sums<G>(c, sh.mtot, mu, inv);
-    }
+    // segment moments: every CTA of the cluster sums all of the segment's
+    // score runs itself (shifted sums, one coalesced load round), so no
+    // cluster exchange is needed
+    if constexpr (G > 0) block_segment_moments<G>(P, seg, mu, inv);
     for (int base = r0 + threadIdx.x; base < r1; base += U * kClThreads) {
       if (base != r0 + (int)threadIdx.x) load_batch(base);
 #pragma unroll
