@@ -48,7 +48,7 @@ __host__ __device__ inline MoveStage move_stage_layout(int k_rb, int ks_rb, int 
   return L;
 }
 
-constexpr int kMoveSmemLimit = 200 * 1024;
+constexpr int kMoveSmemLimit = 216 * 1024;   // with ~6.5 KB of static tables: under the 227 KB per CTA
 constexpr int kMoveMaxWarps = 16;
 
 __host__ __device__ inline int move_warps(const MoveStage& L) {
