@@ -42,6 +42,12 @@ Readings where the pages are silent:
   B < sink + window is an error.
 * Compaction writes kept row i (ascending original order) to row i of K, V,
   the q8_0 scales and pos; rows at or past B keep their old contents.
+* Calibration ([Doc] §2: per-layer, per-head statistics of the pre-RoPE
+  queries, "mean query directions + per-frequency importance weights";
+  §5 Phase C: q_mean / q_abs arrays [layers][heads][frequency pairs]):
+  over the calibration tokens t of one layer, q_mean_{h,f} = mean_t of the
+  complex pair Q_t[h][f] + i Q_t[h][f + hd/2], q_abs_{h,f} = mean_t of its
+  modulus.
 """
 from __future__ import annotations
 
@@ -269,3 +275,23 @@ def should_evict(n_live: int, budget: int, interval: int) -> bool:
     ([Worklog] "Final apples-to-apples check": trigger = kv_budget + divide_length;
     [Doc] §1 "--tri-interval")."""
     return n_live >= budget + interval
+
+
+# ---------------------------------------------------------------------------
+# calibration ([Doc] §2 Calibration file; §5 Phase C q_mean / q_abs layout)
+# ---------------------------------------------------------------------------
+
+def calibrate(q: np.ndarray) -> tuple:
+    """Statistics of a stream of pre-RoPE queries q[tokens][heads][head_dim]:
+    (q_mean [heads][fc][2] as (re, im), q_abs [heads][fc]), means over the
+    tokens of the NEOX pairs q[.., f] + i q[.., f + hd/2] and of their moduli."""
+    q = np.asarray(q, dtype=np.float64)
+    t, h, hd = q.shape
+    if t == 0:
+        raise ValueError("no calibration tokens")
+    fc = hd // 2
+    z = q[:, :, :fc] + 1j * q[:, :, fc:]
+    mean = z.mean(axis=0)
+    q_mean = np.stack([mean.real, mean.imag], axis=-1)
+    q_abs = np.abs(z).mean(axis=0)
+    return q_mean, q_abs

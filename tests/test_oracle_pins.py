@@ -399,3 +399,53 @@ def test_golden_worklog_prompt_accounting():
     assert not O.should_evict(gold["native_rows_before"] - 1, gold["kv_budget"],
                               gold["divide_length"])
     assert gold["dense_cache_length"] - gold["native_rows_before"] == gold["gap"]
+
+
+# ---------------------------------------------------------------------------
+# calibration statistics ([Doc] §2; q_mean / q_abs layout of §5 Phase C)
+# ---------------------------------------------------------------------------
+
+def test_calibrate_constant_stream():
+    # every token the same: the means are that token's pairs and moduli
+    rng = np.random.default_rng(21)
+    one = rng.standard_normal((1, 3, 8))
+    q = np.repeat(one, 5, axis=0)
+    q_mean, q_abs = O.calibrate(q)
+    assert q_mean.shape == (3, 4, 2) and q_abs.shape == (3, 4)
+    np.testing.assert_allclose(q_mean[..., 0], one[0, :, :4], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(q_mean[..., 1], one[0, :, 4:], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(q_abs, np.hypot(one[0, :, :4], one[0, :, 4:]), rtol=1e-15)
+
+
+def test_calibrate_literal_loop():
+    # brute force: a per-token, per-pair loop with math.hypot
+    rng = np.random.default_rng(22)
+    q = rng.standard_normal((7, 2, 6))
+    q_mean, q_abs = O.calibrate(q)
+    for h in range(2):
+        for f in range(3):
+            re = sum(q[t, h, f] for t in range(7)) / 7
+            im = sum(q[t, h, f + 3] for t in range(7)) / 7
+            ab = sum(math.hypot(q[t, h, f], q[t, h, f + 3]) for t in range(7)) / 7
+            assert abs(q_mean[h, f, 0] - re) < 1e-14 and abs(q_mean[h, f, 1] - im) < 1e-14
+            assert abs(q_abs[h, f] - ab) < 1e-14
+
+
+def test_calibrate_concatenation_and_resultant_length():
+    # the means over two batches weight the batch means by their token counts,
+    # and |q_mean| <= q_abs (mean resultant length <= 1) with equality for a
+    # stream whose pairs all point the same way
+    rng = np.random.default_rng(23)
+    a, b = rng.standard_normal((4, 2, 8)), rng.standard_normal((9, 2, 8))
+    ma, aa = O.calibrate(a)
+    mb, ab = O.calibrate(b)
+    m, ab_all = O.calibrate(np.concatenate([a, b]))
+    np.testing.assert_allclose(m, (4 * ma + 9 * mb) / 13, rtol=1e-13)
+    np.testing.assert_allclose(ab_all, (4 * aa + 9 * ab) / 13, rtol=1e-13)
+    assert np.all(np.hypot(m[..., 0], m[..., 1]) <= ab_all + 1e-15)
+    scale = rng.uniform(0.5, 2.0, size=(6, 1, 1))
+    aligned = scale * np.repeat(rng.standard_normal((1, 2, 8)), 6, axis=0)
+    ma2, aa2 = O.calibrate(aligned)
+    np.testing.assert_allclose(np.hypot(ma2[..., 0], ma2[..., 1]), aa2, rtol=1e-13)
+    # M = q_abs - |q_mean| is then zero: no magnitude term
+    np.testing.assert_allclose(O.mlr_weight(ma2.reshape(1, 2, 4, 2)[0], aa2), 0.0, atol=1e-13)
