@@ -227,6 +227,38 @@ tria_status tria_device_status(void* ws, void* stream);
  * (TRIA_ERR_TIMEOUT expected). Synchronises `stream`. For failure tests. */
 tria_status tria_selftest_bounded_wait(int32_t spin_limit, void* ws, size_t ws_bytes, void* stream);
 
+/* ---- Calibration statistics --------------------------------------------
+ * The scoring statistics of one layer from a stream of its pre-RoPE queries
+ * ([Doc] §2 Calibration file: per-layer, per-head statistics "collected from
+ * a calibration corpus", accumulated from the pre-RoPE Q of every layer;
+ * §5 Phase C: q_mean / q_abs arrays laid out [layers][heads][frequency
+ * pairs]). With NEOX pairs z = q[f] + i q[f + head_dim/2]:
+ *   q_mean[h][f] = mean over tokens of z   (stored as re, im)
+ *   q_abs[h][f]  = mean over tokens of |z|
+ * Feed batches with tria_calib_accumulate, then tria_calib_finish.
+ *
+ * tria_calib_accumulate:
+ *   q      device, [n_tokens][n_q_heads][head_dim] values of q_type (TRIA_F32
+ *          or TRIA_F16), row-major, 4-byte aligned; read only.
+ *   acc    device, double [n_q_heads][head_dim/2][3] running sums (re, im,
+ *          modulus), owned by the caller and zeroed before the first batch;
+ *          the batch's sums are added to it (fp32 within a block of tokens,
+ *          fp64 across blocks; the order of the fp64 additions is not fixed,
+ *          so repeated runs may differ in the last bits of acc).
+ *   Errors: TRIA_ERR_INVALID_ARG (null acc, null q with n_tokens > 0,
+ *   n_tokens < 0, n_q_heads < 1, misalignment), TRIA_ERR_UNSUPPORTED (q_type
+ *   other than f32 / f16, head_dim odd, below 2 or above 512). n_tokens = 0
+ *   adds nothing (q may then be null).
+ * tria_calib_finish:
+ *   acc       as above; n_tokens = tokens accumulated (> 0).
+ *   q_mean    device float [n_q_heads][head_dim/2][2]; q_abs device float
+ *             [n_q_heads][head_dim/2]: one layer's rows of the tria_stats_desc
+ *             arrays. Errors as above. */
+tria_status tria_calib_accumulate(const void* q, tria_dtype q_type, int32_t n_tokens, int32_t n_q_heads,
+                                  int32_t head_dim, double* acc, void* stream);
+tria_status tria_calib_finish(const double* acc, int64_t n_tokens, int32_t n_q_heads, int32_t head_dim,
+                              float* q_mean, float* q_abs, void* stream);
+
 const char* tria_status_string(tria_status status);
 int32_t tria_version(void);
 

@@ -33,8 +33,8 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_BUDGET, ERR_CUDA, ERR_WORKSPACE, ERR_T
 EXPORTS = (
     "tria_gate_check", "tria_budget_rows", "tria_should_evict", "tria_load_stats", "tria_free_stats",
     "tria_workspace_size", "tria_workspace_init", "tria_score", "tria_select", "tria_compact",
-    "tria_evict", "tria_evict_profiled", "tria_select_noalloc", "tria_device_status", "tria_selftest_bounded_wait", "tria_status_string",
-    "tria_version",
+    "tria_evict", "tria_evict_profiled", "tria_select_noalloc", "tria_device_status", "tria_selftest_bounded_wait",
+    "tria_calib_accumulate", "tria_calib_finish", "tria_status_string", "tria_version",
 )
 
 
@@ -119,6 +119,10 @@ def load_library(path: str | None = None):
     lib.tria_device_status.restype = i32
     lib.tria_selftest_bounded_wait.argtypes = [i32, vp, sz, vp]
     lib.tria_selftest_bounded_wait.restype = i32
+    lib.tria_calib_accumulate.argtypes = [vp, i32, i32, i32, i32, vp, vp]
+    lib.tria_calib_accumulate.restype = i32
+    lib.tria_calib_finish.argtypes = [vp, i64, i32, i32, vp, vp, vp]
+    lib.tria_calib_finish.restype = i32
     lib.tria_status_string.argtypes = [i32]
     lib.tria_status_string.restype = ctypes.c_char_p
     lib.tria_version.argtypes = []
@@ -338,6 +342,35 @@ def device_status(ws, stream=None) -> int:
 def selftest_bounded_wait(spin_limit: int, ws, stream=None) -> int:
     wp, wb = _ws(ws)
     return load_library().tria_selftest_bounded_wait(spin_limit, wp, wb, _stream_handle(stream))
+
+
+def calib_accumulate(q, acc, *, stream=None):
+    """tria_calib_accumulate: add the sums of a batch of pre-RoPE queries
+    q[tokens][heads][head_dim] (float32 or float16 CUDA tensor) to acc
+    (float64 CUDA tensor [heads][head_dim/2][3], zeroed before the first batch)."""
+    import torch
+    if q.dim() != 3:
+        raise ValueError("q must be [tokens][heads][head_dim]")
+    t, h, hd = q.shape
+    qt = {torch.float32: F32, torch.float16: F16}.get(q.dtype)
+    if qt is None:
+        raise ValueError("q must be float32 or float16")
+    if acc.dtype != torch.float64 or tuple(acc.shape) != (h, hd // 2, 3):
+        raise ValueError("acc must be float64 [heads][head_dim/2][3]")
+    qp = _ptr(q) if t > 0 else None
+    _check(load_library().tria_calib_accumulate(qp, qt, t, h, hd, _ptr(acc), _stream_handle(stream)),
+           "tria_calib_accumulate")
+
+
+def calib_finish(acc, n_tokens: int, *, stream=None):
+    """tria_calib_finish: (q_mean [heads][head_dim/2][2], q_abs [heads][head_dim/2]) float32 CUDA tensors."""
+    import torch
+    h, fc, _ = acc.shape
+    q_mean = torch.empty((h, fc, 2), dtype=torch.float32, device=acc.device)
+    q_abs = torch.empty((h, fc), dtype=torch.float32, device=acc.device)
+    _check(load_library().tria_calib_finish(_ptr(acc), n_tokens, h, 2 * fc, _ptr(q_mean), _ptr(q_abs),
+                                            _stream_handle(stream)), "tria_calib_finish")
+    return q_mean, q_abs
 
 
 def raw_call(name: str, *args):

@@ -132,3 +132,25 @@ def test_load_stats_rejects_ineligible_shapes(lib):
     with pytest.raises(tria.TriaError) as e:    # uneven head map
         tria.Stats(qm, None, n_kv_heads=8, head_dim=128, rope_theta=1e6, kv_of_q=[0] * 32, stream=0)
     assert e.value.status == tria.ERR_INVALID_ARG
+
+
+def test_calibration_argument_checks(lib):
+    # rejected on the host before any launch (fake, aligned pointers are never touched)
+    q, acc = ctypes.c_void_p(0x100000), ctypes.c_void_p(0x200000)
+    call = lambda *a: tria.raw_call("tria_calib_accumulate", *a)
+    assert call(None, tria.F16, 8, 4, 128, acc, None) == tria.ERR_INVALID_ARG
+    assert call(q, tria.F16, 8, 4, 128, None, None) == tria.ERR_INVALID_ARG
+    assert call(q, tria.F16, -1, 4, 128, acc, None) == tria.ERR_INVALID_ARG
+    assert call(q, tria.F16, 8, 0, 128, acc, None) == tria.ERR_INVALID_ARG
+    assert call(ctypes.c_void_p(0x100002), tria.F16, 8, 4, 128, acc, None) == tria.ERR_INVALID_ARG
+    assert call(q, tria.F16, 8, 4, 128, ctypes.c_void_p(0x200004), None) == tria.ERR_INVALID_ARG
+    assert call(q, tria.Q8_0, 8, 4, 128, acc, None) == tria.ERR_UNSUPPORTED
+    assert call(q, tria.F32, 8, 4, 127, acc, None) == tria.ERR_UNSUPPORTED
+    assert call(q, tria.F32, 8, 4, 1024, acc, None) == tria.ERR_UNSUPPORTED
+    assert call(q, tria.F32, 0, 4, 128, acc, None) == tria.OK   # nothing to add, no launch
+    assert call(None, tria.F32, 0, 4, 128, acc, None) == tria.OK
+    fin = lambda *a: tria.raw_call("tria_calib_finish", *a)
+    qm, qa = ctypes.c_void_p(0x300000), ctypes.c_void_p(0x400000)
+    assert fin(acc, 0, 4, 128, qm, qa, None) == tria.ERR_INVALID_ARG
+    assert fin(acc, 10, 4, 128, None, qa, None) == tria.ERR_INVALID_ARG
+    assert fin(acc, 10, 4, 130000, qm, qa, None) == tria.ERR_UNSUPPORTED
