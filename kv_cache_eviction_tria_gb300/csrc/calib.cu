@@ -34,7 +34,7 @@ __device__ __forceinline__ float as_f32<__half>(__half x) { return __half2float(
 // head's half-rows. Block (c, b) takes slots [64 b, 64 b + 64) - whole
 // adjacent half-rows, so every token read is one contiguous span - and token
 // range c, split over kCalibStreams sub-streams of 64 threads; a thread reads
-// two 16-byte vectors per token (real and imaginary half), two tokens in
+// two 16-byte vectors per token (real and imaginary half), four tokens in
 // flight. The sub-streams add into shared memory, then one fp64 atomic per
 // (head, pair, quantity) and block goes to the caller's accumulator.
 constexpr int kCalibSlots = 64;
@@ -72,16 +72,21 @@ __global__ void __launch_bounds__(kCalibVecThreads) k_calib_acc(const T* __restr
         sa[k] += sqrtf(fmaf(x, x, y * y));
       }
     };
+    constexpr int U = 4;   // tokens in flight per thread
+    const size_t step = (size_t)kCalibStreams * stride;
     int t = t0 + stream;
-    for (; t + kCalibStreams < t1; t += 2 * kCalibStreams) {
-      const T* r0 = base + (size_t)t * stride;
-      const T* r1 = r0 + (size_t)kCalibStreams * stride;
-      const uint4 a0 = __ldcs(reinterpret_cast<const uint4*>(r0)), b0 = __ldcs(reinterpret_cast<const uint4*>(r0 + fc));
-      const uint4 a1 = __ldcs(reinterpret_cast<const uint4*>(r1)), b1 = __ldcs(reinterpret_cast<const uint4*>(r1 + fc));
-      add(a0, b0);
-      add(a1, b1);
+    for (; t + (U - 1) * kCalibStreams < t1; t += U * kCalibStreams) {
+      const T* r = base + (size_t)t * stride;
+      uint4 a[U], b[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        a[u] = __ldcs(reinterpret_cast<const uint4*>(r + u * step));
+        b[u] = __ldcs(reinterpret_cast<const uint4*>(r + u * step + fc));
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) add(a[u], b[u]);
     }
-    if (t < t1) {
+    for (; t < t1; t += kCalibStreams) {
       const T* r0 = base + (size_t)t * stride;
       add(__ldcs(reinterpret_cast<const uint4*>(r0)), __ldcs(reinterpret_cast<const uint4*>(r0 + fc)));
     }

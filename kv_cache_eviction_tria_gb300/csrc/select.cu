@@ -355,7 +355,7 @@ constexpr int kClMaxRowsPerCta = 32768;   // 128 KiB of keys
 struct ClShared {
   alignas(16) uint32_t h[2][kHistBins];   // this CTA's histogram, double-buffered by pass
   int sbuf[40];
-  int info[4];                  // prefix, kr after the current pass
+  int info[4];                  // prefix, kr, keys in the cut's bin after the current pass
   int cnt[2];                   // ties, strict keeps (gt + protected) of this CTA
   int warp_tie[kClThreads / 32], warp_keep[kClThreads / 32];
 };
@@ -486,9 +486,13 @@ __global__ void __launch_bounds__(kClThreads) k_select_cl(const __grid_constant_
     }
   }
 
-  // three radix passes over the candidates [lo, hi)
+  // up to three radix passes over the candidates [lo, hi). When the bin that
+  // holds the cut contains exactly the keys still to take, every key with
+  // that prefix is kept: the cut is "key >= prefix * 2^shift" and the later
+  // passes are skipped (all CTAs of the cluster see the same totals).
   uint32_t prefix = 0, T = 0xFFFFFFFFu;
   int kr = sv.k;
+  bool cut_at_prefix = false;
   if (!none) {
 #pragma unroll 1
     for (int pass = 0; pass < 3; ++pass) {
@@ -517,6 +521,7 @@ __global__ void __launch_bounds__(kClThreads) k_select_cl(const __grid_constant_
             sh.info[0] = (int)(pass == 0 ? (uint32_t)b : pass == 1 ? ((prefix << 11) | (uint32_t)b)
                                                                      : ((prefix << 10) | (uint32_t)b));
             sh.info[1] = kr - cum;
+            sh.info[2] = (int)tot[j];   // keys of the cluster in that bin
             break;
           }
           cum += (int)tot[j];
@@ -527,8 +532,17 @@ __global__ void __launch_bounds__(kClThreads) k_select_cl(const __grid_constant_
       __syncthreads();
       prefix = (uint32_t)sh.info[0];
       kr = sh.info[1];
+      if (pass < 2 && kr == sh.info[2]) {
+        const uint32_t lo_key = prefix << (pass == 0 ? 21 : 10);
+        if (lo_key != 0u) {
+          T = lo_key - 1u;   // keep key > T, no ties taken
+          kr = 0;
+          cut_at_prefix = true;
+          break;
+        }
+      }
     }
-    T = prefix;
+    if (!cut_at_prefix) T = prefix;
   }
 
   // counts of my rows; ties at T are kept lowest rows first across the cluster
