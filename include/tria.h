@@ -63,7 +63,8 @@ typedef enum tria_status {
   TRIA_ERR_WORKSPACE = 5,     /* workspace too small or not 256-byte aligned */
   TRIA_ERR_TIMEOUT = 6,       /* device: a bounded wait gave up */
   TRIA_ERR_DEVICE_ARG = 7,    /* device: n_live < 0 or > capacity (sequence skipped) */
-  TRIA_ERR_KEEP_LIST = 8      /* device: keep list not strictly ascending / out of range */
+  TRIA_ERR_KEEP_LIST = 8,     /* device: keep list not strictly ascending / out of range */
+  TRIA_ERR_CAPACITY = 9       /* rows to append do not fit the physical capacity */
 } tria_status;
 
 typedef enum tria_dtype {
@@ -131,6 +132,8 @@ typedef struct tria_policy {
   int32_t sink;               /* first rows always kept */
   int32_t interval;           /* decode steps between passes (used by tria_should_evict) */
   const int64_t* cur_pos;     /* [n_seqs] absolute decode position p_s (not the row count) */
+  const int32_t* sink_rows;   /* [n_seqs] optional per-sequence sink (e.g. the prompt rows
+                                 that a schedule protects); overrides `sink` when not NULL */
 } tria_policy;
 
 /* Host-only gate of [Doc] §4 "GPU scoring requirements" (n_q % n_kv == 0,
@@ -226,6 +229,119 @@ tria_status tria_device_status(void* ws, void* stream);
  * sets, with `spin_limit` polls, and returns what the kernel reported
  * (TRIA_ERR_TIMEOUT expected). Synchronises `stream`. For failure tests. */
 tria_status tria_selftest_bounded_wait(int32_t spin_limit, void* ws, size_t ws_bytes, void* stream);
+
+/* ---- Decode-loop lifecycle ---------------------------------------------
+ * A decode loop appends rows to each sequence and runs a pass when its
+ * schedule says so. Sources, [Worklog] sections: "Why this is still fair even
+ * though the TriAttention bundle is tri12288" (compaction starts once the
+ * cache length reaches kv_budget + divide_length), "Sample9 compaction was
+ * then proven live" (passes at positions 3200, 3328, 3456, ... each taking
+ * 3200 rows to 3072), "Same-prompt boundary runs localized the divergence to
+ * the first compaction" (158-token prompt, first pass at absolute position
+ * 7168 keeping 6144), "Sample9 boundary replay exposed a prompt-token
+ * accounting mismatch" and "Aligned sample9 replay" (prompt rows need not
+ * count toward the cache length), "Phase 6: overflow bug during prompt
+ * prefill" and "4. Separate physical cache limit from logical TriAttention
+ * budget" (no compaction during prefill; physical capacity apart from the
+ * logical budget); [Doc] §1 CLI flags (--tri-interval, --tri-budget,
+ * --tri-sink, --tri-window) and §5 Phase B (the evictor fires only on
+ * single-token decode steps).
+ *
+ * tria_append writes n_tokens new rows after the live rows of every segment
+ * and adds n_tokens to n_live, on the device, so that a loop never has to read
+ * n_live back.
+ *   k_new        device, rows of k_type laid out [n_seqs][n_kv_heads][n_tokens]
+ *                (row bytes as in the cache), 16-byte aligned
+ *   k_scale_new  device, q8_0 keys only (else NULL): scale rows, same layout,
+ *                2-byte aligned
+ *   v_new, v_scale_new  likewise for the values
+ *   pos_new      device int32 [n_seqs][n_tokens]: absolute positions, written
+ *                to the new row of every KV head
+ *   ws           a workspace of this cache (only its control words are used)
+ * Host errors: TRIA_ERR_INVALID_ARG (null or misaligned pointer, n_tokens < 0,
+ * a scale plane given for a non-q8_0 type or missing for q8_0),
+ * TRIA_ERR_WORKSPACE. Device errors (tria_device_status): TRIA_ERR_DEVICE_ARG
+ * when n_live is outside [0, capacity], TRIA_ERR_CAPACITY when n_live +
+ * n_tokens > capacity; that sequence is left unchanged. n_tokens = 0 does
+ * nothing. */
+tria_status tria_append(const tria_layer_cache* cache, const void* k_new, const void* k_scale_new,
+                        const void* v_new, const void* v_scale_new, const int32_t* pos_new,
+                        int32_t n_tokens, void* ws, size_t ws_bytes, void* stream);
+
+/* When a pass runs and what it keeps. Host only; no GPU use. */
+typedef enum tria_trigger {
+  /* [Worklog]: a pass once the counted rows reach kv_budget + divide_length;
+   * it keeps kv_budget counted rows */
+  TRIA_TRIGGER_LENGTH = 0,
+  /* [Doc] §1: a pass every divide_length decode steps (--tri-interval); it
+   * keeps floor(budget_frac * n_ctx) counted rows (--tri-budget) */
+  TRIA_TRIGGER_INTERVAL = 1
+} tria_trigger;
+
+typedef struct tria_schedule {
+  int32_t trigger;             /* tria_trigger */
+  int32_t count_prompt_tokens; /* 1: prompt rows count toward the trigger and the budget;
+                                  0: only rows appended by decode steps count */
+  int32_t protect_prefill;     /* 1: prompt rows are never evicted (they join the sink) */
+  int32_t sink;                /* first rows always kept */
+  int32_t window;              /* most recent rows always kept */
+  int32_t pad;
+  int64_t kv_budget;           /* LENGTH: counted rows a pass keeps (>= 1) */
+  int64_t divide_length;       /* LENGTH: counted rows between passes; INTERVAL: decode
+                                  steps between passes (>= 1) */
+  double budget_frac;          /* INTERVAL: (0, 1] */
+  int64_t n_ctx;               /* INTERVAL: context length the fraction refers to */
+} tria_schedule;
+
+/* One sequence's place in the loop. Owned by the caller; changed only by the
+ * calls below. */
+typedef struct tria_seq_state {
+  int64_t capacity;      /* physical rows per segment */
+  int64_t rows;          /* live rows: the host's copy of n_live */
+  int64_t counted;       /* live rows that count toward the budget */
+  int64_t prompt_rows;   /* rows appended by the prompt (prefill) */
+  int64_t next_pos;      /* absolute position of the next token = tokens appended so far */
+  int64_t decode_steps;  /* single-token steps since the prompt */
+  int64_t passes;        /* passes run */
+  int32_t due;           /* 1: a pass must run before the next append */
+  int32_t pad;
+} tria_seq_state;
+
+#define TRIA_NO_PASS INT32_MAX  /* budget of a sequence whose pass is not due */
+
+/* Checks a schedule: TRIA_ERR_INVALID_ARG for a bad trigger, a flag other
+ * than 0 / 1, a negative sink or window, divide_length < 1, kv_budget < 1
+ * (LENGTH) or budget_frac outside (0, 1] or n_ctx < 0 (INTERVAL). */
+tria_status tria_schedule_check(const tria_schedule* sch);
+
+/* Empty sequence with `capacity` physical rows per segment. */
+tria_status tria_seq_init(tria_seq_state* st, int64_t capacity);
+
+/* The prompt: n_tokens rows appended before the first decode step (never
+ * makes a pass due). TRIA_ERR_CAPACITY when they do not fit (the state is
+ * unchanged: the prompt is not compacted while it is being built);
+ * TRIA_ERR_INVALID_ARG after the first decode step or for n_tokens < 0. */
+tria_status tria_seq_prefill(const tria_schedule* sch, tria_seq_state* st, int64_t n_tokens);
+
+/* One decode step: one row appended; sets st->due by the trigger.
+ * TRIA_ERR_INVALID_ARG while a pass is still due; TRIA_ERR_CAPACITY when the
+ * row does not fit (state unchanged). */
+tria_status tria_seq_decode(const tria_schedule* sch, tria_seq_state* st);
+
+/* The policy values of the next pass over n_seqs sequences: budget_rows[s]
+ * (TRIA_NO_PASS when s is not due), sink_rows[s] and cur_pos[s] = next_pos
+ * (the absolute position, [Worklog] "2026-04-18: later-compaction
+ * absolute-position bug isolated and fixed"), ready for tria_policy's
+ * budget_rows / sink_rows / cur_pos; *n_due = sequences due. A due sequence
+ * keeps B = (counted budget) + (prompt rows outside the count, when
+ * protected) rows, with sink = max(sink, prompt rows) when protected.
+ * TRIA_ERR_BUDGET when B < sink + window for a due sequence. */
+tria_status tria_schedule_plan(const tria_schedule* sch, const tria_seq_state* st, int32_t n_seqs,
+                               int32_t* budget_rows, int32_t* sink_rows, int64_t* cur_pos, int32_t* n_due);
+
+/* Records that the planned pass ran: rows = min(rows, B) and the counts of
+ * every due sequence, clears due. */
+tria_status tria_schedule_passed(const tria_schedule* sch, tria_seq_state* st, int32_t n_seqs);
 
 /* ---- Calibration statistics --------------------------------------------
  * The scoring statistics of one layer from a stream of its pre-RoPE queries

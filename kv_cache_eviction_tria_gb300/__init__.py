@@ -25,16 +25,20 @@ DTYPES = {"f32": F32, "f16": F16, "q8_0": Q8_0}
 STATUS = {
     0: "TRIA_OK", 1: "TRIA_ERR_INVALID_ARG", 2: "TRIA_ERR_UNSUPPORTED", 3: "TRIA_ERR_BUDGET",
     4: "TRIA_ERR_CUDA", 5: "TRIA_ERR_WORKSPACE", 6: "TRIA_ERR_TIMEOUT", 7: "TRIA_ERR_DEVICE_ARG",
-    8: "TRIA_ERR_KEEP_LIST",
+    8: "TRIA_ERR_KEEP_LIST", 9: "TRIA_ERR_CAPACITY",
 }
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_BUDGET, ERR_CUDA, ERR_WORKSPACE, ERR_TIMEOUT, \
-    ERR_DEVICE_ARG, ERR_KEEP_LIST = range(9)
+    ERR_DEVICE_ARG, ERR_KEEP_LIST, ERR_CAPACITY = range(10)
+TRIGGER_LENGTH, TRIGGER_INTERVAL = 0, 1
+NO_PASS = 2 ** 31 - 1
 
 EXPORTS = (
     "tria_gate_check", "tria_budget_rows", "tria_should_evict", "tria_load_stats", "tria_free_stats",
     "tria_workspace_size", "tria_workspace_init", "tria_score", "tria_select", "tria_compact",
     "tria_evict", "tria_evict_profiled", "tria_select_noalloc", "tria_device_status", "tria_selftest_bounded_wait",
-    "tria_calib_accumulate", "tria_calib_finish", "tria_status_string", "tria_version",
+    "tria_calib_accumulate", "tria_calib_finish", "tria_append", "tria_schedule_check", "tria_seq_init",
+    "tria_seq_prefill", "tria_seq_decode", "tria_schedule_plan", "tria_schedule_passed",
+    "tria_status_string", "tria_version",
 )
 
 
@@ -71,7 +75,24 @@ class _Policy(ctypes.Structure):
         ("budget_frac", ctypes.c_double), ("n_ctx", ctypes.POINTER(ctypes.c_int32)),
         ("budget_rows", ctypes.POINTER(ctypes.c_int32)), ("window", ctypes.c_int32),
         ("sink", ctypes.c_int32), ("interval", ctypes.c_int32),
-        ("cur_pos", ctypes.POINTER(ctypes.c_int64)),
+        ("cur_pos", ctypes.POINTER(ctypes.c_int64)), ("sink_rows", ctypes.POINTER(ctypes.c_int32)),
+    ]
+
+
+class _Schedule(ctypes.Structure):
+    _fields_ = [
+        ("trigger", ctypes.c_int32), ("count_prompt_tokens", ctypes.c_int32),
+        ("protect_prefill", ctypes.c_int32), ("sink", ctypes.c_int32), ("window", ctypes.c_int32),
+        ("pad", ctypes.c_int32), ("kv_budget", ctypes.c_int64), ("divide_length", ctypes.c_int64),
+        ("budget_frac", ctypes.c_double), ("n_ctx", ctypes.c_int64),
+    ]
+
+
+class _SeqState(ctypes.Structure):
+    _fields_ = [
+        ("capacity", ctypes.c_int64), ("rows", ctypes.c_int64), ("counted", ctypes.c_int64),
+        ("prompt_rows", ctypes.c_int64), ("next_pos", ctypes.c_int64), ("decode_steps", ctypes.c_int64),
+        ("passes", ctypes.c_int64), ("due", ctypes.c_int32), ("pad", ctypes.c_int32),
     ]
 
 
@@ -123,6 +144,21 @@ def load_library(path: str | None = None):
     lib.tria_calib_accumulate.restype = i32
     lib.tria_calib_finish.argtypes = [vp, i64, i32, i32, vp, vp, vp]
     lib.tria_calib_finish.restype = i32
+    lib.tria_append.argtypes = [ctypes.POINTER(_LayerCache), vp, vp, vp, vp, vp, i32, vp, sz, vp]
+    lib.tria_append.restype = i32
+    sch_p, st_p, i32_p = ctypes.POINTER(_Schedule), ctypes.POINTER(_SeqState), ctypes.POINTER(i32)
+    lib.tria_schedule_check.argtypes = [sch_p]
+    lib.tria_schedule_check.restype = i32
+    lib.tria_seq_init.argtypes = [st_p, i64]
+    lib.tria_seq_init.restype = i32
+    lib.tria_seq_prefill.argtypes = [sch_p, st_p, i64]
+    lib.tria_seq_prefill.restype = i32
+    lib.tria_seq_decode.argtypes = [sch_p, st_p]
+    lib.tria_seq_decode.restype = i32
+    lib.tria_schedule_plan.argtypes = [sch_p, st_p, i32, i32_p, i32_p, ctypes.POINTER(i64), i32_p]
+    lib.tria_schedule_plan.restype = i32
+    lib.tria_schedule_passed.argtypes = [sch_p, st_p, i32]
+    lib.tria_schedule_passed.restype = i32
     lib.tria_status_string.argtypes = [i32]
     lib.tria_status_string.restype = ctypes.c_char_p
     lib.tria_version.argtypes = []
@@ -254,15 +290,16 @@ class Policy:
     """Eviction policy (``tria_policy``)."""
 
     def __init__(self, *, budget_frac: float = 0.0, n_ctx=None, budget_rows=None, window: int = 512,
-                 sink: int = 0, interval: int = 128, cur_pos=None):
+                 sink: int = 0, interval: int = 128, cur_pos=None, sink_rows=None):
         self.budget_frac, self.window, self.sink, self.interval = budget_frac, window, sink, interval
         self.n_ctx, self._n_ctx_p = _host_array(n_ctx, np.int32, ctypes.c_int32)
         self.budget_rows, self._br_p = _host_array(budget_rows, np.int32, ctypes.c_int32)
         self.cur_pos, self._cp_p = _host_array(cur_pos, np.int64, ctypes.c_int64)
+        self.sink_rows, self._sr_p = _host_array(sink_rows, np.int32, ctypes.c_int32)
 
     def c_struct(self) -> _Policy:
         return _Policy(float(self.budget_frac), self._n_ctx_p, self._br_p, self.window, self.sink,
-                       self.interval, self._cp_p)
+                       self.interval, self._cp_p, self._sr_p)
 
 
 # --------------------------------------------------------------------------- the pass
@@ -371,6 +408,80 @@ def calib_finish(acc, n_tokens: int, *, stream=None):
     _check(load_library().tria_calib_finish(_ptr(acc), n_tokens, h, 2 * fc, _ptr(q_mean), _ptr(q_abs),
                                             _stream_handle(stream)), "tria_calib_finish")
     return q_mean, q_abs
+
+
+# --------------------------------------------------------------------------- decode-loop lifecycle
+
+def append(cache: LayerCache, k_new, v_new, pos_new, *, ws, k_scale_new=None, v_scale_new=None, stream=None):
+    """tria_append: rows k_new / v_new [n_seqs][n_kv_heads][n_tokens][...] (cache dtypes) and
+    pos_new int32 [n_seqs][n_tokens] after the live rows of every segment; n_live += n_tokens."""
+    n_tokens = int(pos_new.shape[-1]) if pos_new.dim() == 2 else 0
+    c = cache.c_struct()
+    wp, wb = _ws(ws)
+    _check(load_library().tria_append(ctypes.byref(c), _ptr(k_new), _ptr(k_scale_new), _ptr(v_new),
+                                      _ptr(v_scale_new), _ptr(pos_new), n_tokens, wp, wb,
+                                      _stream_handle(stream)), "tria_append")
+
+
+class Schedule:
+    """Decode-loop schedule (``tria_schedule``)."""
+
+    def __init__(self, *, trigger: int = TRIGGER_LENGTH, kv_budget: int = 0, divide_length: int = 128,
+                 count_prompt_tokens: bool = True, protect_prefill: bool = True, sink: int = 0,
+                 window: int = 0, budget_frac: float = 0.0, n_ctx: int = 0):
+        self.c = _Schedule(int(trigger), int(bool(count_prompt_tokens)), int(bool(protect_prefill)), int(sink),
+                           int(window), 0, int(kv_budget), int(divide_length), float(budget_frac), int(n_ctx))
+        _check(load_library().tria_schedule_check(ctypes.byref(self.c)), "tria_schedule_check")
+
+    @property
+    def window(self) -> int:
+        return self.c.window
+
+
+class Sequences:
+    """The ``tria_seq_state`` of every sequence of a loop (host memory)."""
+
+    def __init__(self, schedule: Schedule, capacity):
+        self.schedule = schedule
+        self.n = len(capacity)
+        self.st = (_SeqState * self.n)()
+        for s, cap in enumerate(capacity):
+            _check(load_library().tria_seq_init(ctypes.byref(self.st[s]), int(cap)), "tria_seq_init")
+
+    def prefill(self, s: int, n_tokens: int):
+        _check(load_library().tria_seq_prefill(ctypes.byref(self.schedule.c), ctypes.byref(self.st[s]),
+                                               int(n_tokens)), "tria_seq_prefill")
+
+    def decode(self, s: int) -> bool:
+        _check(load_library().tria_seq_decode(ctypes.byref(self.schedule.c), ctypes.byref(self.st[s])),
+               "tria_seq_decode")
+        return bool(self.st[s].due)
+
+    def plan(self):
+        """tria_schedule_plan: (budget_rows, sink_rows, cur_pos, n_due)."""
+        b = np.zeros(self.n, np.int32)
+        k = np.zeros(self.n, np.int32)
+        p = np.zeros(self.n, np.int64)
+        nd = ctypes.c_int32()
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        _check(load_library().tria_schedule_plan(ctypes.byref(self.schedule.c), self.st, self.n,
+                                                 b.ctypes.data_as(i32p), k.ctypes.data_as(i32p),
+                                                 p.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                                 ctypes.byref(nd)), "tria_schedule_plan")
+        return b, k, p, nd.value
+
+    def policy(self) -> tuple:
+        """(Policy of the planned pass, sequences due)."""
+        b, k, p, nd = self.plan()
+        return Policy(budget_rows=b, sink_rows=k, cur_pos=p, window=self.schedule.window,
+                      sink=self.schedule.c.sink), nd
+
+    def passed(self):
+        _check(load_library().tria_schedule_passed(ctypes.byref(self.schedule.c), self.st, self.n),
+               "tria_schedule_passed")
+
+    def state(self, s: int) -> dict:
+        return {name: getattr(self.st[s], name) for name, _ in _SeqState._fields_ if name != "pad"}
 
 
 def raw_call(name: str, *args):

@@ -131,7 +131,9 @@ tria_status check_policy(const tria_layer_cache* c, const tria_policy* p, bool n
       b = tria_budget_rows(p->budget_frac, p->n_ctx[s]);
     }
     if (b < 0 || b > INT32_MAX) return TRIA_ERR_INVALID_ARG;
-    if (b < (int64_t)p->sink + p->window) return TRIA_ERR_BUDGET;
+    const int64_t sink = p->sink_rows ? (int64_t)p->sink_rows[s] : (int64_t)p->sink;
+    if (sink < 0) return TRIA_ERR_INVALID_ARG;
+    if (b < sink + p->window) return TRIA_ERR_BUDGET;
     if (need_pos && p->cur_pos[s] < 0) return TRIA_ERR_INVALID_ARG;
     budget[s] = (int)b;
   }
@@ -153,7 +155,6 @@ void fill_pass(Pass& P, const tria_layer_cache* c, const tria_policy* p, const s
   P.G = G;
   P.hd = c->head_dim;
   P.fc = c->head_dim / 2;
-  P.sink = p ? p->sink : 0;
   P.window = p ? p->window : 0;
   P.k_type = c->k_type;
   P.v_type = c->v_type;
@@ -184,6 +185,7 @@ void fill_pass(Pass& P, const tria_layer_cache* c, const tria_policy* p, const s
     P.seq[s].cap = c->capacity[s];
     P.seq[s].budget = budget.empty() ? 0 : budget[s];
     P.seq[s].cur_pos = (p && p->cur_pos) ? p->cur_pos[s] : 0;
+    P.seq[s].sink = !p ? 0 : (p->sink_rows ? p->sink_rows[s] : p->sink);
   }
 }
 
@@ -271,6 +273,33 @@ extern "C" tria_status tria_select(const float* score, const tria_layer_cache* c
   P.score_in = score;
   P.keep = keep_out;
   return cuda_status(launch_select(P, true, (cudaStream_t)stream));
+}
+
+extern "C" tria_status tria_append(const tria_layer_cache* cache, const void* k_new, const void* k_scale_new,
+                                   const void* v_new, const void* v_scale_new, const int32_t* pos_new,
+                                   int32_t n_tokens, void* ws, size_t ws_bytes, void* stream) {
+  tria_status r;
+  if ((r = check_cache(cache)) != TRIA_OK) return r;
+  if (n_tokens < 0) return TRIA_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, 256) || ws_bytes < sizeof(Ctrl)) return TRIA_ERR_WORKSPACE;
+  if (n_tokens == 0) return TRIA_OK;
+  if (!k_new || !v_new || !pos_new) return TRIA_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(pos_new, 4)) return TRIA_ERR_INVALID_ARG;
+  if ((cache->k_type == TRIA_Q8_0) != (k_scale_new != nullptr)) return TRIA_ERR_INVALID_ARG;
+  if ((cache->v_type == TRIA_Q8_0) != (v_scale_new != nullptr)) return TRIA_ERR_INVALID_ARG;
+  if ((k_scale_new && !aligned(k_scale_new, 2)) || (v_scale_new && !aligned(v_scale_new, 2)))
+    return TRIA_ERR_INVALID_ARG;
+  const Layout L = make_layout(cache, 0);
+  Pass P;
+  fill_pass(P, cache, nullptr, {}, L, ws, 0);
+  AppendSrc a;
+  a.k = (const uint8_t*)k_new;
+  a.ks = (const uint8_t*)k_scale_new;
+  a.v = (const uint8_t*)v_new;
+  a.vs = (const uint8_t*)v_scale_new;
+  a.pos = pos_new;
+  a.n_tokens = n_tokens;
+  return cuda_status(launch_append(P, a, (cudaStream_t)stream));
 }
 
 extern "C" tria_status tria_compact(const tria_layer_cache* cache, const tria_policy* policy, const int32_t* keep,
@@ -394,6 +423,7 @@ extern "C" const char* tria_status_string(tria_status s) {
     case TRIA_ERR_WORKSPACE: return "workspace too small or misaligned";
     case TRIA_ERR_TIMEOUT: return "device wait timed out";
     case TRIA_ERR_DEVICE_ARG: return "n_live out of range";
+    case TRIA_ERR_CAPACITY: return "rows do not fit the physical capacity";
     case TRIA_ERR_KEEP_LIST: return "invalid keep list";
   }
   return "unknown status";

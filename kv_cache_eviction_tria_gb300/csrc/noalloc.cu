@@ -73,8 +73,11 @@ extern "C" tria_status tria_select_noalloc(const float* score, const tria_layer_
     if (c->capacity[s] > cap_max) cap_max = c->capacity[s];
     int64_t b = p->budget_rows ? (int64_t)p->budget_rows[s] : tria_budget_rows(p->budget_frac, p->n_ctx[s]);
     if (b < 0 || b > INT32_MAX) return TRIA_ERR_INVALID_ARG;
-    if (b < (int64_t)p->sink + p->window) return TRIA_ERR_BUDGET;
+    const int64_t sink = p->sink_rows ? (int64_t)p->sink_rows[s] : (int64_t)p->sink;
+    if (sink < 0) return TRIA_ERR_INVALID_ARG;
+    if (b < sink + p->window) return TRIA_ERR_BUDGET;
     P.seq[s].row0 = c->seq_row0[s];
+    P.seq[s].sink = (int)sink;
     P.seq[s].cap = c->capacity[s];
     P.seq[s].budget = (int)b;
   }
@@ -109,7 +112,6 @@ extern "C" tria_status tria_select_noalloc(const float* score, const tria_layer_
   P.n_seg = n_seg;
   P.hd = c->head_dim;
   P.fc = c->head_dim / 2;
-  P.sink = p->sink;
   P.window = p->window;
   P.spin_limit = kDefaultSpinLimit;
   P.n_live = c->n_live;

@@ -61,7 +61,7 @@ __device__ void hist_block(const Pass& P, int seg, int blk, const SegView& sv, S
 
   const uint32_t prefix = PASS > 0 ? __ldcg(&P.seg[seg].prefix) : 0u;
   const int r_beg = blk * kHistRowsPerCta, r_end = min(n, r_beg + kHistRowsPerCta);
-  const int lo = P.sink, hi = n - P.window;
+  const int lo = sv.sink, hi = n - P.window;
   const bool do_hist = sv.k > 0;
   for (int r = r_beg + threadIdx.x; r < r_end; r += blockDim.x) {
     float s;
@@ -151,7 +151,7 @@ __device__ void count_block(const Pass& P, int seg, int blk, const SegView& sv, 
     for (int half = 0; half < kChunk / 32; ++half) {
       const int r = c * kChunk + half * 32 + lane;
       const bool in = r < n;
-      const bool pr = in && is_protected(r, n, P.sink, P.window);
+      const bool pr = in && is_protected(r, n, sv.sink, P.window);
       const bool cand = in && !pr && !none;
       const uint32_t key = cand ? score_key(__ldcg(&s[r])) : 0u;
       gt += __popc(__ballot_sync(0xffffffffu, cand && key > T));
@@ -208,7 +208,7 @@ __device__ void count_block(const Pass& P, int seg, int blk, const SegView& sv, 
     for (int half = 0; half < kChunk / 32; ++half) {
       const int r = cstar * kChunk + half * 32 + lane;
       const bool in = r < n;
-      const bool cand = in && !is_protected(r, n, P.sink, P.window);
+      const bool cand = in && !is_protected(r, n, sv.sink, P.window);
       const bool t = cand && score_key(__ldcg(&s[r])) == T;
       const uint32_t b = __ballot_sync(0xffffffffu, t);
       const int cnt = __popc(b);
@@ -273,7 +273,7 @@ __device__ void keeplist_block(const Pass& P, int seg, int blk, const SegView& s
     for (int half = 0; half < kChunk / 32; ++half) {
       const int r = c * kChunk + half * 32 + lane;
       const bool in = r < n;
-      const bool pr = in && is_protected(r, n, P.sink, P.window);
+      const bool pr = in && is_protected(r, n, sv.sink, P.window);
       bool kp = pr;
       if (in && !pr && !none) {
         const uint32_t key = score_key(__ldcg(&s[r]));
@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(kClThreads) k_select_cl(const __grid_constant_
       for (int r = r0 + threadIdx.x; r < r1; r += blockDim.x) keep[r] = r;
     return;
   }
-  const int lo = P.sink, hi = n - P.window;
+  const int lo = sv.sink, hi = n - P.window;
   const bool none = sv.k <= 0;
 
   // keys of my rows (the evict path turns raw scores into the z-max score

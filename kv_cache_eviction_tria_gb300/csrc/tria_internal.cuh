@@ -40,7 +40,8 @@ struct Ctrl {
   uint32_t wait_flag;    // never set: target of the bounded-wait self-test
   uint32_t bar_count;    // grid barrier: CTAs arrived (reset by the last one)
   uint32_t bar_gen;      // grid barrier: generation, bumped when all arrived
-  uint32_t pad[55];
+  uint32_t append_ticket;  // append CTAs that finished (reset by the last one)
+  uint32_t pad[54];
 };
 
 // Per-segment state (one segment = one sequence x KV head of the layer).
@@ -77,13 +78,14 @@ struct SeqInfo {
   int64_t cur_pos;       // absolute decode position
   int32_t cap;           // rows per segment
   int32_t budget;        // B
-  int32_t pad[2];
+  int32_t sink;          // first rows always kept
+  int32_t pad;
 };
 
 // Everything a kernel of the pass needs, passed by value.
 struct Pass {
   int32_t n_seqs, n_kv, n_seg, G, hd, fc;
-  int32_t sink, window;
+  int32_t window;
   int32_t k_type, v_type;
   int32_t k_rb, ks_rb, v_rb, vs_rb;   // bytes per row of each plane (0: absent)
   int32_t only_active;                // skip segments with n_live <= B
@@ -126,7 +128,7 @@ struct Pass {
 struct SegView {
   int s, g;
   int64_t row0;
-  int n, B, k;
+  int n, B, k, sink;
   bool valid, active;
 };
 
@@ -140,7 +142,8 @@ __device__ __forceinline__ SegView seg_view(const Pass& P, int seg) {
   v.B = q.budget;
   v.valid = v.n >= 0 && v.n <= q.cap;
   v.active = v.valid && v.n > v.B;
-  v.k = v.B - P.sink - P.window;
+  v.sink = q.sink;
+  v.k = v.B - v.sink - P.window;
   return v;
 }
 
@@ -491,6 +494,16 @@ cudaError_t launch_select(const Pass& P, bool write_keep, cudaStream_t st, int s
 cudaError_t launch_keep_prepass(const Pass& P, cudaStream_t st);
 cudaError_t launch_move(const Pass& P, cudaStream_t st);
 cudaError_t launch_wait_selftest(const Pass& P, cudaStream_t st);
+// lifecycle.cu: rows [n_seqs][n_kv][n_tokens] appended after the live rows
+struct AppendSrc {
+  const uint8_t* k;
+  const uint8_t* ks;
+  const uint8_t* v;
+  const uint8_t* vs;
+  const int32_t* pos;                  // [n_seqs][n_tokens]
+  int32_t n_tokens;
+};
+cudaError_t launch_append(const Pass& P, const AppendSrc& a, cudaStream_t st);
 // stats.cu
 struct StatsDevice;
 

@@ -252,7 +252,7 @@ def evict_layer(layer_cache: dict, q_mean: np.ndarray, q_abs, *, layer: int, n_k
             kf = keys_f64(layer_cache["k"][r0:r0 + n], ks)
             hs = groups[g]
             raw, sc = segment_scores(kf, qc_all[hs], m_all[hs], omega, int(cur_pos[s]), offsets)
-            keep = select_keep(sc, n, b, sink, window)
+            keep = select_keep(sc, n, b, _per_seq(sink, s), window)
             info[(s, g)] = {"raw": raw, "s": sc, "keep": keep, "B": b, "n": n, "row0": r0}
             if n <= b:
                 continue
@@ -270,11 +270,88 @@ def evict_layer(layer_cache: dict, q_mean: np.ndarray, q_abs, *, layer: int, n_k
     return out, info
 
 
+def _per_seq(value, s):
+    """``value`` itself, or its s-th entry when it is a sequence."""
+    return int(value[s]) if hasattr(value, "__len__") else int(value)
+
+
 def should_evict(n_live: int, budget: int, interval: int) -> bool:
     """Lifecycle trigger: compact once the live rows reach budget + interval
     ([Worklog] "Final apples-to-apples check": trigger = kv_budget + divide_length;
     [Doc] §1 "--tri-interval")."""
     return n_live >= budget + interval
+
+
+# ---------------------------------------------------------------------------
+# decode-loop lifecycle ([Worklog] "Why this is still fair even though the
+# TriAttention bundle is tri12288", "Sample9 compaction was then proven live",
+# "Same-prompt boundary runs localized the divergence to the first
+# compaction", "Sample9 boundary replay exposed a prompt-token accounting
+# mismatch", "Aligned sample9 replay", "Phase 6: overflow bug during prompt
+# prefill"; [Doc] §1 --tri-interval / --tri-budget, §5 Phase B)
+# ---------------------------------------------------------------------------
+
+class CapacityError(ValueError):
+    """Rows appended beyond the physical capacity."""
+
+
+def schedule_events(*, trigger: str, prompt: int, n_decode: int, capacity: int, kv_budget: int = 0,
+                    divide_length: int = 128, count_prompt_tokens: bool = True, protect_prefill: bool = True,
+                    sink: int = 0, window: int = 0, budget_frac: float = 0.0, n_ctx: int = 0):
+    """Passes of one sequence that appends a prompt of ``prompt`` rows and then
+    ``n_decode`` single-token decode steps.
+
+    The cache is tracked as two groups of rows: the prompt rows and the rows
+    the decode steps appended. The prompt is appended whole (no pass during
+    prefill; it must fit the physical capacity). After each decode step:
+
+    * trigger "length" ([Worklog]): a pass once the counted rows - the decode
+      rows, plus the prompt rows when ``count_prompt_tokens`` - reach
+      ``kv_budget + divide_length``; the pass keeps ``kv_budget`` counted rows.
+    * trigger "interval" ([Doc] §1): a pass on every ``divide_length``-th
+      decode step; it keeps ``floor(budget_frac * n_ctx)`` counted rows.
+
+    With ``protect_prefill`` the prompt rows are all kept: they join the sink,
+    and when they are not counted they come on top of the kept count. Without
+    it the prompt rows compete with the rest, and after the first pass that
+    evicts the survivors are plain rows. The pass position is the absolute
+    position of the next token, i.e. the tokens appended so far.
+
+    Returns a list of dicts: step (decode steps so far), pos, rows_before,
+    counted_before, rows_after, budget (rows the pass keeps), sink.
+    """
+    if prompt > capacity:
+        raise CapacityError(f"prompt of {prompt} rows > capacity {capacity}")
+    p_rows, d_rows = prompt, 0
+    keep_counted = kv_budget if trigger == "length" else budget_rows(budget_frac, n_ctx)
+    events = []
+    for step in range(1, n_decode + 1):
+        if p_rows + d_rows + 1 > capacity:
+            raise CapacityError(f"decode step {step}: capacity {capacity} full")
+        d_rows += 1
+        counted = d_rows + (p_rows if count_prompt_tokens else 0)
+        if trigger == "length":
+            due = counted >= kv_budget + divide_length
+        else:
+            due = step % divide_length == 0
+        if not due:
+            continue
+        if protect_prefill:
+            budget = keep_counted + (0 if count_prompt_tokens else p_rows)
+            sink_s = max(sink, p_rows)
+        else:
+            budget, sink_s = keep_counted, sink
+        if budget < sink_s + window:
+            raise BudgetError(f"budget {budget} < sink {sink_s} + window {window}")
+        before = p_rows + d_rows
+        if before > budget:
+            if protect_prefill:
+                d_rows = budget - p_rows
+            else:
+                p_rows, d_rows = 0, budget
+        events.append({"step": step, "pos": prompt + step, "rows_before": before, "counted_before": counted,
+                       "rows_after": p_rows + d_rows, "budget": budget, "sink": sink_s})
+    return events
 
 
 # ---------------------------------------------------------------------------
