@@ -84,7 +84,7 @@ typedef struct tria_stats_desc {
   int32_t n_layers;
   int32_t n_q_heads;
   int32_t n_kv_heads;
-  int32_t head_dim;           /* uniform across layers ([Doc] §6) */
+  int32_t head_dim;           /* every layer's head_dim unless layer_head_dim is given */
   double rope_theta;          /* w_f = theta^(-2f/head_dim) when omega is NULL */
   const double* omega;        /* [head_dim/2] optional RoPE angular frequencies */
   const float* q_mean;        /* [n_layers][n_q_heads][head_dim/2][2] pre-RoPE mean query (re, im) */
@@ -94,6 +94,17 @@ typedef struct tria_stats_desc {
                                  get the same number of query heads. */
   const int64_t* offsets;     /* [n_offsets] future query offsets D; NULL: {1, 2, 4, ..., 65536} */
   int32_t n_offsets;
+  /* Hybrid models ([Doc] §6 "Hybrid head_dim models": head_dim varies across
+   * layers, e.g. 256 / 512; the follow-on it names is a per-layer stats
+   * offset table so that the eligible layers score on the GPU):
+   * layer_head_dim [n_layers] optional; NULL: every layer has head_dim. When
+   * given, head_dim is ignored and q_mean / q_abs (and omega, if given) are
+   * packed layer after layer: layer l holds n_q_heads * layer_head_dim[l] / 2
+   * pairs (omega: layer_head_dim[l] / 2 frequencies). Every entry must be even
+   * and > 0. Layers whose head_dim fails the gate (> 256 or not a multiple of
+   * 32) are not loaded; passes on them return TRIA_ERR_UNSUPPORTED. */
+  const int32_t* layer_head_dim;
+  const double* layer_rope_theta;  /* [n_layers] optional per-layer theta; NULL: rope_theta */
 } tria_stats_desc;
 
 typedef struct tria_stats tria_stats;  /* opaque, device resident, immutable after load */

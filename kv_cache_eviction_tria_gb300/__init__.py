@@ -57,6 +57,7 @@ class _StatsDesc(ctypes.Structure):
         ("omega", ctypes.POINTER(ctypes.c_double)), ("q_mean", ctypes.POINTER(ctypes.c_float)),
         ("q_abs", ctypes.POINTER(ctypes.c_float)), ("kv_of_q", ctypes.POINTER(ctypes.c_int32)),
         ("offsets", ctypes.POINTER(ctypes.c_int64)), ("n_offsets", ctypes.c_int32),
+        ("layer_head_dim", ctypes.POINTER(ctypes.c_int32)), ("layer_rope_theta", ctypes.POINTER(ctypes.c_double)),
     ]
 
 
@@ -227,20 +228,34 @@ def version() -> int:
 class Stats:
     """Device-resident calibration statistics (``tria_load_stats``)."""
 
-    def __init__(self, q_mean, q_abs, *, n_kv_heads: int, head_dim: int, rope_theta: float,
-                 omega=None, kv_of_q=None, offsets=None, stream=None):
+    def __init__(self, q_mean, q_abs, *, n_kv_heads: int, head_dim: int = 0, rope_theta: float = 0.0,
+                 omega=None, kv_of_q=None, offsets=None, layer_head_dim=None, layer_rope_theta=None,
+                 stream=None):
+        """Uniform models: q_mean [L][n_q][hd/2][2], q_abs [L][n_q][hd/2] (or None).
+        Hybrid models (layer_head_dim given): q_mean / q_abs / omega are lists with
+        one array per layer, packed here layer after layer."""
         lib = load_library()
-        q_mean = np.ascontiguousarray(np.asarray(q_mean, dtype=np.float32))
-        n_layers, n_q = q_mean.shape[0], q_mean.shape[1]
+        if layer_head_dim is not None:
+            n_layers, n_q = len(q_mean), len(q_mean[0])
+            q_mean = np.concatenate([np.asarray(x, np.float32).ravel() for x in q_mean])
+            if q_abs is not None:
+                q_abs = np.concatenate([np.asarray(x, np.float32).ravel() for x in q_abs])
+            if omega is not None:
+                omega = np.concatenate([np.asarray(x, np.float64).ravel() for x in omega])
+        else:
+            q_mean = np.ascontiguousarray(np.asarray(q_mean, dtype=np.float32))
+            n_layers, n_q = q_mean.shape[0], q_mean.shape[1]
         self._keep = []
         qm_arr, qm_p = _host_array(q_mean, np.float32, ctypes.c_float)
         qa_arr, qa_p = _host_array(q_abs, np.float32, ctypes.c_float)
         om_arr, om_p = _host_array(omega, np.float64, ctypes.c_double)
         kv_arr, kv_p = _host_array(kv_of_q, np.int32, ctypes.c_int32)
         of_arr, of_p = _host_array(offsets, np.int64, ctypes.c_int64)
-        self._keep += [qm_arr, qa_arr, om_arr, kv_arr, of_arr]
+        lh_arr, lh_p = _host_array(layer_head_dim, np.int32, ctypes.c_int32)
+        lt_arr, lt_p = _host_array(layer_rope_theta, np.float64, ctypes.c_double)
+        self._keep += [qm_arr, qa_arr, om_arr, kv_arr, of_arr, lh_arr, lt_arr]
         desc = _StatsDesc(n_layers, n_q, n_kv_heads, head_dim, float(rope_theta), om_p, qm_p, qa_p,
-                          kv_p, of_p, 0 if of_arr is None else len(of_arr))
+                          kv_p, of_p, 0 if of_arr is None else len(of_arr), lh_p, lt_p)
         handle = ctypes.c_void_p()
         _check(lib.tria_load_stats(ctypes.byref(desc), ctypes.byref(handle), _stream_handle(stream)),
                "tria_load_stats")

@@ -194,15 +194,15 @@ tria_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TRIA_OK : TRI
 tria_status check_stats(const tria_stats* st, int layer, const tria_layer_cache* c) {
   if (!st) return TRIA_ERR_INVALID_ARG;
   if (layer < 0 || layer >= st->n_layers) return TRIA_ERR_INVALID_ARG;
-  if (st->n_kv_heads != c->n_kv_heads || st->head_dim != c->head_dim) return TRIA_ERR_INVALID_ARG;
+  if (st->n_kv_heads != c->n_kv_heads || st->head_dim[layer] != c->head_dim) return TRIA_ERR_INVALID_ARG;
+  if (st->qe_off[layer] < 0) return TRIA_ERR_UNSUPPORTED;   // layer not loaded (fails the gate)
   return TRIA_OK;
 }
 
 void set_stats(Pass& P, const tria_stats* st, int layer) {
-  const size_t per_layer = (size_t)st->n_kv_heads * st->group * (st->head_dim / 2);
-  P.qe = st->qe + per_layer * layer;
-  P.mw = st->mw + per_layer * layer;
-  P.turns = st->turns;
+  P.qe = st->qe + st->qe_off[layer];
+  P.mw = st->mw + st->qe_off[layer];
+  P.turns = st->turns + st->turns_off[layer];
 }
 
 }  // namespace

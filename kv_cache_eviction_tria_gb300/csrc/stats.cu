@@ -17,6 +17,7 @@
 // floating-point range reduction is needed at any context length.
 #include <math.h>
 
+#include <algorithm>
 #include <vector>
 
 #include "tria_internal.cuh"
@@ -88,12 +89,34 @@ extern "C" tria_status tria_load_stats(const tria_stats_desc* d, tria_stats** ou
   if (!out) return TRIA_ERR_INVALID_ARG;
   *out = nullptr;
   if (!d || !d->q_mean || d->n_layers <= 0) return TRIA_ERR_INVALID_ARG;
-  tria_status gate = tria_gate_check(d->n_q_heads, d->n_kv_heads, d->head_dim);
-  if (gate != TRIA_OK) return gate;
-  const int L = d->n_layers, nq = d->n_q_heads, nkv = d->n_kv_heads, hd = d->head_dim;
-  const int fc = hd / 2, G = nq / nkv;
-  if (!d->omega && !(d->rope_theta > 1.0)) return TRIA_ERR_INVALID_ARG;
+  const int L = d->n_layers, nq = d->n_q_heads, nkv = d->n_kv_heads;
+  if (nq <= 0 || nkv <= 0) return TRIA_ERR_INVALID_ARG;
   if (d->offsets && d->n_offsets <= 0) return TRIA_ERR_INVALID_ARG;
+
+  // per-layer head_dim and theta; a layer is loaded when its head_dim passes
+  // the gate ([Doc] §4 GPU scoring requirements, §6 hybrid head_dim models)
+  std::vector<int32_t> hd(L);
+  std::vector<double> theta(L);
+  std::vector<int64_t> src_pairs(L + 1, 0);   // pairs before layer l in q_mean / q_abs (per head)
+  int loaded = 0;
+  tria_status first_gate = TRIA_OK;
+  for (int l = 0; l < L; ++l) {
+    hd[l] = d->layer_head_dim ? d->layer_head_dim[l] : d->head_dim;
+    theta[l] = d->layer_rope_theta ? d->layer_rope_theta[l] : d->rope_theta;
+    if (hd[l] <= 0 || hd[l] % 2 != 0) return TRIA_ERR_INVALID_ARG;
+    if (!d->omega && !(theta[l] > 1.0)) return TRIA_ERR_INVALID_ARG;
+    src_pairs[l + 1] = src_pairs[l] + hd[l] / 2;
+    const tria_status g = tria_gate_check(nq, nkv, hd[l]);
+    if (g == TRIA_OK) {
+      ++loaded;
+    } else if (g == TRIA_ERR_INVALID_ARG || !d->layer_head_dim) {
+      return g;   // uniform models keep the whole-model gate
+    } else if (first_gate == TRIA_OK) {
+      first_gate = g;
+    }
+  }
+  if (loaded == 0) return first_gate == TRIA_OK ? TRIA_ERR_UNSUPPORTED : first_gate;
+  const int G = nq / nkv;
 
   // query heads of each KV head, ascending ([Worklog] "sampled-head mapping")
   std::vector<int> order;
@@ -117,20 +140,33 @@ extern "C" tria_status tria_load_stats(const tria_stats_desc* d, tria_stats** ou
     for (int j = 0; j <= 16; ++j) offs.push_back(1ll << j);
   }
 
-  cudaStream_t st = (cudaStream_t)stream;
   tria_stats* s = new tria_stats();
   s->n_layers = L;
   s->n_q_heads = nq;
   s->n_kv_heads = nkv;
-  s->head_dim = hd;
   s->group = G;
+  s->head_dim = hd;
+  s->qe_off.assign(L, -1);
+  s->turns_off.assign(L, -1);
+  int64_t n_fold = 0, n_turns = 0;
+  int fc_max = 1;
+  for (int l = 0; l < L; ++l) {
+    if (tria_gate_check(nq, nkv, hd[l]) != TRIA_OK) continue;
+    s->qe_off[l] = n_fold;
+    s->turns_off[l] = n_turns;
+    n_fold += (int64_t)nkv * G * (hd[l] / 2);
+    n_turns += hd[l] / 2;
+    fc_max = std::max(fc_max, hd[l] / 2);
+  }
+
+  cudaStream_t st = (cudaStream_t)stream;
   float* qm_d = nullptr;
   float* qa_d = nullptr;
   double* om_d = nullptr;
   long long* off_d = nullptr;
   int* order_d = nullptr;
   double2* ef_d = nullptr;
-  const size_t nqm = (size_t)L * nq * fc;
+  const size_t nqm = (size_t)nq * src_pairs[L];
   cudaError_t e = cudaSuccess;
   auto fail = [&]() {
     cudaFree(qm_d); cudaFree(qa_d); cudaFree(om_d); cudaFree(off_d); cudaFree(order_d); cudaFree(ef_d);
@@ -140,19 +176,27 @@ extern "C" tria_status tria_load_stats(const tria_stats_desc* d, tria_stats** ou
   };
   if ((e = upload(&qm_d, d->q_mean, 2 * nqm)) != cudaSuccess) return fail();
   if (d->q_abs && (e = upload(&qa_d, d->q_abs, nqm)) != cudaSuccess) return fail();
-  if (d->omega && (e = upload(&om_d, d->omega, (size_t)fc)) != cudaSuccess) return fail();
+  if (d->omega && (e = upload(&om_d, d->omega, (size_t)src_pairs[L])) != cudaSuccess) return fail();
   if ((e = upload(&off_d, offs.data(), offs.size())) != cudaSuccess) return fail();
   if ((e = upload(&order_d, order.data(), order.size())) != cudaSuccess) return fail();
-  if ((e = cudaMalloc((void**)&ef_d, fc * sizeof(double2))) != cudaSuccess) return fail();
-  if ((e = cudaMalloc((void**)&s->turns, fc * sizeof(unsigned long long))) != cudaSuccess) return fail();
-  const size_t nfold = (size_t)L * nkv * G * fc;
-  if ((e = cudaMalloc((void**)&s->qe, nfold * sizeof(float2))) != cudaSuccess) return fail();
-  if ((e = cudaMalloc((void**)&s->mw, nfold * sizeof(float))) != cudaSuccess) return fail();
+  if ((e = cudaMalloc((void**)&ef_d, fc_max * sizeof(double2))) != cudaSuccess) return fail();
+  if ((e = cudaMalloc((void**)&s->turns, n_turns * sizeof(unsigned long long))) != cudaSuccess) return fail();
+  if ((e = cudaMalloc((void**)&s->qe, n_fold * sizeof(float2))) != cudaSuccess) return fail();
+  if ((e = cudaMalloc((void**)&s->mw, n_fold * sizeof(float))) != cudaSuccess) return fail();
 
-  k_stats_freq<<<(fc + 127) / 128, 128, 0, st>>>(fc, hd, d->rope_theta, om_d, off_d, (int)offs.size(),
-                                                s->turns, ef_d);
-  const int blocks = (int)((nfold + 255) / 256 < 4096 ? (nfold + 255) / 256 : 4096);
-  k_stats_heads<<<blocks, 256, 0, st>>>(L, nq, nkv, G, fc, qm_d, qa_d, order_d, ef_d, s->qe, s->mw);
+  // one layer at a time (load time, not the pass): its frequencies, then its
+  // folded head weights; the folding buffer is reused in stream order
+  for (int l = 0; l < L; ++l) {
+    if (s->qe_off[l] < 0) continue;
+    const int fc = hd[l] / 2;
+    const size_t src = (size_t)nq * src_pairs[l];
+    k_stats_freq<<<(fc + 127) / 128, 128, 0, st>>>(fc, hd[l], theta[l], om_d ? om_d + src_pairs[l] : nullptr,
+                                                  off_d, (int)offs.size(), s->turns + s->turns_off[l], ef_d);
+    const long long nf = (long long)nkv * G * fc;
+    const int blocks = (int)std::min<long long>((nf + 255) / 256, 4096);
+    k_stats_heads<<<blocks, 256, 0, st>>>(1, nq, nkv, G, fc, qm_d + 2 * src, qa_d ? qa_d + src : nullptr,
+                                          order_d, ef_d, s->qe + s->qe_off[l], s->mw + s->qe_off[l]);
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return fail();
   if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return fail();
   cudaFree(qm_d);

@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <vector>
+
 #include "tria.h"
 
 namespace tria {
@@ -511,8 +513,11 @@ struct StatsDevice;
 
 // Opaque stats handle of the C ABI.
 struct tria_stats {
-  int32_t n_layers, n_q_heads, n_kv_heads, head_dim, group;
-  float2* qe;                  // [L][n_kv][G][fc]
-  float* mw;                   // [L][n_kv][G][fc]
-  unsigned long long* turns;   // [fc]
+  int32_t n_layers, n_q_heads, n_kv_heads, group;
+  float2* qe;                  // per loaded layer l: [n_kv][G][fc_l] from qe_off[l]
+  float* mw;                   // same layout as qe
+  unsigned long long* turns;   // per loaded layer l: [fc_l] from turns_off[l]
+  std::vector<int32_t> head_dim;     // [L]
+  std::vector<int64_t> qe_off;       // [L]; -1: layer not loaded (fails the gate)
+  std::vector<int64_t> turns_off;    // [L]
 };

@@ -222,14 +222,15 @@ def evict_layer(layer_cache: dict, q_mean: np.ndarray, q_abs, *, layer: int, n_k
 
     ``layer_cache`` holds ``k`` (float or int8 codes), ``k_scale`` (or None),
     ``v``, ``pos`` over global rows plus ``n_live``, ``seq_row0``,
-    ``capacity`` per sequence. ``q_mean`` [L][Hq][fc][2], ``q_abs`` [L][Hq][fc].
+    ``capacity`` per sequence. ``q_mean`` [L][Hq][fc][2], ``q_abs`` [L][Hq][fc]
+    (arrays, or per-layer lists when head_dim differs across layers).
     ``segments`` optionally restricts the work to a list of (seq, head).
 
     Returns ``(new_cache, info)``: ``info[(s, g)]`` = dict(raw, s, keep, B, n).
     """
     omega = rope_omega(head_dim, rope_theta) if omega is None else np.asarray(omega, np.float64)
     offsets = default_future_offsets() if offsets is None else np.asarray(offsets, np.int64)
-    n_q = q_mean.shape[1]
+    n_q = len(q_mean[layer])
     groups = heads_of_kv(n_q, n_kv_heads, kv_of_q)
     qc_all = as_complex(q_mean[layer])
     m_all = mlr_weight(q_mean[layer], None if q_abs is None else q_abs[layer])

@@ -134,6 +134,25 @@ def test_load_stats_rejects_ineligible_shapes(lib):
     assert e.value.status == tria.ERR_INVALID_ARG
 
 
+def test_load_stats_hybrid_table_checks(lib):
+    # per-layer head_dim table ([Doc] §6 hybrid models): rejected on the host
+    # before any device allocation
+    def stats(hds, thetas=None):
+        qm = [np.zeros((8, hd // 2 if hd > 0 else 1, 2), np.float32) for hd in hds]
+        return tria.Stats(qm, None, n_kv_heads=2, layer_head_dim=hds, rope_theta=1e4,
+                          layer_rope_theta=thetas, stream=0)
+    for hds in ([128, 0], [127], [64, -2]):
+        with pytest.raises(tria.TriaError) as e:
+            stats(hds)
+        assert e.value.status == tria.ERR_INVALID_ARG, hds
+    with pytest.raises(tria.TriaError) as e:       # no layer passes the gate
+        stats([512, 80, 1024])
+    assert e.value.status == tria.ERR_UNSUPPORTED
+    with pytest.raises(tria.TriaError) as e:       # a theta of a layer <= 1
+        stats([128, 64], thetas=[1e4, 1.0])
+    assert e.value.status == tria.ERR_INVALID_ARG
+
+
 def test_calibration_argument_checks(lib):
     # rejected on the host before any launch (fake, aligned pointers are never touched)
     q, acc = ctypes.c_void_p(0x100000), ctypes.c_void_p(0x200000)
