@@ -167,22 +167,21 @@ extern "C" tria_status tria_load_stats(const tria_stats_desc* d, tria_stats** ou
   int* order_d = nullptr;
   double2* ef_d = nullptr;
   const size_t nqm = (size_t)nq * src_pairs[L];
-  cudaError_t e = cudaSuccess;
   auto fail = [&]() {
     cudaFree(qm_d); cudaFree(qa_d); cudaFree(om_d); cudaFree(off_d); cudaFree(order_d); cudaFree(ef_d);
     cudaFree(s->qe); cudaFree(s->mw); cudaFree(s->turns);
     delete s;
     return TRIA_ERR_CUDA;
   };
-  if ((e = upload(&qm_d, d->q_mean, 2 * nqm)) != cudaSuccess) return fail();
-  if (d->q_abs && (e = upload(&qa_d, d->q_abs, nqm)) != cudaSuccess) return fail();
-  if (d->omega && (e = upload(&om_d, d->omega, (size_t)src_pairs[L])) != cudaSuccess) return fail();
-  if ((e = upload(&off_d, offs.data(), offs.size())) != cudaSuccess) return fail();
-  if ((e = upload(&order_d, order.data(), order.size())) != cudaSuccess) return fail();
-  if ((e = cudaMalloc((void**)&ef_d, fc_max * sizeof(double2))) != cudaSuccess) return fail();
-  if ((e = cudaMalloc((void**)&s->turns, n_turns * sizeof(unsigned long long))) != cudaSuccess) return fail();
-  if ((e = cudaMalloc((void**)&s->qe, n_fold * sizeof(float2))) != cudaSuccess) return fail();
-  if ((e = cudaMalloc((void**)&s->mw, n_fold * sizeof(float))) != cudaSuccess) return fail();
+  if ((upload(&qm_d, d->q_mean, 2 * nqm)) != cudaSuccess) return fail();
+  if (d->q_abs && (upload(&qa_d, d->q_abs, nqm)) != cudaSuccess) return fail();
+  if (d->omega && (upload(&om_d, d->omega, (size_t)src_pairs[L])) != cudaSuccess) return fail();
+  if ((upload(&off_d, offs.data(), offs.size())) != cudaSuccess) return fail();
+  if ((upload(&order_d, order.data(), order.size())) != cudaSuccess) return fail();
+  if ((cudaMalloc((void**)&ef_d, fc_max * sizeof(double2))) != cudaSuccess) return fail();
+  if ((cudaMalloc((void**)&s->turns, n_turns * sizeof(unsigned long long))) != cudaSuccess) return fail();
+  if ((cudaMalloc((void**)&s->qe, n_fold * sizeof(float2))) != cudaSuccess) return fail();
+  if ((cudaMalloc((void**)&s->mw, n_fold * sizeof(float))) != cudaSuccess) return fail();
 
   // one layer at a time (load time, not the pass): its frequencies, then its
   // folded head weights; the folding buffer is reused in stream order
@@ -197,8 +196,8 @@ extern "C" tria_status tria_load_stats(const tria_stats_desc* d, tria_stats** ou
     k_stats_heads<<<blocks, 256, 0, st>>>(1, nq, nkv, G, fc, qm_d + 2 * src, qa_d ? qa_d + src : nullptr,
                                           order_d, ef_d, s->qe + s->qe_off[l], s->mw + s->qe_off[l]);
   }
-  if ((e = cudaGetLastError()) != cudaSuccess) return fail();
-  if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return fail();
+  if ((cudaGetLastError()) != cudaSuccess) return fail();
+  if ((cudaStreamSynchronize(st)) != cudaSuccess) return fail();
   cudaFree(qm_d);
   cudaFree(qa_d);
   cudaFree(om_d);
