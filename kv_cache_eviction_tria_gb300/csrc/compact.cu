@@ -43,12 +43,15 @@ __host__ __device__ inline MoveStage move_stage_layout(int k_rb, int ks_rb, int 
   L.ks = take(kChunk * ks_rb);
   L.v = take(kChunk * v_rb);
   L.vs = take(kChunk * vs_rb);
-  L.pos = take(kChunk * 4);
+  L.pos = -1;   // positions travel in registers and the warp's source-row table
   L.bytes = off;
   return L;
 }
 
-constexpr int kMoveSmemLimit = 216 * 1024;   // with ~6.5 KB of static tables: under the 227 KB per CTA
+// 14 stages of fp16 key + value rows (16 KB each) with ~2.1 KB of static
+// tables: under the 227 KB per CTA, and 152 x 14 warps cover the 2048
+// destination blocks of a 32K-row, 8-head, 25 % layer in one round
+constexpr int kMoveSmemLimit = 224 * 1024;
 constexpr int kMoveMaxWarps = 16;
 
 __host__ __device__ inline int move_warps(const MoveStage& L) {
@@ -139,9 +142,9 @@ struct MoveItem {
 __global__ void k_move(const __grid_constant__ Pass P) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint32_t s_epoch, s_bad;
-  __shared__ int s_nb[kMaxSegments];   // destination blocks of every segment (0: inactive)
   __shared__ int s_nbmax;
-  __shared__ int s_src[kMoveMaxWarps][kChunk];   // moving source rows of each warp's block
+  // moving source rows of each warp's block; once gathered, their positions
+  __shared__ int s_src[kMoveMaxWarps][kChunk];
   const MoveStage L = move_stage_layout(P.k_rb, P.ks_rb, P.v_rb, P.vs_rb);
   if (threadIdx.x == 0) {
     s_epoch = ld_acquire_u32(&P.ctrl->epoch);
@@ -151,13 +154,13 @@ __global__ void k_move(const __grid_constant__ Pass P) {
   // block-major (block j of every segment before block j + 1 of any), so a
   // block's readers - blocks near j * B / n of the same segment - come in
   // earlier rounds of the grid, not beside it
+  auto blocks_of = [&](int sg) {   // destination blocks of a segment (0: inactive)
+    const SegView v = seg_view(P, sg);
+    return v.active ? (v.B + kChunk - 1) / kChunk : 0;
+  };
   if (threadIdx.x == 0) s_nbmax = 0;
   __syncthreads();
-  for (int sg = threadIdx.x; sg < P.n_seg; sg += blockDim.x) {
-    const SegView v = seg_view(P, sg);
-    s_nb[sg] = v.active ? (v.B + kChunk - 1) / kChunk : 0;
-    atomicMax(&s_nbmax, s_nb[sg]);
-  }
+  for (int sg = threadIdx.x; sg < P.n_seg; sg += blockDim.x) atomicMax(&s_nbmax, blocks_of(sg));
   __syncthreads();
   const uint32_t tag = s_epoch + 1u;
   const int total = P.n_seg * s_nbmax;
@@ -167,7 +170,7 @@ __global__ void k_move(const __grid_constant__ Pass P) {
   uint8_t* stg = smem + (size_t)warp * L.bytes;
   int* msrc = s_src[warp];
   const PlaneMap mk = plane_map(P.k_rb, lane), mks = plane_map(P.ks_rb, lane), mv = plane_map(P.v_rb, lane),
-                 mvs = plane_map(P.vs_rb, lane), mp = plane_map(4, lane);
+                 mvs = plane_map(P.vs_rb, lane);
 
   auto row0_of = [&](int sg) {
     const int sq = sg / P.n_kv;
@@ -179,7 +182,7 @@ __global__ void k_move(const __grid_constant__ Pass P) {
     if (t >= total) return;
     m.sg = t % P.n_seg;
     m.j = t / P.n_seg;
-    if (m.j >= s_nb[m.sg]) return;
+    if (m.j >= blocks_of(m.sg)) return;
     m.valid = true;
     const int B = P.seq[m.sg / P.n_kv].budget;
     const int i = m.j * kChunk + lane;
@@ -224,15 +227,21 @@ __global__ void k_move(const __grid_constant__ Pass P) {
       // the previous item's bulk stores must have read the stage
       if (lane == 0) bulk_wait_read_all();
       __syncwarp();
+      int my_pos = 0;
       if (nmove > 0) {
         warp_gather(P.k, row0, mk, stg + L.k, msrc, nmove);
         warp_gather(P.ks, row0, mks, stg + L.ks, msrc, nmove);
         warp_gather(P.v, row0, mv, stg + L.v, msrc, nmove);
         warp_gather(P.vs, row0, mvs, stg + L.vs, msrc, nmove);
-        warp_gather(reinterpret_cast<const uint8_t*>(P.pos), row0, mp, stg + L.pos, msrc, nmove);
+        if (lane < nmove) my_pos = __ldcg(P.pos + row0 + msrc[lane]);
       }
       cp_async_commit();
       cp_async_wait<0>();
+      __syncwarp();
+      // the source table is no longer needed: it holds the positions from
+      // here on (the shared store also completes the position load before
+      // the block is published as read)
+      if (lane < nmove) msrc[lane] = my_pos;
       __syncwarp();
       // publish "read"; then wait for the lower blocks that read my destination rows
       uint32_t* flags = P.flags + (size_t)sg * P.c_max;
@@ -264,7 +273,7 @@ __global__ void k_move(const __grid_constant__ Pass P) {
         }
         warp_scatter(P.ks, row0, P.ks_rb, stg + L.ks, dst0, nmove, lane);
         warp_scatter(P.vs, row0, P.vs_rb, stg + L.vs, dst0, nmove, lane);
-        warp_scatter(reinterpret_cast<uint8_t*>(P.pos), row0, 4, stg + L.pos, dst0, nmove, lane);
+        if (lane < nmove) P.pos[row0 + dst0 + lane] = msrc[lane];
       }
       __syncwarp();
       m = nx;

@@ -617,11 +617,14 @@ __global__ void __launch_bounds__(kScoreThreads, 1) k_score_tc(const __grid_cons
                      kMomTable + (size_t)warp * 2 * kScaleStage;
 
   prefetch_layer_stats(P);
-  score_prologue(P, geo, seg_first, seg_rows, bars, lane);
-  // turn factors of the frequencies in shared memory (the moment-table area,
+  // turn factors of the frequencies: loaded here so that their latency
+  // overlaps the prologue's, kept in shared memory (the moment-table area,
   // which this body does not use)
+  static_assert(FC <= kScoreThreads, "one frequency per thread");
+  const unsigned long long my_turn = (int)threadIdx.x < FC ? __ldg(P.turns + threadIdx.x) : 0ull;
+  score_prologue(P, geo, seg_first, seg_rows, bars, lane);
   unsigned long long* s_turns = reinterpret_cast<unsigned long long*>(seg_rows + (kMaxSegs + 1));
-  for (int i = threadIdx.x; i < FC; i += blockDim.x) s_turns[i] = P.turns[i];
+  if ((int)threadIdx.x < FC) s_turns[threadIdx.x] = my_turn;
   __syncthreads();
 
   const int total = seg_first[P.n_seg];

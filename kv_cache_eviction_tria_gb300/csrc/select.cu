@@ -343,9 +343,12 @@ __global__ void __launch_bounds__(kThreads) k_select(const __grid_constant__ Pas
 // Cluster path: one thread-block cluster of kClusterCtas CTAs per segment. CTA
 // `rank` owns the contiguous, chunk-aligned row range [rank*RPC, rank*RPC+RPC)
 // and keeps the 32-bit keys of its rows in shared memory for all passes.
-// Radix histograms are combined through distributed shared memory after a
-// cluster barrier (every CTA sums all ranks' histograms for itself, so no
-// broadcast step); tie counts and kept counts are exchanged the same way.
+// Radix histograms: each CTA counts its keys locally, then adds its non-zero
+// bins into the cluster-total histogram that every CTA keeps (remote atomic
+// adds through distributed shared memory); after one cluster barrier every
+// CTA holds the totals and finds the cut's bin by itself. Score keys are
+// concentrated in few bins, so the pushes are few, and no CTA reads another's
+// whole histogram. Tie counts and kept counts are read from the other ranks.
 // ---------------------------------------------------------------------------
 
 constexpr int kClusterCtas = 8;
@@ -353,7 +356,8 @@ constexpr int kClThreads = 512;
 constexpr int kClMaxRowsPerCta = 32768;   // 128 KiB of keys
 
 struct ClShared {
-  alignas(16) uint32_t h[2][kHistBins];   // this CTA's histogram, double-buffered by pass
+  alignas(16) uint32_t h[kHistBins];        // this CTA's histogram of the current pass
+  alignas(16) uint32_t tot[2][kHistBins];   // cluster totals, by pass parity (pass p: tot[p & 1])
   int sbuf[40];
   int info[4];                  // prefix, kr, keys in the cut's bin after the current pass
   int cnt[2];                   // ties, strict keeps (gt + protected) of this CTA
@@ -383,40 +387,13 @@ __device__ __forceinline__ void load_raw_row(const float* rp, float* x) {
   }
 }
 
-// Sum of the NB-bin histograms of all cluster ranks for the PER consecutive
-// bins of this thread, read as one PER-word vector per rank. Thread t holds
-// bins NB-1-PER*t-j, j = 0..PER-1 (descending), in tot[j]; returns their sum.
-template <int PER>
-__device__ __forceinline__ int cluster_bins(cg::cluster_group& cluster, uint32_t* hb, int NB, uint32_t* tot) {
-  const int v = NB / PER - 1 - (int)threadIdx.x;   // vector index of this thread's bins
-#pragma unroll
-  for (int j = 0; j < PER; ++j) tot[j] = 0;
-  if (v < 0) return 0;
-  if constexpr (PER == 4) {
-    uint4 r[kClusterCtas];
-#pragma unroll
-    for (int q = 0; q < kClusterCtas; ++q) r[q] = reinterpret_cast<const uint4*>(cluster.map_shared_rank(hb, q))[v];
-#pragma unroll
-    for (int q = 0; q < kClusterCtas; ++q) {
-      tot[0] += r[q].w;
-      tot[1] += r[q].z;
-      tot[2] += r[q].y;
-      tot[3] += r[q].x;
-    }
-  } else {
-    uint2 r[kClusterCtas];
-#pragma unroll
-    for (int q = 0; q < kClusterCtas; ++q) r[q] = reinterpret_cast<const uint2*>(cluster.map_shared_rank(hb, q))[v];
-#pragma unroll
-    for (int q = 0; q < kClusterCtas; ++q) {
-      tot[0] += r[q].y;
-      tot[1] += r[q].x;
-    }
-  }
-  int local = 0;
-#pragma unroll
-  for (int j = 0; j < PER; ++j) local += (int)tot[j];
-  return local;
+// Split cluster barrier (all threads of every CTA): arrive with release
+// semantics, wait with acquire semantics.
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 template <int G>
@@ -443,6 +420,12 @@ __global__ void __launch_bounds__(kClThreads) k_select_cl(const __grid_constant_
   }
   const int lo = sv.sink, hi = n - P.window;
   const bool none = sv.k <= 0;
+  // the cluster-total histograms start at zero; every rank must have cleared
+  // its own before any rank adds into it (the barrier completes before the
+  // first pass, its latency hidden behind the keys)
+  for (int i = threadIdx.x; i < 2 * kHistBins; i += blockDim.x) (&sh.tot[0][0])[i] = 0u;
+  __syncwarp();
+  cluster_arrive_release();
 
   // keys of my rows (the evict path turns raw scores into the z-max score
   // here); loads are batched U rows per thread so that they are in flight
@@ -493,36 +476,69 @@ __global__ void __launch_bounds__(kClThreads) k_select_cl(const __grid_constant_
   uint32_t prefix = 0, T = 0xFFFFFFFFu;
   int kr = sv.k;
   bool cut_at_prefix = false;
+  __syncthreads();
+  cluster_wait_acquire();
   if (!none) {
 #pragma unroll 1
     for (int pass = 0; pass < 3; ++pass) {
       const int NB = pass == 2 ? 1024 : 2048;
-      uint32_t* hb = sh.h[pass & 1];
+      uint32_t* hb = sh.h;
+      uint32_t* T_all = sh.tot[pass & 1];
       for (int i = threadIdx.x; i < NB; i += blockDim.x) hb[i] = 0;
       __syncthreads();
       for (int r = max(r0, lo) + threadIdx.x; r < min(r1, hi); r += blockDim.x) {
         const uint32_t key = keys[r - r0];
-        if (pass == 0) atomicAdd(&hb[key >> 21], 1u);
-        else if (pass == 1) { if ((key >> 21) == prefix) atomicAdd(&hb[(key >> 10) & 0x7FFu], 1u); }
-        else if ((key >> 10) == prefix) atomicAdd(&hb[key & 0x3FFu], 1u);
+        if (pass == 0) {
+          // the top bits of score keys fall in few bins: one add per group
+          // of lanes with the same bin
+          const uint32_t b = key >> 21;
+          const unsigned same = __match_any_sync(__activemask(), b);
+          if ((int)(__ffs(same) - 1) == lane) atomicAdd(&hb[b], (uint32_t)__popc(same));
+        } else if (pass == 1) {
+          if ((key >> 21) == prefix) atomicAdd(&hb[(key >> 10) & 0x7FFu], 1u);
+        } else if ((key >> 10) == prefix) {
+          atomicAdd(&hb[key & 0x3FFu], 1u);
+        }
+      }
+      __syncthreads();
+      // my non-zero bins into every rank's totals (this pass's buffer was
+      // cleared by its owner before the previous barrier)
+      for (int b = threadIdx.x; b < NB; b += blockDim.x) {
+        const uint32_t c = hb[b];
+        if (c != 0u) {
+#pragma unroll
+          for (int q = 0; q < kClusterCtas; ++q) atomicAdd(cluster.map_shared_rank(T_all, q) + b, c);
+        }
       }
       cluster.sync();
-      // every CTA sums all ranks' bins and finds the bin of the kr-th largest
+      // the bin of the kr-th largest key, from this CTA's copy of the totals:
+      // thread t holds bins NB-1-per*t-j, j = 0..per-1 (descending)
       const int per = NB / kClThreads;   // 4 or 2 bins per thread, scanned from the top
-      uint32_t tot[4];
-      const int local = pass == 2 ? cluster_bins<2>(cluster, hb, NB, tot) : cluster_bins<4>(cluster, hb, NB, tot);
+      uint32_t tot[4] = {0u, 0u, 0u, 0u};
+      int local = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (j < per) {
+          tot[j] = T_all[NB - 1 - (per * (int)threadIdx.x + j)];
+          local += (int)tot[j];
+        }
+      }
       int total;
       const int before = block_exclusive_scan(local, &total, sh.sbuf);
       if (before < kr && kr <= before + local) {
         int cum = before;
-        for (int j = 0; j < per; ++j) {
+        bool found = false;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (found || j >= per) continue;
           const int b = NB - 1 - (per * threadIdx.x + j);
           if (cum + (int)tot[j] >= kr) {
             sh.info[0] = (int)(pass == 0 ? (uint32_t)b : pass == 1 ? ((prefix << 11) | (uint32_t)b)
                                                                      : ((prefix << 10) | (uint32_t)b));
             sh.info[1] = kr - cum;
             sh.info[2] = (int)tot[j];   // keys of the cluster in that bin
-            break;
+            found = true;
+            continue;
           }
           cum += (int)tot[j];
         }
@@ -530,6 +546,9 @@ __global__ void __launch_bounds__(kClThreads) k_select_cl(const __grid_constant_
       if (threadIdx.x == 0 && total < kr && rank == 0)
         report(P.ctrl, TRIA_ERR_INVALID_ARG, 0x80000000u | (uint32_t)seg);
       __syncthreads();
+      // clear my copy for pass + 2: the other ranks add into it only after
+      // the next pass's barrier, which this CTA reaches after this
+      for (int i = threadIdx.x; i < NB; i += blockDim.x) T_all[i] = 0u;
       prefix = (uint32_t)sh.info[0];
       kr = sh.info[1];
       if (pass < 2 && kr == sh.info[2]) {

@@ -383,14 +383,21 @@ __device__ void block_run_sums(const Pass& P, int seg, int r_lo, int r_hi, const
 #pragma unroll
   for (int k = 0; k < 1 + 2 * G; ++k) v[k] = 0.f;
   for (int r = r_lo + threadIdx.x; r < r_hi; r += blockDim.x) {
+    // all loads of the run at once (an empty run's mean is not used)
     const float n = __ldcg(&tab[r]);
+    float mean[G], m2[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      mean[h] = __ldcg(&tab[(1 + h) * cs + r]);
+      m2[h] = __ldcg(&tab[(1 + kMaxG + h) * cs + r]);
+    }
     v[0] += n;
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      const float d = n > 0.f ? __ldcg(&tab[(1 + h) * cs + r]) - c[h] : 0.f;
+      const float d = n > 0.f ? mean[h] - c[h] : 0.f;
       const float nd = n * d;
       v[1 + h] += nd;
-      v[1 + G + h] += fmaf(nd, d, __ldcg(&tab[(1 + kMaxG + h) * cs + r]));
+      v[1 + G + h] += fmaf(nd, d, n > 0.f ? m2[h] : 0.f);
     }
   }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (int)(blockDim.x >> 5);
