@@ -343,12 +343,12 @@ __global__ void __launch_bounds__(kThreads) k_select(const __grid_constant__ Pas
 // Cluster path: one thread-block cluster of kClusterCtas CTAs per segment. CTA
 // `rank` owns the contiguous, chunk-aligned row range [rank*RPC, rank*RPC+RPC)
 // and keeps the 32-bit keys of its rows in shared memory for all passes.
-// Radix histograms: each CTA counts its keys locally, then adds its non-zero
-// bins into the cluster-total histogram that every CTA keeps (remote atomic
-// adds through distributed shared memory); after one cluster barrier every
-// CTA holds the totals and finds the cut's bin by itself. Score keys are
-// concentrated in few bins, so the pushes are few, and no CTA reads another's
-// whole histogram. Tie counts and kept counts are read from the other ranks.
+// Radix histograms: each CTA counts its keys locally, then adds each non-zero
+// bin into the cluster total held by the bin's owner (rank = bin / (bins / 8),
+// remote atomic adds through distributed shared memory; score keys fall in
+// few bins, so the adds are few); after one cluster barrier every CTA reads
+// the eight owners' slices (one vector per thread) and finds the cut's bin by
+// itself. Tie counts and kept counts are read from the other ranks.
 // ---------------------------------------------------------------------------
 
 constexpr int kClusterCtas = 8;
@@ -357,7 +357,8 @@ constexpr int kClMaxRowsPerCta = 32768;   // 128 KiB of keys
 
 struct ClShared {
   alignas(16) uint32_t h[kHistBins];        // this CTA's histogram of the current pass
-  alignas(16) uint32_t tot[2][kHistBins];   // cluster totals, by pass parity (pass p: tot[p & 1])
+  // cluster totals of the bins this CTA owns, one buffer per pass (never reused)
+  alignas(16) uint32_t own[3][kHistBins / kClusterCtas];
   int sbuf[40];
   int info[4];                  // prefix, kr, keys in the cut's bin after the current pass
   int cnt[2];                   // ties, strict keeps (gt + protected) of this CTA
@@ -420,10 +421,10 @@ __global__ void __launch_bounds__(kClThreads) k_select_cl(const __grid_constant_
   }
   const int lo = sv.sink, hi = n - P.window;
   const bool none = sv.k <= 0;
-  // the cluster-total histograms start at zero; every rank must have cleared
-  // its own before any rank adds into it (the barrier completes before the
-  // first pass, its latency hidden behind the keys)
-  for (int i = threadIdx.x; i < 2 * kHistBins; i += blockDim.x) (&sh.tot[0][0])[i] = 0u;
+  // the owned totals start at zero; every rank must have cleared its own
+  // before any rank adds into them (the barrier completes before the first
+  // pass, its latency hidden behind the keys)
+  for (int i = threadIdx.x; i < 3 * (kHistBins / kClusterCtas); i += blockDim.x) (&sh.own[0][0])[i] = 0u;
   __syncwarp();
   cluster_arrive_release();
 
@@ -482,46 +483,49 @@ __global__ void __launch_bounds__(kClThreads) k_select_cl(const __grid_constant_
 #pragma unroll 1
     for (int pass = 0; pass < 3; ++pass) {
       const int NB = pass == 2 ? 1024 : 2048;
+      const int SL = NB / kClusterCtas;   // bins per owner
       uint32_t* hb = sh.h;
-      uint32_t* T_all = sh.tot[pass & 1];
+      uint32_t* own = sh.own[pass];
       for (int i = threadIdx.x; i < NB; i += blockDim.x) hb[i] = 0;
       __syncthreads();
       for (int r = max(r0, lo) + threadIdx.x; r < min(r1, hi); r += blockDim.x) {
         const uint32_t key = keys[r - r0];
-        if (pass == 0) {
-          // the top bits of score keys fall in few bins: one add per group
-          // of lanes with the same bin
-          const uint32_t b = key >> 21;
-          const unsigned same = __match_any_sync(__activemask(), b);
-          if ((int)(__ffs(same) - 1) == lane) atomicAdd(&hb[b], (uint32_t)__popc(same));
-        } else if (pass == 1) {
-          if ((key >> 21) == prefix) atomicAdd(&hb[(key >> 10) & 0x7FFu], 1u);
-        } else if ((key >> 10) == prefix) {
-          atomicAdd(&hb[key & 0x3FFu], 1u);
-        }
+        if (pass == 0) atomicAdd(&hb[key >> 21], 1u);
+        else if (pass == 1) { if ((key >> 21) == prefix) atomicAdd(&hb[(key >> 10) & 0x7FFu], 1u); }
+        else if ((key >> 10) == prefix) atomicAdd(&hb[key & 0x3FFu], 1u);
       }
       __syncthreads();
-      // my non-zero bins into every rank's totals (this pass's buffer was
-      // cleared by its owner before the previous barrier)
+      // my non-zero bins into their owners' totals
       for (int b = threadIdx.x; b < NB; b += blockDim.x) {
         const uint32_t c = hb[b];
         if (c != 0u) {
-#pragma unroll
-          for (int q = 0; q < kClusterCtas; ++q) atomicAdd(cluster.map_shared_rank(T_all, q) + b, c);
+          const int q = b / SL;
+          atomicAdd(cluster.map_shared_rank(own, q) + (b - q * SL), c);
         }
       }
       cluster.sync();
-      // the bin of the kr-th largest key, from this CTA's copy of the totals:
-      // thread t holds bins NB-1-per*t-j, j = 0..per-1 (descending)
+      // the bin of the kr-th largest key: thread t reads bins
+      // NB-1-per*t-j, j = 0..per-1 (descending), one vector from their owner
       const int per = NB / kClThreads;   // 4 or 2 bins per thread, scanned from the top
       uint32_t tot[4] = {0u, 0u, 0u, 0u};
       int local = 0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (j < per) {
-          tot[j] = T_all[NB - 1 - (per * (int)threadIdx.x + j)];
-          local += (int)tot[j];
+      {
+        const int b0 = NB - per * ((int)threadIdx.x + 1);   // lowest of my bins
+        const int q = b0 / SL;
+        const uint32_t* src = cluster.map_shared_rank(own, q) + (b0 - q * SL);
+        if (per == 4) {
+          const uint4 v = *reinterpret_cast<const uint4*>(src);
+          tot[0] = v.w;
+          tot[1] = v.z;
+          tot[2] = v.y;
+          tot[3] = v.x;
+        } else {
+          const uint2 v = *reinterpret_cast<const uint2*>(src);
+          tot[0] = v.y;
+          tot[1] = v.x;
         }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) local += (int)tot[j];
       }
       int total;
       const int before = block_exclusive_scan(local, &total, sh.sbuf);
@@ -546,9 +550,6 @@ __global__ void __launch_bounds__(kClThreads) k_select_cl(const __grid_constant_
       if (threadIdx.x == 0 && total < kr && rank == 0)
         report(P.ctrl, TRIA_ERR_INVALID_ARG, 0x80000000u | (uint32_t)seg);
       __syncthreads();
-      // clear my copy for pass + 2: the other ranks add into it only after
-      // the next pass's barrier, which this CTA reaches after this
-      for (int i = threadIdx.x; i < NB; i += blockDim.x) T_all[i] = 0u;
       prefix = (uint32_t)sh.info[0];
       kr = sh.info[1];
       if (pass < 2 && kr == sh.info[2]) {

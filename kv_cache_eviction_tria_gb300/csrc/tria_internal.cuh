@@ -370,53 +370,6 @@ __device__ __forceinline__ int segment_runs(int s0, int s1, int per) {
 // so partial sums over any split of the runs add up (no division per run),
 // and the shifted sums stay small (fp32).
 //
-// block_run_sums: the sums over runs [r_lo, r_hi) of one segment by a whole
-// block: thread t adds runs r_lo + t, r_lo + t + blockDim, ... in order, then
-// fixed butterflies over lanes and warps (deterministic). out (shared, 1 + 2G
-// floats) = {N, sum n d_h, sum (M2 + n d^2)_h}. All threads of the block call it.
-template <int G>
-__device__ void block_run_sums(const Pass& P, int seg, int r_lo, int r_hi, const float* c, float* out) {
-  __shared__ float red[32][1 + 2 * G];
-  const float* tab = run_table(P, seg);
-  const int cs = P.cs_max;
-  float v[1 + 2 * G];
-#pragma unroll
-  for (int k = 0; k < 1 + 2 * G; ++k) v[k] = 0.f;
-  for (int r = r_lo + threadIdx.x; r < r_hi; r += blockDim.x) {
-    // all loads of the run at once (an empty run's mean is not used)
-    const float n = __ldcg(&tab[r]);
-    float mean[G], m2[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      mean[h] = __ldcg(&tab[(1 + h) * cs + r]);
-      m2[h] = __ldcg(&tab[(1 + kMaxG + h) * cs + r]);
-    }
-    v[0] += n;
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float d = n > 0.f ? mean[h] - c[h] : 0.f;
-      const float nd = n * d;
-      v[1 + h] += nd;
-      v[1 + G + h] += fmaf(nd, d, n > 0.f ? m2[h] : 0.f);
-    }
-  }
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (int)(blockDim.x >> 5);
-#pragma unroll
-  for (int mask = 1; mask < 32; mask <<= 1)
-#pragma unroll
-    for (int k = 0; k < 1 + 2 * G; ++k) v[k] += __shfl_xor_sync(0xffffffffu, v[k], mask);
-  if (lane == 0)
-#pragma unroll
-    for (int k = 0; k < 1 + 2 * G; ++k) red[warp][k] = v[k];
-  __syncthreads();
-  if (threadIdx.x < 1 + 2 * G) {
-    float a = 0.f;
-    for (int w = 0; w < nw; ++w) a += red[w][threadIdx.x];
-    out[threadIdx.x] = a;
-  }
-  __syncthreads();
-}
-
 // mean and 1 / (std + 1e-6) of each head from the sums of all runs
 template <int G>
 __device__ __forceinline__ void moments_from_sums(const float* c, const float* sums, float* mu, float* inv) {
@@ -430,24 +383,69 @@ __device__ __forceinline__ void moments_from_sums(const float* c, const float* s
   }
 }
 
-// the shift of the segment's sums (run 0's mean) and its run count
-template <int G>
-__device__ __forceinline__ int segment_shift(const Pass& P, int seg, float* c) {
-  const int s0 = __ldcg(&P.seg[seg].piece_first), s1 = __ldcg(&P.seg[seg].piece_end);
-  const int per = max(1, __ldcg(&P.seg[seg].piece_per));
-  const float* tab = run_table(P, seg);
-#pragma unroll
-  for (int h = 0; h < G; ++h) c[h] = __ldcg(&tab[(1 + h) * P.cs_max]);
-  return segment_runs(s0, s1, per);
-}
-
-// mean and 1 / (std + 1e-6) of the segment's heads, merged by one block
+// Mean and 1 / (std + 1e-6) of the segment's heads, merged by one block
+// (all threads call it). Thread t adds runs t, t + blockDim, ... in order into
+// {N, sum n d_h, sum (M2 + n d^2)_h}, then fixed butterflies over lanes and
+// warps (deterministic). The segment's run layout, the shift c (run 0's mean)
+// and the first round of run partials are loaded together, so the merge waits
+// for one load latency; first-round rows past the run count are loaded and
+// ignored.
 template <int G>
 __device__ void block_segment_moments(const Pass& P, int seg, float* mu, float* inv) {
+  __shared__ float red[32][1 + 2 * G];
   __shared__ float sums[1 + 2 * G];
+  const float* tab = run_table(P, seg);
+  const int cs = P.cs_max;
+  const int s0 = __ldcg(&P.seg[seg].piece_first), s1 = __ldcg(&P.seg[seg].piece_end);
+  const int per = max(1, __ldcg(&P.seg[seg].piece_per));
   float c[G];
-  const int nr = segment_shift<G>(P, seg, c);
-  block_run_sums<G>(P, seg, 0, nr, c, sums);
+#pragma unroll
+  for (int h = 0; h < G; ++h) c[h] = __ldcg(&tab[(1 + h) * cs]);
+  float n = 0.f, mean[G], m2[G];
+  auto load_run = [&](int r) {
+    n = __ldcg(&tab[r]);
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      mean[h] = __ldcg(&tab[(1 + h) * cs + r]);
+      m2[h] = __ldcg(&tab[(1 + kMaxG + h) * cs + r]);
+    }
+  };
+  float v[1 + 2 * G];
+#pragma unroll
+  for (int k = 0; k < 1 + 2 * G; ++k) v[k] = 0.f;
+  auto add_run = [&]() {   // an empty run's mean is not used
+    v[0] += n;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float d = n > 0.f ? mean[h] - c[h] : 0.f;
+      const float nd = n * d;
+      v[1 + h] += nd;
+      v[1 + G + h] += fmaf(nd, d, n > 0.f ? m2[h] : 0.f);
+    }
+  };
+  int r = threadIdx.x;
+  if (r < cs) load_run(r);
+  const int nr = segment_runs(s0, s1, per);
+  if (r < nr) add_run();
+  for (r += blockDim.x; r < nr; r += blockDim.x) {
+    load_run(r);
+    add_run();
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (int)(blockDim.x >> 5);
+#pragma unroll
+  for (int mask = 1; mask < 32; mask <<= 1)
+#pragma unroll
+    for (int k = 0; k < 1 + 2 * G; ++k) v[k] += __shfl_xor_sync(0xffffffffu, v[k], mask);
+  if (lane == 0)
+#pragma unroll
+    for (int k = 0; k < 1 + 2 * G; ++k) red[warp][k] = v[k];
+  __syncthreads();
+  if (threadIdx.x < 1 + 2 * G) {
+    float a = 0.f;
+    for (int w = 0; w < nw; ++w) a += red[w][threadIdx.x];
+    sums[threadIdx.x] = a;
+  }
+  __syncthreads();
   moments_from_sums<G>(c, sums, mu, inv);
 }
 
