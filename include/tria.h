@@ -230,6 +230,16 @@ tria_status tria_evict_profiled(const tria_stats* stats, int32_t layer, const tr
                                 const tria_policy* policy, void* ws, size_t ws_bytes, void* stream,
                                 float* stage_ms, int32_t* launches);
 
+/* tria_evict with the caller's CUDA events (events[4], cudaEvent_t passed as
+ * void*) recorded on `stream` before the scoring kernel, between the kernels
+ * and after the compaction kernel: {start, scored, selected, compacted}.
+ * Does not synchronise, so it can be captured in a CUDA graph; read the
+ * stage times with cudaEventElapsedTime once the stream has reached
+ * events[3]. For benchmarks and tracing. */
+tria_status tria_evict_marked(const tria_stats* stats, int32_t layer, const tria_layer_cache* cache,
+                              const tria_policy* policy, void* ws, size_t ws_bytes, void* stream,
+                              void* const* events);
+
 /* Synchronises `stream`, returns the first device-detected error of the
  * calls since the last check (TRIA_OK if none) and clears it. After
  * TRIA_ERR_TIMEOUT a call may have stopped with its counters mid-way:

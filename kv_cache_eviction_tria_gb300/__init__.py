@@ -35,7 +35,7 @@ NO_PASS = 2 ** 31 - 1
 EXPORTS = (
     "tria_gate_check", "tria_budget_rows", "tria_should_evict", "tria_load_stats", "tria_free_stats",
     "tria_workspace_size", "tria_workspace_init", "tria_score", "tria_select", "tria_compact",
-    "tria_evict", "tria_evict_profiled", "tria_select_noalloc", "tria_device_status", "tria_selftest_bounded_wait",
+    "tria_evict", "tria_evict_profiled", "tria_evict_marked", "tria_select_noalloc", "tria_device_status", "tria_selftest_bounded_wait",
     "tria_calib_accumulate", "tria_calib_finish", "tria_append", "tria_schedule_check", "tria_seq_init",
     "tria_seq_prefill", "tria_seq_decode", "tria_schedule_plan", "tria_schedule_passed",
     "tria_status_string", "tria_version",
@@ -137,6 +137,9 @@ def load_library(path: str | None = None):
     lib.tria_evict_profiled.argtypes = [vp, i32, ctypes.POINTER(_LayerCache), ctypes.POINTER(_Policy), vp, sz,
                                         vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(i32)]
     lib.tria_evict_profiled.restype = i32
+    lib.tria_evict_marked.argtypes = [vp, i32, ctypes.POINTER(_LayerCache), ctypes.POINTER(_Policy), vp, sz, vp,
+                                      ctypes.POINTER(vp)]
+    lib.tria_evict_marked.restype = i32
     lib.tria_device_status.argtypes = [vp, vp]
     lib.tria_device_status.restype = i32
     lib.tria_selftest_bounded_wait.argtypes = [i32, vp, sz, vp]
@@ -385,6 +388,18 @@ def evict_profiled(stats: Stats, layer: int, cache: LayerCache, policy: Policy, 
            "tria_evict_profiled")
     names = ("score", "zscore", "select", "compact", "total")
     return dict(zip(names, list(ms))), nl.value
+
+
+def evict_marked(stats: Stats, layer: int, cache: LayerCache, policy: Policy, events, *, ws, stream=None):
+    """tria_evict_marked: the pass with four torch.cuda.Event (timing) recorded
+    before, between and after its kernels; no synchronisation (capturable)."""
+    c, p = cache.c_struct(), policy.c_struct()
+    wp, wb = _ws(ws)
+    if len(events) != 4:
+        raise ValueError("four events")
+    handles = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(int(e.cuda_event)) for e in events])
+    _check(load_library().tria_evict_marked(stats.handle, layer, ctypes.byref(c), ctypes.byref(p), wp, wb,
+                                            _stream_handle(stream), handles), "tria_evict_marked")
 
 
 def device_status(ws, stream=None) -> int:

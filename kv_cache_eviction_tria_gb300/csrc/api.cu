@@ -343,6 +343,40 @@ extern "C" tria_status tria_evict(const tria_stats* stats, int32_t layer, const 
   return cuda_status(launch_move(P, st));
 }
 
+extern "C" tria_status tria_evict_marked(const tria_stats* stats, int32_t layer, const tria_layer_cache* cache,
+                                         const tria_policy* policy, void* ws, size_t ws_bytes, void* stream,
+                                         void* const* events) {
+  tria_status r;
+  if (!events || !events[0] || !events[1] || !events[2] || !events[3]) return TRIA_ERR_INVALID_ARG;
+  if ((r = check_cache(cache)) != TRIA_OK) return r;
+  if ((r = check_stats(stats, layer, cache)) != TRIA_OK) return r;
+  std::vector<int> budget;
+  if ((r = check_policy(cache, policy, true, budget)) != TRIA_OK) return r;
+  const Layout L = make_layout(cache, stats->group);
+  if ((r = check_ws(ws, ws_bytes, L)) != TRIA_OK) return r;
+  Pass P;
+  fill_pass(P, cache, policy, budget, L, ws, stats->group);
+  set_stats(P, stats, layer);
+  P.only_active = 1;
+  P.raw = (float*)((uint8_t*)ws + L.raw);
+  P.score = (float*)((uint8_t*)ws + L.score);
+  P.score_in = P.score;
+  P.keep = (int32_t*)((uint8_t*)ws + L.keep);
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaEvent_t const* ev = reinterpret_cast<cudaEvent_t const*>(events);
+  // external records: inside a stream capture they become event-record nodes
+  // that can be timed after the graph runs
+  auto mark = [&](int i) { return cudaEventRecordWithFlags(ev[i], st, cudaEventRecordExternal); };
+  cudaError_t e = mark(0);
+  if (e == cudaSuccess) e = launch_score(P, st);
+  if (e == cudaSuccess) e = mark(1);
+  if (e == cudaSuccess) e = launch_select(P, true, st, stats->group);
+  if (e == cudaSuccess) e = mark(2);
+  if (e == cudaSuccess) e = launch_move(P, st);
+  if (e == cudaSuccess) e = mark(3);
+  return cuda_status(e);
+}
+
 extern "C" tria_status tria_evict_profiled(const tria_stats* stats, int32_t layer, const tria_layer_cache* cache,
                                            const tria_policy* policy, void* ws, size_t ws_bytes, void* stream,
                                            float* stage_ms, int32_t* launches) {
