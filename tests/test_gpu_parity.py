@@ -105,6 +105,10 @@ SELECT_CASES = [
     (4, [3000], [3072], [516], 4, 512),                                        # k = 0
     (5, [777, 1000], [800, 1000], [700, 999], 0, 0),                           # no protection
     (6, [20000], [20000], [10000], 1, 3),
+    # larger segments: ragged, no-op and near-budget cases
+    (7, [17000, 9000, 40], [17408, 16384, 64], [4000, 9000, 80], 4, 64),
+    (8, [40000], [40960], [10000], 4, 512),
+    (9, [16384, 16000], [16384, 16384], [4096, 15999], 4, 512),
 ]
 
 
