@@ -193,6 +193,30 @@ __global__ void k_move(const __grid_constant__ Pass P) {
     m.n = *((volatile const int32_t*)(P.n_live + m.sg / P.n_kv));
   };
 
+  // the key / value rows and positions of a staged block to its contiguous
+  // destination rows: one TMA bulk store per plane of the key and value rows
+  // (off the L1 path the gathers use), the small planes with plain stores
+  auto write_out = [&](int64_t row0, int dst0, int nmove) {
+    if (lane == 0) {
+      fence_proxy_async_smem();
+      bulk_s2g(P.k + (size_t)(row0 + dst0) * P.k_rb, stg + L.k, (uint32_t)(nmove * P.k_rb));
+      bulk_s2g(P.v + (size_t)(row0 + dst0) * P.v_rb, stg + L.v, (uint32_t)(nmove * P.v_rb));
+      bulk_commit();
+    }
+    warp_scatter(P.ks, row0, P.ks_rb, stg + L.ks, dst0, nmove, lane);
+    warp_scatter(P.vs, row0, P.vs_rb, stg + L.vs, dst0, nmove, lane);
+    if (lane < nmove) P.pos[row0 + dst0 + lane] = msrc[lane];
+  };
+  // When every block has a warp of its own (one round), all blocks gather,
+  // one grid barrier marks every read done, and all write: the per-block
+  // read flags would be polled while the gathers still load the memory
+  // system, which makes each poll slow. Otherwise blocks publish read flags
+  // and wait only for their readers.
+  const bool one_round = total <= W;
+  bool pend = false;   // one round: a staged block waits for the barrier
+  int64_t pend_row0 = 0;
+  int pend_dst0 = 0, pend_n = 0;
+
   if (s_bad == 0) {
     MoveItem m;
     fetch(blockIdx.x * nwarps_cta + warp, m);
@@ -243,6 +267,13 @@ __global__ void k_move(const __grid_constant__ Pass P) {
       // the block is published as read)
       if (lane < nmove) msrc[lane] = my_pos;
       __syncwarp();
+      if (one_round) {   // the only item of this warp: write after the barrier
+        pend = ok && nmove > 0;
+        pend_row0 = row0;
+        pend_dst0 = i0 + first;
+        pend_n = nmove;
+        break;
+      }
       // publish "read"; then wait for the lower blocks that read my destination rows
       uint32_t* flags = P.flags + (size_t)sg * P.c_max;
       int go = 0;
@@ -260,24 +291,17 @@ __global__ void k_move(const __grid_constant__ Pass P) {
         }
       }
       go = __shfl_sync(0xffffffffu, go, 0);
-      if (go && nmove > 0) {
-        const int dst0 = i0 + first;
-        // key and value rows: one TMA bulk store per plane of the contiguous
-        // destination rows (off the L1 path the gathers use); the small
-        // planes with plain stores
-        if (lane == 0) {
-          fence_proxy_async_smem();
-          bulk_s2g(P.k + (size_t)(row0 + dst0) * P.k_rb, stg + L.k, (uint32_t)(nmove * P.k_rb));
-          bulk_s2g(P.v + (size_t)(row0 + dst0) * P.v_rb, stg + L.v, (uint32_t)(nmove * P.v_rb));
-          bulk_commit();
-        }
-        warp_scatter(P.ks, row0, P.ks_rb, stg + L.ks, dst0, nmove, lane);
-        warp_scatter(P.vs, row0, P.vs_rb, stg + L.vs, dst0, nmove, lane);
-        if (lane < nmove) P.pos[row0 + dst0 + lane] = msrc[lane];
-      }
+      if (go && nmove > 0) write_out(row0, i0 + first, nmove);
       __syncwarp();
       m = nx;
     }
+  }
+  if (one_round && s_bad == 0) {
+    // every warp of the grid (with a block or not) reaches the barrier; after
+    // it every staged block's sources have been read
+    const bool in_time = grid_barrier(P);
+    if (pend && in_time) write_out(pend_row0, pend_dst0, pend_n);
+    __syncwarp();
   }
 
   if (lane == 0) bulk_wait_all();   // this warp's bulk stores are complete

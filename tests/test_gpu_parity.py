@@ -154,6 +154,13 @@ COMPACT_CASES = [
          cur_pos=[0, 0], budget_rows=[300, 399], sink=1, window=5),
     dict(n_kv=2, group=1, hd=32, k_type="f32", v_type="f32", n_live=[129], capacity=[200], cur_pos=[0],
          budget_rows=[2], sink=1, window=1),
+    # more destination blocks than warps in the grid (fp32 rows: 7 warps per
+    # CTA): several rounds, ordered by the per-block read flags; the cases
+    # above take one round and a grid barrier
+    dict(n_kv=4, group=1, hd=128, k_type="f32", v_type="f32", n_live=[40000], capacity=[40000], cur_pos=[0],
+         budget_rows=[20000], sink=4, window=64),
+    dict(n_kv=4, group=1, hd=128, k_type="f16", v_type="q8_0", n_live=[70000, 3000], capacity=[70016, 3008],
+         cur_pos=[0, 0], budget_rows=[17500, 2999], sink=4, window=512),
 ]
 
 
