@@ -40,6 +40,15 @@ constexpr int kScaleRing = kScoreWarps * 2 * kScaleStage;
 constexpr int kScoreSmemMax =
     kScoreWarps * 2 * kPieceBytes + kScoreWarps * 2 * 8 + 2 * (kMaxSegs + 1) * 4 + kMomTable + kScaleRing + 16;
 
+// After a wait that gave up: wait again, bounded, for the copies this warp
+// still has in flight (piece k in stage st and, if issued, piece k + 1 in the
+// other stage), so that the warp does not leave while a bulk copy may still
+// write its shared memory.
+__device__ __forceinline__ void drain_ring(uint64_t* bars, int st, int k, bool next_issued, int limit) {
+  mbar_wait_bounded(&bars[st], (uint32_t)((k >> 1) & 1), limit);
+  if (next_issued) mbar_wait_bounded(&bars[st ^ 1], (uint32_t)(((k + 1) >> 1) & 1), limit);
+}
+
 __device__ __forceinline__ float sqrt_approx(float x) {
   float y;
   asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -393,6 +402,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) k_score(const __grid_constan
     const int64_t grow = seg_row0(seg) + r0;
     if (!mbar_wait_bounded(&bars[st], (uint32_t)((k >> 1) & 1), P.spin_limit)) {
       if (lane == 0) report(P.ctrl, TRIA_ERR_TIMEOUT, (uint32_t)seg);
+      drain_ring(bars, st, k, p + 1 < p_end, P.spin_limit);
       return;
     }
     const uint8_t* buf = ring + st * geo.stage;
@@ -812,6 +822,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1) k_score_tc(const __grid_cons
     const int64_t grow = seg_row0(seg) + r0;
     if (!mbar_wait_bounded(&bars[st], (uint32_t)((kp >> 1) & 1), P.spin_limit)) {
       if (lane == 0) report(P.ctrl, TRIA_ERR_TIMEOUT, (uint32_t)seg);
+      drain_ring(bars, st, kp, p + 1 < p_end, P.spin_limit);
+      if constexpr (kQ8) cp_async_wait<0>();
       return;
     }
     const uint8_t* buf = ring + st * geo.stage;
