@@ -251,6 +251,38 @@ tria_status tria_device_status(void* ws, void* stream);
  * (TRIA_ERR_TIMEOUT expected). Synchronises `stream`. For failure tests. */
 tria_status tria_selftest_bounded_wait(int32_t spin_limit, void* ws, size_t ws_bytes, void* stream);
 
+/* ---- Shared-slot variant -----------------------------------------------
+ * For caches whose token cells are shared by every layer (llama.cpp cells):
+ * one keep-set per token for all layers and KV heads ([Doc] §5 Phase B/C:
+ * per-query-head z-normalisation and max across the GQA group; the Vulkan
+ * port's global z-normalisation shader; [Worklog] cross-layer aggregation).
+ * The pages do not state the combine rule. Reading taken: a token's score is
+ * the maximum of its z-max scores (tria_score, one per layer and KV head)
+ * over all layers and KV heads; NaN scores are ignored unless all are NaN.
+ * A pass over L layers whose caches share one layout:
+ *   tria_score(stats, l, cache_l, ..., scores + l * layer_stride, NULL, ...)  for every l
+ *   tria_shared_combine(scores, layer_stride, L, cache_0, combined, ...)
+ *   tria_shared_select(combined, cache_0, policy, keep, ...)
+ *   tria_compact(cache_l, policy, keep, ...)                                  for every l
+ * Each layer's tria_layer_cache keeps its own n_live array (equal values):
+ * tria_compact sets it for that layer only.
+ *
+ * tria_shared_combine: scores device float [n_layers][layer_stride] (row
+ * index of the cache layout, layer_stride >= the layout's rows); writes
+ * combined[seq_row0[s] + t] for t < n_live[s] (the KV-head-0 slot of every
+ * sequence); other entries are not written. ws: a workspace of this cache
+ * (its control words report a bad n_live, TRIA_ERR_DEVICE_ARG). */
+tria_status tria_shared_combine(const float* scores, int64_t layer_stride, int32_t n_layers,
+                                const tria_layer_cache* cache, float* combined, void* ws, size_t ws_bytes,
+                                void* stream);
+
+/* tria_shared_select: selects on the combined scores of every sequence (the
+ * rules of tria_select, one segment per sequence) and writes the keep list to
+ * keep_out[seq_row0[s] + g * capacity[s] + i] for every KV head g, i.e. the
+ * same list in every segment of the sequence, as tria_compact reads it. */
+tria_status tria_shared_select(const float* combined, const tria_layer_cache* cache, const tria_policy* policy,
+                               int32_t* keep_out, void* ws, size_t ws_bytes, void* stream);
+
 /* ---- Decode-loop lifecycle ---------------------------------------------
  * A decode loop appends rows to each sequence and runs a pass when its
  * schedule says so. Sources, [Worklog] sections: "Why this is still fair even

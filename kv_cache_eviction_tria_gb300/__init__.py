@@ -38,6 +38,7 @@ EXPORTS = (
     "tria_evict", "tria_evict_profiled", "tria_evict_marked", "tria_select_noalloc", "tria_device_status", "tria_selftest_bounded_wait",
     "tria_calib_accumulate", "tria_calib_finish", "tria_append", "tria_schedule_check", "tria_seq_init",
     "tria_seq_prefill", "tria_seq_decode", "tria_schedule_plan", "tria_schedule_passed",
+    "tria_shared_combine", "tria_shared_select",
     "tria_status_string", "tria_version",
 )
 
@@ -148,6 +149,10 @@ def load_library(path: str | None = None):
     lib.tria_calib_accumulate.restype = i32
     lib.tria_calib_finish.argtypes = [vp, i64, i32, i32, vp, vp, vp]
     lib.tria_calib_finish.restype = i32
+    lib.tria_shared_combine.argtypes = [vp, i64, i32, ctypes.POINTER(_LayerCache), vp, vp, sz, vp]
+    lib.tria_shared_combine.restype = i32
+    lib.tria_shared_select.argtypes = [vp, ctypes.POINTER(_LayerCache), ctypes.POINTER(_Policy), vp, vp, sz, vp]
+    lib.tria_shared_select.restype = i32
     lib.tria_append.argtypes = [ctypes.POINTER(_LayerCache), vp, vp, vp, vp, vp, i32, vp, sz, vp]
     lib.tria_append.restype = i32
     sch_p, st_p, i32_p = ctypes.POINTER(_Schedule), ctypes.POINTER(_SeqState), ctypes.POINTER(i32)
@@ -438,6 +443,27 @@ def calib_finish(acc, n_tokens: int, *, stream=None):
     _check(load_library().tria_calib_finish(_ptr(acc), n_tokens, h, 2 * fc, _ptr(q_mean), _ptr(q_abs),
                                             _stream_handle(stream)), "tria_calib_finish")
     return q_mean, q_abs
+
+
+# --------------------------------------------------------------------------- shared-slot variant
+
+def shared_combine(scores, cache: LayerCache, combined, *, ws, stream=None):
+    """tria_shared_combine: scores float32 CUDA tensor [layers][rows] (tria_score output per layer)."""
+    if scores.dim() != 2:
+        raise ValueError("scores must be [layers][rows]")
+    c = cache.c_struct()
+    wp, wb = _ws(ws)
+    _check(load_library().tria_shared_combine(_ptr(scores), scores.stride(0), scores.shape[0], ctypes.byref(c),
+                                              _ptr(combined), wp, wb, _stream_handle(stream)),
+           "tria_shared_combine")
+
+
+def shared_select(combined, cache: LayerCache, policy: Policy, keep_out, *, ws, stream=None):
+    """tria_shared_select: one keep list per sequence, written to every KV head's slot."""
+    c, p = cache.c_struct(), policy.c_struct()
+    wp, wb = _ws(ws)
+    _check(load_library().tria_shared_select(_ptr(combined), ctypes.byref(c), ctypes.byref(p), _ptr(keep_out),
+                                             wp, wb, _stream_handle(stream)), "tria_shared_select")
 
 
 # --------------------------------------------------------------------------- decode-loop lifecycle

@@ -275,6 +275,46 @@ extern "C" tria_status tria_select(const float* score, const tria_layer_cache* c
   return cuda_status(launch_select(P, true, (cudaStream_t)stream));
 }
 
+extern "C" tria_status tria_shared_combine(const float* scores, int64_t layer_stride, int32_t n_layers,
+                                           const tria_layer_cache* cache, float* combined, void* ws,
+                                           size_t ws_bytes, void* stream) {
+  tria_status r;
+  if ((r = check_cache(cache)) != TRIA_OK) return r;
+  if (!scores || !combined || !aligned(scores, 4) || !aligned(combined, 4) || n_layers < 1) return TRIA_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, 256) || ws_bytes < sizeof(Ctrl)) return TRIA_ERR_WORKSPACE;
+  const Layout L = make_layout(cache, 0);
+  if (layer_stride < L.total_rows) return TRIA_ERR_INVALID_ARG;   // layers must not overlap
+  Pass P;
+  fill_pass(P, cache, nullptr, {}, L, ws, 0);
+  return cuda_status(launch_shared_combine(P, scores, layer_stride, n_layers, combined, (cudaStream_t)stream));
+}
+
+extern "C" tria_status tria_shared_select(const float* combined, const tria_layer_cache* cache,
+                                          const tria_policy* policy, int32_t* keep_out, void* ws, size_t ws_bytes,
+                                          void* stream) {
+  tria_status r;
+  if ((r = check_cache(cache)) != TRIA_OK) return r;
+  if (!combined || !keep_out || !aligned(combined, 4) || !aligned(keep_out, 4)) return TRIA_ERR_INVALID_ARG;
+  std::vector<int> budget;
+  if ((r = check_policy(cache, policy, false, budget)) != TRIA_OK) return r;
+  // the selection runs on the KV-head-0 slot of every sequence
+  tria_layer_cache view = *cache;
+  view.n_kv_heads = 1;
+  const Layout L = make_layout(&view, 0);
+  if ((r = check_ws(ws, ws_bytes, L)) != TRIA_OK) return r;
+  Pass P;
+  fill_pass(P, &view, policy, budget, L, ws, 0);
+  P.only_active = 0;
+  P.score_in = combined;
+  P.keep = keep_out;
+  cudaStream_t st = (cudaStream_t)stream;
+  if ((r = cuda_status(launch_select(P, true, st))) != TRIA_OK) return r;
+  if (cache->n_kv_heads == 1) return TRIA_OK;
+  Pass B;
+  fill_pass(B, cache, policy, budget, make_layout(cache, 0), ws, 0);
+  return cuda_status(launch_shared_broadcast(B, keep_out, st));
+}
+
 extern "C" tria_status tria_append(const tria_layer_cache* cache, const void* k_new, const void* k_scale_new,
                                    const void* v_new, const void* v_scale_new, const int32_t* pos_new,
                                    int32_t n_tokens, void* ws, size_t ws_bytes, void* stream) {

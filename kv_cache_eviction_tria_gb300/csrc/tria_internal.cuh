@@ -511,6 +511,10 @@ struct AppendSrc {
   int32_t n_tokens;
 };
 cudaError_t launch_append(const Pass& P, const AppendSrc& a, cudaStream_t st);
+// shared.cu: shared-slot variant (one keep-set per token for all layers)
+cudaError_t launch_shared_combine(const Pass& P, const float* scores, int64_t stride, int n_layers, float* combined,
+                                  cudaStream_t st);
+cudaError_t launch_shared_broadcast(const Pass& P, int32_t* keep, cudaStream_t st);
 // stats.cu
 struct StatsDevice;
 

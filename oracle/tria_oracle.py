@@ -42,6 +42,9 @@ Readings where the pages are silent:
   B < sink + window is an error.
 * Compaction writes kept row i (ascending original order) to row i of K, V,
   the q8_0 scales and pos; rows at or past B keep their old contents.
+* Shared-slot cells (one keep-set per token for all layers): the pages do
+  not state the combine rule; a token's score is the maximum of its z-max
+  scores over all layers and KV heads (NaN ignored unless all are NaN).
 * Calibration ([Doc] §2: per-layer, per-head statistics of the pre-RoPE
   queries, "mean query directions + per-frequency importance weights";
   §5 Phase C: q_mean / q_abs arrays [layers][heads][frequency pairs]):
@@ -268,6 +271,60 @@ def evict_layer(layer_cache: dict, q_mean: np.ndarray, q_abs, *, layer: int, n_k
              else budget_rows(budget_frac, n_ctx[s]))
         if n > b:
             out["n_live"][s] = b
+    return out, info
+
+
+def shared_evict(layer_caches: list, q_mean, q_abs, *, n_kv_heads: int, head_dim: int, rope_theta: float,
+                 cur_pos, n_ctx, budget_frac: float, window: int, sink: int, offsets=None, kv_of_q=None,
+                 budget_rows_override=None):
+    """Shared-slot pass: one keep-set per token for every layer and KV head
+    (cells shared by all layers; [Doc] Phase B/C, the Vulkan port's global
+    z-normalisation shader; [Worklog] cross-layer aggregation).
+
+    The pages do not state how a token's per-(layer, KV head) scores combine.
+    Reading: the combined score is the maximum of the token's z-max scores
+    over all layers and KV heads, NaN ignored unless all are NaN (np.fmax),
+    i.e. the GQA max rule of Phase C extended to every head of every layer.
+    ``layer_caches[l]`` has the layout of :func:`evict_layer`; all layers
+    share seq_row0, capacity and n_live.
+
+    Returns ``(new_caches, info)``; ``info[s]`` = dict(combined, keep, B, n).
+    """
+    omega = rope_omega(head_dim, rope_theta)
+    offsets = default_future_offsets() if offsets is None else np.asarray(offsets, np.int64)
+    base = layer_caches[0]
+    n_seqs = len(base["n_live"])
+    out = [{key: (None if val is None else np.array(val, copy=True)) for key, val in c.items()}
+           for c in layer_caches]
+    info = {}
+    for s in range(n_seqs):
+        n = int(base["n_live"][s])
+        cap = int(base["capacity"][s])
+        row0 = int(base["seq_row0"][s])
+        combined = np.full(n, np.nan)
+        for layer, cache in enumerate(layer_caches):
+            groups = heads_of_kv(len(q_mean[layer]), n_kv_heads, kv_of_q)
+            qc = as_complex(q_mean[layer])
+            mw = mlr_weight(q_mean[layer], None if q_abs is None else q_abs[layer])
+            for g in range(n_kv_heads):
+                r0 = row0 + g * cap
+                ks = None if cache.get("k_scale") is None else cache["k_scale"][r0:r0 + n]
+                kf = keys_f64(cache["k"][r0:r0 + n], ks)
+                _, sc = segment_scores(kf, qc[groups[g]], mw[groups[g]], omega, int(cur_pos[s]), offsets)
+                combined = np.fmax(combined, sc)
+        b = (int(budget_rows_override[s]) if budget_rows_override is not None
+             else budget_rows(budget_frac, n_ctx[s]))
+        keep = select_keep(combined, n, b, _per_seq(sink, s), window)
+        info[s] = {"combined": combined, "keep": keep, "B": b, "n": n}
+        if n <= b:
+            continue
+        for o in out:
+            for g in range(n_kv_heads):
+                r0 = row0 + g * cap
+                for name in ("k", "k_scale", "v", "v_scale", "pos"):
+                    if o.get(name) is not None:
+                        o[name][r0:r0 + cap] = compact_rows(o[name][r0:r0 + cap], keep)
+            o["n_live"][s] = b
     return out, info
 
 
