@@ -119,6 +119,39 @@ def test_host_validation_rejects_before_any_launch(lib):
         == tria.ERR_WORKSPACE
 
 
+def test_shared_slot_and_append_argument_checks(lib):
+    # rejected on the host before any launch (fake, aligned pointers are never touched)
+    c = _fake_cache()
+    cs = c.c_struct()
+    good = tria.Policy(budget_frac=0.5, n_ctx=[1000, 900], window=64, sink=4, cur_pos=[1000, 900])
+    ps = good.c_struct()
+    rows = 8 * 1000 + 8 * 900
+    comb = lambda scores, stride, nl, out, ws, nb: tria.raw_call(
+        "tria_shared_combine", ctypes.c_void_p(scores), stride, nl, ctypes.byref(cs), ctypes.c_void_p(out),
+        ctypes.c_void_p(ws), nb, None)
+    assert comb(0x40000, rows - 1, 2, 0x50000, 0x100000, 4096) == tria.ERR_INVALID_ARG     # layers overlap
+    assert comb(0x40000, rows, 0, 0x50000, 0x100000, 4096) == tria.ERR_INVALID_ARG         # no layer
+    assert comb(0, rows, 1, 0x50000, 0x100000, 4096) == tria.ERR_INVALID_ARG
+    assert comb(0x40002, rows, 1, 0x50000, 0x100000, 4096) == tria.ERR_INVALID_ARG         # misaligned
+    assert comb(0x40000, rows, 1, 0x50000, 0x100010, 4096) == tria.ERR_WORKSPACE
+    assert comb(0x40000, rows, 1, 0x50000, 0x100000, 16) == tria.ERR_WORKSPACE
+    sel = lambda pol, keep, nb: tria.raw_call(
+        "tria_shared_select", ctypes.c_void_p(0x50000), ctypes.byref(cs), ctypes.byref(pol.c_struct()),
+        ctypes.c_void_p(keep), ctypes.c_void_p(0x100000), nb, None)
+    assert sel(good, 0, 1 << 30) == tria.ERR_INVALID_ARG
+    assert sel(good, 0x60000, 16) == tria.ERR_WORKSPACE
+    assert sel(tria.Policy(budget_frac=0.05, n_ctx=[1000, 900], window=64, sink=4), 0x60000, 1 << 30) \
+        == tria.ERR_BUDGET
+    app = lambda k, ks, v, pos, n, ws: tria.raw_call(
+        "tria_append", ctypes.byref(cs), ctypes.c_void_p(k), ctypes.c_void_p(ks), ctypes.c_void_p(v),
+        None, ctypes.c_void_p(pos), n, ctypes.c_void_p(ws), 1 << 20, None)
+    assert app(0x40000, 0, 0x48000, 0x50000, -1, 0x100000) == tria.ERR_INVALID_ARG
+    assert app(0x40000, 0, 0x48000, 0x50000, 1, 0x100010) == tria.ERR_WORKSPACE
+    assert app(0x40008, 0, 0x48000, 0x50000, 1, 0x100000) == tria.ERR_INVALID_ARG         # k not 16-aligned
+    assert app(0x40000, 0x30000, 0x48000, 0x50000, 1, 0x100000) == tria.ERR_INVALID_ARG   # scale for fp16
+    assert app(0, 0, 0, 0, 0, 0x100000) == tria.OK                                        # nothing to append
+
+
 def test_load_stats_rejects_ineligible_shapes(lib):
     qm = np.zeros((1, 30, 64, 2), np.float32)
     with pytest.raises(tria.TriaError) as e:
