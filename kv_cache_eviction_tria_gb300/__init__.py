@@ -449,8 +449,9 @@ def calib_finish(acc, n_tokens: int, *, stream=None):
 
 def shared_combine(scores, cache: LayerCache, combined, *, ws, stream=None):
     """tria_shared_combine: scores float32 CUDA tensor [layers][rows] (tria_score output per layer)."""
-    if scores.dim() != 2:
-        raise ValueError("scores must be [layers][rows]")
+    rows = int(max(r0 + cache.n_kv_heads * c for r0, c in zip(cache.seq_row0, cache.capacity)))
+    if scores.dim() != 2 or scores.stride(1) != 1 or scores.shape[1] < rows:
+        raise ValueError("scores must be [layers][rows] (rows contiguous, at least the cache layout's rows)")
     c = cache.c_struct()
     wp, wb = _ws(ws)
     _check(load_library().tria_shared_combine(_ptr(scores), scores.stride(0), scores.shape[0], ctypes.byref(c),
@@ -471,7 +472,15 @@ def shared_select(combined, cache: LayerCache, policy: Policy, keep_out, *, ws, 
 def append(cache: LayerCache, k_new, v_new, pos_new, *, ws, k_scale_new=None, v_scale_new=None, stream=None):
     """tria_append: rows k_new / v_new [n_seqs][n_kv_heads][n_tokens][...] (cache dtypes) and
     pos_new int32 [n_seqs][n_tokens] after the live rows of every segment; n_live += n_tokens."""
-    n_tokens = int(pos_new.shape[-1]) if pos_new.dim() == 2 else 0
+    n_seqs = len(cache.seq_row0)
+    if pos_new.dim() != 2 or pos_new.shape[0] != n_seqs or pos_new.dtype.itemsize != 4:
+        raise ValueError("pos_new must be int32 [n_seqs][n_tokens]")
+    n_tokens = int(pos_new.shape[-1])
+    row_bytes = {F32: 4, F16: 2, Q8_0: 1}
+    for name, t, dt in (("k_new", k_new, cache.k_type), ("v_new", v_new, cache.v_type)):
+        want = n_seqs * cache.n_kv_heads * n_tokens * cache.head_dim * row_bytes[dt]
+        if t is None or not t.is_contiguous() or t.numel() * t.element_size() != want:
+            raise ValueError(f"{name} must be contiguous [n_seqs][n_kv_heads][n_tokens][head_dim] rows of the cache type")
     c = cache.c_struct()
     wp, wb = _ws(ws)
     _check(load_library().tria_append(ctypes.byref(c), _ptr(k_new), _ptr(k_scale_new), _ptr(v_new),
