@@ -57,6 +57,7 @@ def _planes(cfg, seed=3):
 class Loop:
     def __init__(self, lib, cfg, planes, qm, qa):
         self.lib, self.cfg, self.planes = lib, cfg, planes
+        self.stats_q = (qm, qa)
         caps, n_kv, hd = cfg["capacity"], cfg["n_kv"], cfg["hd"]
         self.row0 = np.cumsum([0] + [n_kv * c for c in caps[:-1]]).astype(np.int64)
         rows = int(sum(n_kv * c for c in caps))
@@ -176,7 +177,6 @@ class Loop:
 def test_decode_loop_matches_oracle(lib, cfg):
     planes, qm, qa = _planes(cfg)
     loop = Loop(lib, cfg, planes, qm, qa)
-    loop.stats_q = (qm, qa)
     final = loop.run(check=True)
     # the schedule the library ran is the oracle's schedule
     trig = "length" if cfg["schedule"]["trigger"] == 0 else "interval"
