@@ -230,6 +230,9 @@ EVICT_CASES = [
          budget_frac=0.5, window=512, sink=4),
     dict(n_kv=2, group=1, hd=96, k_type="f16", v_type="q8_0", n_live=[999], capacity=[1000], cur_pos=[12],
          budget_rows=[500], window=0, sink=0),
+    # the most segments one call takes: 128 sequences x 8 KV heads, ragged short rows
+    dict(n_kv=8, group=4, hd=64, k_type="f16", v_type="f16", n_live=[40 + (i * 37) % 200 for i in range(128)],
+         capacity=[256] * 128, cur_pos=[300 + 7 * i for i in range(128)], budget_frac=0.5, window=8, sink=2),
 ]
 
 
