@@ -221,6 +221,18 @@ tria_status tria_compact(const tria_layer_cache* cache, const tria_policy* polic
 tria_status tria_evict(const tria_stats* stats, int32_t layer, const tria_layer_cache* cache,
                        const tria_policy* policy, void* ws, size_t ws_bytes, void* stream);
 
+/* tria_evict over sequences of different layers in one call (the pass is
+ * per segment, so layers only change which statistics a segment uses): the
+ * caller lays several layers' caches out as the sequences of one
+ * tria_layer_cache (for instance one allocation per plane, a layer's rows
+ * after the previous layer's) and sequence s is scored with the statistics of
+ * layer layer_of_seq[s] (host int32 [n_seqs]). All those layers must be loaded,
+ * have the cache's head_dim and the same RoPE frequencies (else
+ * TRIA_ERR_UNSUPPORTED). The fixed costs of a pass (launches, ramps) are paid
+ * once for all of them. */
+tria_status tria_evict_layers(const tria_stats* stats, const int32_t* layer_of_seq, const tria_layer_cache* cache,
+                              const tria_policy* policy, void* ws, size_t ws_bytes, void* stream);
+
 /* tria_evict with CUDA events recorded on `stream` between its stages;
  * synchronises `stream` and writes the stage times in milliseconds to
  * stage_ms[5] = {raw scores, z-max scores (0: computed inside select), select,

@@ -35,7 +35,7 @@ NO_PASS = 2 ** 31 - 1
 EXPORTS = (
     "tria_gate_check", "tria_budget_rows", "tria_should_evict", "tria_load_stats", "tria_free_stats",
     "tria_workspace_size", "tria_workspace_init", "tria_score", "tria_select", "tria_compact",
-    "tria_evict", "tria_evict_profiled", "tria_evict_marked", "tria_select_noalloc", "tria_device_status", "tria_selftest_bounded_wait",
+    "tria_evict", "tria_evict_layers", "tria_evict_profiled", "tria_evict_marked", "tria_select_noalloc", "tria_device_status", "tria_selftest_bounded_wait",
     "tria_calib_accumulate", "tria_calib_finish", "tria_append", "tria_schedule_check", "tria_seq_init",
     "tria_seq_prefill", "tria_seq_decode", "tria_schedule_plan", "tria_schedule_passed",
     "tria_shared_combine", "tria_shared_select",
@@ -135,6 +135,9 @@ def load_library(path: str | None = None):
     lib.tria_compact.restype = i32
     lib.tria_evict.argtypes = [vp, i32, ctypes.POINTER(_LayerCache), ctypes.POINTER(_Policy), vp, sz, vp]
     lib.tria_evict.restype = i32
+    lib.tria_evict_layers.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(_LayerCache), ctypes.POINTER(_Policy),
+                                      vp, sz, vp]
+    lib.tria_evict_layers.restype = i32
     lib.tria_evict_profiled.argtypes = [vp, i32, ctypes.POINTER(_LayerCache), ctypes.POINTER(_Policy), vp, sz,
                                         vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(i32)]
     lib.tria_evict_profiled.restype = i32
@@ -380,6 +383,18 @@ def evict(stats: Stats, layer: int, cache: LayerCache, policy: Policy, *, ws, st
     wp, wb = _ws(ws)
     _check(load_library().tria_evict(stats.handle, layer, ctypes.byref(c), ctypes.byref(p), wp, wb,
                                      _stream_handle(stream)), "tria_evict")
+
+
+def evict_layers(stats: Stats, layer_of_seq, cache: LayerCache, policy: Policy, *, ws, stream=None):
+    """tria_evict_layers: one pass over sequences of several layers (sequence s
+    scored with the statistics of layer layer_of_seq[s])."""
+    c, p = cache.c_struct(), policy.c_struct()
+    wp, wb = _ws(ws)
+    arr, ptr = _host_array(layer_of_seq, np.int32, ctypes.c_int32)
+    if arr is None or len(arr) != len(cache.seq_row0):
+        raise ValueError("one layer per sequence")
+    _check(load_library().tria_evict_layers(stats.handle, ptr, ctypes.byref(c), ctypes.byref(p), wp, wb,
+                                            _stream_handle(stream)), "tria_evict_layers")
 
 
 def evict_profiled(stats: Stats, layer: int, cache: LayerCache, policy: Policy, *, ws, stream=None):

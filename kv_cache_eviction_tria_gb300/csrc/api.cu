@@ -200,9 +200,10 @@ tria_status check_stats(const tria_stats* st, int layer, const tria_layer_cache*
 }
 
 void set_stats(Pass& P, const tria_stats* st, int layer) {
-  P.qe = st->qe + st->qe_off[layer];
-  P.mw = st->mw + st->qe_off[layer];
+  P.qe = st->qe;
+  P.mw = st->mw;
   P.turns = st->turns + st->turns_off[layer];
+  for (int s = 0; s < P.n_seqs; ++s) P.seq[s].qe_off = (int32_t)st->qe_off[layer];
 }
 
 }  // namespace
@@ -372,6 +373,42 @@ extern "C" tria_status tria_evict(const tria_stats* stats, int32_t layer, const 
   Pass P;
   fill_pass(P, cache, policy, budget, L, ws, stats->group);
   set_stats(P, stats, layer);
+  P.only_active = 1;
+  P.raw = (float*)((uint8_t*)ws + L.raw);
+  P.score = (float*)((uint8_t*)ws + L.score);
+  P.score_in = P.score;
+  P.keep = (int32_t*)((uint8_t*)ws + L.keep);
+  cudaStream_t st = (cudaStream_t)stream;
+  if ((r = cuda_status(launch_score(P, st))) != TRIA_OK) return r;
+  if ((r = cuda_status(launch_select(P, true, st, stats->group))) != TRIA_OK) return r;
+  return cuda_status(launch_move(P, st));
+}
+
+extern "C" tria_status tria_evict_layers(const tria_stats* stats, const int32_t* layer_of_seq,
+                                         const tria_layer_cache* cache, const tria_policy* policy, void* ws,
+                                         size_t ws_bytes, void* stream) {
+  tria_status r;
+  if ((r = check_cache(cache)) != TRIA_OK) return r;
+  if (!layer_of_seq) return TRIA_ERR_INVALID_ARG;
+  const int l0 = layer_of_seq[0];
+  if ((r = check_stats(stats, l0, cache)) != TRIA_OK) return r;
+  // every layer of the call: loaded, the cache's head_dim, the first layer's phases
+  const int64_t f0 = stats->freq_off[l0], f1 = stats->freq_off[l0 + 1];
+  for (int s = 1; s < cache->n_seqs; ++s) {
+    const int l = layer_of_seq[s];
+    if ((r = check_stats(stats, l, cache)) != TRIA_OK) return r;
+    if (stats->freq_off[l + 1] - stats->freq_off[l] != f1 - f0) return TRIA_ERR_UNSUPPORTED;
+    for (int64_t i = 0; i < f1 - f0; ++i)
+      if (stats->freq[stats->freq_off[l] + i] != stats->freq[f0 + i]) return TRIA_ERR_UNSUPPORTED;
+  }
+  std::vector<int> budget;
+  if ((r = check_policy(cache, policy, true, budget)) != TRIA_OK) return r;
+  const Layout L = make_layout(cache, stats->group);
+  if ((r = check_ws(ws, ws_bytes, L)) != TRIA_OK) return r;
+  Pass P;
+  fill_pass(P, cache, policy, budget, L, ws, stats->group);
+  set_stats(P, stats, l0);
+  for (int s = 0; s < cache->n_seqs; ++s) P.seq[s].qe_off = (int32_t)stats->qe_off[layer_of_seq[s]];
   P.only_active = 1;
   P.raw = (float*)((uint8_t*)ws + L.raw);
   P.score = (float*)((uint8_t*)ws + L.score);

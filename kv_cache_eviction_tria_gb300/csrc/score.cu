@@ -177,8 +177,8 @@ __host__ __device__ inline int score_smem_bytes_for(int k_rb) {
   return kScoreWarps * 2 * g.stage + kScoreWarps * 2 * 8 + 2 * (kMaxSegs + 1) * 4 + kMomTable + kScaleRing + 16;
 }
 
-// Ask L2 for this layer's weight inputs (qbar E, M, turn factors: a few tens
-// of KB) before the key stream starts, so that the warps' weight loads hit L2
+// Ask L2 for the weight inputs of the first sequence's layer (qbar E, M, turn
+// factors: a few tens of KB) before the key stream starts, so that the warps' weight loads hit L2
 // instead of queueing in DRAM behind the first pieces. Lines are dealt over
 // all threads of the grid.
 __device__ __forceinline__ void prefetch_layer_stats(const Pass& P) {
@@ -187,8 +187,8 @@ __device__ __forceinline__ void prefetch_layer_stats(const Pass& P) {
                lines_t = ((size_t)P.fc * 8 + 127) / 128;
   const size_t total = lines_qe + lines_mw + lines_t;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
-    const char* a = i < lines_qe ? reinterpret_cast<const char*>(P.qe) + 128 * i
-                    : i < lines_qe + lines_mw ? reinterpret_cast<const char*>(P.mw) + 128 * (i - lines_qe)
+    const char* a = i < lines_qe ? reinterpret_cast<const char*>(P.qe + P.seq[0].qe_off) + 128 * i
+                    : i < lines_qe + lines_mw ? reinterpret_cast<const char*>(P.mw + P.seq[0].qe_off) + 128 * (i - lines_qe)
                                               : reinterpret_cast<const char*>(P.turns) + 128 * (i - lines_qe - lines_mw);
     asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
   }
@@ -320,8 +320,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1) k_score(const __grid_constan
         cs[j] = 0.f;
       }
     }
-    const float2* qe = P.qe + (size_t)v.g * G * fc;
-    const float* mw = P.mw + (size_t)v.g * G * fc;
+    const float2* qe = P.qe + P.seq[v.s].qe_off + (size_t)v.g * G * fc;
+    const float* mw = P.mw + P.seq[v.s].qe_off + (size_t)v.g * G * fc;
 #pragma unroll
     for (int h = 0; h < G; ++h)
 #pragma unroll
@@ -686,8 +686,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1) k_score_tc(const __grid_cons
   float unscale[kHeads];
   auto load_consts = [&](const SegView& v) {
     const unsigned long long pos = (unsigned long long)P.seq[v.s].cur_pos;
-    const float2* qe = P.qe + ((size_t)v.g * G + hl) * FC;
-    const float* mw = P.mw + ((size_t)v.g * G + hl) * FC;
+    const float2* qe = P.qe + P.seq[v.s].qe_off + ((size_t)v.g * G + hl) * FC;
+    const float* mw = P.mw + P.seq[v.s].qe_off + ((size_t)v.g * G + hl) * FC;
     // inputs of this lane's frequencies f = 32 s + 8 q + j (s < S / 2) of head
     // hl, all loaded up front
     float2 a[S / 2][8];

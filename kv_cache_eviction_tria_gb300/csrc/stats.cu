@@ -148,6 +148,14 @@ extern "C" tria_status tria_load_stats(const tria_stats_desc* d, tria_stats** ou
   s->head_dim = hd;
   s->qe_off.assign(L, -1);
   s->turns_off.assign(L, -1);
+  // host copy of each layer's frequency definition (the base, or the given
+  // frequencies), to check that layers scored in one call share their phases
+  s->freq_off.assign(L + 1, 0);
+  for (int l = 0; l < L; ++l) {
+    if (d->omega) s->freq.insert(s->freq.end(), d->omega + src_pairs[l], d->omega + src_pairs[l + 1]);
+    else s->freq.push_back(theta[l]);
+    s->freq_off[l + 1] = (int64_t)s->freq.size();
+  }
   int64_t n_fold = 0, n_turns = 0;
   int fc_max = 1;
   for (int l = 0; l < L; ++l) {

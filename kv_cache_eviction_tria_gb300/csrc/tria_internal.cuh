@@ -81,7 +81,7 @@ struct SeqInfo {
   int32_t cap;           // rows per segment
   int32_t budget;        // B
   int32_t sink;          // first rows always kept
-  int32_t pad;
+  int32_t qe_off;        // this sequence's layer in the folded statistics (elements from P.qe / P.mw)
 };
 
 // Everything a kernel of the pass needs, passed by value.
@@ -529,4 +529,6 @@ struct tria_stats {
   std::vector<int32_t> head_dim;     // [L]
   std::vector<int64_t> qe_off;       // [L]; -1: layer not loaded (fails the gate)
   std::vector<int64_t> turns_off;    // [L]
+  std::vector<double> freq;          // [L][head_dim_l / 2] host copy of the frequencies (theta or omega)
+  std::vector<int64_t> freq_off;     // [L + 1] offsets into freq
 };
