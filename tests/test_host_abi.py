@@ -33,6 +33,23 @@ def test_header_declares_the_pass_entry_points():
         assert n in names
 
 
+def test_header_is_plain_c99(tmp_path):
+    """The boundary is a C ABI: the header compiles as strict C99 (no C++ in it)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use.c"
+    src.write_text('#include "tria.h"\n'
+                   'int main(void) { tria_policy p = {0}; tria_schedule s = {0}; (void)p; (void)s;\n'
+                   '  return tria_should_evict(10, 4, 2); }\n')
+    res = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I",
+                          os.path.dirname(HEADER), "-c", str(src), "-o", str(tmp_path / "use.o")],
+                         capture_output=True, text=True)
+    assert res.returncode == 0, res.stderr
+
+
 def test_library_exports_every_declared_function(lib):
     names = declared_functions()
     assert len(names) >= 15
