@@ -223,3 +223,52 @@ def test_plan_of_several_sequences(lib):
     assert not q.decode(0)
     b, k, p, nd = q.plan()
     assert nd == 0 and list(b) == [tria.NO_PASS] * 3
+
+
+def test_oracle_decode_loop_invariants():
+    """A tiny decode loop on the CPU (oracle pass at every scheduled step):
+    protected prompt rows survive every pass, positions stay strictly
+    increasing, the live rows follow the schedule and the kept rows are
+    always the last window rows plus the best of the rest."""
+    rng = np.random.default_rng(3)
+    hd, n_kv, g, cap, prompt, n_decode = 32, 2, 2, 200, 12, 260
+    sch = dict(trigger="length", kv_budget=64, divide_length=16, count_prompt_tokens=False,
+               protect_prefill=True, window=8, sink=0)
+    events = O.schedule_events(prompt=prompt, n_decode=n_decode, capacity=cap, **sch)
+    qm = rng.standard_normal((1, n_kv * g, hd // 2, 2))
+    qa = np.hypot(qm[..., 0], qm[..., 1]) + 0.3
+    tokens = rng.standard_normal((prompt + n_decode, n_kv, hd)).astype(np.float32)
+    cache = {"k": np.zeros((n_kv * cap, hd), np.float32), "k_scale": None,
+             "v": np.zeros((n_kv * cap, hd), np.float32), "v_scale": None,
+             "pos": np.zeros(n_kv * cap, np.int32), "n_live": np.array([0], np.int32),
+             "seq_row0": np.array([0]), "capacity": np.array([cap], np.int32)}
+
+    def append(t):
+        n = int(cache["n_live"][0])
+        for h in range(n_kv):
+            cache["k"][h * cap + n] = tokens[t, h]
+            cache["v"][h * cap + n] = -tokens[t, h]
+            cache["pos"][h * cap + n] = t
+        cache["n_live"][0] = n + 1
+
+    for t in range(prompt):
+        append(t)
+    ev = iter(events)
+    nxt = next(ev, None)
+    for step in range(1, n_decode + 1):
+        append(prompt + step - 1)
+        if nxt is not None and nxt["step"] == step:
+            assert int(cache["n_live"][0]) == nxt["rows_before"]
+            cache, _ = O.evict_layer(cache, qm, qa, layer=0, n_kv_heads=n_kv, head_dim=hd, rope_theta=1e4,
+                                     cur_pos=[nxt["pos"]], n_ctx=None, budget_frac=0.0, window=8,
+                                     sink=nxt["sink"], budget_rows_override=[nxt["budget"]])
+            n = int(cache["n_live"][0])
+            assert n == nxt["rows_after"]
+            for h in range(n_kv):
+                pos = cache["pos"][h * cap:h * cap + n]
+                assert np.all(np.diff(pos) > 0)
+                np.testing.assert_array_equal(pos[:prompt], np.arange(prompt))          # prompt kept
+                np.testing.assert_array_equal(pos[-8:], np.arange(prompt + step - 8, prompt + step))
+                np.testing.assert_array_equal(cache["v"][h * cap:h * cap + n], -cache["k"][h * cap:h * cap + n])
+            nxt = next(ev, None)
+    assert nxt is None and len(events) >= 10
