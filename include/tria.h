@@ -254,8 +254,9 @@ tria_status tria_evict_marked(const tria_stats* stats, int32_t layer, const tria
 
 /* Synchronises `stream`, returns the first device-detected error of the
  * calls since the last check (TRIA_OK if none) and clears it. After
- * TRIA_ERR_TIMEOUT a call may have stopped with its counters mid-way:
- * re-initialise the workspace (tria_workspace_init) before the next call. */
+ * TRIA_ERR_TIMEOUT a call may have stopped with its counters mid-way and its
+ * cache rows part moved (their contents are then unspecified): re-initialise
+ * the workspace (tria_workspace_init) before the next call. */
 tria_status tria_device_status(void* ws, void* stream);
 
 /* Runs the bounded wait used by the compaction kernel on a flag that nothing
