@@ -151,6 +151,13 @@ typedef struct tria_policy {
  * head_dim <= 256 and % 32 == 0) plus this build's group <= 8. No GPU use. */
 tria_status tria_gate_check(int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim);
 
+/* The gate as one log line, in the form of the [Doc] §4 startup log
+ * ("tria: gpu gate - is_q8_0=1 nh=32 nkv=8 hd=128 nonrot=0 -> eligible"), with
+ * the reason appended when ineligible; written to buf (NUL-terminated,
+ * truncated to buf_size). Returns tria_gate_check's status. No GPU use. */
+tria_status tria_gate_describe(int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, tria_dtype k_type,
+                               char* buf, size_t buf_size);
+
 /* Budget rows floor(budget_frac * n_ctx) computed in double ([Doc] §1). */
 int64_t tria_budget_rows(double budget_frac, int64_t n_ctx);
 

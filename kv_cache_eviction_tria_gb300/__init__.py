@@ -33,7 +33,7 @@ TRIGGER_LENGTH, TRIGGER_INTERVAL = 0, 1
 NO_PASS = 2 ** 31 - 1
 
 EXPORTS = (
-    "tria_gate_check", "tria_budget_rows", "tria_should_evict", "tria_load_stats", "tria_free_stats",
+    "tria_gate_check", "tria_gate_describe", "tria_budget_rows", "tria_should_evict", "tria_load_stats", "tria_free_stats",
     "tria_workspace_size", "tria_workspace_init", "tria_score", "tria_select", "tria_compact",
     "tria_evict", "tria_evict_layers", "tria_evict_profiled", "tria_evict_marked", "tria_select_noalloc", "tria_device_status", "tria_selftest_bounded_wait",
     "tria_calib_accumulate", "tria_calib_finish", "tria_append", "tria_schedule_check", "tria_seq_init",
@@ -113,6 +113,8 @@ def load_library(path: str | None = None):
     vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
     lib.tria_gate_check.argtypes = [i32, i32, i32]
     lib.tria_gate_check.restype = i32
+    lib.tria_gate_describe.argtypes = [i32, i32, i32, i32, ctypes.c_char_p, sz]
+    lib.tria_gate_describe.restype = i32
     lib.tria_budget_rows.argtypes = [ctypes.c_double, i64]
     lib.tria_budget_rows.restype = i64
     lib.tria_should_evict.argtypes = [i64, i64, i64]
@@ -216,6 +218,13 @@ def _host_array(values, dtype, ctype):
 
 def gate_check(n_q_heads: int, n_kv_heads: int, head_dim: int) -> int:
     return load_library().tria_gate_check(n_q_heads, n_kv_heads, head_dim)
+
+
+def gate_describe(n_q_heads: int, n_kv_heads: int, head_dim: int, k_type: str = "q8_0") -> tuple:
+    """tria_gate_describe: (status, the gate log line)."""
+    buf = ctypes.create_string_buffer(256)
+    st = load_library().tria_gate_describe(n_q_heads, n_kv_heads, head_dim, DTYPES[k_type], buf, 256)
+    return st, buf.value.decode()
 
 
 def budget_rows(budget_frac: float, n_ctx: int) -> int:

@@ -4,6 +4,7 @@
 //   [Worklog] "TriAttention Native C++ Worklog"
 //   [Doc]     "TriAttention KV-Cache Eviction (--triattention)"
 #include <math.h>
+#include <stdio.h>
 #include <string.h>
 
 #include <algorithm>
@@ -217,6 +218,24 @@ extern "C" tria_status tria_gate_check(int32_t n_q_heads, int32_t n_kv_heads, in
   const int G = n_q_heads / n_kv_heads;
   if (G != 1 && G != 2 && G != 4 && G != 8) return TRIA_ERR_UNSUPPORTED;
   return TRIA_OK;
+}
+
+extern "C" tria_status tria_gate_describe(int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                                          tria_dtype k_type, char* buf, size_t buf_size) {
+  const tria_status g = tria_gate_check(n_q_heads, n_kv_heads, head_dim);
+  if (!buf || buf_size == 0) return g;
+  const char* why = "";
+  if (g == TRIA_ERR_INVALID_ARG) why = " (heads / head_dim must be > 0)";
+  else if (g == TRIA_ERR_UNSUPPORTED) {
+    if (n_q_heads % n_kv_heads != 0) why = " (nh % nkv != 0)";
+    else if (head_dim > TRIA_MAX_HEAD_DIM) why = " (head_dim > 256)";
+    else if (head_dim % 32 != 0) why = " (head_dim % 32 != 0)";
+    else why = " (group size not 1, 2, 4 or 8)";
+  }
+  snprintf(buf, buf_size, "tria: gpu gate - is_q8_0=%d nh=%d nkv=%d hd=%d nonrot=0 -> %s%s",
+           k_type == TRIA_Q8_0 ? 1 : 0, (int)n_q_heads, (int)n_kv_heads, (int)head_dim,
+           g == TRIA_OK ? "eligible" : "ineligible", why);
+  return g;
 }
 
 extern "C" int64_t tria_budget_rows(double budget_frac, int64_t n_ctx) {

@@ -76,6 +76,17 @@ def test_gate_matches_the_documented_gate(lib):
     assert tria.gate_check(0, 8, 128) == tria.ERR_INVALID_ARG
 
 
+def test_gate_log_line_matches_the_documented_line(lib):
+    gold = json.load(open(os.path.join(ROOT, "tests", "golden", "doc_gpu_gate.json")))
+    want = gold["source"].split("gate log line '")[1].split("'")[0]
+    st, line = tria.gate_describe(32, 8, 128, "q8_0")
+    assert st == tria.OK and line == want
+    st, line = tria.gate_describe(32, 8, 512, "f16")
+    assert st == tria.ERR_UNSUPPORTED and line.endswith("-> ineligible (head_dim > 256)") and "is_q8_0=0" in line
+    st, line = tria.gate_describe(30, 8, 128, "q8_0")
+    assert st == tria.ERR_UNSUPPORTED and "(nh % nkv != 0)" in line
+
+
 def test_budget_rows_and_trigger(lib):
     assert tria.budget_rows(0.5, 512) == 256
     assert tria.budget_rows(0.25, 98710) == 24677
