@@ -13,10 +13,10 @@
  *        raw_h(r) = (1/|D|) sum_{d in D} sum_f Re( qbar_{h,f} e^{i w_f (p_s + d)} conj(k_{r,f}) )
  *                   + sum_f (q_abs_{h,f} - |qbar_{h,f}|) |k_{r,f}|
  *      on the stored RoPE-rotated key k_r (NEOX pairs k_{r,f} = K[r][f] + i K[r][f+hd/2]),
- *      with p_s the absolute decode position ([Worklog] "Phase 9: final root
- *      cause ...": direct K_rot scoring, query-side trig term only, additive
- *      MLR term on |K_rot|; "2026-04-18: later-compaction absolute-position
- *      bug ...": phases from the absolute position). Then per query head
+ *      with p_s the absolute decode position ([Worklog] Phase 9: scored on the
+ *      stored rotated keys, rotation on the query side only, a norm term on
+ *      the keys' magnitudes added; 2026-04-18 section: phases from the
+ *      absolute position). Then per query head
  *      z = (raw - mean) / (std + 1e-6) over the n live rows, and the row's
  *      score s(r) = max over the group ([Doc] §5 Phase C).
  *   2. select - with B = budget rows, keep rows [0, sink) and [n - window, n)
@@ -418,8 +418,8 @@ tria_status tria_schedule_passed(const tria_schedule* sch, tria_seq_state* st, i
 
 /* ---- Calibration statistics --------------------------------------------
  * The scoring statistics of one layer from a stream of its pre-RoPE queries
- * ([Doc] §2 Calibration file: per-layer, per-head statistics "collected from
- * a calibration corpus", accumulated from the pre-RoPE Q of every layer;
+ * ([Doc] §2 Calibration file: statistics per layer and head, gathered over
+ * calibration text from the pre-RoPE Q of every layer;
  * §5 Phase C: q_mean / q_abs arrays laid out [layers][heads][frequency
  * pairs]). With NEOX pairs z = q[f] + i q[f + head_dim/2]:
  *   q_mean[h][f] = mean over tokens of z   (stored as re, im)

@@ -1,8 +1,8 @@
 // Calibration statistics of one layer from a stream of pre-RoPE queries.
 //
 // [Doc] "TriAttention KV-Cache Eviction (--triattention)", §2 Calibration
-// file (per-layer, per-head statistics of the pre-RoPE queries of a
-// calibration corpus: mean query directions and per-frequency weights) and
+// file (statistics per layer and head of the pre-RoPE queries seen on
+// calibration text: the average query direction and a weight per frequency) and
 // §5 Phase C (the q_mean / q_abs arrays, [layers][heads][frequency pairs]).
 // With NEOX pairs z = q[f] + i q[f + hd/2]: q_mean = mean z, q_abs = mean |z|.
 //

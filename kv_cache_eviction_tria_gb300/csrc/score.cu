@@ -1,8 +1,9 @@
 // Score stage: raw per-query-head scores, per-segment moments, z-max score.
 //
-// [Worklog] "TriAttention Native C++ Worklog", Phase 9 (direct K_rot scorer:
-// Q_mean * conj(K_rot), query-side trig term only, additive MLR term on
-// |K_rot|) and 2026-04-18 (phases from the absolute decode position).
+// [Worklog] "TriAttention Native C++ Worklog", Phase 9 (the score is taken on
+// the stored rotated keys: the calibrated mean query times the conjugate key,
+// the rotation applied on the query side only, plus a norm term on the keys'
+// magnitudes) and 2026-04-18 (phases from the absolute decode position).
 // [Doc] "TriAttention KV-Cache Eviction (--triattention)", §5 Phase C
 // (z-normalise each query head, then max over the GQA group).
 //

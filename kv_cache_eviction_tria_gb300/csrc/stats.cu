@@ -1,8 +1,8 @@
 // Calibration statistics: upload and load-time folding.
 //
 // [Doc] "TriAttention KV-Cache Eviction (--triattention)", §2 Calibration file
-// (per-layer, per-head RoPE-direction statistics: mean query directions and
-// per-frequency importance weights) and §5 Phase C (omega and per-head
+// (statistics per layer and head of the queries' RoPE directions: the average
+// query direction and a weight for each frequency) and §5 Phase C (omega and per-head
 // q_mean / q_abs arrays laid out [n_layers x n_heads x freq_count]).
 //
 // What is folded once at load, per (layer, KV head, group member j, pair f):

@@ -25,8 +25,9 @@ Readings where the pages are silent:
 * NEOX pairing: frequency pair f of a head_dim-hd vector is the complex number
   x[f] + i x[f + hd/2]; omega_f = theta ** (-2 f / hd).
 * Score of cached row r for query head h at decode position p
-  ([Worklog] Phase 9: "Q_mean * conj(K_rot)", "only the query-side trig
-  term", "additive MLR term on |K_rot|")::
+  ([Worklog] Phase 9: mean query times the conjugate of the stored rotated
+  key, rotation on the query side only, plus a norm term on the rotated
+  key's magnitudes)::
 
       raw_h(r) = (1/|D|) sum_{d in D} sum_f Re( qbar_{h,f} e^{i w_f (p+d)} conj(k_{r,f}) )
                  + sum_f M_{h,f} |k_{r,f}|
@@ -46,7 +47,7 @@ Readings where the pages are silent:
   not state the combine rule; a token's score is the maximum of its z-max
   scores over all layers and KV heads (NaN ignored unless all are NaN).
 * Calibration ([Doc] §2: per-layer, per-head statistics of the pre-RoPE
-  queries, "mean query directions + per-frequency importance weights";
+  queries, giving the average query direction and a weight per frequency;
   §5 Phase C: q_mean / q_abs arrays [layers][heads][frequency pairs]):
   over the calibration tokens t of one layer, q_mean_{h,f} = mean_t of the
   complex pair Q_t[h][f] + i Q_t[h][f + hd/2], q_abs_{h,f} = mean_t of its
@@ -88,8 +89,8 @@ def as_complex(q_mean: np.ndarray) -> np.ndarray:
 
 
 def mlr_weight(q_mean: np.ndarray, q_abs: np.ndarray | None) -> np.ndarray:
-    """M = q_abs - |qbar| per (head, pair) ([Worklog] Phase 9 "MLR term";
-    [Doc] §2 "per-frequency importance weights", Phase C "q_mean / q_abs").
+    """M = q_abs - |qbar| per (head, pair) ([Worklog] Phase 9, its norm term;
+    [Doc] §2, a weight per frequency; Phase C, the q_mean / q_abs arrays).
     ``q_abs`` None means M = 0."""
     qc = as_complex(q_mean)
     if q_abs is None:
@@ -178,7 +179,7 @@ def segment_scores(k_rot, q_mean_c, m_weight, omega, p, offsets):
 # ---------------------------------------------------------------------------
 
 def budget_rows(budget_frac: float, n_ctx: int) -> int:
-    """B = floor(budget_frac * n_ctx) ([Doc] §1 "--tri-budget": retain N % of n_ctx)."""
+    """B = floor(budget_frac * n_ctx) ([Doc] §1 --tri-budget: the kept share of n_ctx)."""
     return int(math.floor(float(budget_frac) * int(n_ctx)))
 
 
