@@ -207,7 +207,14 @@ tria_status tria_select(const float* score, const tria_layer_cache* cache, const
  *    larger calls return TRIA_ERR_WORKSPACE.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *    before any stream capture. The address belongs to the CUDA context it
+ *    was looked up in: a call made in another context of the device (for
+ *    instance after cudaDeviceReset, which replaces the primary context)
+ *    looks it up again, so after a reset the next call must also be made
+ *    outside stream capture.
+ *  - Host checks are those of tria_select (the cache layout, including
+ *    sequences whose rows overlap, pointer alignment, budget / sink / window
+ *    and n_ctx of every sequence).
  *  - All calls share the one array, which keeps the previous call's contents;
  *    each call clears what must start at zero. Calls that overlap on the GPU
  *    (different streams, no ordering) race and give undefined results.

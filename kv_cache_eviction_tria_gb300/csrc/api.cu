@@ -82,65 +82,6 @@ Layout make_layout(const tria_layer_cache* c, int G) {
   return L;
 }
 
-tria_status check_cache(const tria_layer_cache* c) {
-  if (!c) return TRIA_ERR_INVALID_ARG;
-  if (c->n_seqs < 1 || c->n_seqs > kMaxSeqs || c->n_kv_heads < 1) return TRIA_ERR_INVALID_ARG;
-  if (c->n_seqs * c->n_kv_heads > kMaxSegments) return TRIA_ERR_UNSUPPORTED;
-  const int hd = c->head_dim;
-  if (hd <= 0 || hd > TRIA_MAX_HEAD_DIM || hd % 32 != 0) return TRIA_ERR_UNSUPPORTED;
-  if (!dtype_ok(c->k_type) || !dtype_ok(c->v_type)) return TRIA_ERR_UNSUPPORTED;
-  if (!c->k || !c->v || !c->pos || !c->n_live || !c->seq_row0 || !c->capacity) return TRIA_ERR_INVALID_ARG;
-  if (!aligned(c->k, 16) || !aligned(c->v, 16) || !aligned(c->pos, 4) || !aligned(c->n_live, 4))
-    return TRIA_ERR_INVALID_ARG;
-  if ((c->k_type == TRIA_Q8_0) != (c->k_scale != nullptr)) return TRIA_ERR_INVALID_ARG;
-  if ((c->v_type == TRIA_Q8_0) != (c->v_scale != nullptr)) return TRIA_ERR_INVALID_ARG;
-  if (c->k_scale && !aligned(c->k_scale, 16)) return TRIA_ERR_INVALID_ARG;
-  if (c->v_scale && !aligned(c->v_scale, 16)) return TRIA_ERR_INVALID_ARG;
-  // segments of different sequences must not overlap
-  std::vector<std::pair<int64_t, int64_t>> spans;
-  for (int s = 0; s < c->n_seqs; ++s) {
-    if (c->capacity[s] < 0 || c->seq_row0[s] < 0) return TRIA_ERR_INVALID_ARG;
-    spans.push_back({c->seq_row0[s], c->seq_row0[s] + (int64_t)c->n_kv_heads * c->capacity[s]});
-  }
-  std::sort(spans.begin(), spans.end());
-  for (size_t i = 1; i < spans.size(); ++i)
-    if (spans[i].first < spans[i - 1].second) return TRIA_ERR_INVALID_ARG;
-  return TRIA_OK;
-}
-
-// need_budget = false (scoring only): the budget is not used and not checked.
-tria_status check_policy(const tria_layer_cache* c, const tria_policy* p, bool need_pos, std::vector<int>& budget,
-                         bool need_budget = true) {
-  if (!p) return TRIA_ERR_INVALID_ARG;
-  if (p->window < 0 || p->sink < 0) return TRIA_ERR_INVALID_ARG;
-  if (need_pos && !p->cur_pos) return TRIA_ERR_INVALID_ARG;
-  if (!need_budget) {
-    budget.assign(c->n_seqs, 0);
-    for (int s = 0; s < c->n_seqs; ++s)
-      if (need_pos && p->cur_pos[s] < 0) return TRIA_ERR_INVALID_ARG;
-    return TRIA_OK;
-  }
-  if (!p->budget_rows && (!p->n_ctx || !(p->budget_frac > 0.0) || p->budget_frac > 1.0))
-    return TRIA_ERR_INVALID_ARG;
-  budget.assign(c->n_seqs, 0);
-  for (int s = 0; s < c->n_seqs; ++s) {
-    int64_t b;
-    if (p->budget_rows) {
-      b = p->budget_rows[s];
-    } else {
-      if (p->n_ctx[s] < 0) return TRIA_ERR_INVALID_ARG;
-      b = tria_budget_rows(p->budget_frac, p->n_ctx[s]);
-    }
-    if (b < 0 || b > INT32_MAX) return TRIA_ERR_INVALID_ARG;
-    const int64_t sink = p->sink_rows ? (int64_t)p->sink_rows[s] : (int64_t)p->sink;
-    if (sink < 0) return TRIA_ERR_INVALID_ARG;
-    if (b < sink + p->window) return TRIA_ERR_BUDGET;
-    if (need_pos && p->cur_pos[s] < 0) return TRIA_ERR_INVALID_ARG;
-    budget[s] = (int)b;
-  }
-  return TRIA_OK;
-}
-
 tria_status check_ws(void* ws, size_t ws_bytes, const Layout& L) {
   if (!ws || !aligned(ws, 256)) return TRIA_ERR_WORKSPACE;
   if (ws_bytes < L.total) return TRIA_ERR_WORKSPACE;
@@ -208,6 +149,69 @@ void set_stats(Pass& P, const tria_stats* st, int layer) {
 }
 
 }  // namespace
+
+namespace tria {
+
+tria_status check_cache(const tria_layer_cache* c) {
+  if (!c) return TRIA_ERR_INVALID_ARG;
+  if (c->n_seqs < 1 || c->n_seqs > kMaxSeqs || c->n_kv_heads < 1) return TRIA_ERR_INVALID_ARG;
+  if (c->n_seqs * c->n_kv_heads > kMaxSegments) return TRIA_ERR_UNSUPPORTED;
+  const int hd = c->head_dim;
+  if (hd <= 0 || hd > TRIA_MAX_HEAD_DIM || hd % 32 != 0) return TRIA_ERR_UNSUPPORTED;
+  if (!dtype_ok(c->k_type) || !dtype_ok(c->v_type)) return TRIA_ERR_UNSUPPORTED;
+  if (!c->k || !c->v || !c->pos || !c->n_live || !c->seq_row0 || !c->capacity) return TRIA_ERR_INVALID_ARG;
+  if (!aligned(c->k, 16) || !aligned(c->v, 16) || !aligned(c->pos, 4) || !aligned(c->n_live, 4))
+    return TRIA_ERR_INVALID_ARG;
+  if ((c->k_type == TRIA_Q8_0) != (c->k_scale != nullptr)) return TRIA_ERR_INVALID_ARG;
+  if ((c->v_type == TRIA_Q8_0) != (c->v_scale != nullptr)) return TRIA_ERR_INVALID_ARG;
+  if (c->k_scale && !aligned(c->k_scale, 16)) return TRIA_ERR_INVALID_ARG;
+  if (c->v_scale && !aligned(c->v_scale, 16)) return TRIA_ERR_INVALID_ARG;
+  // segments of different sequences must not overlap
+  std::vector<std::pair<int64_t, int64_t>> spans;
+  for (int s = 0; s < c->n_seqs; ++s) {
+    if (c->capacity[s] < 0 || c->seq_row0[s] < 0) return TRIA_ERR_INVALID_ARG;
+    spans.push_back({c->seq_row0[s], c->seq_row0[s] + (int64_t)c->n_kv_heads * c->capacity[s]});
+  }
+  std::sort(spans.begin(), spans.end());
+  for (size_t i = 1; i < spans.size(); ++i)
+    if (spans[i].first < spans[i - 1].second) return TRIA_ERR_INVALID_ARG;
+  return TRIA_OK;
+}
+
+// need_budget = false (scoring only): the budget is not used and not checked.
+tria_status check_policy(const tria_layer_cache* c, const tria_policy* p, bool need_pos, std::vector<int>& budget,
+                         bool need_budget) {
+  if (!p) return TRIA_ERR_INVALID_ARG;
+  if (p->window < 0 || p->sink < 0) return TRIA_ERR_INVALID_ARG;
+  if (need_pos && !p->cur_pos) return TRIA_ERR_INVALID_ARG;
+  if (!need_budget) {
+    budget.assign(c->n_seqs, 0);
+    for (int s = 0; s < c->n_seqs; ++s)
+      if (need_pos && p->cur_pos[s] < 0) return TRIA_ERR_INVALID_ARG;
+    return TRIA_OK;
+  }
+  if (!p->budget_rows && (!p->n_ctx || !(p->budget_frac > 0.0) || p->budget_frac > 1.0))
+    return TRIA_ERR_INVALID_ARG;
+  budget.assign(c->n_seqs, 0);
+  for (int s = 0; s < c->n_seqs; ++s) {
+    int64_t b;
+    if (p->budget_rows) {
+      b = p->budget_rows[s];
+    } else {
+      if (p->n_ctx[s] < 0) return TRIA_ERR_INVALID_ARG;
+      b = tria_budget_rows(p->budget_frac, p->n_ctx[s]);
+    }
+    if (b < 0 || b > INT32_MAX) return TRIA_ERR_INVALID_ARG;
+    const int64_t sink = p->sink_rows ? (int64_t)p->sink_rows[s] : (int64_t)p->sink;
+    if (sink < 0) return TRIA_ERR_INVALID_ARG;
+    if (b < sink + p->window) return TRIA_ERR_BUDGET;
+    if (need_pos && p->cur_pos[s] < 0) return TRIA_ERR_INVALID_ARG;
+    budget[s] = (int)b;
+  }
+  return TRIA_OK;
+}
+
+}  // namespace tria
 
 // ---------------------------------------------------------------------------
 

@@ -11,8 +11,12 @@
 // The array is a file-scope static device variable, so every GPU that loads
 // the library keeps it for the life of the process. Host code cannot use the
 // array's name as a device address (on the host it names a stand-in), so the
-// address is obtained once per device with cudaGetSymbolAddress, on the first
-// call made while that device is current.
+// address is looked up with cudaGetSymbolAddress, with the device current, on
+// the first call in each CUDA context of that device. The lookup is repeated
+// when the current context is a different one (after cudaDeviceReset the
+// primary context is new and the old address is no longer valid); contexts
+// are told apart by their driver-assigned id.
+#include <cuda.h>
 #include <string.h>
 
 #include <mutex>
@@ -28,23 +32,61 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_select_scratch[kScratchBytes];
 
-std::mutex g_setup_mutex;
-void* g_scratch_addr[kMaxDevices] = {};
+struct ScratchSlot {
+  unsigned long long ctx_id;   // context the address belongs to (0: none yet)
+  void* addr;
+};
 
-// Device address of the scratch array on the current device (set up once).
+std::mutex g_setup_mutex;
+ScratchSlot g_scratch[kMaxDevices] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Id of the calling thread's current context, 0 when there is none or the
+// driver entry points are unavailable (then every call looks the address up).
+unsigned long long current_ctx_id() {
+  static CtxGetCurrentFn get_cur = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static bool looked_up = false;
+  if (!looked_up) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(f);
+    looked_up = true;
+  }
+  if (!get_cur || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  if (get_cur(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  unsigned long long id = 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the scratch array in the current context of the current
+// device (looked up once per context).
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (!g_scratch_addr[dev]) {
+  ScratchSlot& slot = g_scratch[dev];
+  const unsigned long long id = current_ctx_id();
+  if (id == 0 || slot.ctx_id != id || !slot.addr) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_select_scratch);
+    e = cudaGetSymbolAddress(&p, g_select_scratch);   // also makes the primary context current
     if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = p;
+    slot.addr = p;
+    slot.ctx_id = current_ctx_id();
   }
-  *out = g_scratch_addr[dev];
+  *out = slot.addr;
   return cudaSuccess;
 }
 
@@ -54,32 +96,24 @@ size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 extern "C" tria_status tria_select_noalloc(const float* score, const tria_layer_cache* c, const tria_policy* p,
                                            int32_t* keep_out, void* stream) {
-  if (!c || !p || !score || !keep_out) return TRIA_ERR_INVALID_ARG;
-  if (c->n_seqs < 1 || c->n_seqs > kMaxSeqs || c->n_kv_heads < 1) return TRIA_ERR_INVALID_ARG;
-  if (c->n_seqs * c->n_kv_heads > kMaxSegments) return TRIA_ERR_UNSUPPORTED;
-  if (c->head_dim <= 0 || c->head_dim > TRIA_MAX_HEAD_DIM || c->head_dim % 32 != 0) return TRIA_ERR_UNSUPPORTED;
-  if (!c->n_live || !c->seq_row0 || !c->capacity) return TRIA_ERR_INVALID_ARG;
-  if (((uintptr_t)score % 4) != 0 || ((uintptr_t)keep_out % 4) != 0 || ((uintptr_t)c->n_live % 4) != 0)
+  // the same host checks as tria_select (layout, overlap of sequences,
+  // alignment, budget / sink / window of every sequence)
+  tria_status r;
+  if ((r = check_cache(c)) != TRIA_OK) return r;
+  if (!score || !keep_out || ((uintptr_t)score % 4) != 0 || ((uintptr_t)keep_out % 4) != 0)
     return TRIA_ERR_INVALID_ARG;
-  if (p->window < 0 || p->sink < 0) return TRIA_ERR_INVALID_ARG;
-  if (!p->budget_rows && (!p->n_ctx || !(p->budget_frac > 0.0) || p->budget_frac > 1.0))
-    return TRIA_ERR_INVALID_ARG;
+  std::vector<int> budget;
+  if ((r = check_policy(c, p, false, budget)) != TRIA_OK) return r;
 
   Pass P;
   memset(&P, 0, sizeof(P));
   int cap_max = 1;
   for (int s = 0; s < c->n_seqs; ++s) {
-    if (c->capacity[s] < 0 || c->seq_row0[s] < 0) return TRIA_ERR_INVALID_ARG;
     if (c->capacity[s] > cap_max) cap_max = c->capacity[s];
-    int64_t b = p->budget_rows ? (int64_t)p->budget_rows[s] : tria_budget_rows(p->budget_frac, p->n_ctx[s]);
-    if (b < 0 || b > INT32_MAX) return TRIA_ERR_INVALID_ARG;
-    const int64_t sink = p->sink_rows ? (int64_t)p->sink_rows[s] : (int64_t)p->sink;
-    if (sink < 0) return TRIA_ERR_INVALID_ARG;
-    if (b < sink + p->window) return TRIA_ERR_BUDGET;
     P.seq[s].row0 = c->seq_row0[s];
-    P.seq[s].sink = (int)sink;
+    P.seq[s].sink = p->sink_rows ? p->sink_rows[s] : p->sink;
     P.seq[s].cap = c->capacity[s];
-    P.seq[s].budget = (int)b;
+    P.seq[s].budget = budget[s];
   }
   const int n_seg = c->n_seqs * c->n_kv_heads;
   const int c_max = (cap_max + kChunk - 1) / kChunk;

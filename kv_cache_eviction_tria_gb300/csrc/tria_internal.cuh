@@ -517,6 +517,12 @@ cudaError_t launch_shared_combine(const Pass& P, const float* scores, int64_t st
 cudaError_t launch_shared_broadcast(const Pass& P, int32_t* keep, cudaStream_t st);
 // stats.cu
 struct StatsDevice;
+// api.cu: the host-side argument checks every entry point on a layer cache
+// shares (layout, pointers and alignment; budget, sink, window and position
+// of every sequence). need_budget = false: scoring only, no budget checked.
+tria_status check_cache(const tria_layer_cache* c);
+tria_status check_policy(const tria_layer_cache* c, const tria_policy* p, bool need_pos, std::vector<int>& budget,
+                         bool need_budget = true);
 
 }  // namespace tria
 

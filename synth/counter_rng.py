@@ -69,15 +69,35 @@ def words(key: int, idx: np.ndarray) -> np.ndarray:
 
 
 def normal12(key: int, first: int, count: int) -> np.ndarray:
-    """float32 draws number ``first .. first+count-1`` of stream ``key``."""
+    """float32 draws number ``first .. first+count-1`` of stream ``key``.
+
+    Same words as :func:`words` (``mix64(key + (3j + t + 1) * GAMMA)``), computed
+    in place to keep the host twin fast on full-size segments."""
     j = np.arange(first, first + count, dtype=np.uint64)
-    s = np.zeros(count, dtype=np.int64)
+    s = np.zeros(count, dtype=np.uint32)
     m16 = np.uint64(0xFFFF)
-    for t in range(3):
-        w = words(key, np.uint64(3) * j + np.uint64(t))
-        for sh in (0, 16, 32, 48):
-            s += ((w >> np.uint64(sh)) & m16).astype(np.int64)
-    m = s - _U16_SUM_MEAN
+    m1, m2, gamma = np.uint64(_M1), np.uint64(_M2), np.uint64(GAMMA)
+    z = np.empty(count, dtype=np.uint64)
+    tmp = np.empty(count, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        for t in range(3):
+            np.multiply(j, np.uint64(3), out=z)
+            z += np.uint64(t + 1)
+            z *= gamma
+            z += np.uint64(key)
+            np.right_shift(z, np.uint64(30), out=tmp)
+            z ^= tmp
+            z *= m1
+            np.right_shift(z, np.uint64(27), out=tmp)
+            z ^= tmp
+            z *= m2
+            np.right_shift(z, np.uint64(31), out=tmp)
+            z ^= tmp
+            for sh in (0, 16, 32, 48):
+                np.right_shift(z, np.uint64(sh), out=tmp)
+                tmp &= m16
+                s += tmp.astype(np.uint32)
+    m = s.astype(np.int64) - _U16_SUM_MEAN
     return m.astype(np.float32) * np.float32(1.0 / 65536.0)
 
 

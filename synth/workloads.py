@@ -228,12 +228,13 @@ def tiny_pre_rope(w: Workload):
     return k_pre, v
 
 
-def segment_host(w: Workload, layer: int, seq: int, head: int, rows: int | None = None):
+def segment_host(w: Workload, layer: int, seq: int, head: int, rows: int | None = None, values: bool = True):
     """Host twin of one segment's contents.
 
     Returns a dict with ``k`` (float32/float16 ``[rows, hd]``, or int8 codes for
-    q8_0), ``k_scale`` (float16 ``[rows, hd/32]``, q8_0 only), ``v`` and
-    ``pos`` - bit-identical to what the device generator writes.
+    q8_0), ``k_scale`` (float16 ``[rows, hd/32]``, q8_0 only), ``v`` (None when
+    ``values`` is false: keys only) and ``pos`` - bit-identical to what the
+    device generator writes.
     """
     cap = w.capacity[seq]
     rows = cap if rows is None else rows
@@ -247,7 +248,7 @@ def segment_host(w: Workload, layer: int, seq: int, head: int, rows: int | None 
     vkey = crng.stream_key(seed, crng.TENSOR_V, layer, seq, head)
     scale = pair_scales(w, layer)[head]
     kx = crng.segment_values(kkey, rows, w.head_dim, scale)
-    vx = crng.segment_values(vkey, rows, w.head_dim, None)
+    vx = crng.segment_values(vkey, rows, w.head_dim, None) if values else None
     out = {"pos": pos, "k_scale": None}
     if w.k_type == "f16":
         out["k"] = crng.to_f16(kx)
@@ -255,7 +256,10 @@ def segment_host(w: Workload, layer: int, seq: int, head: int, rows: int | None 
         out["k"] = kx
     else:
         out["k"], out["k_scale"] = crng.quantize_q8_0(kx)
-    out["v"] = crng.to_f16(vx) if w.v_type == "f16" else vx
+    if vx is None:
+        out["v"] = None
+    else:
+        out["v"] = crng.to_f16(vx) if w.v_type == "f16" else vx
     return out
 
 

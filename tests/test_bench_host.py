@@ -16,12 +16,11 @@ from synth import workloads as W  # noqa: E402
 
 def test_algorithmic_bytes_of_the_qwen3_layer():
     w = W.get_workload("qwen3_8b_layer")
-    moved = [8000] * 8
-    score_b, move_b = bench.algorithmic_bytes(w, moved)
+    score_b, move_b = bench.algorithmic_bytes(w, 8 * 8000)
     assert score_b == 8 * 32768 * 256                     # every fp16 key row read once
     assert move_b == 8 * 8000 * (2 * 256 + 2 * 256 + 8)   # read + write of K, V and pos
     w8 = W.get_workload("q8_0")
-    s8, _ = bench.algorithmic_bytes(w8, [0] * 8)
+    s8, _ = bench.algorithmic_bytes(w8, 0)
     assert s8 == 8 * 65536 * (128 + 8)                    # q8_0 codes + fp16 block scales
 
 
@@ -46,3 +45,20 @@ def test_reference_arm_prints_one_line_on_the_host():
                 "higher_is_better", "scaling", "dtype", "config", "cpu_baseline", "e2e"):
         assert key in d, key
     assert d["impl"] == "reference" and d["value"] > 0 and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_both_arms_describe_the_workload_with_the_same_config():
+    """The reference arm's config is the one the GPU arm reports (same keys and
+    values), so the two lines compare the same workload."""
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                          "tiny", "--steps", "1", "--warmup", "1"], capture_output=True, text=True, env=env,
+                         timeout=300)
+    d = json.loads([ln for ln in res.stdout.splitlines() if ln.startswith("{")][0])
+    assert d["config"] == json.loads(json.dumps(bench.config_of(W.get_workload("tiny"), 1)))
+
+
+def test_default_workload_is_the_whole_batched_model():
+    args = bench.parse([])
+    assert args.workload == "batched_long" and args.layers == 0
+    assert W.get_workload(args.workload).n_layers == 48

@@ -234,3 +234,28 @@ def test_calibration_argument_checks(lib):
     assert fin(acc, 0, 4, 128, qm, qa, None) == tria.ERR_INVALID_ARG
     assert fin(acc, 10, 4, 128, None, qa, None) == tria.ERR_INVALID_ARG
     assert fin(acc, 10, 4, 130000, qm, qa, None) == tria.ERR_UNSUPPORTED
+
+
+def test_select_noalloc_host_checks_match_select(lib):
+    """tria_select_noalloc rejects on the host exactly what tria_select rejects
+    (checks that need no workspace): overlapping sequences, a negative n_ctx,
+    misaligned pointers, a budget below sink + window."""
+    def both(c, pol, score=0x50000, keep=0x60000):
+        cs, ps = c.c_struct(), pol.c_struct()
+        a = _call_select(c, pol, score=score, keep=keep)
+        b = tria.raw_call("tria_select_noalloc", ctypes.c_void_p(score), ctypes.byref(cs), ctypes.byref(ps),
+                          ctypes.c_void_p(keep), None)
+        return a, b
+    overlap = tria.LayerCache(k=0x10000, v=0x20000, pos=0x30000, n_live=0x40000, seq_row0=[0, 100],
+                              capacity=[64, 64], head_dim=64, n_kv_heads=2)
+    pol2 = tria.Policy(budget_rows=[32, 32], window=0, sink=0)
+    assert both(overlap, pol2) == (tria.ERR_INVALID_ARG, tria.ERR_INVALID_ARG)
+    c = _fake_cache()
+    assert both(c, tria.Policy(budget_frac=0.5, n_ctx=[1000, -1], window=0, sink=0)) \
+        == (tria.ERR_INVALID_ARG, tria.ERR_INVALID_ARG)
+    good = tria.Policy(budget_frac=0.5, n_ctx=[1000, 900], window=64, sink=4)
+    assert both(c, good, score=0x50002) == (tria.ERR_INVALID_ARG, tria.ERR_INVALID_ARG)
+    assert both(c, good, keep=0x60001) == (tria.ERR_INVALID_ARG, tria.ERR_INVALID_ARG)
+    assert both(_fake_cache(k=0x10008), good) == (tria.ERR_INVALID_ARG, tria.ERR_INVALID_ARG)
+    assert both(c, tria.Policy(budget_frac=0.05, n_ctx=[1000, 900], window=64, sink=4)) \
+        == (tria.ERR_BUDGET, tria.ERR_BUDGET)

@@ -54,3 +54,17 @@ def test_outlier_pairs_scale_both_dims():
     w = W.get_workload("qwen3_8b_layer")
     sc = W.pair_scales(w, 0)
     assert sc.shape == (8, 64) and (sc == 8.0).sum(axis=1).tolist() == [8] * 8
+
+
+def test_normal12_equals_the_scalar_definition():
+    """The vectorised draws equal the definition written out with Python ints:
+    element j sums the twelve 16-bit fields of words 3j, 3j+1, 3j+2."""
+    key = C.stream_key(3, C.TENSOR_V, 2, 1, 0)
+    first = 12345
+    got = C.normal12(key, first, 40)
+    for i, j in enumerate(range(first, first + 40)):
+        s = 0
+        for t in range(3):
+            w = C.mix64_int(key + (3 * j + t + 1) * C.GAMMA)
+            s += sum((w >> sh) & 0xFFFF for sh in (0, 16, 32, 48))
+        assert got[i] == np.float32((s - 393210) / 65536.0)
