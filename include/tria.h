@@ -231,9 +231,45 @@ tria_status tria_select_noalloc(const float* score, const tria_layer_cache* cach
 tria_status tria_compact(const tria_layer_cache* cache, const tria_policy* policy,
                          const int32_t* keep, void* ws, size_t ws_bytes, void* stream);
 
-/* The whole pass (steps 1-3) for one layer and all sequences of the call. */
+/* The whole pass (steps 1-3) for one layer and all sequences of the call.
+ * fp16 or q8_0 keys with head_dim 64 or 128 (any group) or 256 (group <= 4)
+ * run as one fused persistent kernel (see tria_evict_model); other shapes run
+ * the three staged kernels of tria_evict_staged. Same results either way. */
 tria_status tria_evict(const tria_stats* stats, int32_t layer, const tria_layer_cache* cache,
                        const tria_policy* policy, void* ws, size_t ws_bytes, void* stream);
+
+/* tria_evict as three kernels in sequence (score; select with the z-max
+ * score; compaction), whatever the shape. */
+tria_status tria_evict_staged(const tria_stats* stats, int32_t layer, const tria_layer_cache* cache,
+                              const tria_policy* policy, void* ws, size_t ws_bytes, void* stream);
+
+/* Workspace bytes for tria_evict_model over n_layers layers of caches shaped
+ * like `cache` (also enough for every single-layer call on one of them). 0 on
+ * invalid input (n_layers outside 1 .. 128). */
+size_t tria_model_workspace_size(const tria_layer_cache* cache, int32_t n_layers, int32_t group);
+
+/* The pass over several layers of a model in one call ([Doc] §5 Phase B: the
+ * pass runs per layer and KV head; layers only change the statistics and the
+ * cache planes). caches[i] (host array of n_layers structs) is the cache of
+ * layer layers[i] (host int32 [n_layers]): the same sequences (n_seqs,
+ * seq_row0, capacity), n_kv_heads, head_dim and dtypes in every layer, each
+ * with its own planes and its own n_live array (device, updated in place).
+ * Every layer must be loaded with the first layer's RoPE frequencies
+ * (TRIA_ERR_UNSUPPORTED otherwise) and appear once. One policy for all
+ * layers. Shapes of the fused kernel (see tria_evict) with at most 2048
+ * segments (n_layers x n_seqs x n_kv_heads) run as ONE persistent kernel for
+ * all layers: score items stream the keys, the CTA that scores a segment's
+ * last rows selects it at once, and the segment's rows move while other
+ * segments are still scored; other shapes run tria_evict_staged per layer.
+ * score_out (device float, optional): the z-max score s(r) of every live row
+ * of every compacted segment, at score_out[i * layer_rows + row] for layer
+ * i of the call (layer_rows = max over s of seq_row0[s] + n_kv_heads *
+ * capacity[s]); rows of segments at or below budget are not written. Only
+ * with the fused kernel (else TRIA_ERR_UNSUPPORTED). ws: at least
+ * tria_model_workspace_size(caches, n_layers, group) bytes. */
+tria_status tria_evict_model(const tria_stats* stats, const int32_t* layers, int32_t n_layers,
+                             const tria_layer_cache* caches, const tria_policy* policy, float* score_out,
+                             void* ws, size_t ws_bytes, void* stream);
 
 /* tria_evict over sequences of different layers in one call (the pass is
  * per segment, so layers only change which statistics a segment uses): the

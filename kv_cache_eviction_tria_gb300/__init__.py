@@ -35,7 +35,8 @@ NO_PASS = 2 ** 31 - 1
 EXPORTS = (
     "tria_gate_check", "tria_gate_describe", "tria_budget_rows", "tria_should_evict", "tria_load_stats", "tria_free_stats",
     "tria_workspace_size", "tria_workspace_init", "tria_score", "tria_select", "tria_compact",
-    "tria_evict", "tria_evict_layers", "tria_evict_profiled", "tria_evict_marked", "tria_select_noalloc", "tria_device_status", "tria_selftest_bounded_wait",
+    "tria_evict", "tria_evict_staged", "tria_evict_model", "tria_model_workspace_size", "tria_evict_layers",
+    "tria_evict_profiled", "tria_evict_marked", "tria_select_noalloc", "tria_device_status", "tria_selftest_bounded_wait",
     "tria_calib_accumulate", "tria_calib_finish", "tria_append", "tria_schedule_check", "tria_seq_init",
     "tria_seq_prefill", "tria_seq_decode", "tria_schedule_plan", "tria_schedule_passed",
     "tria_shared_combine", "tria_shared_select",
@@ -137,6 +138,13 @@ def load_library(path: str | None = None):
     lib.tria_compact.restype = i32
     lib.tria_evict.argtypes = [vp, i32, ctypes.POINTER(_LayerCache), ctypes.POINTER(_Policy), vp, sz, vp]
     lib.tria_evict.restype = i32
+    lib.tria_evict_staged.argtypes = [vp, i32, ctypes.POINTER(_LayerCache), ctypes.POINTER(_Policy), vp, sz, vp]
+    lib.tria_evict_staged.restype = i32
+    lib.tria_model_workspace_size.argtypes = [ctypes.POINTER(_LayerCache), i32, i32]
+    lib.tria_model_workspace_size.restype = sz
+    lib.tria_evict_model.argtypes = [vp, ctypes.POINTER(i32), i32, ctypes.POINTER(_LayerCache),
+                                     ctypes.POINTER(_Policy), vp, vp, sz, vp]
+    lib.tria_evict_model.restype = i32
     lib.tria_evict_layers.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(_LayerCache), ctypes.POINTER(_Policy),
                                       vp, sz, vp]
     lib.tria_evict_layers.restype = i32
@@ -392,6 +400,37 @@ def evict(stats: Stats, layer: int, cache: LayerCache, policy: Policy, *, ws, st
     wp, wb = _ws(ws)
     _check(load_library().tria_evict(stats.handle, layer, ctypes.byref(c), ctypes.byref(p), wp, wb,
                                      _stream_handle(stream)), "tria_evict")
+
+
+def evict_staged(stats: Stats, layer: int, cache: LayerCache, policy: Policy, *, ws, stream=None):
+    """tria_evict_staged: the pass as three kernels (score, select, compact)."""
+    c, p = cache.c_struct(), policy.c_struct()
+    wp, wb = _ws(ws)
+    _check(load_library().tria_evict_staged(stats.handle, layer, ctypes.byref(c), ctypes.byref(p), wp, wb,
+                                            _stream_handle(stream)), "tria_evict_staged")
+
+
+def model_workspace_size(cache: LayerCache, n_layers: int, group: int) -> int:
+    c = cache.c_struct()
+    n = load_library().tria_model_workspace_size(ctypes.byref(c), n_layers, group)
+    if n == 0:
+        raise TriaError(ERR_INVALID_ARG, "tria_model_workspace_size")
+    return n
+
+
+def evict_model(stats: Stats, layers, caches, policy: Policy, *, ws, score_out=None, stream=None):
+    """tria_evict_model: one pass over several layers (caches[i] is the cache
+    of layer layers[i]); score_out (optional device float tensor) receives the
+    z-max scores of the compacted segments' live rows, [n_layers][layer rows]."""
+    if len(caches) != len(layers) or not caches:
+        raise ValueError("one cache per layer")
+    structs = (_LayerCache * len(caches))(*[c.c_struct() for c in caches])
+    arr, ptr = _host_array(layers, np.int32, ctypes.c_int32)
+    p = policy.c_struct()
+    wp, wb = _ws(ws)
+    _check(load_library().tria_evict_model(stats.handle, ptr, len(layers), structs, ctypes.byref(p),
+                                           _ptr(score_out) if score_out is not None else None, wp, wb,
+                                           _stream_handle(stream)), "tria_evict_model")
 
 
 def evict_layers(stats: Stats, layer_of_seq, cache: LayerCache, policy: Policy, *, ws, stream=None):

@@ -17,7 +17,8 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libtria.so")
 BUILD_DIR = os.path.join(ROOT, "_build", "tria")
 
-SOURCES = ["api.cu", "stats.cu", "score.cu", "select.cu", "compact.cu", "noalloc.cu", "calib.cu", "lifecycle.cu", "shared.cu"]
+SOURCES = ["api.cu", "stats.cu", "score.cu", "select.cu", "compact.cu", "noalloc.cu", "calib.cu", "lifecycle.cu",
+           "shared.cu", "pass_f16.cu", "pass_q8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-Xptxas", "-warn-spills"]

@@ -10,7 +10,7 @@
 #include <algorithm>
 #include <vector>
 
-#include "tria_internal.cuh"
+#include "pass.cuh"
 
 using namespace tria;
 
@@ -32,15 +32,17 @@ bool dtype_ok(int t) { return t == TRIA_F32 || t == TRIA_F16 || t == TRIA_Q8_0; 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 struct Layout {
-  size_t ctrl, seg, runs, chunk, prefix, hist, flags, score, keep, raw, total;
+  size_t ctrl, pass_ctl, seg, runs, chunk, prefix, hist, flags, score, keep, raw, total;
   int cs_rows, cs_max, c_max, n_seg;
-  int64_t total_rows;
+  int64_t total_rows;       // rows of one layer
 };
 
 size_t up(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Everything but `raw` is independent of the group size, and `raw` comes last,
-// so one workspace serves every entry point on the same cache.
+// Workspace layout of the single-layer calls on `cache`. Everything but `raw`
+// is independent of the group size, and `raw` comes last, so one workspace
+// serves every entry point on the same cache. The control words and the fused
+// pass's fixed state come first.
 Layout make_layout(const tria_layer_cache* c, int G) {
   Layout L{};
   const int hd = c->head_dim;
@@ -60,6 +62,8 @@ Layout make_layout(const tria_layer_cache* c, int G) {
   size_t off = 0;
   L.ctrl = off;
   off = up(off + sizeof(Ctrl));
+  L.pass_ctl = off;
+  off = up(off + sizeof(PassCtl));
   L.seg = off;
   off = up(off + (size_t)L.n_seg * sizeof(SegState));
   L.runs = off;
@@ -79,6 +83,39 @@ Layout make_layout(const tria_layer_cache* c, int G) {
   L.raw = off;
   off = up(off + (size_t)total_rows * std::max(G, 0) * sizeof(float));
   L.total = off;
+  return L;
+}
+
+// Layout of a fused pass over n_layers > 1 layers: the single-layer layout
+// (so that every single-layer call on one of the layers fits and finds its
+// state where it left it), then the pass's own tables for all layers'
+// segments and rows (item moment partials, chunk prefixes, read-done flags,
+// keys, keep lists, raw scores).
+Layout make_model_layout(const tria_layer_cache* c, int G, int n_layers) {
+  const Layout L1 = make_layout(c, G);
+  if (n_layers <= 1) return L1;
+  Layout L = L1;
+  const int k_rb = row_bytes(c->k_type, c->head_dim);
+  const int cap_max = L1.c_max * kChunk;
+  const int item_rows = kPassWarps * kPassPPW * pass_piece_rows(k_rb);
+  L.n_seg = n_layers * L1.n_seg;
+  L.cs_max = (cap_max + item_rows - 1) / item_rows;
+  const int64_t rows = L1.total_rows * n_layers;
+  size_t off = L1.total;
+  L.runs = off;
+  off = up(off + (size_t)L.n_seg * kRunCols * L.cs_max * sizeof(float));
+  L.prefix = off;
+  off = up(off + (size_t)L.n_seg * (L.c_max + 1) * sizeof(int32_t));
+  L.flags = off;
+  off = up(off + (size_t)L.n_seg * L.c_max * sizeof(uint32_t));
+  L.score = off;
+  off = up(off + (size_t)rows * sizeof(float));
+  L.keep = off;
+  off = up(off + (size_t)rows * sizeof(int32_t));
+  L.raw = off;
+  off = up(off + (size_t)rows * std::max(G, 0) * sizeof(float));
+  L.total = off;
+  L.seg = L.chunk = L.hist = 0;   // not used by the pass
   return L;
 }
 
@@ -146,6 +183,71 @@ void set_stats(Pass& P, const tria_stats* st, int layer) {
   P.mw = st->mw;
   P.turns = st->turns + st->turns_off[layer];
   for (int s = 0; s < P.n_seqs; ++s) P.seq[s].qe_off = (int32_t)st->qe_off[layer];
+}
+
+// The fused pass (k_pass) over layers[0 .. n_layers) of the statistics, one
+// cache per layer (same sequences, shapes and types; checked by the caller).
+tria_status launch_fused(const tria_stats* st, const int32_t* layers, int n_layers, const tria_layer_cache* caches,
+                         const tria_policy* p, const std::vector<int>& budget, const Layout& L, void* ws,
+                         float* score_out, cudaStream_t stream) {
+  const tria_layer_cache* c = caches;
+  FPass* F = new FPass;   // ~12 KB: off the stack
+  memset(F, 0, sizeof(FPass));
+  F->n_layers = n_layers;
+  F->n_seqs = c->n_seqs;
+  F->n_kv = c->n_kv_heads;
+  F->n_seg = L.n_seg;
+  F->G = st->group;
+  F->hd = c->head_dim;
+  F->fc = c->head_dim / 2;
+  F->window = p->window;
+  F->k_rb = row_bytes(c->k_type, c->head_dim);
+  F->ks_rb = scale_row_bytes(c->k_type, c->head_dim);
+  F->v_rb = row_bytes(c->v_type, c->head_dim);
+  F->vs_rb = scale_row_bytes(c->v_type, c->head_dim);
+  F->spin_limit = kDefaultSpinLimit;
+  F->piece_rows = pass_piece_rows(F->k_rb);
+  F->item_rows = kPassWarps * kPassPPW * F->piece_rows;
+  F->cs_max = L.cs_max;
+  F->c_max = L.c_max;
+  F->rows_per_layer = L.total_rows;
+  F->qe = st->qe;
+  F->mw = st->mw;
+  F->turns = st->turns + st->turns_off[layers[0]];
+  uint8_t* w = (uint8_t*)ws;
+  F->raw = (float*)(w + L.raw);
+  F->keys = (uint32_t*)(w + L.score);
+  F->score_out = score_out;
+  F->keep = (int32_t*)(w + L.keep);
+  F->ctrl = (Ctrl*)(w + L.ctrl);
+  F->ctl = (PassCtl*)(w + L.pass_ctl);
+  F->parts = (float*)(w + L.runs);
+  F->prefix = (int32_t*)(w + L.prefix);
+  F->flags = (uint32_t*)(w + L.flags);
+  for (int s = 0; s < c->n_seqs; ++s) {
+    F->seq[s].row0 = c->seq_row0[s];
+    F->seq[s].cap = c->capacity[s];
+    F->seq[s].budget = budget[s];
+    F->seq[s].cur_pos = p->cur_pos[s];
+    F->seq[s].sink = p->sink_rows ? p->sink_rows[s] : p->sink;
+  }
+  for (int i = 0; i < n_layers; ++i) {
+    F->lay[i].k = (uint8_t*)caches[i].k;
+    F->lay[i].ks = (uint8_t*)caches[i].k_scale;
+    F->lay[i].v = (uint8_t*)caches[i].v;
+    F->lay[i].vs = (uint8_t*)caches[i].v_scale;
+    F->lay[i].pos = caches[i].pos;
+    F->lay[i].n_live = caches[i].n_live;
+    F->lay[i].qe_off = st->qe_off[layers[i]];
+  }
+  const cudaError_t e = c->k_type == TRIA_F16 ? launch_pass_f16(*F, stream) : launch_pass_q8(*F, stream);
+  delete F;
+  return cuda_status(e);
+}
+
+bool fused_ok(const tria_layer_cache* c, int G, int n_layers) {
+  return pass_supported(c->k_type, c->head_dim, G) && n_layers >= 1 && n_layers <= kPassMaxLayers &&
+         (int64_t)n_layers * c->n_seqs * c->n_kv_heads <= kPassMaxSegs;
 }
 
 }  // namespace
@@ -384,6 +486,28 @@ extern "C" tria_status tria_compact(const tria_layer_cache* cache, const tria_po
   return cuda_status(launch_move(P, st));
 }
 
+namespace {
+
+// The staged pass: three kernels (score, select with the z-max score, move).
+tria_status evict_staged(const tria_stats* stats, int32_t layer, const tria_layer_cache* cache,
+                         const tria_policy* policy, const std::vector<int>& budget, const Layout& L, void* ws,
+                         cudaStream_t st) {
+  tria_status r;
+  Pass P;
+  fill_pass(P, cache, policy, budget, L, ws, stats->group);
+  set_stats(P, stats, layer);
+  P.only_active = 1;
+  P.raw = (float*)((uint8_t*)ws + L.raw);
+  P.score = (float*)((uint8_t*)ws + L.score);
+  P.score_in = P.score;
+  P.keep = (int32_t*)((uint8_t*)ws + L.keep);
+  if ((r = cuda_status(launch_score(P, st))) != TRIA_OK) return r;
+  if ((r = cuda_status(launch_select(P, true, st, stats->group))) != TRIA_OK) return r;
+  return cuda_status(launch_move(P, st));
+}
+
+}  // namespace
+
 extern "C" tria_status tria_evict(const tria_stats* stats, int32_t layer, const tria_layer_cache* cache,
                                   const tria_policy* policy, void* ws, size_t ws_bytes, void* stream) {
   tria_status r;
@@ -393,18 +517,84 @@ extern "C" tria_status tria_evict(const tria_stats* stats, int32_t layer, const 
   if ((r = check_policy(cache, policy, true, budget)) != TRIA_OK) return r;
   const Layout L = make_layout(cache, stats->group);
   if ((r = check_ws(ws, ws_bytes, L)) != TRIA_OK) return r;
-  Pass P;
-  fill_pass(P, cache, policy, budget, L, ws, stats->group);
-  set_stats(P, stats, layer);
-  P.only_active = 1;
-  P.raw = (float*)((uint8_t*)ws + L.raw);
-  P.score = (float*)((uint8_t*)ws + L.score);
-  P.score_in = P.score;
-  P.keep = (int32_t*)((uint8_t*)ws + L.keep);
   cudaStream_t st = (cudaStream_t)stream;
-  if ((r = cuda_status(launch_score(P, st))) != TRIA_OK) return r;
-  if ((r = cuda_status(launch_select(P, true, st, stats->group))) != TRIA_OK) return r;
-  return cuda_status(launch_move(P, st));
+  if (fused_ok(cache, stats->group, 1))
+    return launch_fused(stats, &layer, 1, cache, policy, budget, L, ws, nullptr, st);
+  return evict_staged(stats, layer, cache, policy, budget, L, ws, st);
+}
+
+extern "C" tria_status tria_evict_staged(const tria_stats* stats, int32_t layer, const tria_layer_cache* cache,
+                                         const tria_policy* policy, void* ws, size_t ws_bytes, void* stream) {
+  tria_status r;
+  if ((r = check_cache(cache)) != TRIA_OK) return r;
+  if ((r = check_stats(stats, layer, cache)) != TRIA_OK) return r;
+  std::vector<int> budget;
+  if ((r = check_policy(cache, policy, true, budget)) != TRIA_OK) return r;
+  const Layout L = make_layout(cache, stats->group);
+  if ((r = check_ws(ws, ws_bytes, L)) != TRIA_OK) return r;
+  return evict_staged(stats, layer, cache, policy, budget, L, ws, (cudaStream_t)stream);
+}
+
+namespace {
+
+// The caches of a model pass describe the same sequences with the same shapes
+// and types; each layer is loaded, has the cache's head_dim and the first
+// layer's RoPE frequencies.
+tria_status check_model(const tria_stats* stats, const int32_t* layers, int32_t n_layers,
+                        const tria_layer_cache* caches) {
+  tria_status r;
+  if (!layers || !caches || n_layers < 1) return TRIA_ERR_INVALID_ARG;
+  if (n_layers > kPassMaxLayers) return TRIA_ERR_UNSUPPORTED;
+  const tria_layer_cache& c0 = caches[0];
+  for (int i = 0; i < n_layers; ++i) {
+    const tria_layer_cache& c = caches[i];
+    if ((r = check_cache(&c)) != TRIA_OK) return r;
+    if ((r = check_stats(stats, layers[i], &c)) != TRIA_OK) return r;
+    if (c.n_seqs != c0.n_seqs || c.n_kv_heads != c0.n_kv_heads || c.head_dim != c0.head_dim ||
+        c.k_type != c0.k_type || c.v_type != c0.v_type)
+      return TRIA_ERR_INVALID_ARG;
+    for (int s = 0; s < c0.n_seqs; ++s)
+      if (c.seq_row0[s] != c0.seq_row0[s] || c.capacity[s] != c0.capacity[s]) return TRIA_ERR_INVALID_ARG;
+    const int64_t f0 = stats->freq_off[layers[0]], f1 = stats->freq_off[layers[0] + 1];
+    const int64_t g0 = stats->freq_off[layers[i]], g1 = stats->freq_off[layers[i] + 1];
+    if (g1 - g0 != f1 - f0) return TRIA_ERR_UNSUPPORTED;
+    for (int64_t k = 0; k < f1 - f0; ++k)
+      if (stats->freq[g0 + k] != stats->freq[f0 + k]) return TRIA_ERR_UNSUPPORTED;
+    for (int j = 0; j < i; ++j)   // one pass must not compact a layer twice
+      if (caches[j].k == c.k || caches[j].n_live == c.n_live) return TRIA_ERR_INVALID_ARG;
+  }
+  return TRIA_OK;
+}
+
+}  // namespace
+
+extern "C" size_t tria_model_workspace_size(const tria_layer_cache* cache, int32_t n_layers, int32_t group) {
+  if (check_cache(cache) != TRIA_OK || group < 0 || group > kMaxG || n_layers < 1 || n_layers > kPassMaxLayers)
+    return 0;
+  return make_model_layout(cache, group, n_layers).total;
+}
+
+extern "C" tria_status tria_evict_model(const tria_stats* stats, const int32_t* layers, int32_t n_layers,
+                                        const tria_layer_cache* caches, const tria_policy* policy,
+                                        float* score_out, void* ws, size_t ws_bytes, void* stream) {
+  tria_status r;
+  if ((r = check_model(stats, layers, n_layers, caches)) != TRIA_OK) return r;
+  std::vector<int> budget;
+  if ((r = check_policy(caches, policy, true, budget)) != TRIA_OK) return r;
+  if (score_out && ((uintptr_t)score_out % 4) != 0) return TRIA_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (fused_ok(caches, stats->group, n_layers)) {
+    const Layout L = make_model_layout(caches, stats->group, n_layers);
+    if ((r = check_ws(ws, ws_bytes, L)) != TRIA_OK) return r;
+    return launch_fused(stats, layers, n_layers, caches, policy, budget, L, ws, score_out, st);
+  }
+  // shapes without the fused kernel: one staged pass per layer (no scores out)
+  if (score_out) return TRIA_ERR_UNSUPPORTED;
+  const Layout L = make_layout(caches, stats->group);
+  if ((r = check_ws(ws, ws_bytes, L)) != TRIA_OK) return r;
+  for (int i = 0; i < n_layers; ++i)
+    if ((r = evict_staged(stats, layers[i], &caches[i], policy, budget, L, ws, st)) != TRIA_OK) return r;
+  return TRIA_OK;
 }
 
 extern "C" tria_status tria_evict_layers(const tria_stats* stats, const int32_t* layer_of_seq,

@@ -43,8 +43,14 @@ struct Ctrl {
   uint32_t bar_count;    // grid barrier: CTAs arrived (reset by the last one)
   uint32_t bar_gen;      // grid barrier: generation, bumped when all arrived
   uint32_t append_ticket;  // append CTAs that finished (reset by the last one)
-  uint32_t pad[54];
+  // fused pass (k_pass): reset by its last CTA
+  uint32_t score_next;   // next score item to claim
+  uint32_t ready_count;  // segments whose selection is published (slots of the ready list)
+  uint32_t move_cursor;  // first ready slot that may still have unclaimed move blocks
+  uint32_t pass_done;    // CTAs of the pass that finished
+  uint32_t pad[50];
 };
+static_assert(sizeof(Ctrl) == 256, "Ctrl layout");
 
 // Per-segment state (one segment = one sequence x KV head of the layer).
 struct SegState {
@@ -162,6 +168,26 @@ __device__ __forceinline__ uint32_t score_key(float s) {
   if (u == 0x80000000u) u = 0u;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
+
+// Tag of the compaction read-done flags of the call with control epoch e:
+// (e + 1) times an odd constant (mod 2^32), so consecutive calls' tags differ
+// and a tag is unlike the small counts or float bit patterns that other
+// calls may have left in the same workspace bytes; never 0.
+__host__ __device__ __forceinline__ uint32_t flag_tag(uint32_t epoch) {
+  const uint32_t x = (epoch + 1u) * 0x9E3779B1u;
+  return x ? x : 1u;
+}
+
+// Fixed-position state of the fused pass, right after the control words in
+// every workspace layout (so calls with different layer counts on one
+// workspace never read each other's data as counters): per segment of the
+// call, the ready list, the completed score items and the next move block.
+constexpr int kPassCtlSegs = 2048;
+struct PassCtl {
+  int32_t ready[kPassCtlSegs];        // segment + 1 in publication order (0: not yet)
+  int32_t items_done[kPassCtlSegs];
+  int32_t move_next[kPassCtlSegs];
+};
 
 __device__ __forceinline__ bool is_protected(int r, int n, int sink, int window) {
   return r < sink || r >= n - window;
@@ -383,21 +409,12 @@ __device__ __forceinline__ void moments_from_sums(const float* c, const float* s
   }
 }
 
-// Mean and 1 / (std + 1e-6) of the segment's heads, merged by one block
-// (all threads call it). Thread t adds runs t, t + blockDim, ... in order into
-// {N, sum n d_h, sum (M2 + n d^2)_h}, then fixed butterflies over lanes and
-// warps (deterministic). The segment's run layout, the shift c (run 0's mean)
-// and the first round of run partials are loaded together, so the merge waits
-// for one load latency; first-round rows past the run count are loaded and
-// ignored.
+// Moments of one segment from its run partials (tab: kRunCols columns of cs
+// floats, runs 0 .. nr-1), merged by one block; see block_segment_moments.
 template <int G>
-__device__ void block_segment_moments(const Pass& P, int seg, float* mu, float* inv) {
+__device__ void block_moments_of_runs(const float* tab, int cs, int nr, float* mu, float* inv) {
   __shared__ float red[32][1 + 2 * G];
   __shared__ float sums[1 + 2 * G];
-  const float* tab = run_table(P, seg);
-  const int cs = P.cs_max;
-  const int s0 = __ldcg(&P.seg[seg].piece_first), s1 = __ldcg(&P.seg[seg].piece_end);
-  const int per = max(1, __ldcg(&P.seg[seg].piece_per));
   float c[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) c[h] = __ldcg(&tab[(1 + h) * cs]);
@@ -425,7 +442,6 @@ __device__ void block_segment_moments(const Pass& P, int seg, float* mu, float* 
   };
   int r = threadIdx.x;
   if (r < cs) load_run(r);
-  const int nr = segment_runs(s0, s1, per);
   if (r < nr) add_run();
   for (r += blockDim.x; r < nr; r += blockDim.x) {
     load_run(r);
@@ -447,6 +463,20 @@ __device__ void block_segment_moments(const Pass& P, int seg, float* mu, float* 
   }
   __syncthreads();
   moments_from_sums<G>(c, sums, mu, inv);
+}
+
+// Mean and 1 / (std + 1e-6) of the segment's heads, merged by one block
+// (all threads call it) from the segment's score-run partials. Thread t adds
+// runs t, t + blockDim, ... in order into {N, sum n d_h, sum (M2 + n d^2)_h},
+// then fixed butterflies over lanes and warps (deterministic). The shift c
+// (run 0's mean) and the first round of run partials are loaded together, so
+// the merge waits for one load latency; first-round rows past the run count
+// are loaded and ignored.
+template <int G>
+__device__ void block_segment_moments(const Pass& P, int seg, float* mu, float* inv) {
+  const int s0 = __ldcg(&P.seg[seg].piece_first), s1 = __ldcg(&P.seg[seg].piece_end);
+  const int per = max(1, __ldcg(&P.seg[seg].piece_per));
+  block_moments_of_runs<G>(run_table(P, seg), P.cs_max, segment_runs(s0, s1, per), mu, inv);
 }
 
 // Dynamic shared-memory limit and the largest shared-memory carveout of a

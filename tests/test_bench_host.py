@@ -26,7 +26,7 @@ def test_algorithmic_bytes_of_the_qwen3_layer():
 
 def test_traffic_table_names_known_workloads_and_kernels():
     for (name, kernel), val in bench.TRAFFIC.items():
-        assert name in W.WORKLOADS and kernel in ("k_score", "k_move")
+        assert name in W.WORKLOADS and kernel in ("k_score", "k_move", "k_pass")
         assert isinstance(val, int) and val > 0
 
 
