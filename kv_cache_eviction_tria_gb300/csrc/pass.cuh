@@ -12,16 +12,18 @@
 //
 // Schedule. A segment is (layer, sequence, KV head). One CTA per SM (a
 // cooperative launch: every CTA is resident, so waits on other CTAs end).
-//  * Score items: a segment's live rows are cut into items of 12 warps x 2
-//    pieces (a piece is at most 8 KB of keys). A CTA claims items one ahead
-//    (an atomic counter in segment order); each warp streams its pieces
+//  * Score items: a segment's live rows are cut into items of 12 warps x ppw
+//    pieces (a piece is at most 8 KB of keys; ppw from 1 to 8, larger for
+//    larger passes). A CTA claims items two ahead (an atomic counter in
+//    segment order); each warp streams its pieces
 //    through a two-stage ring (bulk async copies completing on mbarriers) and
 //    issues the first piece of the CTA's next item while it computes its last
 //    piece of the current one, so the key stream does not stop between
 //    items. At the end of an item the CTA merges its warps' moments into one
 //    partial per item.
-//  * Select: the CTA that completes a segment's last item (an atomic count)
-//    selects that segment at once: segment moments from the item partials,
+//  * Select: the CTA that completes a segment's last item (an atomic count,
+//    read back one item later) selects that segment: segment moments from
+//    the item partials,
 //    z-max keys and the first radix histogram in one sweep, up to two more
 //    radix passes over the keys, then the keep list and the kept-row prefix
 //    of every 32-row chunk; it publishes the segment in the ready list. The
@@ -46,7 +48,7 @@ namespace tria {
 
 constexpr int kPassWarps = 12;
 constexpr int kPassThreads = kPassWarps * 32;
-constexpr int kPassPPW = 2;                  // pieces per warp per score item
+constexpr int kPassPPWMax = 8;               // pieces per warp per score item (at most)
 constexpr int kPassPieceBytes = 8192;
 constexpr int kPassScaleStage = kPassPieceBytes / 16;   // q8_0 block scales of a piece
 constexpr int kPassRing = kPassWarps * 2 * kPassPieceBytes;
@@ -69,11 +71,11 @@ struct FPass {
   int32_t n_layers, n_seqs, n_kv, n_seg, G, hd, fc, window;
   int32_t k_rb, ks_rb, v_rb, vs_rb;
   int32_t spin_limit;
-  int32_t item_rows;    // key rows per score item
+  int32_t item_rows;    // key rows per score item (kPassWarps x ppw x piece_rows)
   int32_t piece_rows;   // key rows per piece
+  int32_t ppw;          // pieces per warp per score item
   int32_t cs_max;       // columns of a segment's item-partial table (>= items per segment)
   int32_t c_max;        // chunks per segment (max)
-  int32_t pad0;
   int64_t rows_per_layer;   // workspace rows of one layer
   const float2* qe;
   const float* mw;
@@ -152,7 +154,7 @@ __device__ __forceinline__ void load_raw_g(const float* rp, float* x) {
 // Selection of one segment by the whole CTA (see the file comment). Writes
 // the keep list (B entries) and the kept-row prefix of every chunk.
 template <int G>
-__device__ void pass_select(const FPass& P, int sg, int n_items, uint32_t* hist) {
+__device__ __noinline__ void pass_select(const FPass& P, int sg, int n_items, uint32_t* hist) {
   __shared__ int s_info[4];
   __shared__ int s_sbuf[40];
   __shared__ int s_wt[kPassWarps], s_wk[kPassWarps];
@@ -170,7 +172,7 @@ __device__ void pass_select(const FPass& P, int sg, int n_items, uint32_t* hist)
   // z-max keys of every live row and the first radix histogram of the
   // candidates [lo, hi); loads of U rows per thread are in flight together
   {
-    constexpr int U = 4;
+    constexpr int U = G > 4 ? 4 : 8;
     const float* raw = P.raw + (size_t)v.wrow0 * G;
     float* so = P.score_out ? P.score_out + v.wrow0 : nullptr;
     for (int base = tid; base < n; base += U * kPassThreads) {
@@ -212,12 +214,23 @@ __device__ void pass_select(const FPass& P, int sg, int n_items, uint32_t* hist)
       if (pass > 0) {
         for (int i = tid; i < NB; i += blockDim.x) hist[i] = 0u;
         __syncthreads();
-        for (int r = lo + tid; r < hi; r += blockDim.x) {
-          const uint32_t key = __ldcg(keys + r);
-          if (pass == 1) {
-            if ((key >> 21) == prefix) atomicAdd(&hist[(key >> 10) & 0x7FFu], 1u);
-          } else if ((key >> 10) == prefix) {
-            atomicAdd(&hist[key & 0x3FFu], 1u);
+        constexpr int UB = 8;   // key loads in flight per thread
+        for (int base = lo + tid; base < hi; base += UB * kPassThreads) {
+          uint32_t kk[UB];
+#pragma unroll
+          for (int u = 0; u < UB; ++u) {
+            const int r = base + u * kPassThreads;
+            kk[u] = r < hi ? __ldcg(keys + r) : 0u;
+          }
+#pragma unroll
+          for (int u = 0; u < UB; ++u) {
+            if (base + u * kPassThreads >= hi) break;
+            const uint32_t key = kk[u];
+            if (pass == 1) {
+              if ((key >> 21) == prefix) atomicAdd(&hist[(key >> 10) & 0x7FFu], 1u);
+            } else if ((key >> 10) == prefix) {
+              atomicAdd(&hist[key & 0x3FFu], 1u);
+            }
           }
         }
         __syncthreads();
@@ -274,16 +287,26 @@ __device__ void pass_select(const FPass& P, int sg, int n_items, uint32_t* hist)
   const int nch = (n + kChunk - 1) / kChunk;
   const int cpw = (nch + kPassWarps - 1) / kPassWarps;
   const int c0 = min(nch, warp * cpw), c1 = min(nch, c0 + cpw);
+  constexpr int CB = 8;   // chunks whose keys load together
   {
     int wt = 0, wk = 0;
-    for (int ci = c0; ci < c1; ++ci) {
-      const int r = ci * kChunk + lane;
-      const bool in = r < n;
-      const bool pr = in && (r < lo || r >= hi);
-      const bool cand = in && !pr && k > 0;
-      const uint32_t key = cand ? __ldcg(keys + r) : 0u;
-      wt += __popc(__ballot_sync(0xffffffffu, cand && key == T));
-      wk += __popc(__ballot_sync(0xffffffffu, pr || (cand && key > T)));
+    for (int cb = c0; cb < c1; cb += CB) {
+      uint32_t kk[CB];
+#pragma unroll
+      for (int u = 0; u < CB; ++u) {
+        const int r = (cb + u) * kChunk + lane;
+        kk[u] = (cb + u < c1 && r < n && r >= lo && r < hi && k > 0) ? __ldcg(keys + r) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < CB; ++u) {
+        if (cb + u >= c1) break;
+        const int r = (cb + u) * kChunk + lane;
+        const bool in = r < n;
+        const bool pr = in && (r < lo || r >= hi);
+        const bool cand = in && !pr && k > 0;
+        wt += __popc(__ballot_sync(0xffffffffu, cand && kk[u] == T));
+        wk += __popc(__ballot_sync(0xffffffffu, pr || (cand && kk[u] > T)));
+      }
     }
     if (lane == 0) {
       s_wt[warp] = wt;
@@ -298,21 +321,31 @@ __device__ void pass_select(const FPass& P, int sg, int n_items, uint32_t* hist)
   }
   int32_t* keep = P.keep + v.wrow0;
   int* pre = P.prefix + (size_t)sg * (P.c_max + 1);
-  for (int ci = c0; ci < c1; ++ci) {
-    const int r = ci * kChunk + lane;
-    const bool in = r < n;
-    const bool pr = in && (r < lo || r >= hi);
-    const bool cand = in && !pr && k > 0;
-    const uint32_t key = cand ? __ldcg(keys + r) : 0u;
-    const bool is_tie = cand && key == T;
-    const uint32_t bt = __ballot_sync(0xffffffffu, is_tie);
-    const int trank = tie_run + __popc(bt & ((1u << lane) - 1u));
-    const bool kp = pr || (cand && key > T) || (is_tie && trank < kr);
-    const uint32_t bk = __ballot_sync(0xffffffffu, kp);
-    if (lane == 0) pre[ci] = keep_run;
-    if (kp) keep[keep_run + __popc(bk & ((1u << lane) - 1u))] = r;
-    tie_run += __popc(bt);
-    keep_run += __popc(bk);
+  for (int cb = c0; cb < c1; cb += CB) {
+    uint32_t kk[CB];
+#pragma unroll
+    for (int u = 0; u < CB; ++u) {
+      const int r = (cb + u) * kChunk + lane;
+      kk[u] = (cb + u < c1 && r < n && r >= lo && r < hi && k > 0) ? __ldcg(keys + r) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < CB; ++u) {
+      const int ci = cb + u;
+      if (ci >= c1) break;
+      const int r = ci * kChunk + lane;
+      const bool in = r < n;
+      const bool pr = in && (r < lo || r >= hi);
+      const bool cand = in && !pr && k > 0;
+      const bool is_tie = cand && kk[u] == T;
+      const uint32_t bt = __ballot_sync(0xffffffffu, is_tie);
+      const int trank = tie_run + __popc(bt & ((1u << lane) - 1u));
+      const bool kp = pr || (cand && kk[u] > T) || (is_tie && trank < kr);
+      const uint32_t bk = __ballot_sync(0xffffffffu, kp);
+      if (lane == 0) pre[ci] = keep_run;
+      if (kp) keep[keep_run + __popc(bk & ((1u << lane) - 1u))] = r;
+      tie_run += __popc(bt);
+      keep_run += __popc(bk);
+    }
   }
   if (warp == kPassWarps - 1 && lane == 0) {
     pre[nch] = v.B;
@@ -325,6 +358,130 @@ __device__ void pass_select(const FPass& P, int sg, int n_items, uint32_t* hist)
     const uint32_t slot = atomicAdd(&P.ctrl->ready_count, 1u);
     st_release_u32(reinterpret_cast<uint32_t*>(P.ctl->ready + slot), (uint32_t)(sg + 1));
   }
+}
+
+// One warp's share of the moves: claim 32-row destination blocks of ready
+// segments (the next claim is issued while the current block's rows load)
+// and move each as k_move does. Returns when every active segment's blocks
+// are claimed (or a bounded wait gave up).
+__device__ __noinline__ void pass_moves(const FPass& P, uint8_t* stg, int* msrc, uint32_t tag, int n_active) {
+  const int lane = threadIdx.x & 31;
+  const MoveStage L = move_stage_layout(P.k_rb, P.ks_rb, P.v_rb, P.vs_rb);
+  const PlaneMap mk = plane_map(P.k_rb, lane), mks = plane_map(P.ks_rb, lane), mv = plane_map(P.v_rb, lane),
+                 mvs = plane_map(P.vs_rb, lane);
+  // lane 0: 0 = block (sg, j), 1 = none ready yet, 2 = every block claimed
+  auto claim = [&](int& sg, int& j) {
+    int state = 1;
+    sg = 0;
+    j = 0;
+    if (lane == 0) {
+      while (true) {
+        const uint32_t c = ld_acquire_u32(&P.ctrl->move_cursor);
+        if ((int)c >= n_active) {
+          state = 2;
+          break;
+        }
+        const uint32_t e = ld_acquire_u32(reinterpret_cast<const uint32_t*>(P.ctl->ready + c));
+        if (e == 0u) break;
+        sg = (int)e - 1;
+        if (sg >= P.n_seg) {   // cannot happen: the list holds this call's segments
+          report(P.ctrl, TRIA_ERR_INVALID_ARG, 0x08000000u);
+          state = 2;
+          break;
+        }
+        const int nb = (P.seq[(sg % (P.n_seqs * P.n_kv)) / P.n_kv].budget + kChunk - 1) / kChunk;
+        j = atomicAdd(&P.ctl->move_next[sg], 1);
+        if (j >= 0 && j < nb) {
+          state = 0;
+          break;
+        }
+        atomicCAS(&P.ctrl->move_cursor, c, c + 1u);   // exhausted: move past it
+      }
+    }
+    return state;
+  };
+  int nsg, nj;
+  int nstate = claim(nsg, nj);
+  int idle = 0;
+  while (true) {
+    const int state = __shfl_sync(0xffffffffu, nstate, 0);
+    if (state == 2) break;
+    if (state == 1) {
+      if (++idle > P.spin_limit) {
+        if (lane == 0) report(P.ctrl, TRIA_ERR_TIMEOUT, 0xA0000000u);
+        break;
+      }
+      __nanosleep(idle < 64 ? 64 : 512);
+      nstate = claim(nsg, nj);
+      continue;
+    }
+    idle = 0;
+    const int sg = __shfl_sync(0xffffffffu, nsg, 0);
+    const int j = __shfl_sync(0xffffffffu, nj, 0);
+    const PSeg v = pass_seg(P, sg);
+    const LayerRef& lr = P.lay[v.li];
+    const int B = v.B, n = v.n;
+    const int i0 = j * kChunk, cnt = min(kChunk, B - i0);
+    const int a = lane < cnt ? __ldcg(P.keep + v.wrow0 + i0 + lane) : -1;
+    const int* pre = P.prefix + (size_t)sg * (P.c_max + 1);
+    const int p0 = __ldcg(&pre[j]), p1 = __ldcg(&pre[j + 1]);
+    const bool bad_entry = lane < cnt && (a < i0 + lane || a >= n);
+    const bool ok = !__any_sync(0xffffffffu, bad_entry) && p0 >= 0 && p0 <= p1 && p1 - p0 <= kChunk && p1 <= B;
+    if (!ok && lane == 0) report(P.ctrl, TRIA_ERR_INVALID_ARG, 0x10000000u | (uint32_t)sg);
+    // moving entries (keep[i] != i) are a suffix of the block
+    const unsigned mvm = __ballot_sync(0xffffffffu, ok && lane < cnt && a != i0 + lane);
+    const int first = mvm ? __ffs(mvm) - 1 : cnt;
+    const int nmove = ok ? cnt - first : 0;
+    if (lane == 0) bulk_wait_read_all();   // the previous block's stores have read the stage
+    __syncwarp();
+    if (lane >= first && lane < cnt) msrc[lane - first] = a;
+    __syncwarp();
+    int my_pos = 0;
+    if (nmove > 0) {
+      warp_gather(lr.k, v.row0, mk, stg + L.k, msrc, nmove);
+      warp_gather(lr.ks, v.row0, mks, stg + L.ks, msrc, nmove);
+      warp_gather(lr.v, v.row0, mv, stg + L.v, msrc, nmove);
+      warp_gather(lr.vs, v.row0, mvs, stg + L.vs, msrc, nmove);
+      if (lane < nmove) my_pos = __ldcg(lr.pos + v.row0 + msrc[lane]);
+    }
+    cp_async_commit();
+    nstate = claim(nsg, nj);   // the next block's claim travels while the rows load
+    cp_async_wait<0>();
+    __syncwarp();
+    if (lane < nmove) msrc[lane] = my_pos;
+    __syncwarp();
+    // publish "read"; then wait for the lower blocks that read my destination rows
+    uint32_t* flags = P.flags + (size_t)sg * P.c_max;
+    int go = 0;
+    if (lane == 0) {
+      st_relaxed_u32(&flags[j], tag);
+      go = ok;
+      if (go && nmove > 0 && p1 > p0) {
+        const int lo_b = p0 / kChunk, hi_b = min((p1 - 1) / kChunk, j - 1);
+        for (int cc = lo_b; cc <= hi_b; ++cc)
+          if (!wait_flag_bounded(&flags[cc], tag, P.spin_limit)) {
+            go = 0;
+            report(P.ctrl, TRIA_ERR_TIMEOUT, (uint32_t)sg);
+            break;
+          }
+      }
+    }
+    go = __shfl_sync(0xffffffffu, go, 0);
+    if (go && nmove > 0) {
+      const int dst0 = i0 + first;
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        bulk_s2g(lr.k + (size_t)(v.row0 + dst0) * P.k_rb, stg + L.k, (uint32_t)(nmove * P.k_rb));
+        bulk_s2g(lr.v + (size_t)(v.row0 + dst0) * P.v_rb, stg + L.v, (uint32_t)(nmove * P.v_rb));
+        bulk_commit();
+      }
+      warp_scatter(lr.ks, v.row0, P.ks_rb, stg + L.ks, dst0, nmove, lane);
+      warp_scatter(lr.vs, v.row0, P.vs_rb, stg + L.vs, dst0, nmove, lane);
+      if (lane < nmove) lr.pos[v.row0 + dst0 + lane] = msrc[lane];
+    }
+    __syncwarp();
+  }
+  if (lane == 0) bulk_wait_all();
 }
 
 template <int KT, int G, int S>
@@ -432,72 +589,95 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
   int n_issued = 0, n_done = 0;   // pieces of this warp through its ring
   int carried = 0;                // pieces of the current item issued during the previous one
   bool failed = false;
+  // thread 0: the claim of the item after next (in flight during the current
+  // item) and the completion count of the previous item, checked one item
+  // later so that neither round trip sits between two items
+  int pend_sg = -1, pend_items = 0, pend_old = 0;
 
-  // piece i (of this warp) of item `it`: rows [r0, r0 + rows) of segment sg
-  struct Piece {
-    int sg, rows;
-    int64_t row0, wrow0;   // first row of the piece: planes / workspace
-    int li;
+  // item `it` as seen by this warp: its segment, the segment's geometry (live
+  // rows are read only for a segment's last item: the others are full), and
+  // this warp's pieces in it
+  struct ItemView {
+    int it, sg, n_pieces, rows_end;   // rows_end: first row past the item
   };
-  auto my_pieces = [&](int it, int& sg_out, PSeg& v) {
-    if (it < 0) return 0;
-    sg_out = seg_of_item(it);
-    v = pass_seg(P, sg_out);
-    const int j = it - item0[sg_out];
-    const int r_beg = j * P.item_rows + warp * kPassPPW * P.piece_rows;
-    const int left = v.n - r_beg;
-    return left <= 0 ? 0 : min(kPassPPW, (left + P.piece_rows - 1) / P.piece_rows);
+  auto view_of = [&](int it) {
+    ItemView iv;
+    iv.it = it;
+    iv.sg = 0;
+    iv.n_pieces = 0;
+    iv.rows_end = 0;
+    if (it < 0) return iv;
+    iv.sg = seg_of_item(it);
+    const int j = it - item0[iv.sg];
+    if (it == item0[iv.sg + 1] - 1) {   // a segment's last item ends at its live rows
+      const int li = iv.sg / (P.n_seqs * P.n_kv);
+      const int s = (iv.sg - li * P.n_seqs * P.n_kv) / P.n_kv;
+      iv.rows_end = *((volatile const int32_t*)(P.lay[li].n_live + s));
+    } else {
+      iv.rows_end = (j + 1) * P.item_rows;
+    }
+    const int r_beg = j * P.item_rows + warp * P.ppw * P.piece_rows;
+    const int left = iv.rows_end - r_beg;
+    iv.n_pieces = left <= 0 ? 0 : min(P.ppw, (left + P.piece_rows - 1) / P.piece_rows);
+    return iv;
   };
-  auto piece_of = [&](int it, int sg, const PSeg& v, int i) {
-    Piece pc;
-    const int j = it - item0[sg];
-    const int r0 = j * P.item_rows + (warp * kPassPPW + i) * P.piece_rows;
-    pc.sg = sg;
-    pc.li = v.li;
-    pc.rows = min(P.piece_rows, v.n - r0);
-    pc.row0 = v.row0 + r0;
-    pc.wrow0 = v.wrow0 + r0;
-    return pc;
+  // first row of segment sg in its layer's planes
+  auto seg_row0 = [&](int sg) {
+    const int r = sg % (P.n_seqs * P.n_kv);
+    const int s = r / P.n_kv;
+    return P.seq[s].row0 + (int64_t)(r - s * P.n_kv) * P.seq[s].cap;
   };
-  auto issue = [&](const Piece& pc) {   // warp-collective
+  // rows [r0, r0 + rows) of piece i of this warp in item iv
+  auto piece_r0 = [&](const ItemView& iv, int i) {
+    return (iv.it - item0[iv.sg]) * P.item_rows + (warp * P.ppw + i) * P.piece_rows;
+  };
+  auto issue = [&](const ItemView& iv, int i) {   // warp-collective
     const int st = n_issued & 1;
+    const int r0 = piece_r0(iv, i);
+    const int rows = min(P.piece_rows, iv.rows_end - r0);
+    const int64_t grow = seg_row0(iv.sg) + r0;
+    const int li = iv.sg / (P.n_seqs * P.n_kv);
     if (lane == 0) {
-      const uint32_t bytes = (uint32_t)(pc.rows * P.k_rb);
+      const uint32_t bytes = (uint32_t)(rows * P.k_rb);
       mbar_arrive_expect_tx(&bars[st], bytes);
-      bulk_g2s(ring + st * kPassPieceBytes, P.lay[pc.li].k + (size_t)pc.row0 * P.k_rb, bytes, &bars[st]);
+      bulk_g2s(ring + st * kPassPieceBytes, P.lay[li].k + (size_t)grow * P.k_rb, bytes, &bars[st]);
     }
     if constexpr (kQ8) {
-      const uint8_t* src = P.lay[pc.li].ks + (size_t)pc.row0 * P.ks_rb;
+      const uint8_t* src = P.lay[li].ks + (size_t)grow * P.ks_rb;
       uint8_t* dst = sc_ring + st * kPassScaleStage;
-      for (int u = lane; u < pc.rows * P.ks_rb / 4; u += 32) cp_async4(dst + 4 * u, src + 4 * u);
+      for (int u = lane; u < rows * P.ks_rb / 4; u += 32) cp_async4(dst + 4 * u, src + 4 * u);
       cp_async_commit();
     }
     ++n_issued;
   };
 
+  ItemView nv = view_of(s_item[1]);
   while (s_item[0] >= 0) {
     const int cur = s_item[0], nxt = s_item[1];
-    int sg = 0, sg_n = 0;
-    PSeg v, vn;
-    const int nc = my_pieces(cur, sg, v);
-    const int nn = failed ? 0 : my_pieces(nxt, sg_n, vn);
-    if (sg != body_seg) {
-      body.load_consts(P.qe + P.lay[v.li].qe_off + (size_t)v.g * G * FC,
-                       P.mw + P.lay[v.li].qe_off + (size_t)v.g * G * FC, s_turns,
-                       (unsigned long long)P.seq[v.s].cur_pos);
-      body_seg = sg;
+    const ItemView cv = nv.it == cur ? nv : view_of(cur);
+    nv = failed ? view_of(-1) : view_of(nxt);
+    int claim = -1;
+    if (tid == 0 && nxt >= 0) claim = (int)atomicAdd(&P.ctrl->score_next, 1u);   // used after this item
+    const int nc = cv.n_pieces, nn = nv.n_pieces;
+    if (cv.sg != body_seg) {
+      const int li = cv.sg / (P.n_seqs * P.n_kv);
+      const int r = cv.sg - li * P.n_seqs * P.n_kv;
+      const int s = r / P.n_kv;
+      const size_t qo = P.lay[li].qe_off + (size_t)(r - s * P.n_kv) * G * FC;
+      body.load_consts(P.qe + qo, P.mw + qo, s_turns, (unsigned long long)P.seq[s].cur_pos);
+      body_seg = cv.sg;
     }
-    int iss = carried;   // pieces of [cur..., next...] issued so far
+    int iss = carried;   // pieces of [current item..., next item...] issued so far
     auto issue_seq = [&](int idx) {
-      if (idx < nc) issue(piece_of(cur, sg, v, idx));
-      else issue(piece_of(nxt, sg_n, vn, idx - nc));
+      if (idx < nc) issue(cv, idx);
+      else issue(nv, idx - nc);
     };
     for (int i = 0; i < nc && !failed; ++i) {
       while (iss <= i) issue_seq(iss++);
-      if (iss == i + 1 && i + 1 < nc + nn) issue_seq(iss++);   // one ahead, possibly the next item's
+      if (iss == i + 1 && (i + 1 < nc || i + 1 - nc < nn)) issue_seq(iss++);   // one ahead, possibly the next item's
       const int st = n_done & 1;
       if (!mbar_wait_bounded(&bars[st], (uint32_t)((n_done >> 1) & 1), P.spin_limit)) {
-        if (lane == 0) report(P.ctrl, TRIA_ERR_TIMEOUT, (uint32_t)sg);
+        if (lane == 0) report(P.ctrl, TRIA_ERR_TIMEOUT, (uint32_t)cv.sg);
         // wait again (bounded) for every copy still in flight, then stop scoring
         for (int d = n_done; d < n_issued; ++d) mbar_wait_bounded(&bars[d & 1], (uint32_t)((d >> 1) & 1), P.spin_limit);
         if constexpr (kQ8) cp_async_wait<0>();
@@ -510,9 +690,10 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
         else cp_async_wait<0>();
         __syncwarp();
       }
-      const Piece pc = piece_of(cur, sg, v, i);
-      body.piece(ring + st * kPassPieceBytes, sc_ring + st * kPassScaleStage, pc.rows, P.k_rb, P.ks_rb,
-                 P.raw + (size_t)pc.wrow0 * G);
+      const int r0 = piece_r0(cv, i);
+      const int64_t wrow = (int64_t)(cv.sg / (P.n_seqs * P.n_kv)) * P.rows_per_layer + seg_row0(cv.sg) + r0;
+      body.piece(ring + st * kPassPieceBytes, sc_ring + st * kPassScaleStage, min(P.piece_rows, cv.rows_end - r0),
+                 P.k_rb, P.ks_rb, P.raw + (size_t)wrow * G);
       __syncwarp();
       ++n_done;
     }
@@ -533,146 +714,49 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
     if (tid < G) {
       Mom a{0.f, 0.f, 0.f};
       for (int w = 0; w < kPassWarps; ++w) a = mom_merge(a, s_mom[w][tid]);
-      float* tab = P.parts + (size_t)sg * kRunCols * P.cs_max;
-      const int j = cur - item0[sg];
+      float* tab = P.parts + (size_t)cv.sg * kRunCols * P.cs_max;
+      const int j = cur - item0[cv.sg];
       tab[(1 + tid) * P.cs_max + j] = a.mean;
       tab[(1 + kMaxG + tid) * P.cs_max + j] = a.m2;
       if (tid == 0) tab[j] = a.n;
     }
-    __threadfence();
     __syncthreads();
     if (tid == 0) {
-      const int n_items = item0[sg + 1] - item0[sg];
-      s_last = atomicAdd(&P.ctl->items_done[sg], 1) == n_items - 1;
+      // the previous item's completion count has arrived by now
+      s_last = (pend_sg >= 0 && pend_old == pend_items - 1) ? pend_sg : -1;
+      // this item's raw scores and moments (every thread's, ordered by the
+      // barrier) before its completion count
       __threadfence();
+      pend_sg = cv.sg;
+      pend_items = item0[cv.sg + 1] - item0[cv.sg];
+      pend_old = atomicAdd(&P.ctl->items_done[cv.sg], 1);
       s_item[0] = nxt;
-      int b = -1;
-      if (nxt >= 0) {
-        b = (int)atomicAdd(&P.ctrl->score_next, 1u);
-        if (b >= total) b = -1;
-      }
-      s_item[1] = b;
+      s_item[1] = claim < total ? claim : -1;
     }
     __syncthreads();
-    if (s_last) pass_select<G>(P, sg, item0[sg + 1] - item0[sg], hist);
+    // selections due: the segment the previous item completed (s_last), and
+    // once no item is left, the one the last item completed
+    while (true) {
+      if (s_last >= 0) {
+        __threadfence();
+        pass_select<G>(P, s_last, item0[s_last + 1] - item0[s_last], hist);
+      }
+      if (s_item[0] >= 0) break;
+      __syncthreads();
+      if (tid == 0) {
+        s_last = (pend_sg >= 0 && pend_old == pend_items - 1) ? pend_sg : -1;
+        pend_sg = -1;
+      }
+      __syncthreads();
+      if (s_last < 0) break;
+    }
   }
 
   // ---- moves: warps claim destination blocks of ready segments
-  const MoveStage L = move_stage_layout(P.k_rb, P.ks_rb, P.v_rb, P.vs_rb);
-  const int move_warps_n = min(kPassWarps, kPassRing / L.bytes);
-  if (warp < move_warps_n && n_active > 0) {
-    uint8_t* stg = smem + PassSmem::kRing + (size_t)warp * L.bytes;
-    int* msrc = s_src[warp];
-    const uint32_t tag = flag_tag(s_epoch);
-    const PlaneMap mk = plane_map(P.k_rb, lane), mks = plane_map(P.ks_rb, lane), mv = plane_map(P.v_rb, lane),
-                   mvs = plane_map(P.vs_rb, lane);
-    int idle = 0;
-    while (true) {
-      // claim: 0 = a block (sg, j), 1 = none ready yet, 2 = all claimed
-      int state = 1, sg = 0, j = 0;
-      if (lane == 0) {
-        while (true) {
-          const uint32_t c = ld_acquire_u32(&P.ctrl->move_cursor);
-          if ((int)c >= n_active) {
-            state = 2;
-            break;
-          }
-          const uint32_t e = ld_acquire_u32(reinterpret_cast<const uint32_t*>(P.ctl->ready + c));
-          if (e == 0u) {
-            state = 1;
-            break;
-          }
-          sg = (int)e - 1;
-          if (sg >= P.n_seg) {   // cannot happen: the list holds this call's segments
-            report(P.ctrl, TRIA_ERR_INVALID_ARG, 0x08000000u);
-            state = 2;
-            break;
-          }
-          const int nb = (P.seq[(sg % (P.n_seqs * P.n_kv)) / P.n_kv].budget + kChunk - 1) / kChunk;
-          j = atomicAdd(&P.ctl->move_next[sg], 1);
-          if (j >= 0 && j < nb) {
-            state = 0;
-            break;
-          }
-          atomicCAS(&P.ctrl->move_cursor, c, c + 1u);   // exhausted: move past it
-        }
-      }
-      state = __shfl_sync(0xffffffffu, state, 0);
-      if (state == 2) break;
-      if (state == 1) {
-        if (++idle > P.spin_limit) {
-          if (lane == 0) report(P.ctrl, TRIA_ERR_TIMEOUT, 0xA0000000u);
-          break;
-        }
-        __nanosleep(idle < 64 ? 64 : 512);
-        continue;
-      }
-      idle = 0;
-      sg = __shfl_sync(0xffffffffu, sg, 0);
-      j = __shfl_sync(0xffffffffu, j, 0);
-      const PSeg v = pass_seg(P, sg);
-      const LayerRef& lr = P.lay[v.li];
-      const int B = v.B, n = v.n;
-      const int i0 = j * kChunk, cnt = min(kChunk, B - i0);
-      const int a = lane < cnt ? __ldcg(P.keep + v.wrow0 + i0 + lane) : -1;
-      const int* pre = P.prefix + (size_t)sg * (P.c_max + 1);
-      const int p0 = __ldcg(&pre[j]), p1 = __ldcg(&pre[j + 1]);
-      const bool bad_entry = lane < cnt && (a < i0 + lane || a >= n);
-      const bool ok = !__any_sync(0xffffffffu, bad_entry) && p0 >= 0 && p0 <= p1 && p1 - p0 <= kChunk && p1 <= B;
-      if (!ok && lane == 0) report(P.ctrl, TRIA_ERR_INVALID_ARG, 0x10000000u | (uint32_t)sg);
-      // moving entries (keep[i] != i) are a suffix of the block
-      const unsigned mvm = __ballot_sync(0xffffffffu, ok && lane < cnt && a != i0 + lane);
-      const int first = mvm ? __ffs(mvm) - 1 : cnt;
-      const int nmove = ok ? cnt - first : 0;
-      if (lane == 0) bulk_wait_read_all();   // the previous block's stores have read the stage
-      __syncwarp();
-      if (lane >= first && lane < cnt) msrc[lane - first] = a;
-      __syncwarp();
-      int my_pos = 0;
-      if (nmove > 0) {
-        warp_gather(lr.k, v.row0, mk, stg + L.k, msrc, nmove);
-        warp_gather(lr.ks, v.row0, mks, stg + L.ks, msrc, nmove);
-        warp_gather(lr.v, v.row0, mv, stg + L.v, msrc, nmove);
-        warp_gather(lr.vs, v.row0, mvs, stg + L.vs, msrc, nmove);
-        if (lane < nmove) my_pos = __ldcg(lr.pos + v.row0 + msrc[lane]);
-      }
-      cp_async_commit();
-      cp_async_wait<0>();
-      __syncwarp();
-      if (lane < nmove) msrc[lane] = my_pos;
-      __syncwarp();
-      // publish "read"; then wait for the lower blocks that read my destination rows
-      uint32_t* flags = P.flags + (size_t)sg * P.c_max;
-      int go = 0;
-      if (lane == 0) {
-        st_relaxed_u32(&flags[j], tag);
-        go = ok;
-        if (go && nmove > 0 && p1 > p0) {
-          const int lo_b = p0 / kChunk, hi_b = min((p1 - 1) / kChunk, j - 1);
-          for (int cc = lo_b; cc <= hi_b; ++cc)
-            if (!wait_flag_bounded(&flags[cc], tag, P.spin_limit)) {
-              go = 0;
-              report(P.ctrl, TRIA_ERR_TIMEOUT, (uint32_t)sg);
-              break;
-            }
-        }
-      }
-      go = __shfl_sync(0xffffffffu, go, 0);
-      if (go && nmove > 0) {
-        const int dst0 = i0 + first;
-        if (lane == 0) {
-          fence_proxy_async_smem();
-          bulk_s2g(lr.k + (size_t)(v.row0 + dst0) * P.k_rb, stg + L.k, (uint32_t)(nmove * P.k_rb));
-          bulk_s2g(lr.v + (size_t)(v.row0 + dst0) * P.v_rb, stg + L.v, (uint32_t)(nmove * P.v_rb));
-          bulk_commit();
-        }
-        warp_scatter(lr.ks, v.row0, P.ks_rb, stg + L.ks, dst0, nmove, lane);
-        warp_scatter(lr.vs, v.row0, P.vs_rb, stg + L.vs, dst0, nmove, lane);
-        if (lane < nmove) lr.pos[v.row0 + dst0 + lane] = msrc[lane];
-      }
-      __syncwarp();
-    }
-    if (lane == 0) bulk_wait_all();
+  {
+    const MoveStage L = move_stage_layout(P.k_rb, P.ks_rb, P.v_rb, P.vs_rb);
+    if (warp < min(kPassWarps, kPassRing / L.bytes) && n_active > 0)
+      pass_moves(P, smem + PassSmem::kRing + (size_t)warp * L.bytes, s_src[warp], flag_tag(s_epoch), n_active);
   }
 
   // ---- the last CTA: n_live of the active sequences, counters reset
