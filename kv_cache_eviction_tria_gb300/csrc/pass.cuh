@@ -364,7 +364,7 @@ __device__ __noinline__ void pass_select(const FPass& P, int sg, int n_items, ui
 // segments (the next claim is issued while the current block's rows load)
 // and move each as k_move does. Returns when every active segment's blocks
 // are claimed (or a bounded wait gave up).
-__device__ __noinline__ void pass_moves(const FPass& P, uint8_t* stg, int* msrc, uint32_t tag, int n_active) {
+static __device__ __noinline__ void pass_moves(const FPass& P, uint8_t* stg, int* msrc, uint32_t tag, int n_active) {
   const int lane = threadIdx.x & 31;
   const MoveStage L = move_stage_layout(P.k_rb, P.ks_rb, P.v_rb, P.vs_rb);
   const PlaneMap mk = plane_map(P.k_rb, lane), mks = plane_map(P.ks_rb, lane), mv = plane_map(P.v_rb, lane),
