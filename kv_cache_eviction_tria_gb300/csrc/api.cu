@@ -97,9 +97,13 @@ Layout make_model_layout(const tria_layer_cache* c, int G, int n_layers) {
   Layout L = L1;
   const int k_rb = row_bytes(c->k_type, c->head_dim);
   const int cap_max = L1.c_max * kChunk;
-  const int item_rows = kPassWarps * pass_piece_rows(k_rb);   // the smallest item (one piece per warp)
+  // score runs of a segment: at most one per warp of the grid, plus one
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 1024;
+  const int piece_rows = pass_piece_rows(k_rb);
   L.n_seg = n_layers * L1.n_seg;
-  L.cs_max = (cap_max + item_rows - 1) / item_rows;
+  L.cs_max = std::min((cap_max + piece_rows - 1) / piece_rows, kPassWarps * sms + 2);
   const int64_t rows = L1.total_rows * n_layers;
   size_t off = L1.total;
   L.runs = off;
@@ -207,22 +211,6 @@ tria_status launch_fused(const tria_stats* st, const int32_t* layers, int n_laye
   F->vs_rb = scale_row_bytes(c->v_type, c->head_dim);
   F->spin_limit = kDefaultSpinLimit;
   F->piece_rows = pass_piece_rows(F->k_rb);
-  // pieces per warp per score item: as many as keep at least four items per
-  // CTA (larger items pay the item boundary less often), 2 to 8
-  {
-    static int sms = 0;
-    if (sms == 0) {
-      int dev = 0;
-      if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        sms = 1;
-    }
-    int64_t pieces = 0;
-    for (int s = 0; s < c->n_seqs; ++s)
-      pieces += (int64_t)n_layers * c->n_kv_heads * ((c->capacity[s] + F->piece_rows - 1) / F->piece_rows);
-    const int64_t per = pieces / ((int64_t)kPassWarps * sms * 4);
-    F->ppw = (int)std::max<int64_t>(2, std::min<int64_t>(kPassPPWMax, per));
-  }
-  F->item_rows = kPassWarps * F->ppw * F->piece_rows;
   F->cs_max = L.cs_max;
   F->c_max = L.c_max;
   F->rows_per_layer = L.total_rows;

@@ -12,33 +12,29 @@
 //
 // Schedule. A segment is (layer, sequence, KV head). One CTA per SM (a
 // cooperative launch: every CTA is resident, so waits on other CTAs end).
-//  * Score items: a segment's live rows are cut into items of 12 warps x ppw
-//    pieces (a piece is at most 8 KB of keys; ppw from 1 to 8, larger for
-//    larger passes). A CTA claims items two ahead (an atomic counter in
-//    segment order); each warp streams its pieces
-//    through a two-stage ring (bulk async copies completing on mbarriers) and
-//    issues the first piece of the CTA's next item while it computes its last
-//    piece of the current one, so the key stream does not stop between
-//    items. At the end of an item the CTA merges its warps' moments into one
-//    partial per item.
-//  * Select: the CTA that completes a segment's last item (an atomic count,
-//    read back one item later) selects that segment: segment moments from
-//    the item partials,
-//    z-max keys and the first radix histogram in one sweep, up to two more
-//    radix passes over the keys, then the keep list and the kept-row prefix
-//    of every 32-row chunk; it publishes the segment in the ready list. The
-//    ring keeps loading the next item meanwhile (the select uses its own
-//    shared memory).
-//  * Moves: once the score items are all claimed, a CTA's warps claim 32-row
-//    destination blocks of ready segments (in order, one counter per
-//    segment) and move them as k_move does: gather the block's moving rows
-//    into the warp's stage, publish "read", wait (bounded) for the lower
-//    blocks that read its destination rows, store. The ready list and the
-//    per-segment counters live at a fixed place of the workspace (PassCtl).
+//  * Scoring: the live rows of all segments, in segment order, are cut into
+//    pieces of at most 8 KB of keys, and every warp of the grid takes one
+//    contiguous run of them, streamed through a private two-stage ring (bulk
+//    async copies completing on mbarriers), exactly as the staged scorer
+//    does; no CTA-wide step interrupts the stream. A warp writes one moment
+//    partial per (run, segment) and adds its pieces to the segment's scored
+//    count; the warp that completes a segment appends it to the scored list.
+//  * Service: a CTA whose warps have all finished scoring selects scored
+//    segments (one CTA per segment: segment moments from the run partials,
+//    z-max keys in shared memory where they fit, radix select, keep list and
+//    the kept-row prefix of every 32-row chunk) and appends each to the ready
+//    list; while no segment waits for selection its warps move one block
+//    each; once every segment is selected they only move. A move claims a
+//    32-row destination block of a ready segment (one counter per segment)
+//    and moves it as k_move does: gather the block's moving rows into the
+//    warp's stage, publish "read", wait (bounded) for the lower blocks that
+//    read its destination rows, store. The next block's claim and keep
+//    entries load while the current block's rows load.
 //  * The last CTA to finish sets n_live and resets the call's counters.
-// Every wait is bounded (TRIA_ERR_TIMEOUT after the spin limit); a wait only
-// ever waits for work that an earlier claim started, so the schedule cannot
-// deadlock.
+// The scored / ready lists and the per-segment counters live at a fixed
+// place of the workspace (PassCtl). Every wait is bounded
+// (TRIA_ERR_TIMEOUT after the spin limit), and a wait only ever waits for
+// work that a running warp has started, so the schedule cannot deadlock.
 #pragma once
 
 #include "move.cuh"
@@ -48,12 +44,12 @@ namespace tria {
 
 constexpr int kPassWarps = 12;
 constexpr int kPassThreads = kPassWarps * 32;
-constexpr int kPassPPWMax = 8;               // pieces per warp per score item (at most)
 constexpr int kPassPieceBytes = 8192;
 constexpr int kPassScaleStage = kPassPieceBytes / 16;   // q8_0 block scales of a piece
 constexpr int kPassRing = kPassWarps * 2 * kPassPieceBytes;
 constexpr int kPassMaxSegs = kPassCtlSegs;   // layers x sequences x KV heads per call
 constexpr int kPassMaxLayers = 128;
+constexpr int kPassSmemKeys = kPassRing / 4;  // z-max keys a select keeps in shared memory
 
 // One layer of the call: its cache planes, live rows and statistics.
 struct LayerRef {
@@ -71,22 +67,20 @@ struct FPass {
   int32_t n_layers, n_seqs, n_kv, n_seg, G, hd, fc, window;
   int32_t k_rb, ks_rb, v_rb, vs_rb;
   int32_t spin_limit;
-  int32_t item_rows;    // key rows per score item (kPassWarps x ppw x piece_rows)
   int32_t piece_rows;   // key rows per piece
-  int32_t ppw;          // pieces per warp per score item
-  int32_t cs_max;       // columns of a segment's item-partial table (>= items per segment)
+  int32_t cs_max;       // columns of a segment's run-partial table (>= its score runs)
   int32_t c_max;        // chunks per segment (max)
   int64_t rows_per_layer;   // workspace rows of one layer
   const float2* qe;
   const float* mw;
   const unsigned long long* turns;   // [fc] frac(w_f / 2pi) * 2^64 (shared by the call's layers)
   float* raw;                        // [layer rows][G]
-  uint32_t* keys;                    // [layer rows] z-max keys
+  uint32_t* keys;                    // [layer rows] z-max keys of segments too long for shared memory
   float* score_out;                  // [layer rows] z-max scores, or null
   int32_t* keep;                     // [layer rows]
   Ctrl* ctrl;
-  PassCtl* ctl;                      // ready list and per-segment counters
-  float* parts;                      // [n_seg][kRunCols][cs_max] item moment partials
+  PassCtl* ctl;                      // scored / ready lists and per-segment counters
+  float* parts;                      // [n_seg][kRunCols][cs_max] score-run moment partials
   int32_t* prefix;                   // [n_seg][c_max + 1]
   uint32_t* flags;                   // [n_seg][c_max]
   SeqInfo seq[kMaxSeqs];             // shared by the call's layers (qe_off unused)
@@ -119,14 +113,15 @@ __device__ __forceinline__ PSeg pass_seg(const FPass& P, int sg) {
   return v;
 }
 
-// dynamic shared memory: ring (or move stages) | q8_0 scale ring | mbarriers |
-// item table | turn factors | select histogram
+// dynamic shared memory: ring (score stream; z-max keys of a select; move
+// stages) | q8_0 scale ring | mbarriers | piece table | turn factors | select
+// histogram
 struct PassSmem {
   static constexpr int kRing = 0;
   static constexpr int kScales = kRing + kPassRing;
   static constexpr int kBars = kScales + kPassWarps * 2 * kPassScaleStage;
-  static constexpr int kItem0 = kBars + kPassWarps * 2 * 8;
-  static constexpr int kTurns = kItem0 + ((kPassMaxSegs + 1) * 4 + 15) / 16 * 16;
+  static constexpr int kFirst = kBars + kPassWarps * 2 * 8;
+  static constexpr int kTurns = kFirst + ((kPassMaxSegs + 1) * 4 + 15) / 16 * 16;
   static constexpr int kHist = kTurns + 128 * 8;
   static constexpr int kBytes = kHist + kHistBins * 4;
 };
@@ -151,10 +146,26 @@ __device__ __forceinline__ void load_raw_g(const float* rp, float* x) {
   }
 }
 
-// Selection of one segment by the whole CTA (see the file comment). Writes
-// the keep list (B entries) and the kept-row prefix of every chunk.
-template <int G>
-__device__ __noinline__ void pass_select(const FPass& P, int sg, int n_items, uint32_t* hist) {
+// z-max keys: in shared memory (kSmem) or in the workspace
+template <bool kSmem>
+struct KeyStore {
+  uint32_t* p;
+  __device__ __forceinline__ uint32_t get(int r) const {
+    if constexpr (kSmem) return p[r];
+    else return __ldcg(p + r);
+  }
+  __device__ __forceinline__ void put(int r, uint32_t k) const {
+    if constexpr (kSmem) p[r] = k;
+    else __stcg(p + r, k);
+  }
+};
+
+// Selection of one segment by the whole CTA: segment moments from its nr
+// score-run partials, z-max keys and the first radix histogram in one sweep,
+// up to two more radix passes, then the keep list (B entries) and the
+// kept-row prefix of every chunk; publishes the segment in the ready list.
+template <int G, bool kSmem>
+__device__ __noinline__ void pass_select(const FPass& P, int sg, int nr, uint32_t* smem_keys, uint32_t* hist) {
   __shared__ int s_info[4];
   __shared__ int s_sbuf[40];
   __shared__ int s_wt[kPassWarps], s_wk[kPassWarps];
@@ -162,10 +173,11 @@ __device__ __noinline__ void pass_select(const FPass& P, int sg, int n_items, ui
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n = v.n, lo = v.sink, hi = n - P.window;
   const int k = v.B - v.sink - P.window;
-  uint32_t* keys = P.keys + v.wrow0;
+  const KeyStore<kSmem> keys{kSmem ? smem_keys : P.keys + v.wrow0};
+  constexpr int UB = kSmem ? 1 : 8;   // key loads in flight per thread (global keys)
 
   float mu[G], inv[G];
-  block_moments_of_runs<G>(P.parts + (size_t)sg * kRunCols * P.cs_max, P.cs_max, n_items, mu, inv);
+  block_moments_of_runs<G>(P.parts + (size_t)sg * kRunCols * P.cs_max, P.cs_max, nr, mu, inv);
   for (int i = tid; i < kHistBins; i += blockDim.x) hist[i] = 0u;
   __syncthreads();
 
@@ -190,7 +202,7 @@ __device__ __noinline__ void pass_select(const FPass& P, int sg, int n_items, ui
 #pragma unroll
           for (int h = 1; h < G; ++h) s = fmaxf(s, (x[u][h] - mu[h]) * inv[h]);
           const uint32_t key = score_key(s);
-          __stcg(keys + r, key);
+          keys.put(r, key);
           if (so) so[r] = s;
           if (k > 0 && r >= lo && r < hi) atomicAdd(&hist[key >> 21], 1u);
         }
@@ -214,13 +226,12 @@ __device__ __noinline__ void pass_select(const FPass& P, int sg, int n_items, ui
       if (pass > 0) {
         for (int i = tid; i < NB; i += blockDim.x) hist[i] = 0u;
         __syncthreads();
-        constexpr int UB = 8;   // key loads in flight per thread
         for (int base = lo + tid; base < hi; base += UB * kPassThreads) {
           uint32_t kk[UB];
 #pragma unroll
           for (int u = 0; u < UB; ++u) {
             const int r = base + u * kPassThreads;
-            kk[u] = r < hi ? __ldcg(keys + r) : 0u;
+            kk[u] = r < hi ? keys.get(r) : 0u;
           }
 #pragma unroll
           for (int u = 0; u < UB; ++u) {
@@ -287,7 +298,7 @@ __device__ __noinline__ void pass_select(const FPass& P, int sg, int n_items, ui
   const int nch = (n + kChunk - 1) / kChunk;
   const int cpw = (nch + kPassWarps - 1) / kPassWarps;
   const int c0 = min(nch, warp * cpw), c1 = min(nch, c0 + cpw);
-  constexpr int CB = 8;   // chunks whose keys load together
+  constexpr int CB = kSmem ? 1 : 8;   // chunks whose keys load together (global keys)
   {
     int wt = 0, wk = 0;
     for (int cb = c0; cb < c1; cb += CB) {
@@ -295,7 +306,7 @@ __device__ __noinline__ void pass_select(const FPass& P, int sg, int n_items, ui
 #pragma unroll
       for (int u = 0; u < CB; ++u) {
         const int r = (cb + u) * kChunk + lane;
-        kk[u] = (cb + u < c1 && r < n && r >= lo && r < hi && k > 0) ? __ldcg(keys + r) : 0u;
+        kk[u] = (cb + u < c1 && r < n && r >= lo && r < hi && k > 0) ? keys.get(r) : 0u;
       }
 #pragma unroll
       for (int u = 0; u < CB; ++u) {
@@ -326,7 +337,7 @@ __device__ __noinline__ void pass_select(const FPass& P, int sg, int n_items, ui
 #pragma unroll
     for (int u = 0; u < CB; ++u) {
       const int r = (cb + u) * kChunk + lane;
-      kk[u] = (cb + u < c1 && r < n && r >= lo && r < hi && k > 0) ? __ldcg(keys + r) : 0u;
+      kk[u] = (cb + u < c1 && r < n && r >= lo && r < hi && k > 0) ? keys.get(r) : 0u;
     }
 #pragma unroll
     for (int u = 0; u < CB; ++u) {
@@ -351,135 +362,162 @@ __device__ __noinline__ void pass_select(const FPass& P, int sg, int n_items, ui
     pre[nch] = v.B;
     if (keep_run != v.B) report(P.ctrl, TRIA_ERR_INVALID_ARG, 0x20000000u | (uint32_t)sg);
   }
-  __threadfence();
   __syncthreads();
   if (tid == 0) {
-    P.ctl->items_done[sg] = 0;
+    __threadfence();
     const uint32_t slot = atomicAdd(&P.ctrl->ready_count, 1u);
     st_release_u32(reinterpret_cast<uint32_t*>(P.ctl->ready + slot), (uint32_t)(sg + 1));
   }
+  __syncthreads();
 }
 
-// One warp's share of the moves: claim 32-row destination blocks of ready
-// segments (the next claim is issued while the current block's rows load)
-// and move each as k_move does. Returns when every active segment's blocks
-// are claimed (or a bounded wait gave up).
-static __device__ __noinline__ void pass_moves(const FPass& P, uint8_t* stg, int* msrc, uint32_t tag, int n_active) {
+// A claimed destination block: segment, block index, the lane's keep entry
+// and the keep-index range that reads the block's source rows.
+struct MoveClaim {
+  int state;   // 0 block, 1 none ready yet, 2 every block claimed
+  int sg, j, a, p0, p1;
+};
+
+// lane 0 claims the next block of the oldest ready segment that has one;
+// then every lane loads the block's keep entries (warp-collective)
+__device__ __forceinline__ MoveClaim pass_claim(const FPass& P, int n_active) {
+  const int lane = threadIdx.x & 31;
+  int state = 1, sg = 0, j = 0;
+  if (lane == 0) {
+    while (true) {
+      const uint32_t c = ld_acquire_u32(&P.ctrl->move_cursor);
+      if ((int)c >= n_active) {
+        state = 2;
+        break;
+      }
+      const uint32_t e = ld_acquire_u32(reinterpret_cast<const uint32_t*>(P.ctl->ready + c));
+      if (e == 0u) break;
+      sg = (int)e - 1;
+      if (sg >= P.n_seg) {   // cannot happen: the list holds this call's segments
+        report(P.ctrl, TRIA_ERR_INVALID_ARG, 0x08000000u);
+        state = 2;
+        break;
+      }
+      const int nb = (P.seq[(sg % (P.n_seqs * P.n_kv)) / P.n_kv].budget + kChunk - 1) / kChunk;
+      j = atomicAdd(&P.ctl->move_next[sg], 1);
+      if (j >= 0 && j < nb) {
+        state = 0;
+        break;
+      }
+      atomicCAS(&P.ctrl->move_cursor, c, c + 1u);   // exhausted: move past it
+    }
+  }
+  MoveClaim m;
+  m.state = __shfl_sync(0xffffffffu, state, 0);
+  m.sg = __shfl_sync(0xffffffffu, sg, 0);
+  m.j = __shfl_sync(0xffffffffu, j, 0);
+  m.a = -1;
+  m.p0 = m.p1 = 0;
+  if (m.state == 0) {
+    const int r = m.sg % (P.n_seqs * P.n_kv);
+    const int s = r / P.n_kv;
+    const int B = P.seq[s].budget;
+    const int i = m.j * kChunk + lane;
+    const int64_t wrow0 = (int64_t)(m.sg / (P.n_seqs * P.n_kv)) * P.rows_per_layer + P.seq[s].row0 +
+                          (int64_t)(r - s * P.n_kv) * P.seq[s].cap;
+    m.a = i < B ? __ldcg(P.keep + wrow0 + i) : -1;
+    const int* pre = P.prefix + (size_t)m.sg * (P.c_max + 1);
+    m.p0 = __ldcg(&pre[m.j]);
+    m.p1 = __ldcg(&pre[m.j + 1]);
+  }
+  return m;
+}
+
+// Moves the claimed block m (k_move's steps); when `next` is given, the next
+// block is claimed while this block's rows load.
+__device__ __forceinline__ void pass_move_block(const FPass& P, const MoveClaim& m, uint8_t* stg, int* msrc,
+                                                uint32_t tag, int n_active, MoveClaim* next) {
   const int lane = threadIdx.x & 31;
   const MoveStage L = move_stage_layout(P.k_rb, P.ks_rb, P.v_rb, P.vs_rb);
   const PlaneMap mk = plane_map(P.k_rb, lane), mks = plane_map(P.ks_rb, lane), mv = plane_map(P.v_rb, lane),
                  mvs = plane_map(P.vs_rb, lane);
-  // lane 0: 0 = block (sg, j), 1 = none ready yet, 2 = every block claimed
-  auto claim = [&](int& sg, int& j) {
-    int state = 1;
-    sg = 0;
-    j = 0;
-    if (lane == 0) {
-      while (true) {
-        const uint32_t c = ld_acquire_u32(&P.ctrl->move_cursor);
-        if ((int)c >= n_active) {
-          state = 2;
+  const PSeg v = pass_seg(P, m.sg);
+  const LayerRef& lr = P.lay[v.li];
+  const int B = v.B, n = v.n, j = m.j;
+  const int i0 = j * kChunk, cnt = min(kChunk, B - i0);
+  const bool bad_entry = lane < cnt && (m.a < i0 + lane || m.a >= n);
+  const bool ok =
+      !__any_sync(0xffffffffu, bad_entry) && m.p0 >= 0 && m.p0 <= m.p1 && m.p1 - m.p0 <= kChunk && m.p1 <= B;
+  if (!ok && lane == 0) report(P.ctrl, TRIA_ERR_INVALID_ARG, 0x10000000u | (uint32_t)m.sg);
+  // moving entries (keep[i] != i) are a suffix of the block
+  const unsigned mvm = __ballot_sync(0xffffffffu, ok && lane < cnt && m.a != i0 + lane);
+  const int first = mvm ? __ffs(mvm) - 1 : cnt;
+  const int nmove = ok ? cnt - first : 0;
+  if (lane == 0) bulk_wait_read_all();   // the previous block's stores have read the stage
+  __syncwarp();
+  if (lane >= first && lane < cnt) msrc[lane - first] = m.a;
+  __syncwarp();
+  int my_pos = 0;
+  if (nmove > 0) {
+    warp_gather(lr.k, v.row0, mk, stg + L.k, msrc, nmove);
+    warp_gather(lr.ks, v.row0, mks, stg + L.ks, msrc, nmove);
+    warp_gather(lr.v, v.row0, mv, stg + L.v, msrc, nmove);
+    warp_gather(lr.vs, v.row0, mvs, stg + L.vs, msrc, nmove);
+    if (lane < nmove) my_pos = __ldcg(lr.pos + v.row0 + msrc[lane]);
+  }
+  cp_async_commit();
+  if (next) *next = pass_claim(P, n_active);   // travels while the rows load
+  cp_async_wait<0>();
+  __syncwarp();
+  if (lane < nmove) msrc[lane] = my_pos;
+  __syncwarp();
+  // publish "read"; then wait for the lower blocks that read my destination rows
+  uint32_t* flags = P.flags + (size_t)m.sg * P.c_max;
+  int go = 0;
+  if (lane == 0) {
+    st_relaxed_u32(&flags[j], tag);
+    go = ok;
+    if (go && nmove > 0 && m.p1 > m.p0) {
+      const int lo_b = m.p0 / kChunk, hi_b = min((m.p1 - 1) / kChunk, j - 1);
+      for (int cc = lo_b; cc <= hi_b; ++cc)
+        if (!wait_flag_bounded(&flags[cc], tag, P.spin_limit)) {
+          go = 0;
+          report(P.ctrl, TRIA_ERR_TIMEOUT, (uint32_t)m.sg);
           break;
         }
-        const uint32_t e = ld_acquire_u32(reinterpret_cast<const uint32_t*>(P.ctl->ready + c));
-        if (e == 0u) break;
-        sg = (int)e - 1;
-        if (sg >= P.n_seg) {   // cannot happen: the list holds this call's segments
-          report(P.ctrl, TRIA_ERR_INVALID_ARG, 0x08000000u);
-          state = 2;
-          break;
-        }
-        const int nb = (P.seq[(sg % (P.n_seqs * P.n_kv)) / P.n_kv].budget + kChunk - 1) / kChunk;
-        j = atomicAdd(&P.ctl->move_next[sg], 1);
-        if (j >= 0 && j < nb) {
-          state = 0;
-          break;
-        }
-        atomicCAS(&P.ctrl->move_cursor, c, c + 1u);   // exhausted: move past it
-      }
     }
-    return state;
-  };
-  int nsg, nj;
-  int nstate = claim(nsg, nj);
+  }
+  go = __shfl_sync(0xffffffffu, go, 0);
+  if (go && nmove > 0) {
+    const int dst0 = i0 + first;
+    if (lane == 0) {
+      fence_proxy_async_smem();
+      bulk_s2g(lr.k + (size_t)(v.row0 + dst0) * P.k_rb, stg + L.k, (uint32_t)(nmove * P.k_rb));
+      bulk_s2g(lr.v + (size_t)(v.row0 + dst0) * P.v_rb, stg + L.v, (uint32_t)(nmove * P.v_rb));
+      bulk_commit();
+    }
+    warp_scatter(lr.ks, v.row0, P.ks_rb, stg + L.ks, dst0, nmove, lane);
+    warp_scatter(lr.vs, v.row0, P.vs_rb, stg + L.vs, dst0, nmove, lane);
+    if (lane < nmove) lr.pos[v.row0 + dst0 + lane] = msrc[lane];
+  }
+  __syncwarp();
+}
+
+// One warp's moves once every segment is selected: claim, move, repeat, the
+// next claim travelling with the current block's loads.
+static __device__ __noinline__ void pass_moves(const FPass& P, uint8_t* stg, int* msrc, uint32_t tag, int n_active) {
+  const int lane = threadIdx.x & 31;
+  MoveClaim m = pass_claim(P, n_active);
   int idle = 0;
-  while (true) {
-    const int state = __shfl_sync(0xffffffffu, nstate, 0);
-    if (state == 2) break;
-    if (state == 1) {
+  while (m.state != 2) {
+    if (m.state == 1) {
       if (++idle > P.spin_limit) {
         if (lane == 0) report(P.ctrl, TRIA_ERR_TIMEOUT, 0xA0000000u);
         break;
       }
       __nanosleep(idle < 64 ? 64 : 512);
-      nstate = claim(nsg, nj);
+      m = pass_claim(P, n_active);
       continue;
     }
     idle = 0;
-    const int sg = __shfl_sync(0xffffffffu, nsg, 0);
-    const int j = __shfl_sync(0xffffffffu, nj, 0);
-    const PSeg v = pass_seg(P, sg);
-    const LayerRef& lr = P.lay[v.li];
-    const int B = v.B, n = v.n;
-    const int i0 = j * kChunk, cnt = min(kChunk, B - i0);
-    const int a = lane < cnt ? __ldcg(P.keep + v.wrow0 + i0 + lane) : -1;
-    const int* pre = P.prefix + (size_t)sg * (P.c_max + 1);
-    const int p0 = __ldcg(&pre[j]), p1 = __ldcg(&pre[j + 1]);
-    const bool bad_entry = lane < cnt && (a < i0 + lane || a >= n);
-    const bool ok = !__any_sync(0xffffffffu, bad_entry) && p0 >= 0 && p0 <= p1 && p1 - p0 <= kChunk && p1 <= B;
-    if (!ok && lane == 0) report(P.ctrl, TRIA_ERR_INVALID_ARG, 0x10000000u | (uint32_t)sg);
-    // moving entries (keep[i] != i) are a suffix of the block
-    const unsigned mvm = __ballot_sync(0xffffffffu, ok && lane < cnt && a != i0 + lane);
-    const int first = mvm ? __ffs(mvm) - 1 : cnt;
-    const int nmove = ok ? cnt - first : 0;
-    if (lane == 0) bulk_wait_read_all();   // the previous block's stores have read the stage
-    __syncwarp();
-    if (lane >= first && lane < cnt) msrc[lane - first] = a;
-    __syncwarp();
-    int my_pos = 0;
-    if (nmove > 0) {
-      warp_gather(lr.k, v.row0, mk, stg + L.k, msrc, nmove);
-      warp_gather(lr.ks, v.row0, mks, stg + L.ks, msrc, nmove);
-      warp_gather(lr.v, v.row0, mv, stg + L.v, msrc, nmove);
-      warp_gather(lr.vs, v.row0, mvs, stg + L.vs, msrc, nmove);
-      if (lane < nmove) my_pos = __ldcg(lr.pos + v.row0 + msrc[lane]);
-    }
-    cp_async_commit();
-    nstate = claim(nsg, nj);   // the next block's claim travels while the rows load
-    cp_async_wait<0>();
-    __syncwarp();
-    if (lane < nmove) msrc[lane] = my_pos;
-    __syncwarp();
-    // publish "read"; then wait for the lower blocks that read my destination rows
-    uint32_t* flags = P.flags + (size_t)sg * P.c_max;
-    int go = 0;
-    if (lane == 0) {
-      st_relaxed_u32(&flags[j], tag);
-      go = ok;
-      if (go && nmove > 0 && p1 > p0) {
-        const int lo_b = p0 / kChunk, hi_b = min((p1 - 1) / kChunk, j - 1);
-        for (int cc = lo_b; cc <= hi_b; ++cc)
-          if (!wait_flag_bounded(&flags[cc], tag, P.spin_limit)) {
-            go = 0;
-            report(P.ctrl, TRIA_ERR_TIMEOUT, (uint32_t)sg);
-            break;
-          }
-      }
-    }
-    go = __shfl_sync(0xffffffffu, go, 0);
-    if (go && nmove > 0) {
-      const int dst0 = i0 + first;
-      if (lane == 0) {
-        fence_proxy_async_smem();
-        bulk_s2g(lr.k + (size_t)(v.row0 + dst0) * P.k_rb, stg + L.k, (uint32_t)(nmove * P.k_rb));
-        bulk_s2g(lr.v + (size_t)(v.row0 + dst0) * P.v_rb, stg + L.v, (uint32_t)(nmove * P.v_rb));
-        bulk_commit();
-      }
-      warp_scatter(lr.ks, v.row0, P.ks_rb, stg + L.ks, dst0, nmove, lane);
-      warp_scatter(lr.vs, v.row0, P.vs_rb, stg + L.vs, dst0, nmove, lane);
-      if (lane < nmove) lr.pos[v.row0 + dst0 + lane] = msrc[lane];
-    }
-    __syncwarp();
+    MoveClaim nx;
+    pass_move_block(P, m, stg, msrc, tag, n_active, &nx);
+    m = nx;
   }
   if (lane == 0) bulk_wait_all();
 }
@@ -493,10 +531,8 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
   static_assert(FC <= 128, "turn table");
 
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ int s_item[2];      // current and next score item (-1: none)
-  __shared__ int s_total, s_active, s_last;
+  __shared__ int s_active, s_sel, s_last;
   __shared__ uint32_t s_epoch;
-  __shared__ Mom s_mom[kPassWarps][kMaxG];
   __shared__ int s_src[kPassWarps][kChunk];
   __shared__ int s_sbuf[40];
 
@@ -504,13 +540,17 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
   uint8_t* ring = smem + PassSmem::kRing + (size_t)warp * 2 * kPassPieceBytes;
   uint8_t* sc_ring = smem + PassSmem::kScales + (size_t)warp * 2 * kPassScaleStage;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + PassSmem::kBars) + warp * 2;
-  int* item0 = reinterpret_cast<int*>(smem + PassSmem::kItem0);
+  int* seg_first = reinterpret_cast<int*>(smem + PassSmem::kFirst);   // first piece of every segment
   unsigned long long* s_turns = reinterpret_cast<unsigned long long*>(smem + PassSmem::kTurns);
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem + PassSmem::kHist);
 
-  // ---- prologue: item table (first score item of every segment), active
-  // segments, turn factors, ring barriers
+  // ---- prologue: piece table (pieces of the active segments, in segment
+  // order), active segments, turn factors, ring barriers
   if (tid < FC) s_turns[tid] = __ldg(P.turns + tid);
+  if (tid == 0) {
+    s_active = 0;
+    s_epoch = ld_acquire_u32(&P.ctrl->epoch);
+  }
   {
     constexpr int kPer = (kPassMaxSegs + kPassThreads - 1) / kPassThreads;
     const int sb = min(P.n_seg, tid * kPer), se = min(P.n_seg, sb + kPer);
@@ -525,7 +565,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
         if (!v.valid) {
           if (blockIdx.x == 0 && v.g == 0) report(P.ctrl, TRIA_ERR_DEVICE_ARG, (uint32_t)(v.li * P.n_seqs + v.s));
         } else if (v.active) {
-          cnt[i] = (v.n + P.item_rows - 1) / P.item_rows;
+          cnt[i] = (v.n + P.piece_rows - 1) / P.piece_rows;
           ++act;
         }
         local += cnt[i];
@@ -537,16 +577,11 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
     for (int i = 0; i < kPer; ++i) {
       const int sg = sb + i;
       if (sg < se) {
-        item0[sg] = before;
+        seg_first[sg] = before;
         before += cnt[i];
       }
     }
-    if (tid == 0) {
-      item0[P.n_seg] = tot;
-      s_total = tot;
-      s_active = 0;
-    }
-    __syncthreads();
+    if (tid == 0) seg_first[P.n_seg] = tot;
     if (act) atomicAdd(&s_active, act);
   }
   if (lane == 0) {
@@ -555,208 +590,180 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
     fence_mbar_init();
   }
   __syncthreads();
-  const int total = s_total, n_active = s_active;
-  if (tid == 0) {
-    s_epoch = ld_acquire_u32(&P.ctrl->epoch);
-    int a = -1, b = -1;
-    if (total > 0) {
-      a = (int)atomicAdd(&P.ctrl->score_next, 1u);
-      if (a >= total) a = -1;
-      if (a >= 0) {
-        b = (int)atomicAdd(&P.ctrl->score_next, 1u);
-        if (b >= total) b = -1;
-      }
-    }
-    s_item[0] = a;
-    s_item[1] = b;
-  }
-  __syncthreads();
+  const int total = seg_first[P.n_seg], n_active = s_active;
+  const int nwarps = gridDim.x * kPassWarps;
+  const int per = (total + nwarps - 1) / nwarps;   // pieces per warp run
 
-  auto seg_of_item = [&](int it) {   // largest sg with item0[sg] <= it
-    int lo = 0, hi = P.n_seg - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (item0[mid] <= it) lo = mid;
-      else hi = mid - 1;
-    }
-    return lo;
-  };
-
-  // ---- score items
-  Body body;
-  body.init(lane);
-  int body_seg = -1;
-  int n_issued = 0, n_done = 0;   // pieces of this warp through its ring
-  int carried = 0;                // pieces of the current item issued during the previous one
-  bool failed = false;
-  // thread 0: the claim of the item after next (in flight during the current
-  // item) and the completion count of the previous item, checked one item
-  // later so that neither round trip sits between two items
-  int pend_sg = -1, pend_items = 0, pend_old = 0;
-
-  // item `it` as seen by this warp: its segment, the segment's geometry (live
-  // rows are read only for a segment's last item: the others are full), and
-  // this warp's pieces in it
-  struct ItemView {
-    int it, sg, n_pieces, rows_end;   // rows_end: first row past the item
-  };
-  auto view_of = [&](int it) {
-    ItemView iv;
-    iv.it = it;
-    iv.sg = 0;
-    iv.n_pieces = 0;
-    iv.rows_end = 0;
-    if (it < 0) return iv;
-    iv.sg = seg_of_item(it);
-    const int j = it - item0[iv.sg];
-    if (it == item0[iv.sg + 1] - 1) {   // a segment's last item ends at its live rows
-      const int li = iv.sg / (P.n_seqs * P.n_kv);
-      const int s = (iv.sg - li * P.n_seqs * P.n_kv) / P.n_kv;
-      iv.rows_end = *((volatile const int32_t*)(P.lay[li].n_live + s));
-    } else {
-      iv.rows_end = (j + 1) * P.item_rows;
-    }
-    const int r_beg = j * P.item_rows + warp * P.ppw * P.piece_rows;
-    const int left = iv.rows_end - r_beg;
-    iv.n_pieces = left <= 0 ? 0 : min(P.ppw, (left + P.piece_rows - 1) / P.piece_rows);
-    return iv;
-  };
-  // first row of segment sg in its layer's planes
-  auto seg_row0 = [&](int sg) {
-    const int r = sg % (P.n_seqs * P.n_kv);
-    const int s = r / P.n_kv;
-    return P.seq[s].row0 + (int64_t)(r - s * P.n_kv) * P.seq[s].cap;
-  };
-  // rows [r0, r0 + rows) of piece i of this warp in item iv
-  auto piece_r0 = [&](const ItemView& iv, int i) {
-    return (iv.it - item0[iv.sg]) * P.item_rows + (warp * P.ppw + i) * P.piece_rows;
-  };
-  auto issue = [&](const ItemView& iv, int i) {   // warp-collective
-    const int st = n_issued & 1;
-    const int r0 = piece_r0(iv, i);
-    const int rows = min(P.piece_rows, iv.rows_end - r0);
-    const int64_t grow = seg_row0(iv.sg) + r0;
-    const int li = iv.sg / (P.n_seqs * P.n_kv);
-    if (lane == 0) {
-      const uint32_t bytes = (uint32_t)(rows * P.k_rb);
-      mbar_arrive_expect_tx(&bars[st], bytes);
-      bulk_g2s(ring + st * kPassPieceBytes, P.lay[li].k + (size_t)grow * P.k_rb, bytes, &bars[st]);
-    }
-    if constexpr (kQ8) {
-      const uint8_t* src = P.lay[li].ks + (size_t)grow * P.ks_rb;
-      uint8_t* dst = sc_ring + st * kPassScaleStage;
-      for (int u = lane; u < rows * P.ks_rb / 4; u += 32) cp_async4(dst + 4 * u, src + 4 * u);
-      cp_async_commit();
-    }
-    ++n_issued;
-  };
-
-  ItemView nv = view_of(s_item[1]);
-  while (s_item[0] >= 0) {
-    const int cur = s_item[0], nxt = s_item[1];
-    const ItemView cv = nv.it == cur ? nv : view_of(cur);
-    nv = failed ? view_of(-1) : view_of(nxt);
-    int claim = -1;
-    if (tid == 0 && nxt >= 0) claim = (int)atomicAdd(&P.ctrl->score_next, 1u);   // used after this item
-    const int nc = cv.n_pieces, nn = nv.n_pieces;
-    if (cv.sg != body_seg) {
-      const int li = cv.sg / (P.n_seqs * P.n_kv);
-      const int r = cv.sg - li * P.n_seqs * P.n_kv;
-      const int s = r / P.n_kv;
-      const size_t qo = P.lay[li].qe_off + (size_t)(r - s * P.n_kv) * G * FC;
-      body.load_consts(P.qe + qo, P.mw + qo, s_turns, (unsigned long long)P.seq[s].cur_pos);
-      body_seg = cv.sg;
-    }
-    int iss = carried;   // pieces of [current item..., next item...] issued so far
-    auto issue_seq = [&](int idx) {
-      if (idx < nc) issue(cv, idx);
-      else issue(nv, idx - nc);
+  // ---- scoring: this warp's run of pieces [p_beg, p_end)
+  {
+    const int gw = blockIdx.x * kPassWarps + warp;
+    const int p_beg = min(total, gw * per), p_end = min(total, p_beg + per);
+    auto seg_of = [&](int p, int from) {
+      int sg = from;
+      while (seg_first[sg + 1] <= p) ++sg;
+      return sg;
     };
-    for (int i = 0; i < nc && !failed; ++i) {
-      while (iss <= i) issue_seq(iss++);
-      if (iss == i + 1 && (i + 1 < nc || i + 1 - nc < nn)) issue_seq(iss++);   // one ahead, possibly the next item's
-      const int st = n_done & 1;
-      if (!mbar_wait_bounded(&bars[st], (uint32_t)((n_done >> 1) & 1), P.spin_limit)) {
-        if (lane == 0) report(P.ctrl, TRIA_ERR_TIMEOUT, (uint32_t)cv.sg);
-        // wait again (bounded) for every copy still in flight, then stop scoring
-        for (int d = n_done; d < n_issued; ++d) mbar_wait_bounded(&bars[d & 1], (uint32_t)((d >> 1) & 1), P.spin_limit);
-        if constexpr (kQ8) cp_async_wait<0>();
-        n_done = n_issued;
-        failed = true;
-        break;
+    // bulk copy of piece p of segment sg (v: the segment, its live rows)
+    auto issue = [&](int p, int sg, const PSeg& v, int stage_i) {   // warp-collective
+      const int r = (p - seg_first[sg]) * P.piece_rows;
+      const int rows = min(P.piece_rows, v.n - r);
+      const int64_t grow = v.row0 + r;
+      if (lane == 0) {
+        const uint32_t bytes = (uint32_t)(rows * P.k_rb);
+        mbar_arrive_expect_tx(&bars[stage_i], bytes);
+        bulk_g2s(ring + stage_i * kPassPieceBytes, P.lay[v.li].k + (size_t)grow * P.k_rb, bytes, &bars[stage_i]);
       }
       if constexpr (kQ8) {
-        if (n_issued - n_done >= 2) cp_async_wait<1>();
-        else cp_async_wait<0>();
-        __syncwarp();
+        const uint8_t* src = P.lay[v.li].ks + (size_t)grow * P.ks_rb;
+        uint8_t* dst = sc_ring + stage_i * kPassScaleStage;
+        for (int u = lane; u < rows * P.ks_rb / 4; u += 32) cp_async4(dst + 4 * u, src + 4 * u);
+        cp_async_commit();
       }
-      const int r0 = piece_r0(cv, i);
-      const int64_t wrow = (int64_t)(cv.sg / (P.n_seqs * P.n_kv)) * P.rows_per_layer + seg_row0(cv.sg) + r0;
-      body.piece(ring + st * kPassPieceBytes, sc_ring + st * kPassScaleStage, min(P.piece_rows, cv.rows_end - r0),
-                 P.k_rb, P.ks_rb, P.raw + (size_t)wrow * G);
-      __syncwarp();
-      ++n_done;
-    }
-    if (nc == 0 && !failed)
-      while (iss < min(2, nn)) issue_seq(iss++);   // an idle warp starts the next item's pieces
-    carried = failed ? 0 : iss - nc;
-
-    // the item's moments: per warp, then merged over the warps in order
-    {
-      Mom m[kHeads];
-      body.flush(m);
-      if (body.flush_writer()) {
+    };
+    if (p_beg < p_end) {
+      Body body;
+      body.init(lane);
+      int seg = seg_of(p_beg, 0);
+      PSeg sv = pass_seg(P, seg);
+      issue(p_beg, seg, sv, 0);
+      auto load_consts = [&]() {
+        const size_t qo = P.lay[sv.li].qe_off + (size_t)sv.g * G * FC;
+        body.load_consts(P.qe + qo, P.mw + qo, s_turns, (unsigned long long)P.seq[sv.s].cur_pos);
+      };
+      load_consts();
+      int run_first = p_beg;
+      // the run's moment partial, then its pieces into the segment's scored
+      // count; the warp that completes the segment lists it as scored
+      auto finish_run = [&](int p_stop) {
+        Mom m[kHeads];
+        body.flush(m);
+        if (body.flush_writer()) {
+          float* tab = P.parts + (size_t)seg * kRunCols * P.cs_max;
+          const int r = run_index(run_first, seg_first[seg], per);
 #pragma unroll
-        for (int kk = 0; kk < kHeads; ++kk) s_mom[warp][body.oh + kk] = m[kk];
+          for (int kk = 0; kk < kHeads; ++kk) {
+            tab[(1 + body.oh + kk) * P.cs_max + r] = m[kk].mean;
+            tab[(1 + kMaxG + body.oh + kk) * P.cs_max + r] = m[kk].m2;
+          }
+          if (body.q == 0) tab[r] = m[0].n;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence();
+          const int np = p_stop - run_first;
+          const int want = seg_first[seg + 1] - seg_first[seg];
+          if (atomicAdd(&P.ctl->pieces_done[seg], np) + np == want) {
+            __threadfence();
+            const uint32_t slot = atomicAdd(&P.ctrl->scored_count, 1u);
+            st_release_u32(reinterpret_cast<uint32_t*>(P.ctl->scored + slot), (uint32_t)(seg + 1));
+          }
+        }
+      };
+      for (int p = p_beg; p < p_end; ++p) {
+        const int kp = p - p_beg;
+        const int st = kp & 1;
+        // next piece into the other stage (its previous contents were consumed)
+        if (p + 1 < p_end) {
+          const int sn = seg_of(p + 1, seg);
+          if (sn == seg) issue(p + 1, sn, sv, st ^ 1);
+          else issue(p + 1, sn, pass_seg(P, sn), st ^ 1);   // the next segment's first piece
+        } else if constexpr (kQ8) {
+          cp_async_commit();   // keep one group per piece
+        }
+        if (seg_first[seg + 1] <= p) {
+          finish_run(p);
+          seg = seg_of(p, seg);
+          sv = pass_seg(P, seg);
+          load_consts();
+          run_first = p;
+        }
+        const int r0 = (p - seg_first[seg]) * P.piece_rows;
+        const int rows = min(P.piece_rows, sv.n - r0);
+        if (!mbar_wait_bounded(&bars[st], (uint32_t)((kp >> 1) & 1), P.spin_limit)) {
+          if (lane == 0) report(P.ctrl, TRIA_ERR_TIMEOUT, (uint32_t)seg);
+          // wait again (bounded) for the copies still in flight before leaving
+          mbar_wait_bounded(&bars[st], (uint32_t)((kp >> 1) & 1), P.spin_limit);
+          if (p + 1 < p_end) mbar_wait_bounded(&bars[st ^ 1], (uint32_t)(((kp + 1) >> 1) & 1), P.spin_limit);
+          if constexpr (kQ8) cp_async_wait<0>();
+          break;
+        }
+        if constexpr (kQ8) {
+          cp_async_wait<1>();   // this piece's scales (the next piece's may still be in flight)
+          __syncwarp();
+        }
+        body.piece(ring + st * kPassPieceBytes, sc_ring + st * kPassScaleStage, rows, P.k_rb, P.ks_rb,
+                   P.raw + (size_t)(sv.wrow0 + r0) * G);
+        __syncwarp();
+        if (p + 1 == p_end) finish_run(p_end);
       }
-    }
-    __syncthreads();
-    if (tid < G) {
-      Mom a{0.f, 0.f, 0.f};
-      for (int w = 0; w < kPassWarps; ++w) a = mom_merge(a, s_mom[w][tid]);
-      float* tab = P.parts + (size_t)cv.sg * kRunCols * P.cs_max;
-      const int j = cur - item0[cv.sg];
-      tab[(1 + tid) * P.cs_max + j] = a.mean;
-      tab[(1 + kMaxG + tid) * P.cs_max + j] = a.m2;
-      if (tid == 0) tab[j] = a.n;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      // the previous item's completion count has arrived by now
-      s_last = (pend_sg >= 0 && pend_old == pend_items - 1) ? pend_sg : -1;
-      // this item's raw scores and moments (every thread's, ordered by the
-      // barrier) before its completion count
-      __threadfence();
-      pend_sg = cv.sg;
-      pend_items = item0[cv.sg + 1] - item0[cv.sg];
-      pend_old = atomicAdd(&P.ctl->items_done[cv.sg], 1);
-      s_item[0] = nxt;
-      s_item[1] = claim < total ? claim : -1;
-    }
-    __syncthreads();
-    // selections due: the segment the previous item completed (s_last), and
-    // once no item is left, the one the last item completed
-    while (true) {
-      if (s_last >= 0) {
-        __threadfence();
-        pass_select<G>(P, s_last, item0[s_last + 1] - item0[s_last], hist);
-      }
-      if (s_item[0] >= 0) break;
-      __syncthreads();
-      if (tid == 0) {
-        s_last = (pend_sg >= 0 && pend_old == pend_items - 1) ? pend_sg : -1;
-        pend_sg = -1;
-      }
-      __syncthreads();
-      if (s_last < 0) break;
     }
   }
+  __syncthreads();   // the ring is free from here on
 
-  // ---- moves: warps claim destination blocks of ready segments
-  {
-    const MoveStage L = move_stage_layout(P.k_rb, P.ks_rb, P.v_rb, P.vs_rb);
-    if (warp < min(kPassWarps, kPassRing / L.bytes) && n_active > 0)
-      pass_moves(P, smem + PassSmem::kRing + (size_t)warp * L.bytes, s_src[warp], flag_tag(s_epoch), n_active);
+  // ---- service: select scored segments; while none is waiting, move
+  const MoveStage L = move_stage_layout(P.k_rb, P.ks_rb, P.v_rb, P.vs_rb);
+  const bool mover = warp < min(kPassWarps, kPassRing / L.bytes);
+  uint8_t* stg = smem + PassSmem::kRing + (size_t)warp * L.bytes;
+  const uint32_t tag = flag_tag(s_epoch);
+  if (n_active > 0) {
+    int idle = 0;
+    while (true) {
+      if (tid == 0) {
+        // -2: every segment is selected or being selected; -1: none waits now
+        int sel = -1;
+        while (true) {
+          const uint32_t h = ld_acquire_u32(&P.ctrl->sel_next);
+          if ((int)h >= n_active) {
+            sel = -2;
+            break;
+          }
+          if (h >= ld_acquire_u32(&P.ctrl->scored_count)) break;
+          if (atomicCAS(&P.ctrl->sel_next, h, h + 1u) == h) {
+            // the slot is written right after its count was taken (bounded wait)
+            const uint32_t* q = reinterpret_cast<const uint32_t*>(P.ctl->scored + h);
+            uint32_t e = 0;
+            for (int it = 0; it < P.spin_limit && (e = ld_acquire_u32(q)) == 0u; ++it) __nanosleep(32);
+            if (e == 0u) report(P.ctrl, TRIA_ERR_TIMEOUT, 0xC0000000u);
+            sel = e == 0u ? -1 : (int)e - 1;
+            break;
+          }
+        }
+        s_sel = sel;
+      }
+      __syncthreads();
+      const int sel = s_sel;
+      if (sel >= 0) {
+        idle = 0;
+        __threadfence();
+        const int nr = segment_runs(seg_first[sel], seg_first[sel + 1], per);
+        if (pass_seg(P, sel).n <= kPassSmemKeys)
+          pass_select<G, true>(P, sel, nr, reinterpret_cast<uint32_t*>(smem + PassSmem::kRing), hist);
+        else
+          pass_select<G, false>(P, sel, nr, nullptr, hist);
+        continue;
+      }
+      if (sel == -2) break;
+      // no segment waits for selection: each warp moves at most one block
+      int moved = 0;
+      if (mover) {
+        const MoveClaim m = pass_claim(P, n_active);
+        if (m.state == 0) {
+          pass_move_block(P, m, stg, s_src[warp], tag, n_active, nullptr);
+          moved = 1;
+        }
+        if (lane == 0) bulk_wait_read_all();   // the stage may hold keys next
+      }
+      if (__syncthreads_or(moved)) {
+        idle = 0;
+      } else {
+        if (++idle > P.spin_limit) {
+          if (tid == 0) report(P.ctrl, TRIA_ERR_TIMEOUT, 0xB0000001u);
+          break;
+        }
+        __nanosleep(idle < 64 ? 64 : 512);
+      }
+    }
+    if (mover) pass_moves(P, stg, s_src[warp], tag, n_active);
   }
 
   // ---- the last CTA: n_live of the active sequences, counters reset
@@ -774,15 +781,16 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
     const int n = *((volatile int32_t*)nl);
     if (n >= 0 && n <= P.seq[s].cap && n > P.seq[s].budget) *nl = P.seq[s].budget;
   }
-  const int n_ready = (int)ld_acquire_u32(&P.ctrl->ready_count);
-  for (int i = tid; i < min(n_ready, P.n_seg); i += blockDim.x) P.ctl->ready[i] = 0;
   for (int sg = tid; sg < P.n_seg; sg += blockDim.x) {
-    P.ctl->items_done[sg] = 0;
+    P.ctl->ready[sg] = 0;
+    P.ctl->scored[sg] = 0;
+    P.ctl->pieces_done[sg] = 0;
     P.ctl->move_next[sg] = 0;
   }
   __syncthreads();
   if (tid == 0) {
-    P.ctrl->score_next = 0u;
+    P.ctrl->scored_count = 0u;
+    P.ctrl->sel_next = 0u;
     P.ctrl->ready_count = 0u;
     P.ctrl->move_cursor = 0u;
     P.ctrl->pass_done = 0u;

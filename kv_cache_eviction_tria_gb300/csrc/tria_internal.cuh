@@ -44,11 +44,12 @@ struct Ctrl {
   uint32_t bar_gen;      // grid barrier: generation, bumped when all arrived
   uint32_t append_ticket;  // append CTAs that finished (reset by the last one)
   // fused pass (k_pass): reset by its last CTA
-  uint32_t score_next;   // next score item to claim
+  uint32_t scored_count; // segments completely scored (slots of the scored list)
+  uint32_t sel_next;     // next scored segment to select
   uint32_t ready_count;  // segments whose selection is published (slots of the ready list)
   uint32_t move_cursor;  // first ready slot that may still have unclaimed move blocks
   uint32_t pass_done;    // CTAs of the pass that finished
-  uint32_t pad[50];
+  uint32_t pad[49];
 };
 static_assert(sizeof(Ctrl) == 256, "Ctrl layout");
 
@@ -184,9 +185,10 @@ __host__ __device__ __forceinline__ uint32_t flag_tag(uint32_t epoch) {
 // call, the ready list, the completed score items and the next move block.
 constexpr int kPassCtlSegs = 2048;
 struct PassCtl {
-  int32_t ready[kPassCtlSegs];        // segment + 1 in publication order (0: not yet)
-  int32_t items_done[kPassCtlSegs];
-  int32_t move_next[kPassCtlSegs];
+  int32_t ready[kPassCtlSegs];        // selected segments + 1 in publication order (0: not yet)
+  int32_t scored[kPassCtlSegs];       // segments + 1 whose last pieces are scored, in that order
+  int32_t pieces_done[kPassCtlSegs];  // scored pieces per segment
+  int32_t move_next[kPassCtlSegs];    // next destination block to claim per segment
 };
 
 __device__ __forceinline__ bool is_protected(int r, int n, int sink, int window) {
