@@ -711,21 +711,22 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
       if (tid == 0) {
         // -2: every segment is selected or being selected; -1: none waits now
         int sel = -1;
-        while (true) {
-          const uint32_t h = ld_acquire_u32(&P.ctrl->sel_next);
-          if ((int)h >= n_active) {
+        const uint32_t h = ld_acquire_u32(&P.ctrl->sel_next);
+        if ((int)h >= n_active) {
+          sel = -2;
+        } else if (h < ld_acquire_u32(&P.ctrl->scored_count)) {
+          // a ticket in the scored list; taken past the scored count only in
+          // a race with other CTAs, when its segment is being scored now
+          // (bounded wait for the slot)
+          const uint32_t t = atomicAdd(&P.ctrl->sel_next, 1u);
+          if ((int)t >= n_active) {
             sel = -2;
-            break;
-          }
-          if (h >= ld_acquire_u32(&P.ctrl->scored_count)) break;
-          if (atomicCAS(&P.ctrl->sel_next, h, h + 1u) == h) {
-            // the slot is written right after its count was taken (bounded wait)
-            const uint32_t* q = reinterpret_cast<const uint32_t*>(P.ctl->scored + h);
+          } else {
+            const uint32_t* q = reinterpret_cast<const uint32_t*>(P.ctl->scored + t);
             uint32_t e = 0;
-            for (int it = 0; it < P.spin_limit && (e = ld_acquire_u32(q)) == 0u; ++it) __nanosleep(32);
+            for (int it = 0; it < P.spin_limit && (e = ld_acquire_u32(q)) == 0u; ++it) __nanosleep(64);
             if (e == 0u) report(P.ctrl, TRIA_ERR_TIMEOUT, 0xC0000000u);
             sel = e == 0u ? -1 : (int)e - 1;
-            break;
           }
         }
         s_sel = sel;
