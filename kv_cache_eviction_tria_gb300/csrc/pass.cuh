@@ -371,20 +371,34 @@ __device__ __noinline__ void pass_select(const FPass& P, int sg, int nr, uint32_
   __syncthreads();
 }
 
-// A claimed destination block: segment, block index, the lane's keep entry
-// and the keep-index range that reads the block's source rows.
+// A claimed destination block: segment, block index, the lane's keep entry,
+// the keep-index range that reads the block's source rows, and the
+// segment's geometry.
 struct MoveClaim {
   int state;   // 0 block, 1 none ready yet, 2 every block claimed
   int sg, j, a, p0, p1;
+  int n, B, li;
+  int64_t row0, wrow0;
 };
 
-// lane 0 claims the next block of the oldest ready segment that has one;
-// then every lane loads the block's keep entries (warp-collective)
-__device__ __forceinline__ MoveClaim pass_claim(const FPass& P, int n_active) {
+// lane 0 claims the next block, first from the segment of its previous claim
+// (one atomic), else from the oldest ready segment that has one; then every
+// lane loads the block's keep entries (warp-collective)
+__device__ __forceinline__ MoveClaim pass_claim(const FPass& P, int n_active, int& last_sg) {
   const int lane = threadIdx.x & 31;
   int state = 1, sg = 0, j = 0;
+  auto blocks_of = [&](int g) {
+    return (P.seq[(g % (P.n_seqs * P.n_kv)) / P.n_kv].budget + kChunk - 1) / kChunk;
+  };
   if (lane == 0) {
-    while (true) {
+    if (last_sg >= 0) {
+      j = atomicAdd(&P.ctl->move_next[last_sg], 1);
+      if (j < blocks_of(last_sg)) {
+        state = 0;
+        sg = last_sg;
+      }
+    }
+    while (state != 0) {
       const uint32_t c = ld_acquire_u32(&P.ctrl->move_cursor);
       if ((int)c >= n_active) {
         state = 2;
@@ -398,14 +412,14 @@ __device__ __forceinline__ MoveClaim pass_claim(const FPass& P, int n_active) {
         state = 2;
         break;
       }
-      const int nb = (P.seq[(sg % (P.n_seqs * P.n_kv)) / P.n_kv].budget + kChunk - 1) / kChunk;
       j = atomicAdd(&P.ctl->move_next[sg], 1);
-      if (j >= 0 && j < nb) {
+      if (j >= 0 && j < blocks_of(sg)) {
         state = 0;
         break;
       }
       atomicCAS(&P.ctrl->move_cursor, c, c + 1u);   // exhausted: move past it
     }
+    last_sg = state == 0 ? sg : -1;
   }
   MoveClaim m;
   m.state = __shfl_sync(0xffffffffu, state, 0);
@@ -414,13 +428,14 @@ __device__ __forceinline__ MoveClaim pass_claim(const FPass& P, int n_active) {
   m.a = -1;
   m.p0 = m.p1 = 0;
   if (m.state == 0) {
-    const int r = m.sg % (P.n_seqs * P.n_kv);
-    const int s = r / P.n_kv;
-    const int B = P.seq[s].budget;
+    const PSeg v = pass_seg(P, m.sg);
+    m.n = v.n;
+    m.B = v.B;
+    m.li = v.li;
+    m.row0 = v.row0;
+    m.wrow0 = v.wrow0;
     const int i = m.j * kChunk + lane;
-    const int64_t wrow0 = (int64_t)(m.sg / (P.n_seqs * P.n_kv)) * P.rows_per_layer + P.seq[s].row0 +
-                          (int64_t)(r - s * P.n_kv) * P.seq[s].cap;
-    m.a = i < B ? __ldcg(P.keep + wrow0 + i) : -1;
+    m.a = i < v.B ? __ldcg(P.keep + v.wrow0 + i) : -1;
     const int* pre = P.prefix + (size_t)m.sg * (P.c_max + 1);
     m.p0 = __ldcg(&pre[m.j]);
     m.p1 = __ldcg(&pre[m.j + 1]);
@@ -428,52 +443,62 @@ __device__ __forceinline__ MoveClaim pass_claim(const FPass& P, int n_active) {
   return m;
 }
 
-// Moves the claimed block m (k_move's steps); when `next` is given, the next
-// block is claimed while this block's rows load.
-__device__ __forceinline__ void pass_move_block(const FPass& P, const MoveClaim& m, uint8_t* stg, int* msrc,
-                                                uint32_t tag, int n_active, MoveClaim* next) {
+// k_move's steps for one claimed block, split at the gather: start_gather
+// validates the block, records its moving source rows in msrc and starts
+// the cp.async gathers into stg (one commit group); finish writes the rows
+// out once they have landed (publish "read", wait for the lower blocks that
+// read the destination rows, TMA bulk stores, one bulk group).
+struct MoveWork {
+  int first, nmove, my_pos;
+  bool ok;
+};
+
+__device__ __forceinline__ MoveWork pass_gather(const FPass& P, const MoveClaim& m, uint8_t* stg, int* msrc) {
   const int lane = threadIdx.x & 31;
   const MoveStage L = move_stage_layout(P.k_rb, P.ks_rb, P.v_rb, P.vs_rb);
   const PlaneMap mk = plane_map(P.k_rb, lane), mks = plane_map(P.ks_rb, lane), mv = plane_map(P.v_rb, lane),
                  mvs = plane_map(P.vs_rb, lane);
-  const PSeg v = pass_seg(P, m.sg);
-  const LayerRef& lr = P.lay[v.li];
-  const int B = v.B, n = v.n, j = m.j;
-  const int i0 = j * kChunk, cnt = min(kChunk, B - i0);
-  const bool bad_entry = lane < cnt && (m.a < i0 + lane || m.a >= n);
-  const bool ok =
-      !__any_sync(0xffffffffu, bad_entry) && m.p0 >= 0 && m.p0 <= m.p1 && m.p1 - m.p0 <= kChunk && m.p1 <= B;
-  if (!ok && lane == 0) report(P.ctrl, TRIA_ERR_INVALID_ARG, 0x10000000u | (uint32_t)m.sg);
+  const LayerRef& lr = P.lay[m.li];
+  const int i0 = m.j * kChunk, cnt = min(kChunk, m.B - i0);
+  const bool bad_entry = lane < cnt && (m.a < i0 + lane || m.a >= m.n);
+  MoveWork w;
+  w.ok = !__any_sync(0xffffffffu, bad_entry) && m.p0 >= 0 && m.p0 <= m.p1 && m.p1 - m.p0 <= kChunk &&
+         m.p1 <= m.B;
+  if (!w.ok && lane == 0) report(P.ctrl, TRIA_ERR_INVALID_ARG, 0x10000000u | (uint32_t)m.sg);
   // moving entries (keep[i] != i) are a suffix of the block
-  const unsigned mvm = __ballot_sync(0xffffffffu, ok && lane < cnt && m.a != i0 + lane);
-  const int first = mvm ? __ffs(mvm) - 1 : cnt;
-  const int nmove = ok ? cnt - first : 0;
-  if (lane == 0) bulk_wait_read_all();   // the previous block's stores have read the stage
+  const unsigned mvm = __ballot_sync(0xffffffffu, w.ok && lane < cnt && m.a != i0 + lane);
+  w.first = mvm ? __ffs(mvm) - 1 : cnt;
+  w.nmove = w.ok ? cnt - w.first : 0;
+  if (lane >= w.first && lane < cnt) msrc[lane - w.first] = m.a;
   __syncwarp();
-  if (lane >= first && lane < cnt) msrc[lane - first] = m.a;
-  __syncwarp();
-  int my_pos = 0;
-  if (nmove > 0) {
-    warp_gather(lr.k, v.row0, mk, stg + L.k, msrc, nmove);
-    warp_gather(lr.ks, v.row0, mks, stg + L.ks, msrc, nmove);
-    warp_gather(lr.v, v.row0, mv, stg + L.v, msrc, nmove);
-    warp_gather(lr.vs, v.row0, mvs, stg + L.vs, msrc, nmove);
-    if (lane < nmove) my_pos = __ldcg(lr.pos + v.row0 + msrc[lane]);
+  w.my_pos = 0;
+  if (w.nmove > 0) {
+    warp_gather(lr.k, m.row0, mk, stg + L.k, msrc, w.nmove);
+    warp_gather(lr.ks, m.row0, mks, stg + L.ks, msrc, w.nmove);
+    warp_gather(lr.v, m.row0, mv, stg + L.v, msrc, w.nmove);
+    warp_gather(lr.vs, m.row0, mvs, stg + L.vs, msrc, w.nmove);
+    if (lane < w.nmove) w.my_pos = __ldcg(lr.pos + m.row0 + msrc[lane]);
   }
   cp_async_commit();
-  if (next) *next = pass_claim(P, n_active);   // travels while the rows load
-  cp_async_wait<0>();
-  __syncwarp();
-  if (lane < nmove) msrc[lane] = my_pos;
+  return w;
+}
+
+// call once the block's gather group has completed (cp.async wait + syncwarp)
+__device__ __forceinline__ void pass_store(const FPass& P, const MoveClaim& m, const MoveWork& w, uint8_t* stg,
+                                           int* msrc, uint32_t tag) {
+  const int lane = threadIdx.x & 31;
+  const MoveStage L = move_stage_layout(P.k_rb, P.ks_rb, P.v_rb, P.vs_rb);
+  const LayerRef& lr = P.lay[m.li];
+  if (lane < w.nmove) msrc[lane] = w.my_pos;
   __syncwarp();
   // publish "read"; then wait for the lower blocks that read my destination rows
   uint32_t* flags = P.flags + (size_t)m.sg * P.c_max;
   int go = 0;
   if (lane == 0) {
-    st_relaxed_u32(&flags[j], tag);
-    go = ok;
-    if (go && nmove > 0 && m.p1 > m.p0) {
-      const int lo_b = m.p0 / kChunk, hi_b = min((m.p1 - 1) / kChunk, j - 1);
+    st_relaxed_u32(&flags[m.j], tag);
+    go = w.ok;
+    if (go && w.nmove > 0 && m.p1 > m.p0) {
+      const int lo_b = m.p0 / kChunk, hi_b = min((m.p1 - 1) / kChunk, m.j - 1);
       for (int cc = lo_b; cc <= hi_b; ++cc)
         if (!wait_flag_bounded(&flags[cc], tag, P.spin_limit)) {
           go = 0;
@@ -483,41 +508,71 @@ __device__ __forceinline__ void pass_move_block(const FPass& P, const MoveClaim&
     }
   }
   go = __shfl_sync(0xffffffffu, go, 0);
-  if (go && nmove > 0) {
-    const int dst0 = i0 + first;
+  if (go && w.nmove > 0) {
+    const int dst0 = m.j * kChunk + w.first;
     if (lane == 0) {
       fence_proxy_async_smem();
-      bulk_s2g(lr.k + (size_t)(v.row0 + dst0) * P.k_rb, stg + L.k, (uint32_t)(nmove * P.k_rb));
-      bulk_s2g(lr.v + (size_t)(v.row0 + dst0) * P.v_rb, stg + L.v, (uint32_t)(nmove * P.v_rb));
-      bulk_commit();
+      bulk_s2g(lr.k + (size_t)(m.row0 + dst0) * P.k_rb, stg + L.k, (uint32_t)(w.nmove * P.k_rb));
+      bulk_s2g(lr.v + (size_t)(m.row0 + dst0) * P.v_rb, stg + L.v, (uint32_t)(w.nmove * P.v_rb));
     }
-    warp_scatter(lr.ks, v.row0, P.ks_rb, stg + L.ks, dst0, nmove, lane);
-    warp_scatter(lr.vs, v.row0, P.vs_rb, stg + L.vs, dst0, nmove, lane);
-    if (lane < nmove) lr.pos[v.row0 + dst0 + lane] = msrc[lane];
+    warp_scatter(lr.ks, m.row0, P.ks_rb, stg + L.ks, dst0, w.nmove, lane);
+    warp_scatter(lr.vs, m.row0, P.vs_rb, stg + L.vs, dst0, w.nmove, lane);
+    if (lane < w.nmove) lr.pos[m.row0 + dst0 + lane] = msrc[lane];
   }
+  if (lane == 0) bulk_commit();   // one bulk group per block (possibly empty)
   __syncwarp();
 }
 
-// One warp's moves once every segment is selected: claim, move, repeat, the
-// next claim travelling with the current block's loads.
-static __device__ __noinline__ void pass_moves(const FPass& P, uint8_t* stg, int* msrc, uint32_t tag, int n_active) {
+// One warp's moves once every segment is selected, two blocks in flight:
+// the next block is claimed and its gather started before the current
+// block's rows are written out. stg0 / stg1: the warp's two stages; msrc:
+// 2 x kChunk ints.
+static __device__ __noinline__ void pass_moves(const FPass& P, uint8_t* stg0, uint8_t* stg1, int* msrc,
+                                               uint32_t tag, int n_active) {
   const int lane = threadIdx.x & 31;
-  MoveClaim m = pass_claim(P, n_active);
+  uint8_t* stg[2] = {stg0, stg1};
+  int last_sg = -1;
   int idle = 0;
-  while (m.state != 2) {
-    if (m.state == 1) {
-      if (++idle > P.spin_limit) {
-        if (lane == 0) report(P.ctrl, TRIA_ERR_TIMEOUT, 0xA0000000u);
-        break;
+  MoveClaim cur = pass_claim(P, n_active, last_sg);
+  MoveWork wc{};
+  int s = 0;
+  bool have = false;   // cur's gather started
+  while (true) {
+    if (!have) {
+      if (cur.state == 2) break;
+      if (cur.state == 1) {
+        if (++idle > P.spin_limit) {
+          if (lane == 0) report(P.ctrl, TRIA_ERR_TIMEOUT, 0xA0000000u);
+          break;
+        }
+        __nanosleep(idle < 64 ? 64 : 512);
+        cur = pass_claim(P, n_active, last_sg);
+        continue;
       }
-      __nanosleep(idle < 64 ? 64 : 512);
-      m = pass_claim(P, n_active);
-      continue;
+      idle = 0;
+      if (lane == 0) bulk_wait_read_all();   // the stage's last stores have read it
+      __syncwarp();
+      wc = pass_gather(P, cur, stg[s], msrc + s * kChunk);
+      have = true;
     }
-    idle = 0;
-    MoveClaim nx;
-    pass_move_block(P, m, stg, msrc, tag, n_active, &nx);
-    m = nx;
+    // the next block: claimed and its gather started into the other stage
+    MoveClaim nx = pass_claim(P, n_active, last_sg);
+    MoveWork wn{};
+    const bool go_next = nx.state == 0;
+    if (go_next) {
+      if (lane == 0) bulk_wait_read_all();   // the other stage's stores (the previous block) have read it
+      __syncwarp();
+      wn = pass_gather(P, nx, stg[s ^ 1], msrc + (s ^ 1) * kChunk);
+      cp_async_wait<1>();   // cur's rows have landed
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncwarp();
+    pass_store(P, cur, wc, stg[s], msrc + s * kChunk, tag);
+    cur = nx;
+    wc = wn;
+    have = go_next;
+    s ^= 1;
   }
   if (lane == 0) bulk_wait_all();
 }
@@ -704,6 +759,8 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
   const MoveStage L = move_stage_layout(P.k_rb, P.ks_rb, P.v_rb, P.vs_rb);
   const bool mover = warp < min(kPassWarps, kPassRing / L.bytes);
   uint8_t* stg = smem + PassSmem::kRing + (size_t)warp * L.bytes;
+  // once every segment is selected: half the warps, two stages each
+  const bool mover2 = warp < min(kPassWarps, kPassRing / (2 * L.bytes));
   const uint32_t tag = flag_tag(s_epoch);
   if (n_active > 0) {
     int idle = 0;
@@ -747,9 +804,13 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
       // no segment waits for selection: each warp moves at most one block
       int moved = 0;
       if (mover) {
-        const MoveClaim m = pass_claim(P, n_active);
+        int last_sg = -1;
+        const MoveClaim m = pass_claim(P, n_active, last_sg);
         if (m.state == 0) {
-          pass_move_block(P, m, stg, s_src[warp], tag, n_active, nullptr);
+          const MoveWork w = pass_gather(P, m, stg, s_src[warp]);
+          cp_async_wait<0>();
+          __syncwarp();
+          pass_store(P, m, w, stg, s_src[warp], tag);
           moved = 1;
         }
         if (lane == 0) bulk_wait_read_all();   // the stage may hold keys next
@@ -764,7 +825,12 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
         __nanosleep(idle < 64 ? 64 : 512);
       }
     }
-    if (mover) pass_moves(P, stg, s_src[warp], tag, n_active);
+    if (mover && lane == 0) bulk_wait_all();   // the single-stage stores of the service loop
+    __syncthreads();
+    if (mover2)
+      pass_moves(P, smem + PassSmem::kRing + (size_t)(2 * warp) * L.bytes,
+                 smem + PassSmem::kRing + (size_t)(2 * warp + 1) * L.bytes, &s_src[2 * warp][0],
+                 tag, n_active);
   }
 
   // ---- the last CTA: n_live of the active sequences, counters reset
