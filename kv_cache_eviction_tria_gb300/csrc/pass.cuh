@@ -588,7 +588,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_active, s_sel, s_last;
   __shared__ uint32_t s_epoch;
-  __shared__ int s_src[kPassWarps][kChunk];
+  __shared__ int s_src[2 * kPassWarps][kChunk];   // per warp and stage: a block's source rows, then positions
   __shared__ int s_sbuf[40];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
