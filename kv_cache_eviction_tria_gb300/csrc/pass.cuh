@@ -49,7 +49,10 @@ constexpr int kPassScaleStage = kPassPieceBytes / 16;   // q8_0 block scales of 
 constexpr int kPassRing = kPassWarps * 2 * kPassPieceBytes;
 constexpr int kPassMaxSegs = kPassCtlSegs;   // layers x sequences x KV heads per call
 constexpr int kPassMaxLayers = 128;
-constexpr int kPassSmemKeys = kPassRing / 4;  // z-max keys a select keeps in shared memory
+// A select keeps its radix histogram in the last 8 KB of the ring area and up
+// to kPassSmemKeys z-max keys before it (the ring is free once scoring ends).
+constexpr int kPassHistOff = kPassRing - kHistBins * 4;
+constexpr int kPassSmemKeys = kPassHistOff / 4;
 
 // One layer of the call: its cache planes, live rows and statistics.
 struct LayerRef {
@@ -113,17 +116,16 @@ __device__ __forceinline__ PSeg pass_seg(const FPass& P, int sg) {
   return v;
 }
 
-// dynamic shared memory: ring (score stream; z-max keys of a select; move
-// stages) | q8_0 scale ring | mbarriers | piece table | turn factors | select
-// histogram
+// dynamic shared memory: ring (score stream; then a select's z-max keys and
+// histogram, or move stages) | q8_0 scale ring | mbarriers | piece table |
+// turn factors
 struct PassSmem {
   static constexpr int kRing = 0;
   static constexpr int kScales = kRing + kPassRing;
   static constexpr int kBars = kScales + kPassWarps * 2 * kPassScaleStage;
   static constexpr int kFirst = kBars + kPassWarps * 2 * 8;
   static constexpr int kTurns = kFirst + ((kPassMaxSegs + 1) * 4 + 15) / 16 * 16;
-  static constexpr int kHist = kTurns + 128 * 8;
-  static constexpr int kBytes = kHist + kHistBins * 4;
+  static constexpr int kBytes = kTurns + 128 * 8;
 };
 
 template <int G>
@@ -597,7 +599,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + PassSmem::kBars) + warp * 2;
   int* seg_first = reinterpret_cast<int*>(smem + PassSmem::kFirst);   // first piece of every segment
   unsigned long long* s_turns = reinterpret_cast<unsigned long long*>(smem + PassSmem::kTurns);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(smem + PassSmem::kHist);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem + PassSmem::kRing + kPassHistOff);   // service phase only
 
   // ---- prologue: piece table (pieces of the active segments, in segment
   // order), active segments, turn factors, ring barriers
