@@ -525,58 +525,119 @@ __device__ __forceinline__ void pass_store(const FPass& P, const MoveClaim& m, c
   __syncwarp();
 }
 
-// One warp's moves once every segment is selected, two blocks in flight:
-// the next block is claimed and its gather started before the current
-// block's rows are written out. stg0 / stg1: the warp's two stages; msrc:
-// 2 x kChunk ints.
-static __device__ __noinline__ void pass_moves(const FPass& P, uint8_t* stg0, uint8_t* stg1, int* msrc,
-                                               uint32_t tag, int n_active) {
-  const int lane = threadIdx.x & 31;
-  uint8_t* stg[2] = {stg0, stg1};
-  int last_sg = -1;
-  int idle = 0;
-  MoveClaim cur = pass_claim(P, n_active, last_sg);
-  MoveWork wc{};
-  int s = 0;
-  bool have = false;   // cur's gather started
-  while (true) {
-    if (!have) {
-      if (cur.state == 2) break;
-      if (cur.state == 1) {
-        if (++idle > P.spin_limit) {
-          if (lane == 0) report(P.ctrl, TRIA_ERR_TIMEOUT, 0xA0000000u);
+// Grid barrier of the pass (every CTA resident), bounded: after the spin
+// limit it records TRIA_ERR_TIMEOUT and lets the CTA go on.
+__device__ __forceinline__ bool pass_grid_barrier(const FPass& P) {
+  __shared__ int s_to;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    s_to = 0;
+    const uint32_t gen = ld_acquire_u32(&P.ctrl->bar_gen);
+    __threadfence();
+    if (atomicAdd(&P.ctrl->bar_count, 1u) == gridDim.x - 1) {
+      atomicExch(&P.ctrl->bar_count, 0u);
+      __threadfence();
+      atomicAdd(&P.ctrl->bar_gen, 1u);
+    } else if (!wait_flag_bounded_ne(&P.ctrl->bar_gen, gen, P.spin_limit)) {
+      s_to = 1;
+      report(P.ctrl, TRIA_ERR_TIMEOUT, 0xB0000002u);
+    }
+    __threadfence();
+  }
+  __syncthreads();
+  return s_to == 0;
+}
+
+// The moves left once every segment is selected, in k_move's order: item t
+// is block base[sg] + t / n_act of the segment in ready slot t % n_act
+// (block-major, so the lower blocks that read a block's rows come in earlier
+// rounds), mover warp w of the grid takes items w, w + Wm, ... and loads the
+// next item's keep entries while it moves the current one. When every item
+// has a warp of its own, all gather, one grid barrier marks every read done,
+// and all write (no read-done flags). Every CTA calls it (grid barriers).
+static __device__ __noinline__ void pass_moves_final(const FPass& P, uint8_t* stg, int* msrc, uint32_t tag, int n_act,
+                                              int mover_warps, int j_span) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool mover = warp < mover_warps;
+  const int Wm = gridDim.x * mover_warps;
+  const int total = n_act * j_span;
+  const bool one_round = total <= Wm;
+  auto fetch = [&](int t, MoveClaim& m) {
+    m.state = 2;
+    if (t >= total) return;
+    const int slot = t % n_act;
+    const int sg = __ldcg(P.ctl->ready + slot) - 1;
+    const PSeg v = pass_seg(P, sg);
+    const int nb = (v.B + kChunk - 1) / kChunk;
+    const int j = __ldcg(P.ctl->move_next + sg) + t / n_act;   // blocks below were moved while selecting
+    m.state = j < nb ? 0 : 1;   // 1: no such block in this segment
+    m.sg = sg;
+    m.j = j;
+    m.n = v.n;
+    m.B = v.B;
+    m.li = v.li;
+    m.row0 = v.row0;
+    m.wrow0 = v.wrow0;
+    m.a = -1;
+    m.p0 = m.p1 = 0;
+    if (m.state == 0) {
+      const int i = j * kChunk + lane;
+      m.a = i < v.B ? __ldcg(P.keep + v.wrow0 + i) : -1;
+      const int* pre = P.prefix + (size_t)sg * (P.c_max + 1);
+      m.p0 = __ldcg(&pre[j]);
+      m.p1 = __ldcg(&pre[j + 1]);
+    }
+  };
+  MoveClaim pend{};
+  MoveWork pend_w{};
+  bool pending = false;
+  // this warp's items, in order
+  if (mover) {
+    int t = blockIdx.x * mover_warps + warp;
+    MoveClaim m;
+    fetch(t, m);
+    while (m.state != 2) {
+      MoveClaim nx;
+      fetch(t + Wm, nx);   // the next item's keep entries load while this one moves
+      if (m.state == 0) {
+        if (lane == 0) bulk_wait_read_all();   // the previous item's stores have read the stage
+        __syncwarp();
+        const MoveWork w = pass_gather(P, m, stg, msrc);
+        cp_async_wait<0>();
+        __syncwarp();
+        if (one_round) {   // the only item of this warp: write after the barrier
+          pend = m;
+          pend_w = w;
+          pending = true;
+          if (lane < w.nmove) msrc[lane] = w.my_pos;
+          __syncwarp();
           break;
         }
-        __nanosleep(idle < 64 ? 64 : 512);
-        cur = pass_claim(P, n_active, last_sg);
-        continue;
+        pass_store(P, m, w, stg, msrc, tag);
       }
-      idle = 0;
-      if (lane == 0) bulk_wait_read_all();   // the stage's last stores have read it
-      __syncwarp();
-      wc = pass_gather(P, cur, stg[s], msrc + s * kChunk);
-      have = true;
+      m = nx;
+      t += Wm;
     }
-    // the next block: claimed and its gather started into the other stage
-    MoveClaim nx = pass_claim(P, n_active, last_sg);
-    MoveWork wn{};
-    const bool go_next = nx.state == 0;
-    if (go_next) {
-      if (lane == 0) bulk_wait_read_all();   // the other stage's stores (the previous block) have read it
-      __syncwarp();
-      wn = pass_gather(P, nx, stg[s ^ 1], msrc + (s ^ 1) * kChunk);
-      cp_async_wait<1>();   // cur's rows have landed
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncwarp();
-    pass_store(P, cur, wc, stg[s], msrc + s * kChunk, tag);
-    cur = nx;
-    wc = wn;
-    have = go_next;
-    s ^= 1;
   }
-  if (lane == 0) bulk_wait_all();
+  if (one_round) {
+    const bool in_time = pass_grid_barrier(P);
+    if (pending && in_time && pend_w.nmove > 0) {
+      const MoveStage L = move_stage_layout(P.k_rb, P.ks_rb, P.v_rb, P.vs_rb);
+      const LayerRef& lr = P.lay[pend.li];
+      const int dst0 = pend.j * kChunk + pend_w.first;
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        bulk_s2g(lr.k + (size_t)(pend.row0 + dst0) * P.k_rb, stg + L.k, (uint32_t)(pend_w.nmove * P.k_rb));
+        bulk_s2g(lr.v + (size_t)(pend.row0 + dst0) * P.v_rb, stg + L.v, (uint32_t)(pend_w.nmove * P.v_rb));
+        bulk_commit();
+      }
+      warp_scatter(lr.ks, pend.row0, P.ks_rb, stg + L.ks, dst0, pend_w.nmove, lane);
+      warp_scatter(lr.vs, pend.row0, P.vs_rb, stg + L.vs, dst0, pend_w.nmove, lane);
+      if (lane < pend_w.nmove) lr.pos[pend.row0 + dst0 + lane] = msrc[lane];
+      __syncwarp();
+    }
+  }
+  if (mover && lane == 0) bulk_wait_all();
 }
 
 template <int KT, int G, int S>
@@ -590,7 +651,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_active, s_sel, s_last;
   __shared__ uint32_t s_epoch;
-  __shared__ int s_src[2 * kPassWarps][kChunk];   // per warp and stage: a block's source rows, then positions
+  __shared__ int s_src[kPassWarps][kChunk];   // per warp: a block's source rows, then positions
   __shared__ int s_sbuf[40];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -761,8 +822,6 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
   const MoveStage L = move_stage_layout(P.k_rb, P.ks_rb, P.v_rb, P.vs_rb);
   const bool mover = warp < min(kPassWarps, kPassRing / L.bytes);
   uint8_t* stg = smem + PassSmem::kRing + (size_t)warp * L.bytes;
-  // once every segment is selected: half the warps, two stages each
-  const bool mover2 = warp < min(kPassWarps, kPassRing / (2 * L.bytes));
   const uint32_t tag = flag_tag(s_epoch);
   if (n_active > 0) {
     int idle = 0;
@@ -827,12 +886,20 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
         __nanosleep(idle < 64 ? 64 : 512);
       }
     }
-    if (mover && lane == 0) bulk_wait_all();   // the single-stage stores of the service loop
+    if (mover && lane == 0) bulk_wait_all();   // the stores of the service loop
+    // every segment is selected (each CTA finished its selects before here):
+    // the moves left, in k_move's order
+    __shared__ int s_span;
+    if (tid == 0) s_span = 0;
+    pass_grid_barrier(P);
+    for (int slot = tid; slot < n_active; slot += blockDim.x) {
+      const int sg = __ldcg(P.ctl->ready + slot) - 1;
+      if (sg < 0 || sg >= P.n_seg) continue;
+      const int nb = (P.seq[(sg % (P.n_seqs * P.n_kv)) / P.n_kv].budget + kChunk - 1) / kChunk;
+      atomicMax(&s_span, nb - min(nb, __ldcg(P.ctl->move_next + sg)));
+    }
     __syncthreads();
-    if (mover2)
-      pass_moves(P, smem + PassSmem::kRing + (size_t)(2 * warp) * L.bytes,
-                 smem + PassSmem::kRing + (size_t)(2 * warp + 1) * L.bytes, &s_src[2 * warp][0],
-                 tag, n_active);
+    pass_moves_final(P, stg, s_src[warp], tag, n_active, min(kPassWarps, kPassRing / L.bytes), s_span);
   }
 
   // ---- the last CTA: n_live of the active sequences, counters reset
