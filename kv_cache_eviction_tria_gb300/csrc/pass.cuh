@@ -160,7 +160,11 @@ constexpr int kSelStages = 3;
 constexpr int kSelStageBytes = 16384 + 16;   // a 16 KB window and the 16-byte alignment slack
 constexpr int kSelStageOff = kPassHistOff - kSelStages * kSelStageBytes;
 constexpr int kSelSmemKeys = 32768;          // segments up to this many rows keep their keys in shared memory
+constexpr int kSelSample = 2048;             // candidate keys sampled for the estimate of the cut
+constexpr int kSelBand = 1024;               // band keys a warp buffers
 static_assert(kSelSmemKeys * 4 <= kSelStageOff, "select shared-memory layout");
+static_assert(kSelSample * 4 <= kHistBins * 4, "the sample lives in the histogram area");
+static_assert(kPassWarps * kSelBand * 4 <= kSelStages * kSelStageBytes, "band buffers in the stage area");
 
 // mbarriers of the stages and how many times each has completed
 struct SelBars {
@@ -245,10 +249,15 @@ __device__ __noinline__ void pass_select(const FPass& P, int sg, int nr, uint8_t
 
   float mu[G], inv[G];
   block_moments_of_runs<G>(P.parts + (size_t)sg * kRunCols * P.cs_max, P.cs_max, nr, mu, inv);
-  for (int i = tid; i < kHistBins; i += blockDim.x) hist[i] = 0u;
+  // a sample of the candidates' keys (every stride-th candidate) in the
+  // histogram area, for the estimate of the cut
+  const int ncand = hi - lo;
+  const int stride = max(1, (ncand + kSelSample - 1) / kSelSample);
+  const int ns = k > 0 ? (ncand + stride - 1) / stride : 0;
+  uint32_t* sample = hist;
   __syncthreads();
 
-  // z-max keys and the first radix histogram of the candidates [lo, hi)
+  // z-max keys of every live row, and the sample
   {
     float* so = P.score_out ? P.score_out + v.wrow0 : nullptr;
     sel_stream(P, reinterpret_cast<const uint8_t*>(P.raw + (size_t)v.wrow0 * G), (int64_t)n * G * 4, stages, sb,
@@ -264,7 +273,10 @@ __device__ __noinline__ void pass_select(const FPass& P, int sg, int nr, uint8_t
                    if constexpr (kSmem) skeys[r] = key;
                    else __stcg(gkeys + r, key);
                    if (so) so[r] = s;
-                   if (k > 0 && r >= lo && r < hi) atomicAdd(&hist[key >> 21], 1u);
+                   if (k > 0 && r >= lo && r < hi) {
+                     const int c = r - lo, q = c / stride;
+                     if (c == q * stride) sample[q] = key;
+                   }
                  }
                });
     if constexpr (!kSmem) asm volatile("fence.proxy.async.global;" ::: "memory");   // keys before their bulk reads
@@ -286,78 +298,140 @@ __device__ __noinline__ void pass_select(const FPass& P, int sg, int nr, uint8_t
     }
   };
 
-  // radix select of the k-th largest key over the candidates: T = that key,
-  // kr = how many candidates with key == T are kept (lowest rows first); a
-  // bin holding exactly the keys still to take ends the search early
+  // The k-th largest candidate key T and kr = how many candidates with key
+  // == T are kept (lowest rows first). First from the sample: its quantiles
+  // around the cut's expected rank bound a band [kl, kh] of keys; one pass
+  // counts the candidates above kh (ballots, no atomics) and gathers the
+  // band's keys into per-warp buffers; the cut is then found in the band by a
+  // radix select on the bits below the band's common prefix (well spread, so
+  // its histogram atomics rarely collide). When the band misses the cut or
+  // overflows its buffers, a radix select over all candidates (11 + 11 + 10
+  // bits) finds it instead. Exact either way.
   uint32_t T = 0xFFFFFFFFu;
   int kr = 0;
   if (k > 0) {
-    uint32_t prefix = 0;
-    kr = k;
-    bool cut = false;
-#pragma unroll 1
-    for (int pass = 0; pass < 3; ++pass) {
-      const int NB = pass == 2 ? 1024 : 2048;
-      if (pass > 0) {
-        for (int i = tid; i < NB; i += blockDim.x) hist[i] = 0u;
-        __syncthreads();
-        for_keys(lo, hi, [&](const uint32_t* kk, int r0, int r1) {
-          for (int i = tid; i < r1 - r0; i += kPassThreads) {
-            const uint32_t key = kk[i];
-            if (pass == 1) {
-              if ((key >> 21) == prefix) atomicAdd(&hist[(key >> 10) & 0x7FFu], 1u);
-            } else if ((key >> 10) == prefix) {
-              atomicAdd(&hist[key & 0x3FFu], 1u);
-            }
+    // sort the sample descending (bitonic, padded with the lowest key)
+    int np = 1;
+    while (np < ns) np <<= 1;
+    for (int i = ns + tid; i < np; i += blockDim.x) sample[i] = 0u;
+    __syncthreads();
+    for (int size = 2; size <= np; size <<= 1)
+      for (int st = size >> 1; st > 0; st >>= 1) {
+        for (int i = tid; i < (np >> 1); i += blockDim.x) {
+          const int a = 2 * st * (i / st) + (i % st), b = a + st;
+          const bool desc = (a & size) == 0;
+          const uint32_t x = sample[a], y = sample[b];
+          if ((x < y) == desc) {
+            sample[a] = y;
+            sample[b] = x;
           }
-        });
+        }
         __syncthreads();
       }
-      // thread t scans bins NB-1-per*t .. NB-per*(t+1) (descending)
-      const int per = (NB + kPassThreads - 1) / kPassThreads;
-      uint32_t cnt[6];
-      int local = 0;
-#pragma unroll
-      for (int j = 0; j < 6; ++j) {
-        const int b = NB - 1 - (per * tid + j);
-        cnt[j] = (j < per && b >= 0) ? hist[b] : 0u;
-        local += (int)cnt[j];
+    // the band: sample ranks q -+ 4 sigma (+4), q = the cut's expected rank
+    const double pk = (double)k / ncand;
+    const int q = (int)(pk * ns + 0.5);
+    const int ms = (int)(4.0 * sqrt((double)ns * pk * (1.0 - pk))) + 4;
+    const uint32_t kh = q - ms >= 1 ? sample[q - ms - 1] : 0xFFFFFFFFu;
+    const uint32_t kl = q + ms <= ns ? sample[q + ms - 1] : 0u;
+    __syncthreads();   // the sample area becomes the histogram
+    uint32_t* band = kSmem ? reinterpret_cast<uint32_t*>(stages) : skeys;   // kPassWarps x kSelBand keys
+    uint32_t* wb = band + warp * kSelBand;
+    int nb = 0, na = 0;   // this warp's band keys and keys above kh
+    for_keys(lo, hi, [&](const uint32_t* kk, int r0, int r1) {
+      for (int i0 = warp * 32; i0 < r1 - r0; i0 += kPassThreads) {
+        const int i = i0 + lane;
+        const uint32_t key = i < r1 - r0 ? kk[i] : 0u;
+        const bool valid = i < r1 - r0;
+        na += __popc(__ballot_sync(0xffffffffu, valid && key > kh));
+        const bool inb = valid && key >= kl && key <= kh;
+        const uint32_t bb = __ballot_sync(0xffffffffu, inb);
+        const int at = nb + __popc(bb & ((1u << lane) - 1u));
+        if (inb && at < kSelBand) wb[at] = key;
+        nb += __popc(bb);
       }
-      int total;
-      const int before = block_exclusive_scan(local, &total, s_sbuf);
-      if (before < kr && kr <= before + local) {
-        int cum = before;
+    });
+    if (lane == 0) {
+      s_wt[warp] = nb;
+      s_wk[warp] = na;
+    }
+    __syncthreads();
+    int above = 0, nband = 0;
+    bool over = false;
+    for (int w = 0; w < kPassWarps; ++w) {
+      above += s_wk[w];
+      nband += s_wt[w];
+      over = over || s_wt[w] > kSelBand;
+    }
+    // radix select over one population: the band's keys (band) or all
+    // candidates; m-th largest within keys that share `cur` on bits above R
+    auto radix = [&](bool use_band, uint32_t cur, int R, int m, uint32_t& t_out, int& kr_out) {
+      while (R > 0) {
+        const int d = min(11, R), sh = R - d;
+        const uint32_t mask = (1u << d) - 1u;
+        for (int i = tid; i < kHistBins; i += blockDim.x) hist[i] = 0u;
+        __syncthreads();
+        auto add = [&](uint32_t key) {
+          if ((uint32_t)((uint64_t)key >> (sh + d)) == cur) atomicAdd(&hist[(key >> sh) & mask], 1u);
+        };
+        if (use_band) {
+          for (int w = 0; w < kPassWarps; ++w)
+            for (int i = tid; i < s_wt[w]; i += blockDim.x) add(band[w * kSelBand + i]);
+        } else {
+          for_keys(lo, hi, [&](const uint32_t* kk, int r0, int r1) {
+            for (int i = tid; i < r1 - r0; i += kPassThreads) add(kk[i]);
+          });
+        }
+        __syncthreads();
+        // the bin of the m-th largest: thread t scans bins NB-1-per*t .. (descending)
+        const int NB = 1 << d;
+        const int per = (NB + kPassThreads - 1) / kPassThreads;
+        uint32_t cnt[6];
+        int local = 0;
 #pragma unroll
         for (int j = 0; j < 6; ++j) {
           const int b = NB - 1 - (per * tid + j);
-          if (j >= per || b < 0) break;
-          if (cum + (int)cnt[j] >= kr) {
-            s_info[0] = (int)(pass == 0 ? (uint32_t)b : pass == 1 ? ((prefix << 11) | (uint32_t)b)
-                                                                   : ((prefix << 10) | (uint32_t)b));
-            s_info[1] = kr - cum;
-            s_info[2] = (int)cnt[j];
-            break;
+          cnt[j] = (j < per && b >= 0) ? hist[b] : 0u;
+          local += (int)cnt[j];
+        }
+        int total;
+        const int before = block_exclusive_scan(local, &total, s_sbuf);
+        if (before < m && m <= before + local) {
+          int cum = before;
+#pragma unroll
+          for (int j = 0; j < 6; ++j) {
+            const int b = NB - 1 - (per * tid + j);
+            if (j >= per || b < 0) break;
+            if (cum + (int)cnt[j] >= m) {
+              s_info[0] = b;
+              s_info[1] = m - cum;
+              break;
+            }
+            cum += (int)cnt[j];
           }
-          cum += (int)cnt[j];
         }
+        if (tid == 0 && total < m) report(P.ctrl, TRIA_ERR_INVALID_ARG, 0x80000000u | (uint32_t)sg);
+        __syncthreads();
+        cur = (cur << d) | (uint32_t)s_info[0];
+        m = s_info[1];
+        R = sh;
+        __syncthreads();
       }
-      if (tid == 0 && total < kr) report(P.ctrl, TRIA_ERR_INVALID_ARG, 0x80000000u | (uint32_t)sg);
-      __syncthreads();
-      prefix = (uint32_t)s_info[0];
-      kr = s_info[1];
-      const int in_bin = s_info[2];
-      __syncthreads();
-      if (pass < 2 && kr == in_bin) {
-        const uint32_t lo_key = prefix << (pass == 0 ? 21 : 10);
-        if (lo_key != 0u) {
-          T = lo_key - 1u;   // keep key > T, no ties taken
-          kr = 0;
-          cut = true;
-          break;
-        }
+      t_out = cur;
+      kr_out = m;
+    };
+    if (!over && above < k && k <= above + nband) {
+      const int m = k - above;
+      if (kl == kh) {
+        T = kh;
+        kr = m;
+      } else {
+        const int pbits = __clz((int)(kl ^ kh));   // the band's keys share the top pbits bits
+        radix(true, pbits == 0 ? 0u : (kh >> (32 - pbits)), 32 - pbits, m, T, kr);
       }
+    } else {
+      radix(false, 0u, 32, k, T, kr);
     }
-    if (!cut) T = prefix;
   }
 
   // keep list in one sweep over tiles of whole chunks: per tile each warp
