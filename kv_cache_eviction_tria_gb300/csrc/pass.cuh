@@ -1015,9 +1015,13 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
         continue;
       }
       if (sel == -2) break;
-      // no segment waits for selection: each warp moves at most one block
+      // no segment waits for selection: when a ready segment may still have
+      // blocks (thread 0 checks, so idle CTAs poll with one thread), each
+      // warp moves at most one block
+      if (tid == 0) s_sel = ld_acquire_u32(&P.ctrl->move_cursor) < ld_acquire_u32(&P.ctrl->ready_count) ? 1 : 0;
+      __syncthreads();
       int moved = 0;
-      if (mover) {
+      if (mover && s_sel) {
         int last_sg = -1;
         const MoveClaim m = pass_claim(P, n_active, last_sg);
         if (m.state == 0) {
@@ -1036,7 +1040,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
           if (tid == 0) report(P.ctrl, TRIA_ERR_TIMEOUT, 0xB0000001u);
           break;
         }
-        __nanosleep(idle < 64 ? 64 : 512);
+        __nanosleep(min(4096, 128 << min(idle, 5)));   // back off: idle CTAs poll rarely
       }
     }
     if (mover && lane == 0) bulk_wait_all();   // the stores of the service loop
