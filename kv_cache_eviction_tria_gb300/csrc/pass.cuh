@@ -49,9 +49,10 @@ constexpr int kPassScaleStage = kPassPieceBytes / 16;   // q8_0 block scales of 
 constexpr int kPassRing = kPassWarps * 2 * kPassPieceBytes;
 constexpr int kPassMaxSegs = kPassCtlSegs;   // layers x sequences x KV heads per call
 constexpr int kPassMaxLayers = 128;
-// A select keeps its radix histogram in the last 8 KB of the ring area (the
-// ring is free once scoring ends).
+// A select keeps its radix histogram in the last 8 KB of the ring area and up
+// to kPassSmemKeys z-max keys before it (the ring is free once scoring ends).
 constexpr int kPassHistOff = kPassRing - kHistBins * 4;
+constexpr int kPassSmemKeys = kPassHistOff / 4;
 
 // One layer of the call: its cache planes, live rows and statistics.
 struct LayerRef {
@@ -147,94 +148,26 @@ __device__ __forceinline__ void load_raw_g(const float* rp, float* x) {
   }
 }
 
-// ---------------------------------------------------------------------------
-// Selection of one segment by one CTA. Raw scores (and, for segments too long
-// to keep their keys in shared memory, the keys) stream through kSelStages
-// shared-memory stages filled by bulk async copies (TMA, non-tensor form),
-// so the CTA reads them at copy-engine rate instead of one load latency per
-// few rows. Layout of the ring area during a select:
-//   [keys: up to kSelSmemKeys x 4 B][stages: kSelStages x kSelStageBytes][histogram 8 KB]
-// ---------------------------------------------------------------------------
-
-constexpr int kSelStages = 3;
-constexpr int kSelStageBytes = 16384 + 16;   // a 16 KB window and the 16-byte alignment slack
-constexpr int kSelStageOff = kPassHistOff - kSelStages * kSelStageBytes;
-constexpr int kSelSmemKeys = 32768;          // segments up to this many rows keep their keys in shared memory
-constexpr int kSelSample = 2048;             // candidate keys sampled for the estimate of the cut
-constexpr int kSelBand = 1024;               // band keys a warp buffers
-static_assert(kSelSmemKeys * 4 <= kSelStageOff, "select shared-memory layout");
-static_assert(kSelSample * 4 <= kHistBins * 4, "the sample lives in the histogram area");
-static_assert(kPassWarps * kSelBand * 4 <= kSelStages * kSelStageBytes, "band buffers in the stage area");
-
-// mbarriers of the stages and how many times each has completed
-struct SelBars {
-  uint64_t bar[kSelStages];
-  uint32_t uses[kSelStages];
+// z-max keys: in shared memory (kSmem) or in the workspace
+template <bool kSmem>
+struct KeyStore {
+  uint32_t* p;
+  __device__ __forceinline__ uint32_t get(int r) const {
+    if constexpr (kSmem) return p[r];
+    else return __ldcg(p + r);
+  }
+  __device__ __forceinline__ void put(int r, uint32_t k) const {
+    if constexpr (kSmem) p[r] = k;
+    else __stcg(p + r, k);
+  }
 };
 
-// Streams the bytes [src, src + nbytes) of global memory (4-byte aligned)
-// through the stages in windows of 16 KB of the range: window w holds bytes
-// [16384 w, 16384 w + 16384) of the range, copied from the 16-byte boundary
-// at or below its start (so the stage holds up to 15 leading bytes more, and
-// the last window up to 15 bytes past the range, both inside the
-// workspace's rounded regions). consume(ptr, b0, b1) runs on the CTA's
-// threads for each window in order; ptr points at byte b0 of the range in
-// shared memory and [b0, b1) is the part of the range the window holds, so
-// windows start at multiples of 16 KB of the range (rows of raw scores and
-// 32-key chunks never straddle two). Returns false when a wait gave up
-// (TRIA_ERR_TIMEOUT recorded; the window's contents are then skipped).
-template <typename F>
-__device__ __forceinline__ bool sel_stream(const FPass& P, const uint8_t* src, int64_t nbytes, uint8_t* stages,
-                                           SelBars& sb, F&& consume) {
-  if (nbytes <= 0) return true;
-  const uintptr_t a = reinterpret_cast<uintptr_t>(src);
-  const int skip = (int)(a & 15u);
-  const int nwin = (int)((nbytes + 16383) / 16384);
-  auto issue = [&](int w) {                                // thread 0
-    const int st = w % kSelStages;
-    const int64_t off = (int64_t)w * 16384;
-    const int64_t len = min((int64_t)16384, nbytes - off);
-    const uint32_t bytes = (uint32_t)((skip + len + 15) & ~(int64_t)15);
-    // earlier generic accesses (reads of this stage, writes of the data by
-    // this CTA or, released to it, by others) before the async-proxy copy
-    asm volatile("fence.proxy.async;" ::: "memory");
-    mbar_arrive_expect_tx(&sb.bar[st], bytes);
-    bulk_g2s(stages + st * kSelStageBytes, reinterpret_cast<const uint8_t*>(a + off - skip), bytes, &sb.bar[st]);
-  };
-  if (threadIdx.x == 0)
-    for (int w = 0; w < min(kSelStages, nwin); ++w) issue(w);
-  bool ok = true;
-  for (int w = 0; w < nwin; ++w) {
-    const int st = w % kSelStages;
-    const uint32_t parity = (sb.uses[st] + (uint32_t)(w / kSelStages)) & 1u;
-    if (!mbar_wait_bounded(&sb.bar[st], parity, P.spin_limit)) {
-      if (threadIdx.x == 0) report(P.ctrl, TRIA_ERR_TIMEOUT, 0xD0000000u);
-      ok = false;
-    }
-    const int64_t off = (int64_t)w * 16384;
-    if (ok) consume(stages + st * kSelStageBytes + skip, off, min(nbytes, off + 16384));
-    __syncthreads();   // every thread is done with the window
-    if (threadIdx.x == 0 && ok && w + kSelStages < nwin) issue(w + kSelStages);
-  }
-  // each stage completed one phase per window it held (a wait that gave up
-  // leaves the copies it waited for in flight: after it the stages are not
-  // reused by this call)
-  __syncthreads();
-  if (threadIdx.x < kSelStages) {
-    const int st = threadIdx.x;
-    sb.uses[st] += (uint32_t)(nwin / kSelStages + (st < nwin % kSelStages ? 1 : 0));
-  }
-  __syncthreads();
-  return ok;
-}
-
 // Selection of one segment by the whole CTA: segment moments from its nr
-// score-run partials; z-max keys of every live row and the first radix
-// histogram in one streamed sweep of the raw scores; up to two more radix
-// passes; one tiled sweep that writes the keep list (B entries) and the
-// kept-row prefix of every chunk. Publishes the segment in the ready list.
+// score-run partials, z-max keys and the first radix histogram in one sweep,
+// up to two more radix passes, then the keep list (B entries) and the
+// kept-row prefix of every chunk; publishes the segment in the ready list.
 template <int G, bool kSmem>
-__device__ __noinline__ void pass_select(const FPass& P, int sg, int nr, uint8_t* ring, SelBars& sb) {
+__device__ __noinline__ void pass_select(const FPass& P, int sg, int nr, uint32_t* smem_keys, uint32_t* hist) {
   __shared__ int s_info[4];
   __shared__ int s_sbuf[40];
   __shared__ int s_wt[kPassWarps], s_wk[kPassWarps];
@@ -242,278 +175,197 @@ __device__ __noinline__ void pass_select(const FPass& P, int sg, int nr, uint8_t
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n = v.n, lo = v.sink, hi = n - P.window;
   const int k = v.B - v.sink - P.window;
-  uint32_t* skeys = reinterpret_cast<uint32_t*>(ring);                  // kSmem
-  uint32_t* gkeys = P.keys + v.wrow0;                                    // !kSmem
-  uint8_t* stages = ring + kSelStageOff;
-  uint32_t* hist = reinterpret_cast<uint32_t*>(ring + kPassHistOff);
+  const KeyStore<kSmem> keys{kSmem ? smem_keys : P.keys + v.wrow0};
+  constexpr int UB = kSmem ? 1 : 8;   // key loads in flight per thread (global keys)
 
   float mu[G], inv[G];
   block_moments_of_runs<G>(P.parts + (size_t)sg * kRunCols * P.cs_max, P.cs_max, nr, mu, inv);
-  // a sample of the candidates' keys (every stride-th candidate) in the
-  // histogram area, for the estimate of the cut
-  const int ncand = hi - lo;
-  const int stride = max(1, (ncand + kSelSample - 1) / kSelSample);
-  const int ns = k > 0 ? (ncand + stride - 1) / stride : 0;
-  uint32_t* sample = hist;
+  for (int i = tid; i < kHistBins; i += blockDim.x) hist[i] = 0u;
   __syncthreads();
 
-  // z-max keys of every live row, and the sample
+  // z-max keys of every live row and the first radix histogram of the
+  // candidates [lo, hi); loads of U rows per thread are in flight together
   {
+    constexpr int U = G > 4 ? 4 : 8;
+    const float* raw = P.raw + (size_t)v.wrow0 * G;
     float* so = P.score_out ? P.score_out + v.wrow0 : nullptr;
-    sel_stream(P, reinterpret_cast<const uint8_t*>(P.raw + (size_t)v.wrow0 * G), (int64_t)n * G * 4, stages, sb,
-               [&](const uint8_t* w, int64_t b0, int64_t b1) {
-                 const int r0 = (int)(b0 / (G * 4)), r1 = (int)(b1 / (G * 4));
-                 const float* x = reinterpret_cast<const float*>(w);
-                 for (int r = r0 + tid; r < r1; r += kPassThreads) {
-                   const float* rp = x + (size_t)(r - r0) * G;
-                   float s = (rp[0] - mu[0]) * inv[0];
+    for (int base = tid; base < n; base += U * kPassThreads) {
+      float x[U][G];
 #pragma unroll
-                   for (int h = 1; h < G; ++h) s = fmaxf(s, (rp[h] - mu[h]) * inv[h]);
-                   const uint32_t key = score_key(s);
-                   if constexpr (kSmem) skeys[r] = key;
-                   else __stcg(gkeys + r, key);
-                   if (so) so[r] = s;
-                   if (k > 0 && r >= lo && r < hi) {
-                     const int c = r - lo, q = c / stride;
-                     if (c == q * stride) sample[q] = key;
-                   }
-                 }
-               });
-    if constexpr (!kSmem) asm volatile("fence.proxy.async.global;" ::: "memory");   // keys before their bulk reads
+      for (int u = 0; u < U; ++u) {
+        const int r = base + u * kPassThreads;
+        if (r < n) load_raw_g<G>(raw + (size_t)r * G, x[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int r = base + u * kPassThreads;
+        if (r < n) {
+          float s = (x[u][0] - mu[0]) * inv[0];
+#pragma unroll
+          for (int h = 1; h < G; ++h) s = fmaxf(s, (x[u][h] - mu[h]) * inv[h]);
+          const uint32_t key = score_key(s);
+          keys.put(r, key);
+          if (so) so[r] = s;
+          if (k > 0 && r >= lo && r < hi) atomicAdd(&hist[key >> 21], 1u);
+        }
+      }
+    }
   }
   __syncthreads();
 
-  // keys of rows [r0, r1) of the candidates: from shared memory, or streamed
-  // (consume(keys, r0, r1): keys[i] is the key of row r0 + i)
-  auto for_keys = [&](int a, int b, auto&& consume) {
-    if (a >= b) return;
-    if constexpr (kSmem) {
-      consume(skeys + a, a, b);
-      __syncthreads();
-    } else {
-      sel_stream(P, reinterpret_cast<const uint8_t*>(gkeys + a), (int64_t)(b - a) * 4, stages, sb,
-                 [&](const uint8_t* w, int64_t b0, int64_t b1) {
-                   consume(reinterpret_cast<const uint32_t*>(w), a + (int)(b0 / 4), a + (int)(b1 / 4));
-                 });
-    }
-  };
-
-  // The k-th largest candidate key T and kr = how many candidates with key
-  // == T are kept (lowest rows first). First from the sample: its quantiles
-  // around the cut's expected rank bound a band [kl, kh] of keys; one pass
-  // counts the candidates above kh (ballots, no atomics) and gathers the
-  // band's keys into per-warp buffers; the cut is then found in the band by a
-  // radix select on the bits below the band's common prefix (well spread, so
-  // its histogram atomics rarely collide). When the band misses the cut or
-  // overflows its buffers, a radix select over all candidates (11 + 11 + 10
-  // bits) finds it instead. Exact either way.
+  // radix select of the k-th largest key over the candidates: T = that key,
+  // kr = how many candidates with key == T are kept (lowest rows first); a
+  // bin holding exactly the keys still to take ends the search early
   uint32_t T = 0xFFFFFFFFu;
   int kr = 0;
   if (k > 0) {
-    // sort the sample descending (bitonic, padded with the lowest key)
-    int np = 1;
-    while (np < ns) np <<= 1;
-    for (int i = ns + tid; i < np; i += blockDim.x) sample[i] = 0u;
-    __syncthreads();
-    for (int size = 2; size <= np; size <<= 1)
-      for (int st = size >> 1; st > 0; st >>= 1) {
-        for (int i = tid; i < (np >> 1); i += blockDim.x) {
-          const int a = 2 * st * (i / st) + (i % st), b = a + st;
-          const bool desc = (a & size) == 0;
-          const uint32_t x = sample[a], y = sample[b];
-          if ((x < y) == desc) {
-            sample[a] = y;
-            sample[b] = x;
+    uint32_t prefix = 0;
+    kr = k;
+    bool cut = false;
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+      const int NB = pass == 2 ? 1024 : 2048;
+      if (pass > 0) {
+        for (int i = tid; i < NB; i += blockDim.x) hist[i] = 0u;
+        __syncthreads();
+        for (int base = lo + tid; base < hi; base += UB * kPassThreads) {
+          uint32_t kk[UB];
+#pragma unroll
+          for (int u = 0; u < UB; ++u) {
+            const int r = base + u * kPassThreads;
+            kk[u] = r < hi ? keys.get(r) : 0u;
+          }
+#pragma unroll
+          for (int u = 0; u < UB; ++u) {
+            if (base + u * kPassThreads >= hi) break;
+            const uint32_t key = kk[u];
+            if (pass == 1) {
+              if ((key >> 21) == prefix) atomicAdd(&hist[(key >> 10) & 0x7FFu], 1u);
+            } else if ((key >> 10) == prefix) {
+              atomicAdd(&hist[key & 0x3FFu], 1u);
+            }
           }
         }
         __syncthreads();
       }
-    // the band: sample ranks q -+ 4 sigma (+4), q = the cut's expected rank
-    const double pk = (double)k / ncand;
-    const int q = (int)(pk * ns + 0.5);
-    const int ms = (int)(4.0 * sqrt((double)ns * pk * (1.0 - pk))) + 4;
-    const uint32_t kh = q - ms >= 1 ? sample[q - ms - 1] : 0xFFFFFFFFu;
-    const uint32_t kl = q + ms <= ns ? sample[q + ms - 1] : 0u;
-    __syncthreads();   // the sample area becomes the histogram
-    uint32_t* band = kSmem ? reinterpret_cast<uint32_t*>(stages) : skeys;   // kPassWarps x kSelBand keys
-    uint32_t* wb = band + warp * kSelBand;
-    int nb = 0, na = 0;   // this warp's band keys and keys above kh
-    for_keys(lo, hi, [&](const uint32_t* kk, int r0, int r1) {
-      for (int i0 = warp * 32; i0 < r1 - r0; i0 += kPassThreads) {
-        const int i = i0 + lane;
-        const uint32_t key = i < r1 - r0 ? kk[i] : 0u;
-        const bool valid = i < r1 - r0;
-        na += __popc(__ballot_sync(0xffffffffu, valid && key > kh));
-        const bool inb = valid && key >= kl && key <= kh;
-        const uint32_t bb = __ballot_sync(0xffffffffu, inb);
-        const int at = nb + __popc(bb & ((1u << lane) - 1u));
-        if (inb && at < kSelBand) wb[at] = key;
-        nb += __popc(bb);
+      // thread t scans bins NB-1-per*t .. NB-per*(t+1) (descending)
+      const int per = (NB + kPassThreads - 1) / kPassThreads;
+      uint32_t cnt[6];
+      int local = 0;
+#pragma unroll
+      for (int j = 0; j < 6; ++j) {
+        const int b = NB - 1 - (per * tid + j);
+        cnt[j] = (j < per && b >= 0) ? hist[b] : 0u;
+        local += (int)cnt[j];
       }
-    });
-    if (lane == 0) {
-      s_wt[warp] = nb;
-      s_wk[warp] = na;
-    }
-    __syncthreads();
-    int above = 0, nband = 0;
-    bool over = false;
-    for (int w = 0; w < kPassWarps; ++w) {
-      above += s_wk[w];
-      nband += s_wt[w];
-      over = over || s_wt[w] > kSelBand;
-    }
-    // radix select over one population: the band's keys (band) or all
-    // candidates; m-th largest within keys that share `cur` on bits above R
-    auto radix = [&](bool use_band, uint32_t cur, int R, int m, uint32_t& t_out, int& kr_out) {
-      while (R > 0) {
-        const int d = min(11, R), sh = R - d;
-        const uint32_t mask = (1u << d) - 1u;
-        for (int i = tid; i < kHistBins; i += blockDim.x) hist[i] = 0u;
-        __syncthreads();
-        auto add = [&](uint32_t key) {
-          if ((uint32_t)((uint64_t)key >> (sh + d)) == cur) atomicAdd(&hist[(key >> sh) & mask], 1u);
-        };
-        if (use_band) {
-          for (int w = 0; w < kPassWarps; ++w)
-            for (int i = tid; i < s_wt[w]; i += blockDim.x) add(band[w * kSelBand + i]);
-        } else {
-          for_keys(lo, hi, [&](const uint32_t* kk, int r0, int r1) {
-            for (int i = tid; i < r1 - r0; i += kPassThreads) add(kk[i]);
-          });
-        }
-        __syncthreads();
-        // the bin of the m-th largest: thread t scans bins NB-1-per*t .. (descending)
-        const int NB = 1 << d;
-        const int per = (NB + kPassThreads - 1) / kPassThreads;
-        uint32_t cnt[6];
-        int local = 0;
+      int total;
+      const int before = block_exclusive_scan(local, &total, s_sbuf);
+      if (before < kr && kr <= before + local) {
+        int cum = before;
 #pragma unroll
         for (int j = 0; j < 6; ++j) {
           const int b = NB - 1 - (per * tid + j);
-          cnt[j] = (j < per && b >= 0) ? hist[b] : 0u;
-          local += (int)cnt[j];
-        }
-        int total;
-        const int before = block_exclusive_scan(local, &total, s_sbuf);
-        if (before < m && m <= before + local) {
-          int cum = before;
-#pragma unroll
-          for (int j = 0; j < 6; ++j) {
-            const int b = NB - 1 - (per * tid + j);
-            if (j >= per || b < 0) break;
-            if (cum + (int)cnt[j] >= m) {
-              s_info[0] = b;
-              s_info[1] = m - cum;
-              break;
-            }
-            cum += (int)cnt[j];
+          if (j >= per || b < 0) break;
+          if (cum + (int)cnt[j] >= kr) {
+            s_info[0] = (int)(pass == 0 ? (uint32_t)b : pass == 1 ? ((prefix << 11) | (uint32_t)b)
+                                                                   : ((prefix << 10) | (uint32_t)b));
+            s_info[1] = kr - cum;
+            s_info[2] = (int)cnt[j];
+            break;
           }
+          cum += (int)cnt[j];
         }
-        if (tid == 0 && total < m) report(P.ctrl, TRIA_ERR_INVALID_ARG, 0x80000000u | (uint32_t)sg);
-        __syncthreads();
-        cur = (cur << d) | (uint32_t)s_info[0];
-        m = s_info[1];
-        R = sh;
-        __syncthreads();
       }
-      t_out = cur;
-      kr_out = m;
-    };
-    if (!over && above < k && k <= above + nband) {
-      const int m = k - above;
-      if (kl == kh) {
-        T = kh;
-        kr = m;
-      } else {
-        const int pbits = __clz((int)(kl ^ kh));   // the band's keys share the top pbits bits
-        radix(true, pbits == 0 ? 0u : (kh >> (32 - pbits)), 32 - pbits, m, T, kr);
+      if (tid == 0 && total < kr) report(P.ctrl, TRIA_ERR_INVALID_ARG, 0x80000000u | (uint32_t)sg);
+      __syncthreads();
+      prefix = (uint32_t)s_info[0];
+      kr = s_info[1];
+      const int in_bin = s_info[2];
+      __syncthreads();
+      if (pass < 2 && kr == in_bin) {
+        const uint32_t lo_key = prefix << (pass == 0 ? 21 : 10);
+        if (lo_key != 0u) {
+          T = lo_key - 1u;   // keep key > T, no ties taken
+          kr = 0;
+          cut = true;
+          break;
+        }
       }
-    } else {
-      radix(false, 0u, 32, k, T, kr);
     }
+    if (!cut) T = prefix;
   }
 
-  // keep list in one sweep over tiles of whole chunks: per tile each warp
-  // counts the ties and strict keeps of its chunks, a scan over the warps
-  // (and the running totals of earlier tiles) places them, then each warp
-  // writes its kept rows and chunk prefixes (ties at T kept lowest rows first)
-  int32_t* keep = P.keep + v.wrow0;
-  int* pre = P.prefix + (size_t)sg * (P.c_max + 1);
+  // keep list: warps take contiguous chunk ranges; sweep 1 counts each warp's
+  // ties and strict keeps, sweep 2 writes the kept rows and chunk prefixes
   const int nch = (n + kChunk - 1) / kChunk;
-  int tie_run = 0, keep_run = 0;   // CTA-uniform
-  constexpr int U = 11;            // chunks per warp per tile (at most)
-  auto tile = [&](const uint32_t* kk, int t_r0, int c_beg, int c_end) {
-    // this warp's chunks of the tile: [cw0, cw1)
-    const int per_w = (c_end - c_beg + kPassWarps - 1) / kPassWarps;
-    const int cw0 = min(c_end, c_beg + warp * per_w), cw1 = min(c_end, cw0 + per_w);
-    uint32_t bt[U], bs[U];
-    int wt = 0, ws = 0;
+  const int cpw = (nch + kPassWarps - 1) / kPassWarps;
+  const int c0 = min(nch, warp * cpw), c1 = min(nch, c0 + cpw);
+  constexpr int CB = kSmem ? 1 : 8;   // chunks whose keys load together (global keys)
+  {
+    int wt = 0, wk = 0;
+    for (int cb = c0; cb < c1; cb += CB) {
+      uint32_t kk[CB];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      bt[u] = bs[u] = 0u;
-      const int c = cw0 + u;
-      if (c < cw1) {
-        const int r = c * kChunk + lane;
+      for (int u = 0; u < CB; ++u) {
+        const int r = (cb + u) * kChunk + lane;
+        kk[u] = (cb + u < c1 && r < n && r >= lo && r < hi && k > 0) ? keys.get(r) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < CB; ++u) {
+        if (cb + u >= c1) break;
+        const int r = (cb + u) * kChunk + lane;
         const bool in = r < n;
         const bool pr = in && (r < lo || r >= hi);
         const bool cand = in && !pr && k > 0;
-        const uint32_t key = cand ? kk[r - t_r0] : 0u;
-        bt[u] = __ballot_sync(0xffffffffu, cand && key == T);
-        bs[u] = __ballot_sync(0xffffffffu, pr || (cand && key > T));
-        wt += __popc(bt[u]);
-        ws += __popc(bs[u]);
+        wt += __popc(__ballot_sync(0xffffffffu, cand && kk[u] == T));
+        wk += __popc(__ballot_sync(0xffffffffu, pr || (cand && kk[u] > T)));
       }
     }
     if (lane == 0) {
       s_wt[warp] = wt;
-      s_wk[warp] = ws;
+      s_wk[warp] = wk;
     }
-    __syncthreads();
-    int t_run = tie_run, k_run = keep_run;
-    for (int w = 0; w < warp; ++w) {
-      k_run += s_wk[w] + max(0, min(s_wt[w], kr - t_run));
-      t_run += s_wt[w];
+  }
+  __syncthreads();
+  int tie_run = 0, keep_run = 0;
+  for (int w = 0; w < warp; ++w) {
+    keep_run += s_wk[w] + max(0, min(s_wt[w], kr - tie_run));
+    tie_run += s_wt[w];
+  }
+  int32_t* keep = P.keep + v.wrow0;
+  int* pre = P.prefix + (size_t)sg * (P.c_max + 1);
+  for (int cb = c0; cb < c1; cb += CB) {
+    uint32_t kk[CB];
+#pragma unroll
+    for (int u = 0; u < CB; ++u) {
+      const int r = (cb + u) * kChunk + lane;
+      kk[u] = (cb + u < c1 && r < n && r >= lo && r < hi && k > 0) ? keys.get(r) : 0u;
     }
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int c = cw0 + u;
-      if (c < cw1) {
-        const int r = c * kChunk + lane;
-        const uint32_t lt = (1u << lane) - 1u;
-        const bool is_tie = (bt[u] >> lane) & 1u;
-        const int trank = t_run + __popc(bt[u] & lt);
-        const bool kp = ((bs[u] >> lane) & 1u) || (is_tie && trank < kr);
-        const uint32_t bk = __ballot_sync(0xffffffffu, kp);
-        if (lane == 0) pre[c] = k_run;
-        if (kp) keep[k_run + __popc(bk & lt)] = r;
-        t_run += __popc(bt[u]);
-        k_run += __popc(bk);
-      }
+    for (int u = 0; u < CB; ++u) {
+      const int ci = cb + u;
+      if (ci >= c1) break;
+      const int r = ci * kChunk + lane;
+      const bool in = r < n;
+      const bool pr = in && (r < lo || r >= hi);
+      const bool cand = in && !pr && k > 0;
+      const bool is_tie = cand && kk[u] == T;
+      const uint32_t bt = __ballot_sync(0xffffffffu, is_tie);
+      const int trank = tie_run + __popc(bt & ((1u << lane) - 1u));
+      const bool kp = pr || (cand && kk[u] > T) || (is_tie && trank < kr);
+      const uint32_t bk = __ballot_sync(0xffffffffu, kp);
+      if (lane == 0) pre[ci] = keep_run;
+      if (kp) keep[keep_run + __popc(bk & ((1u << lane) - 1u))] = r;
+      tie_run += __popc(bt);
+      keep_run += __popc(bk);
     }
-    // running totals after the tile (every thread, from the warp counts)
-    for (int w = 0; w < kPassWarps; ++w) {
-      keep_run += s_wk[w] + max(0, min(s_wt[w], kr - tie_run));
-      tie_run += s_wt[w];
-    }
-    __syncthreads();   // s_wt / s_wk are rewritten by the next tile
-  };
-  if constexpr (kSmem) {
-    constexpr int kTile = kPassWarps * 4;   // 4 chunks per warp per tile
-    for (int c = 0; c < nch; c += kTile) tile(skeys, 0, c, min(nch, c + kTile));
-  } else {
-    // windows of 4096 keys = 128 chunks, streamed; the window of chunk-aligned
-    // rows [32 c, 32 c + 4096) (key rows outside [lo, hi) are not read)
-    sel_stream(P, reinterpret_cast<const uint8_t*>(gkeys), (int64_t)n * 4, stages, sb,
-               [&](const uint8_t* w, int64_t b0, int64_t b1) {
-                 const int r0 = (int)(b0 / 4), r1 = (int)(b1 / 4);
-                 // r0 is a multiple of 4096 unless the window is the first one
-                 tile(reinterpret_cast<const uint32_t*>(w), r0, r0 / kChunk, (r1 + kChunk - 1) / kChunk);
-               });
   }
-  if (tid == 0) {
+  if (warp == kPassWarps - 1 && lane == 0) {
     pre[nch] = v.B;
     if (keep_run != v.B) report(P.ctrl, TRIA_ERR_INVALID_ARG, 0x20000000u | (uint32_t)sg);
+  }
+  __syncthreads();
+  if (tid == 0) {
     __threadfence();
     const uint32_t slot = atomicAdd(&P.ctrl->ready_count, 1u);
     st_release_u32(reinterpret_cast<uint32_t*>(P.ctl->ready + slot), (uint32_t)(sg + 1));
@@ -800,7 +652,6 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
   __shared__ int s_active, s_sel, s_last;
   __shared__ uint32_t s_epoch;
   __shared__ int s_src[kPassWarps][kChunk];   // per warp: a block's source rows, then positions
-  __shared__ __align__(8) SelBars s_selbars;
   __shared__ int s_sbuf[40];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -809,6 +660,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + PassSmem::kBars) + warp * 2;
   int* seg_first = reinterpret_cast<int*>(smem + PassSmem::kFirst);   // first piece of every segment
   unsigned long long* s_turns = reinterpret_cast<unsigned long long*>(smem + PassSmem::kTurns);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem + PassSmem::kRing + kPassHistOff);   // service phase only
 
   // ---- prologue: piece table (pieces of the active segments, in segment
   // order), active segments, turn factors, ring barriers
@@ -853,11 +705,6 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
   if (lane == 0) {
     mbar_init(&bars[0], 1);
     mbar_init(&bars[1], 1);
-    if (warp == 0)
-      for (int i = 0; i < kSelStages; ++i) {
-        mbar_init(&s_selbars.bar[i], 1);
-        s_selbars.uses[i] = 0u;
-      }
     fence_mbar_init();
   }
   __syncthreads();
@@ -1008,10 +855,10 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
         idle = 0;
         __threadfence();
         const int nr = segment_runs(seg_first[sel], seg_first[sel + 1], per);
-        if (pass_seg(P, sel).n <= kSelSmemKeys)
-          pass_select<G, true>(P, sel, nr, smem + PassSmem::kRing, s_selbars);
+        if (pass_seg(P, sel).n <= kPassSmemKeys)
+          pass_select<G, true>(P, sel, nr, reinterpret_cast<uint32_t*>(smem + PassSmem::kRing), hist);
         else
-          pass_select<G, false>(P, sel, nr, smem + PassSmem::kRing, s_selbars);
+          pass_select<G, false>(P, sel, nr, nullptr, hist);
         continue;
       }
       if (sel == -2) break;
