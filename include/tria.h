@@ -232,9 +232,10 @@ tria_status tria_compact(const tria_layer_cache* cache, const tria_policy* polic
                          const int32_t* keep, void* ws, size_t ws_bytes, void* stream);
 
 /* The whole pass (steps 1-3) for one layer and all sequences of the call.
- * fp16 or q8_0 keys with head_dim 64 or 128 (any group) or 256 (group <= 4)
- * run as one fused persistent kernel (see tria_evict_model); other shapes run
- * the three staged kernels of tria_evict_staged. Same results either way. */
+ * Calls of at least 128 segments (n_seqs x n_kv_heads) with fp16 or q8_0
+ * keys and head_dim 64 or 128 (any group) or 256 (group <= 4) run as one
+ * fused persistent kernel (see tria_evict_model); the others run the three
+ * staged kernels of tria_evict_staged. Same results either way. */
 tria_status tria_evict(const tria_stats* stats, int32_t layer, const tria_layer_cache* cache,
                        const tria_policy* policy, void* ws, size_t ws_bytes, void* stream);
 
@@ -256,11 +257,12 @@ size_t tria_model_workspace_size(const tria_layer_cache* cache, int32_t n_layers
  * with its own planes and its own n_live array (device, updated in place).
  * Every layer must be loaded with the first layer's RoPE frequencies
  * (TRIA_ERR_UNSUPPORTED otherwise) and appear once. One policy for all
- * layers. Shapes of the fused kernel (see tria_evict) with at most 2048
- * segments (n_layers x n_seqs x n_kv_heads) run as ONE persistent kernel for
- * all layers: score items stream the keys, the CTA that scores a segment's
- * last rows selects it at once, and the segment's rows move while other
- * segments are still scored; other shapes run tria_evict_staged per layer.
+ * layers. Shapes of the fused kernel (see tria_evict) with 128 to 2048
+ * segments (n_layers x n_seqs x n_kv_heads; any count from 1 when score_out is
+ * given) run as ONE persistent kernel for all layers: every warp streams a
+ * run of the keys, each scored segment is selected by one CTA as soon as its
+ * warps finish, and the rows move once segments are selected; other calls run
+ * tria_evict_staged per layer.
  * score_out (device float, optional): the z-max score s(r) of every live row
  * of every compacted segment, at score_out[i * layer_rows + row] for layer
  * i of the call (layer_rows = max over s of seq_row0[s] + n_kv_heads *

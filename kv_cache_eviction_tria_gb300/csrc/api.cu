@@ -253,6 +253,16 @@ bool fused_ok(const tria_layer_cache* c, int G, int n_layers) {
          (int64_t)n_layers * c->n_seqs * c->n_kv_heads <= kPassMaxSegs;
 }
 
+// The fused kernel pays the staged path's ramps and launch gaps once, but
+// selects each segment on one CTA; measured on GB300 it is ahead once a call
+// has enough segments to spread the selections over the grid (36 Qwen3-8B
+// layers: 0.47 ms against 1.44 ms), and behind for a few long segments (one
+// Qwen3-8B layer of 8 x 32768 rows: 111 us against 62 us).
+constexpr int kFusedMinSegs = 128;
+bool fused_preferred(const tria_layer_cache* c, int G, int n_layers) {
+  return fused_ok(c, G, n_layers) && (int64_t)n_layers * c->n_seqs * c->n_kv_heads >= kFusedMinSegs;
+}
+
 }  // namespace
 
 namespace tria {
@@ -521,7 +531,7 @@ extern "C" tria_status tria_evict(const tria_stats* stats, int32_t layer, const 
   const Layout L = make_layout(cache, stats->group);
   if ((r = check_ws(ws, ws_bytes, L)) != TRIA_OK) return r;
   cudaStream_t st = (cudaStream_t)stream;
-  if (fused_ok(cache, stats->group, 1))
+  if (fused_preferred(cache, stats->group, 1))
     return launch_fused(stats, &layer, 1, cache, policy, budget, L, ws, nullptr, st);
   return evict_staged(stats, layer, cache, policy, budget, L, ws, st);
 }
@@ -586,7 +596,7 @@ extern "C" tria_status tria_evict_model(const tria_stats* stats, const int32_t* 
   if ((r = check_policy(caches, policy, true, budget)) != TRIA_OK) return r;
   if (score_out && ((uintptr_t)score_out % 4) != 0) return TRIA_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
-  if (fused_ok(caches, stats->group, n_layers)) {
+  if (fused_ok(caches, stats->group, n_layers) && (score_out || fused_preferred(caches, stats->group, n_layers))) {
     const Layout L = make_model_layout(caches, stats->group, n_layers);
     if ((r = check_ws(ws, ws_bytes, L)) != TRIA_OK) return r;
     return launch_fused(stats, layers, n_layers, caches, policy, budget, L, ws, score_out, st);
