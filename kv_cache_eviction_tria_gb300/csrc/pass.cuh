@@ -176,7 +176,7 @@ __device__ __noinline__ void pass_select(const FPass& P, int sg, int nr, uint32_
   const int n = v.n, lo = v.sink, hi = n - P.window;
   const int k = v.B - v.sink - P.window;
   const KeyStore<kSmem> keys{kSmem ? smem_keys : P.keys + v.wrow0};
-  constexpr int UB = kSmem ? 1 : 8;   // key loads in flight per thread (global keys)
+  constexpr int UB = kSmem ? 1 : 16;   // key loads in flight per thread (global keys)
 
   float mu[G], inv[G];
   block_moments_of_runs<G>(P.parts + (size_t)sg * kRunCols * P.cs_max, P.cs_max, nr, mu, inv);
@@ -186,7 +186,7 @@ __device__ __noinline__ void pass_select(const FPass& P, int sg, int nr, uint32_
   // z-max keys of every live row and the first radix histogram of the
   // candidates [lo, hi); loads of U rows per thread are in flight together
   {
-    constexpr int U = G > 4 ? 4 : 8;
+    constexpr int U = G > 4 ? 8 : 16;   // raw rows in flight per thread
     const float* raw = P.raw + (size_t)v.wrow0 * G;
     float* so = P.score_out ? P.score_out + v.wrow0 : nullptr;
     for (int base = tid; base < n; base += U * kPassThreads) {
@@ -300,7 +300,7 @@ __device__ __noinline__ void pass_select(const FPass& P, int sg, int nr, uint32_
   const int nch = (n + kChunk - 1) / kChunk;
   const int cpw = (nch + kPassWarps - 1) / kPassWarps;
   const int c0 = min(nch, warp * cpw), c1 = min(nch, c0 + cpw);
-  constexpr int CB = kSmem ? 1 : 8;   // chunks whose keys load together (global keys)
+  constexpr int CB = kSmem ? 1 : 16;   // chunks whose keys load together (global keys)
   {
     int wt = 0, wk = 0;
     for (int cb = c0; cb < c1; cb += CB) {
