@@ -186,7 +186,7 @@ __device__ __noinline__ void pass_select(const FPass& P, int sg, int nr, uint32_
   // z-max keys of every live row and the first radix histogram of the
   // candidates [lo, hi); loads of U rows per thread are in flight together
   {
-    constexpr int U = G >= 4 ? 8 : 16;   // raw rows in flight per thread
+    constexpr int U = G > 4 ? 4 : (G == 4 ? 8 : 16);   // raw rows in flight per thread
     const float* raw = P.raw + (size_t)v.wrow0 * G;
     float* so = P.score_out ? P.score_out + v.wrow0 : nullptr;
     for (int base = tid; base < n; base += U * kPassThreads) {
