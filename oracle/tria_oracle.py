@@ -35,6 +35,16 @@ Readings where the pages are silent:
   with M = q_abs - |qbar|: "MLR" read as the mean resultant length
   R_f = |qbar_f| / q_abs_f, the norm term weighted by (1 - R_f) q_abs_f.
   D (future query offsets) is a load-time parameter; default {1, 2, 4, ..., 2^16}.
+* Non-rotary (content) dims ([Doc] §4 gate line field ``nonrot=``, §6 "Non-
+  rotary models": such models carry a content term besides the RoPE-direction
+  term; the pages give no formula). Reading: the first rot = hd - nonrot_dim
+  dims are rotary, NEOX-paired as (f, f + rot/2) with omega_f =
+  theta ** (-2 f / rot); the last nonrot_dim dims are never rotated, so their
+  share of a future query's logit does not depend on the position and its
+  mean over the queries is the mean non-rotary query qn_h (calibrated like
+  q_mean) dotted with the key's non-rotary dims:
+      raw_h(r) += sum_e qn_{h,e} K[r][rot + e]
+  with no offset average, no phase and no norm term.
 * z-normalisation: population mean/std over all n live rows of the segment,
   z = (raw - mu) / (sigma + 1e-6); KV-head score s = max over its query heads.
 * Budget B = floor(budget_frac * n_ctx) survivors in total, sink and window
@@ -70,11 +80,12 @@ class BudgetError(ValueError):
 # RoPE frequencies, future offsets, calibration weights
 # ---------------------------------------------------------------------------
 
-def rope_omega(head_dim: int, theta: float) -> np.ndarray:
-    """omega_f = theta^(-2f/hd), f = 0 .. hd/2 - 1 (NEOX pairs; [Doc] At a glance,
-    Phase C "calibration omega")."""
-    fc = head_dim // 2
-    return np.array([theta ** (-2.0 * f / head_dim) for f in range(fc)], dtype=np.float64)
+def rope_omega(head_dim: int, theta: float, nonrot_dim: int = 0) -> np.ndarray:
+    """omega_f = theta^(-2f/rot), f = 0 .. rot/2 - 1, rot = head_dim - nonrot_dim
+    the rotary dims (NEOX pairs; [Doc] At a glance, Phase C "calibration omega";
+    §4 gate line ``nonrot=``: dims past the rotary ones are never rotated)."""
+    rot = head_dim - nonrot_dim
+    return np.array([theta ** (-2.0 * f / rot) for f in range(rot // 2)], dtype=np.float64)
 
 
 def default_future_offsets() -> np.ndarray:
@@ -131,18 +142,22 @@ def keys_f64(k: np.ndarray, k_scale: np.ndarray | None = None) -> np.ndarray:
 # ---------------------------------------------------------------------------
 
 def raw_scores(k_rot: np.ndarray, q_mean_c: np.ndarray, m_weight: np.ndarray,
-               omega: np.ndarray, p: int, offsets) -> np.ndarray:
+               omega: np.ndarray, p: int, offsets, q_nonrot: np.ndarray | None = None) -> np.ndarray:
     """raw[r, j] for rows r of one segment and the segment's query heads j.
 
-    ``k_rot`` float64 [n, hd] stored (already rotated) keys; ``q_mean_c``
-    complex [G, fc]; ``m_weight`` [G, fc]; ``p`` absolute decode position
-    ([Worklog] 2026-04-18: phases from the absolute position, not the row count).
+    ``k_rot`` float64 [n, hd] stored keys (rotary dims already rotated);
+    ``omega`` the rot/2 frequencies of the rotary dims [0, rot) (rot = hd when
+    every dim is rotary); ``q_mean_c`` complex [G, rot/2]; ``m_weight``
+    [G, rot/2]; ``q_nonrot`` [G, hd - rot] the mean non-rotary query, None for
+    no content term; ``p`` absolute decode position ([Worklog] 2026-04-18:
+    phases from the absolute position, not the row count).
     Loops over the offsets literally; each offset is one complex matmul.
     """
     k_rot = np.asarray(k_rot, dtype=np.float64)
     n, hd = k_rot.shape
-    fc = hd // 2
-    kc = k_rot[:, :fc] + 1j * k_rot[:, fc:]
+    fc = len(omega)
+    rot = 2 * fc
+    kc = k_rot[:, :fc] + 1j * k_rot[:, fc:rot]
     g = q_mean_c.shape[0]
     trig = np.zeros((n, g), dtype=np.float64)
     offsets = list(offsets)
@@ -153,7 +168,12 @@ def raw_scores(k_rot: np.ndarray, q_mean_c: np.ndarray, m_weight: np.ndarray,
         trig += np.real(np.conj(kc) @ q_rot.T)              # sum_f Re(q_rot conj(k))
     trig /= len(offsets)
     norm = np.abs(kc) @ np.asarray(m_weight, dtype=np.float64).T   # sum_f M |k_f|
-    return trig + norm
+    if q_nonrot is None or rot == hd:
+        return trig + norm
+    # non-rotary dims: no rotation at any position, so every future query's
+    # mean logit there is the mean query's plain dot product with the key
+    content = k_rot[:, rot:] @ np.asarray(q_nonrot, dtype=np.float64).T
+    return trig + norm + content
 
 
 def znorm(raw: np.ndarray) -> np.ndarray:
@@ -168,9 +188,9 @@ def gqa_max(z: np.ndarray) -> np.ndarray:
     return z.max(axis=1)
 
 
-def segment_scores(k_rot, q_mean_c, m_weight, omega, p, offsets):
+def segment_scores(k_rot, q_mean_c, m_weight, omega, p, offsets, q_nonrot=None):
     """(raw [n, G], s [n]) of one segment."""
-    raw = raw_scores(k_rot, q_mean_c, m_weight, omega, p, offsets)
+    raw = raw_scores(k_rot, q_mean_c, m_weight, omega, p, offsets, q_nonrot)
     return raw, gqa_max(znorm(raw))
 
 
@@ -221,7 +241,7 @@ def compact_rows(plane: np.ndarray, keep: np.ndarray) -> np.ndarray:
 def evict_layer(layer_cache: dict, q_mean: np.ndarray, q_abs, *, layer: int, n_kv_heads: int,
                 head_dim: int, rope_theta: float, cur_pos, n_ctx, budget_frac: float,
                 window: int, sink: int, offsets=None, kv_of_q=None, omega=None,
-                budget_rows_override=None, segments=None):
+                budget_rows_override=None, segments=None, nonrot_dim: int = 0, q_nonrot=None):
     """Run the pass on one layer's host cache.
 
     ``layer_cache`` holds ``k`` (float or int8 codes), ``k_scale`` (or None),
@@ -229,10 +249,17 @@ def evict_layer(layer_cache: dict, q_mean: np.ndarray, q_abs, *, layer: int, n_k
     ``capacity`` per sequence. ``q_mean`` [L][Hq][fc][2], ``q_abs`` [L][Hq][fc]
     (arrays, or per-layer lists when head_dim differs across layers).
     ``segments`` optionally restricts the work to a list of (seq, head).
+    ``nonrot_dim`` > 0: the last nonrot_dim dims of each head are not rotary
+    (``q_mean`` / ``q_abs`` then cover (head_dim - nonrot_dim) / 2 pairs) and
+    ``q_nonrot`` [L][Hq][nonrot_dim] (or None: no content term) is the mean
+    non-rotary query.
 
     Returns ``(new_cache, info)``: ``info[(s, g)]`` = dict(raw, s, keep, B, n).
     """
-    omega = rope_omega(head_dim, rope_theta) if omega is None else np.asarray(omega, np.float64)
+    omega = (rope_omega(head_dim, rope_theta, nonrot_dim) if omega is None
+             else np.asarray(omega, np.float64))
+    if 2 * len(omega) + nonrot_dim != head_dim:
+        raise ValueError("omega must hold (head_dim - nonrot_dim) / 2 frequencies")
     offsets = default_future_offsets() if offsets is None else np.asarray(offsets, np.int64)
     n_q = len(q_mean[layer])
     groups = heads_of_kv(n_q, n_kv_heads, kv_of_q)
@@ -256,7 +283,8 @@ def evict_layer(layer_cache: dict, q_mean: np.ndarray, q_abs, *, layer: int, n_k
             ks = None if layer_cache.get("k_scale") is None else layer_cache["k_scale"][r0:r0 + n]
             kf = keys_f64(layer_cache["k"][r0:r0 + n], ks)
             hs = groups[g]
-            raw, sc = segment_scores(kf, qc_all[hs], m_all[hs], omega, int(cur_pos[s]), offsets)
+            qn = None if q_nonrot is None else np.asarray(q_nonrot[layer], np.float64)[hs]
+            raw, sc = segment_scores(kf, qc_all[hs], m_all[hs], omega, int(cur_pos[s]), offsets, qn)
             keep = select_keep(sc, n, b, _per_seq(sink, s), window)
             info[(s, g)] = {"raw": raw, "s": sc, "keep": keep, "B": b, "n": n, "row0": r0}
             if n <= b:
@@ -417,17 +445,28 @@ def schedule_events(*, trigger: str, prompt: int, n_decode: int, capacity: int, 
 # calibration ([Doc] §2 Calibration file; §5 Phase C q_mean / q_abs layout)
 # ---------------------------------------------------------------------------
 
-def calibrate(q: np.ndarray) -> tuple:
+def calibrate(q: np.ndarray, nonrot_dim: int = 0) -> tuple:
     """Statistics of a stream of pre-RoPE queries q[tokens][heads][head_dim]:
     (q_mean [heads][fc][2] as (re, im), q_abs [heads][fc]), means over the
-    tokens of the NEOX pairs q[.., f] + i q[.., f + hd/2] and of their moduli."""
+    tokens of the NEOX pairs q[.., f] + i q[.., f + rot/2] of the rotary dims
+    rot = head_dim - nonrot_dim (fc = rot/2) and of their moduli."""
     q = np.asarray(q, dtype=np.float64)
     t, h, hd = q.shape
     if t == 0:
         raise ValueError("no calibration tokens")
-    fc = hd // 2
-    z = q[:, :, :fc] + 1j * q[:, :, fc:]
+    fc = (hd - nonrot_dim) // 2
+    z = q[:, :, :fc] + 1j * q[:, :, fc:2 * fc]
     mean = z.mean(axis=0)
     q_mean = np.stack([mean.real, mean.imag], axis=-1)
     q_abs = np.abs(z).mean(axis=0)
     return q_mean, q_abs
+
+
+def calibrate_nonrot(q: np.ndarray, nonrot_dim: int) -> np.ndarray:
+    """Mean non-rotary query [heads][nonrot_dim]: the token mean of the last
+    ``nonrot_dim`` dims of each head (the reading of the content term above)."""
+    q = np.asarray(q, dtype=np.float64)
+    if q.shape[0] == 0:
+        raise ValueError("no calibration tokens")
+    hd = q.shape[2]
+    return q[:, :, hd - nonrot_dim:].mean(axis=0)

@@ -449,3 +449,144 @@ def test_calibrate_concatenation_and_resultant_length():
     np.testing.assert_allclose(np.hypot(ma2[..., 0], ma2[..., 1]), aa2, rtol=1e-13)
     # M = q_abs - |q_mean| is then zero: no magnitude term
     np.testing.assert_allclose(O.mlr_weight(ma2.reshape(1, 2, 4, 2)[0], aa2), 0.0, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# non-rotary (content) dims ([Doc] §4 gate line ``nonrot=``, §6 "Non-rotary
+# models"; reading: the first rot dims are NEOX-rotary, the rest never rotate)
+# ---------------------------------------------------------------------------
+
+def _brute_raw_partial(k_row, qm_head, q_abs_head, qn_head, theta, rot, p, offsets):
+    """One score by real arithmetic on a head whose first ``rot`` dims are
+    rotary: rotate the rotary half-pairs (f, f + rot/2) of the mean query by
+    2x2 matrices at p + d, leave the other dims as the mean non-rotary query,
+    dot the whole vector with the key, average over d, add the norm term on
+    the rotary pairs only."""
+    hd = len(k_row)
+    fr = rot // 2
+    total = 0.0
+    for d in offsets:
+        qvec = [0.0] * hd
+        for f in range(fr):
+            w = math.pow(theta, -2.0 * f / rot)
+            a, b = qm_head[f][0], qm_head[f][1]
+            c, s = math.cos(w * (p + d)), math.sin(w * (p + d))
+            qvec[f] = a * c - b * s
+            qvec[f + fr] = a * s + b * c
+        for e in range(hd - rot):
+            qvec[rot + e] = qn_head[e]
+        total += sum(qvec[i] * k_row[i] for i in range(hd))
+    total /= len(offsets)
+    for f in range(fr):
+        m = q_abs_head[f] - math.hypot(qm_head[f][0], qm_head[f][1])
+        total += m * math.sqrt(k_row[f] ** 2 + k_row[f + fr] ** 2)
+    return total
+
+
+@pytest.mark.parametrize("hd,nonrot,g,theta,p,offsets", [
+    (8, 4, 2, 100.0, 13, [1, 3, 7]),
+    (16, 8, 4, 1e4, 4096, [1, 2, 4, 8, 16]),
+    (12, 2, 1, 10.0, 5, [0, 2]),
+    (16, 14, 2, 500.0, 70000, [1, 65536]),
+])
+def test_nonrot_raw_score_matches_real_vector_bruteforce(hd, nonrot, g, theta, p, offsets):
+    rng = np.random.default_rng(hd * 31 + nonrot)
+    rot = hd - nonrot
+    k = rng.standard_normal((5, hd))
+    qm, q_abs = _rand_stats(rng, g, rot // 2)
+    qn = rng.standard_normal((g, nonrot))
+    got = O.raw_scores(k, O.as_complex(qm), O.mlr_weight(qm, q_abs),
+                       O.rope_omega(hd, theta, nonrot), p, offsets, qn)
+    for r in range(5):
+        for j in range(g):
+            want = _brute_raw_partial(list(k[r]), qm[j].tolist(), list(q_abs[j]), list(qn[j]),
+                                      theta, rot, p, offsets)
+            # the brute force takes cos / sin of angles up to w (p + d) unreduced:
+            # an absolute error of about 2^-53 (p + d) per unit of |q| |k|
+            slack = 1e-15 * (p + max(offsets)) * float(np.abs(k[r]).sum() * (np.abs(qm[j]).sum() + 1.0))
+            assert abs(got[r, j] - want) <= 1e-12 * max(1.0, abs(want)) + slack
+
+
+def _rope_partial(x, pos, theta, rot):
+    """Partial NEOX RoPE of rows x at positions pos: pairs (f, f + rot/2) of the
+    first rot dims rotated by pos * theta^(-2f/rot), the other dims unchanged."""
+    fr = rot // 2
+    w = np.array([math.pow(theta, -2.0 * f / rot) for f in range(fr)])
+    ang = np.asarray(pos, np.float64)[:, None] * w[None, :]
+    c, s = np.cos(ang), np.sin(ang)
+    a, b = x[:, :fr], x[:, fr:rot]
+    return np.concatenate([a * c - b * s, a * s + b * c, x[:, rot:]], axis=1)
+
+
+def test_nonrot_score_is_the_mean_logit_of_the_calibration_queries():
+    """With M = 0 the score is the expected attention logit: the mean, over a
+    stream of real pre-RoPE queries and over the offsets, of the partial-RoPE
+    query at p + d dotted with the partial-RoPE key at its own position. The
+    statistics come from calibrate / calibrate_nonrot of the same stream."""
+    rng = np.random.default_rng(41)
+    hd, nonrot, theta, n_tok = 16, 6, 1e4, 9
+    rot = hd - nonrot
+    q = rng.standard_normal((n_tok, 1, hd)) + 0.7
+    qm, _ = O.calibrate(q, nonrot)
+    qn = O.calibrate_nonrot(q, nonrot)
+    k_pre = rng.standard_normal((6, hd))
+    kpos = np.array([0, 3, 17, 100, 2048, 5000])
+    k_rot = _rope_partial(k_pre, kpos, theta, rot)
+    p, offsets = 6000, [1, 4, 64, 1024]
+    got = O.raw_scores(k_rot, O.as_complex(qm), np.zeros((1, rot // 2)),
+                       O.rope_omega(hd, theta, nonrot), p, offsets, qn)
+    want = np.zeros(6)
+    for d in offsets:
+        for t in range(n_tok):
+            q_at = _rope_partial(q[t], [p + d], theta, rot)[0]
+            want += k_rot @ q_at
+    want /= n_tok * len(offsets)
+    np.testing.assert_allclose(got[:, 0], want, rtol=1e-11, atol=1e-11)
+
+
+def test_nonrot_special_cases():
+    rng = np.random.default_rng(43)
+    hd, nonrot = 12, 4
+    rot = hd - nonrot
+    k = rng.standard_normal((7, hd))
+    qn = rng.standard_normal((2, nonrot))
+    zero = np.zeros((2, rot // 2, 2))
+    om = O.rope_omega(hd, 1e4, nonrot)
+    # no rotary statistics: the score is the textbook dot product on the content dims
+    got = O.raw_scores(k, O.as_complex(zero), np.zeros((2, rot // 2)), om, 99, [1, 2], qn)
+    np.testing.assert_allclose(got, k[:, rot:] @ qn.T, rtol=1e-14, atol=1e-14)
+    # the content term does not depend on the position or the offsets
+    qm, qa = _rand_stats(rng, 2, rot // 2)
+    args = (O.as_complex(qm), O.mlr_weight(qm, qa), om)
+    a = O.raw_scores(k, *args, 10, [1, 2], qn) - O.raw_scores(k, *args, 10, [1, 2], None)
+    b = O.raw_scores(k, *args, 77777, [3], qn) - O.raw_scores(k, *args, 77777, [3], None)
+    np.testing.assert_allclose(a, k[:, rot:] @ qn.T, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(b, a, rtol=1e-12, atol=1e-12)
+    # the rotary part only sees the first rot dims: changing a content dim of
+    # the key moves the score by exactly the matching query entry
+    k2 = k.copy()
+    k2[:, rot + 1] += 1.0
+    d = O.raw_scores(k2, *args, 5, [1], qn) - O.raw_scores(k, *args, 5, [1], qn)
+    np.testing.assert_allclose(d, np.broadcast_to(qn[:, 1], d.shape), rtol=1e-12, atol=1e-12)
+    # frequencies over the rotary dims only
+    np.testing.assert_allclose(om, [1e4 ** (-2.0 * f / rot) for f in range(rot // 2)], rtol=1e-15)
+    # nonrot = 0 is the all-rotary score
+    qm8, qa8 = _rand_stats(rng, 2, hd // 2)
+    np.testing.assert_array_equal(
+        O.raw_scores(k, O.as_complex(qm8), O.mlr_weight(qm8, qa8), O.rope_omega(hd, 1e4, 0), 8, [1, 2]),
+        O.raw_scores(k, O.as_complex(qm8), O.mlr_weight(qm8, qa8), O.rope_omega(hd, 1e4), 8, [1, 2]))
+
+
+def test_calibrate_nonrot_literal_loop():
+    rng = np.random.default_rng(44)
+    q = rng.standard_normal((5, 2, 10))
+    qm, qa = O.calibrate(q, 4)
+    qn = O.calibrate_nonrot(q, 4)
+    assert qm.shape == (2, 3, 2) and qa.shape == (2, 3) and qn.shape == (2, 4)
+    for h in range(2):
+        for f in range(3):
+            re = sum(q[t, h, f] for t in range(5)) / 5
+            im = sum(q[t, h, f + 3] for t in range(5)) / 5
+            assert abs(qm[h, f, 0] - re) < 1e-14 and abs(qm[h, f, 1] - im) < 1e-14
+        for e in range(4):
+            assert abs(qn[h, e] - sum(q[t, h, 6 + e] for t in range(5)) / 5) < 1e-14
