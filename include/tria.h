@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define TRIA_VERSION 1
+#define TRIA_VERSION 2
 #define TRIA_MAX_SEQS 128      /* sequences per call */
 #define TRIA_MAX_HEAD_DIM 256  /* [Doc] §4/§6: head_dim <= 256, freq_count <= 128 */
 #define TRIA_MAX_GROUP 8       /* query heads per KV head supported */
@@ -85,10 +85,10 @@ typedef struct tria_stats_desc {
   int32_t n_q_heads;
   int32_t n_kv_heads;
   int32_t head_dim;           /* every layer's head_dim unless layer_head_dim is given */
-  double rope_theta;          /* w_f = theta^(-2f/head_dim) when omega is NULL */
-  const double* omega;        /* [head_dim/2] optional RoPE angular frequencies */
-  const float* q_mean;        /* [n_layers][n_q_heads][head_dim/2][2] pre-RoPE mean query (re, im) */
-  const float* q_abs;         /* [n_layers][n_q_heads][head_dim/2] mean |q_f|; NULL: no norm term */
+  double rope_theta;          /* w_f = theta^(-2f/rot) when omega is NULL (rot = head_dim - nonrot_dim) */
+  const double* omega;        /* [rot/2] optional RoPE angular frequencies */
+  const float* q_mean;        /* [n_layers][n_q_heads][rot/2][2] pre-RoPE mean query (re, im) */
+  const float* q_abs;         /* [n_layers][n_q_heads][rot/2] mean |q_f|; NULL: no norm term */
   const int32_t* kv_of_q;     /* [n_q_heads] optional query->KV head map ([Worklog] "sampled-head
                                  mapping"); NULL: h / (n_q_heads / n_kv_heads). Each KV head must
                                  get the same number of query heads. */
@@ -99,12 +99,26 @@ typedef struct tria_stats_desc {
    * offset table so that the eligible layers score on the GPU):
    * layer_head_dim [n_layers] optional; NULL: every layer has head_dim. When
    * given, head_dim is ignored and q_mean / q_abs (and omega, if given) are
-   * packed layer after layer: layer l holds n_q_heads * layer_head_dim[l] / 2
-   * pairs (omega: layer_head_dim[l] / 2 frequencies). Every entry must be even
-   * and > 0. Layers whose head_dim fails the gate (> 256 or not a multiple of
-   * 32) are not loaded; passes on them return TRIA_ERR_UNSUPPORTED. */
+   * packed layer after layer: layer l holds n_q_heads * (layer_head_dim[l] -
+   * nonrot_dim) / 2 pairs (omega: (layer_head_dim[l] - nonrot_dim) / 2
+   * frequencies). Every entry must be even and > nonrot_dim. Layers whose
+   * head_dim fails the gate (> 256, not a multiple of 32, rotary dims not a
+   * multiple of 16) are not loaded; passes on them return
+   * TRIA_ERR_UNSUPPORTED. */
   const int32_t* layer_head_dim;
   const double* layer_rope_theta;  /* [n_layers] optional per-layer theta; NULL: rope_theta */
+  /* Non-rotary (content) dims ([Doc] §4 gate line field nonrot=, §6 "Non-
+   * rotary models"; the pages give no formula, the reading here): the last
+   * nonrot_dim dims of every head are never rotated and the first
+   * rot = head_dim - nonrot_dim are NEOX-rotary, paired (f, f + rot/2), with
+   * w_f = theta^(-2f/rot). q_mean / q_abs / omega then hold rot/2 pairs per
+   * head (per layer: layer_head_dim[l] - nonrot_dim), and a row's score gains
+   *   sum_e q_nonrot[h][e] * K[r][rot + e]
+   * (the mean non-rotary query dotted with the key's non-rotary dims: no
+   * phase, no offset average, no norm term). 0: every dim is rotary. */
+  int32_t nonrot_dim;
+  const float* q_nonrot;      /* [n_layers][n_q_heads][nonrot_dim] mean non-rotary query;
+                                 NULL: no content term */
 } tria_stats_desc;
 
 typedef struct tria_stats tria_stats;  /* opaque, device resident, immutable after load */
@@ -148,15 +162,19 @@ typedef struct tria_policy {
 } tria_policy;
 
 /* Host-only gate of [Doc] §4 "GPU scoring requirements" (n_q % n_kv == 0,
- * head_dim <= 256 and % 32 == 0) plus this build's group <= 8. No GPU use. */
-tria_status tria_gate_check(int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim);
+ * head_dim <= 256 and % 32 == 0) plus this build's group <= 8. The page's gate
+ * also wants no non-rotary dims ([Doc] §6 "Non-rotary models" are scored on the
+ * CPU there); here heads with nonrot_dim non-rotary dims are eligible when the
+ * rotary dims head_dim - nonrot_dim are a multiple of 16 (UNSUPPORTED
+ * otherwise). nonrot_dim < 0 or >= head_dim: INVALID_ARG. No GPU use. */
+tria_status tria_gate_check(int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t nonrot_dim);
 
 /* The gate as one log line, in the form of the [Doc] §4 startup log
  * ("tria: gpu gate - is_q8_0=1 nh=32 nkv=8 hd=128 nonrot=0 -> eligible"), with
  * the reason appended when ineligible; written to buf (NUL-terminated,
  * truncated to buf_size). Returns tria_gate_check's status. No GPU use. */
-tria_status tria_gate_describe(int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, tria_dtype k_type,
-                               char* buf, size_t buf_size);
+tria_status tria_gate_describe(int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t nonrot_dim,
+                               tria_dtype k_type, char* buf, size_t buf_size);
 
 /* Budget rows floor(budget_frac * n_ctx) computed in double ([Doc] §1). */
 int64_t tria_budget_rows(double budget_frac, int64_t n_ctx);
@@ -233,9 +251,10 @@ tria_status tria_compact(const tria_layer_cache* cache, const tria_policy* polic
 
 /* The whole pass (steps 1-3) for one layer and all sequences of the call.
  * Calls of at least 128 segments (n_seqs x n_kv_heads) with fp16 or q8_0
- * keys and head_dim 64 or 128 (any group) or 256 (group <= 4) run as one
- * fused persistent kernel (see tria_evict_model); the others run the three
- * staged kernels of tria_evict_staged. Same results either way. */
+ * keys, head_dim 64 or 128 (any group) or 256 (group <= 4) and every dim
+ * rotary (statistics with nonrot_dim 0) run as one fused persistent kernel
+ * (see tria_evict_model); the others run the three staged kernels of
+ * tria_evict_staged. Same results either way. */
 tria_status tria_evict(const tria_stats* stats, int32_t layer, const tria_layer_cache* cache,
                        const tria_policy* policy, void* ws, size_t ws_bytes, void* stream);
 
@@ -466,16 +485,22 @@ tria_status tria_schedule_passed(const tria_schedule* sch, tria_seq_state* st, i
  * ([Doc] §2 Calibration file: statistics per layer and head, gathered over
  * calibration text from the pre-RoPE Q of every layer;
  * §5 Phase C: q_mean / q_abs arrays laid out [layers][heads][frequency
- * pairs]). With NEOX pairs z = q[f] + i q[f + head_dim/2]:
- *   q_mean[h][f] = mean over tokens of z   (stored as re, im)
- *   q_abs[h][f]  = mean over tokens of |z|
- * Feed batches with tria_calib_accumulate, then tria_calib_finish.
+ * pairs]). With rot = head_dim - nonrot_dim rotary dims and NEOX pairs
+ * z = q[f] + i q[f + rot/2] (f < rot/2):
+ *   q_mean[h][f]   = mean over tokens of z   (stored as re, im)
+ *   q_abs[h][f]    = mean over tokens of |z|
+ *   q_nonrot[h][e] = mean over tokens of q[rot + e]   (e < nonrot_dim; the
+ *                    content term of tria_stats_desc)
+ * Feed batches with tria_calib_accumulate, then tria_calib_finish; both take
+ * the same nonrot_dim (even, in [0, head_dim); else TRIA_ERR_INVALID_ARG).
  *
  * tria_calib_accumulate:
  *   q      device, [n_tokens][n_q_heads][head_dim] values of q_type (TRIA_F32
  *          or TRIA_F16), row-major, 4-byte aligned; read only.
  *   acc    device, double [n_q_heads][head_dim/2][3] running sums (re, im,
- *          modulus), owned by the caller and zeroed before the first batch;
+ *          modulus) of the rot/2 rotary pairs, then of nonrot_dim/2 content
+ *          pairs (q[rot + e], q[rot + nonrot_dim/2 + e]), owned by the
+ *          caller and zeroed before the first batch;
  *          the batch's sums are added to it (fp32 within a block of tokens,
  *          fp64 across blocks; the order of the fp64 additions is not fixed,
  *          so repeated runs may differ in the last bits of acc).
@@ -485,13 +510,14 @@ tria_status tria_schedule_passed(const tria_schedule* sch, tria_seq_state* st, i
  *   adds nothing (q may then be null).
  * tria_calib_finish:
  *   acc       as above; n_tokens = tokens accumulated (> 0).
- *   q_mean    device float [n_q_heads][head_dim/2][2]; q_abs device float
- *             [n_q_heads][head_dim/2]: one layer's rows of the tria_stats_desc
- *             arrays. Errors as above. */
+ *   q_mean    device float [n_q_heads][rot/2][2]; q_abs device float
+ *             [n_q_heads][rot/2]; q_nonrot device float
+ *             [n_q_heads][nonrot_dim] (may be NULL when nonrot_dim is 0): one
+ *             layer's rows of the tria_stats_desc arrays. Errors as above. */
 tria_status tria_calib_accumulate(const void* q, tria_dtype q_type, int32_t n_tokens, int32_t n_q_heads,
-                                  int32_t head_dim, double* acc, void* stream);
+                                  int32_t head_dim, int32_t nonrot_dim, double* acc, void* stream);
 tria_status tria_calib_finish(const double* acc, int64_t n_tokens, int32_t n_q_heads, int32_t head_dim,
-                              float* q_mean, float* q_abs, void* stream);
+                              int32_t nonrot_dim, float* q_mean, float* q_abs, float* q_nonrot, void* stream);
 
 const char* tria_status_string(tria_status status);
 int32_t tria_version(void);

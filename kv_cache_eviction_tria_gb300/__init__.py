@@ -60,6 +60,7 @@ class _StatsDesc(ctypes.Structure):
         ("q_abs", ctypes.POINTER(ctypes.c_float)), ("kv_of_q", ctypes.POINTER(ctypes.c_int32)),
         ("offsets", ctypes.POINTER(ctypes.c_int64)), ("n_offsets", ctypes.c_int32),
         ("layer_head_dim", ctypes.POINTER(ctypes.c_int32)), ("layer_rope_theta", ctypes.POINTER(ctypes.c_double)),
+        ("nonrot_dim", ctypes.c_int32), ("q_nonrot", ctypes.POINTER(ctypes.c_float)),
     ]
 
 
@@ -112,9 +113,9 @@ def load_library(path: str | None = None):
         raise RuntimeError(f"{path} not found: build it first (python -c 'import __graft_entry__ as g; g.build()')")
     lib = ctypes.CDLL(path)
     vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
-    lib.tria_gate_check.argtypes = [i32, i32, i32]
+    lib.tria_gate_check.argtypes = [i32, i32, i32, i32]
     lib.tria_gate_check.restype = i32
-    lib.tria_gate_describe.argtypes = [i32, i32, i32, i32, ctypes.c_char_p, sz]
+    lib.tria_gate_describe.argtypes = [i32, i32, i32, i32, i32, ctypes.c_char_p, sz]
     lib.tria_gate_describe.restype = i32
     lib.tria_budget_rows.argtypes = [ctypes.c_double, i64]
     lib.tria_budget_rows.restype = i64
@@ -158,9 +159,9 @@ def load_library(path: str | None = None):
     lib.tria_device_status.restype = i32
     lib.tria_selftest_bounded_wait.argtypes = [i32, vp, sz, vp]
     lib.tria_selftest_bounded_wait.restype = i32
-    lib.tria_calib_accumulate.argtypes = [vp, i32, i32, i32, i32, vp, vp]
+    lib.tria_calib_accumulate.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp]
     lib.tria_calib_accumulate.restype = i32
-    lib.tria_calib_finish.argtypes = [vp, i64, i32, i32, vp, vp, vp]
+    lib.tria_calib_finish.argtypes = [vp, i64, i32, i32, i32, vp, vp, vp, vp]
     lib.tria_calib_finish.restype = i32
     lib.tria_shared_combine.argtypes = [vp, i64, i32, ctypes.POINTER(_LayerCache), vp, vp, sz, vp]
     lib.tria_shared_combine.restype = i32
@@ -224,14 +225,15 @@ def _host_array(values, dtype, ctype):
 
 # --------------------------------------------------------------------------- host-only helpers
 
-def gate_check(n_q_heads: int, n_kv_heads: int, head_dim: int) -> int:
-    return load_library().tria_gate_check(n_q_heads, n_kv_heads, head_dim)
+def gate_check(n_q_heads: int, n_kv_heads: int, head_dim: int, nonrot_dim: int = 0) -> int:
+    return load_library().tria_gate_check(n_q_heads, n_kv_heads, head_dim, nonrot_dim)
 
 
-def gate_describe(n_q_heads: int, n_kv_heads: int, head_dim: int, k_type: str = "q8_0") -> tuple:
+def gate_describe(n_q_heads: int, n_kv_heads: int, head_dim: int, k_type: str = "q8_0",
+                  nonrot_dim: int = 0) -> tuple:
     """tria_gate_describe: (status, the gate log line)."""
     buf = ctypes.create_string_buffer(256)
-    st = load_library().tria_gate_describe(n_q_heads, n_kv_heads, head_dim, DTYPES[k_type], buf, 256)
+    st = load_library().tria_gate_describe(n_q_heads, n_kv_heads, head_dim, nonrot_dim, DTYPES[k_type], buf, 256)
     return st, buf.value.decode()
 
 
@@ -258,8 +260,10 @@ class Stats:
 
     def __init__(self, q_mean, q_abs, *, n_kv_heads: int, head_dim: int = 0, rope_theta: float = 0.0,
                  omega=None, kv_of_q=None, offsets=None, layer_head_dim=None, layer_rope_theta=None,
-                 stream=None):
-        """Uniform models: q_mean [L][n_q][hd/2][2], q_abs [L][n_q][hd/2] (or None).
+                 nonrot_dim: int = 0, q_nonrot=None, stream=None):
+        """Uniform models: q_mean [L][n_q][rot/2][2], q_abs [L][n_q][rot/2] (or None),
+        rot = hd - nonrot_dim the rotary dims; q_nonrot [L][n_q][nonrot_dim] the
+        mean non-rotary query (or None: no content term).
         Hybrid models (layer_head_dim given): q_mean / q_abs / omega are lists with
         one array per layer, packed here layer after layer."""
         lib = load_library()
@@ -281,14 +285,16 @@ class Stats:
         of_arr, of_p = _host_array(offsets, np.int64, ctypes.c_int64)
         lh_arr, lh_p = _host_array(layer_head_dim, np.int32, ctypes.c_int32)
         lt_arr, lt_p = _host_array(layer_rope_theta, np.float64, ctypes.c_double)
-        self._keep += [qm_arr, qa_arr, om_arr, kv_arr, of_arr, lh_arr, lt_arr]
+        qn_arr, qn_p = _host_array(q_nonrot, np.float32, ctypes.c_float)
+        self._keep += [qm_arr, qa_arr, om_arr, kv_arr, of_arr, lh_arr, lt_arr, qn_arr]
         desc = _StatsDesc(n_layers, n_q, n_kv_heads, head_dim, float(rope_theta), om_p, qm_p, qa_p,
-                          kv_p, of_p, 0 if of_arr is None else len(of_arr), lh_p, lt_p)
+                          kv_p, of_p, 0 if of_arr is None else len(of_arr), lh_p, lt_p, int(nonrot_dim), qn_p)
         handle = ctypes.c_void_p()
         _check(lib.tria_load_stats(ctypes.byref(desc), ctypes.byref(handle), _stream_handle(stream)),
                "tria_load_stats")
         self.handle = handle
         self.n_layers, self.n_q_heads, self.n_kv_heads, self.head_dim = n_layers, n_q, n_kv_heads, head_dim
+        self.nonrot_dim = int(nonrot_dim)
         self.group = n_q // n_kv_heads
 
     def close(self):
@@ -479,10 +485,11 @@ def selftest_bounded_wait(spin_limit: int, ws, stream=None) -> int:
     return load_library().tria_selftest_bounded_wait(spin_limit, wp, wb, _stream_handle(stream))
 
 
-def calib_accumulate(q, acc, *, stream=None):
+def calib_accumulate(q, acc, *, nonrot_dim: int = 0, stream=None):
     """tria_calib_accumulate: add the sums of a batch of pre-RoPE queries
     q[tokens][heads][head_dim] (float32 or float16 CUDA tensor) to acc
-    (float64 CUDA tensor [heads][head_dim/2][3], zeroed before the first batch)."""
+    (float64 CUDA tensor [heads][head_dim/2][3], zeroed before the first batch);
+    the last nonrot_dim dims of each head are the non-rotary ones."""
     import torch
     if q.dim() != 3:
         raise ValueError("q must be [tokens][heads][head_dim]")
@@ -493,19 +500,24 @@ def calib_accumulate(q, acc, *, stream=None):
     if acc.dtype != torch.float64 or tuple(acc.shape) != (h, hd // 2, 3):
         raise ValueError("acc must be float64 [heads][head_dim/2][3]")
     qp = _ptr(q) if t > 0 else None
-    _check(load_library().tria_calib_accumulate(qp, qt, t, h, hd, _ptr(acc), _stream_handle(stream)),
+    _check(load_library().tria_calib_accumulate(qp, qt, t, h, hd, nonrot_dim, _ptr(acc), _stream_handle(stream)),
            "tria_calib_accumulate")
 
 
-def calib_finish(acc, n_tokens: int, *, stream=None):
-    """tria_calib_finish: (q_mean [heads][head_dim/2][2], q_abs [heads][head_dim/2]) float32 CUDA tensors."""
+def calib_finish(acc, n_tokens: int, *, nonrot_dim: int = 0, stream=None):
+    """tria_calib_finish: (q_mean [heads][rot/2][2], q_abs [heads][rot/2]) float32
+    CUDA tensors, rot = head_dim - nonrot_dim; with nonrot_dim > 0 also the mean
+    non-rotary query [heads][nonrot_dim] as a third element."""
     import torch
     h, fc, _ = acc.shape
-    q_mean = torch.empty((h, fc, 2), dtype=torch.float32, device=acc.device)
-    q_abs = torch.empty((h, fc), dtype=torch.float32, device=acc.device)
-    _check(load_library().tria_calib_finish(_ptr(acc), n_tokens, h, 2 * fc, _ptr(q_mean), _ptr(q_abs),
+    fcr = fc - nonrot_dim // 2
+    q_mean = torch.empty((h, fcr, 2), dtype=torch.float32, device=acc.device)
+    q_abs = torch.empty((h, fcr), dtype=torch.float32, device=acc.device)
+    q_nonrot = torch.empty((h, nonrot_dim), dtype=torch.float32, device=acc.device) if nonrot_dim else None
+    _check(load_library().tria_calib_finish(_ptr(acc), n_tokens, h, 2 * fc, nonrot_dim, _ptr(q_mean), _ptr(q_abs),
+                                            _ptr(q_nonrot) if q_nonrot is not None else None,
                                             _stream_handle(stream)), "tria_calib_finish")
-    return q_mean, q_abs
+    return (q_mean, q_abs) if not nonrot_dim else (q_mean, q_abs, q_nonrot)
 
 
 # --------------------------------------------------------------------------- shared-slot variant

@@ -138,6 +138,7 @@ void fill_pass(Pass& P, const tria_layer_cache* c, const tria_policy* p, const s
   P.G = G;
   P.hd = c->head_dim;
   P.fc = c->head_dim / 2;
+  P.fcr = P.fc;
   P.window = p ? p->window : 0;
   P.k_type = c->k_type;
   P.v_type = c->v_type;
@@ -186,6 +187,7 @@ void set_stats(Pass& P, const tria_stats* st, int layer) {
   P.qe = st->qe;
   P.mw = st->mw;
   P.turns = st->turns + st->turns_off[layer];
+  P.fcr = (P.hd - st->nonrot_dim) / 2;
   for (int s = 0; s < P.n_seqs; ++s) P.seq[s].qe_off = (int32_t)st->qe_off[layer];
 }
 
@@ -248,8 +250,11 @@ tria_status launch_fused(const tria_stats* st, const int32_t* layers, int n_laye
   return cuda_status(e);
 }
 
-bool fused_ok(const tria_layer_cache* c, int G, int n_layers) {
-  return pass_supported(c->k_type, c->head_dim, G) && n_layers >= 1 && n_layers <= kPassMaxLayers &&
+// The fused kernel scores all-rotary heads only (heads with non-rotary dims
+// take the staged kernels).
+bool fused_ok(const tria_stats* st, const tria_layer_cache* c, int n_layers) {
+  return st->nonrot_dim == 0 && pass_supported(c->k_type, c->head_dim, st->group) && n_layers >= 1 &&
+         n_layers <= kPassMaxLayers &&
          (int64_t)n_layers * c->n_seqs * c->n_kv_heads <= kPassMaxSegs;
 }
 
@@ -259,8 +264,8 @@ bool fused_ok(const tria_layer_cache* c, int G, int n_layers) {
 // layers: 0.47 ms against 1.44 ms), and behind for a few long segments (one
 // Qwen3-8B layer of 8 x 32768 rows: 111 us against 62 us).
 constexpr int kFusedMinSegs = 128;
-bool fused_preferred(const tria_layer_cache* c, int G, int n_layers) {
-  return fused_ok(c, G, n_layers) && (int64_t)n_layers * c->n_seqs * c->n_kv_heads >= kFusedMinSegs;
+bool fused_preferred(const tria_stats* st, const tria_layer_cache* c, int n_layers) {
+  return fused_ok(st, c, n_layers) && (int64_t)n_layers * c->n_seqs * c->n_kv_heads >= kFusedMinSegs;
 }
 
 }  // namespace
@@ -330,29 +335,36 @@ tria_status check_policy(const tria_layer_cache* c, const tria_policy* p, bool n
 
 // ---------------------------------------------------------------------------
 
-extern "C" tria_status tria_gate_check(int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim) {
+extern "C" tria_status tria_gate_check(int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                                       int32_t nonrot_dim) {
   if (n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0) return TRIA_ERR_INVALID_ARG;
+  if (nonrot_dim < 0 || nonrot_dim >= head_dim) return TRIA_ERR_INVALID_ARG;
   if (n_q_heads % n_kv_heads != 0) return TRIA_ERR_UNSUPPORTED;          // [Doc] §4: nh % nkv == 0
   if (head_dim > TRIA_MAX_HEAD_DIM || head_dim % 32 != 0) return TRIA_ERR_UNSUPPORTED;  // hd <= 256, % 32
   const int G = n_q_heads / n_kv_heads;
   if (G != 1 && G != 2 && G != 4 && G != 8) return TRIA_ERR_UNSUPPORTED;
+  // the scorers take a lane's rotary pairs in whole runs of 8
+  if ((head_dim - nonrot_dim) % 16 != 0) return TRIA_ERR_UNSUPPORTED;
   return TRIA_OK;
 }
 
 extern "C" tria_status tria_gate_describe(int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
-                                          tria_dtype k_type, char* buf, size_t buf_size) {
-  const tria_status g = tria_gate_check(n_q_heads, n_kv_heads, head_dim);
+                                          int32_t nonrot_dim, tria_dtype k_type, char* buf, size_t buf_size) {
+  const tria_status g = tria_gate_check(n_q_heads, n_kv_heads, head_dim, nonrot_dim);
   if (!buf || buf_size == 0) return g;
   const char* why = "";
-  if (g == TRIA_ERR_INVALID_ARG) why = " (heads / head_dim must be > 0)";
-  else if (g == TRIA_ERR_UNSUPPORTED) {
+  if (g == TRIA_ERR_INVALID_ARG) {
+    why = n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 ? " (heads / head_dim must be > 0)"
+                                                            : " (nonrot must be in [0, head_dim))";
+  } else if (g == TRIA_ERR_UNSUPPORTED) {
     if (n_q_heads % n_kv_heads != 0) why = " (nh % nkv != 0)";
     else if (head_dim > TRIA_MAX_HEAD_DIM) why = " (head_dim > 256)";
     else if (head_dim % 32 != 0) why = " (head_dim % 32 != 0)";
+    else if ((head_dim - nonrot_dim) % 16 != 0) why = " (rotary dims % 16 != 0)";
     else why = " (group size not 1, 2, 4 or 8)";
   }
-  snprintf(buf, buf_size, "tria: gpu gate - is_q8_0=%d nh=%d nkv=%d hd=%d nonrot=0 -> %s%s",
-           k_type == TRIA_Q8_0 ? 1 : 0, (int)n_q_heads, (int)n_kv_heads, (int)head_dim,
+  snprintf(buf, buf_size, "tria: gpu gate - is_q8_0=%d nh=%d nkv=%d hd=%d nonrot=%d -> %s%s",
+           k_type == TRIA_Q8_0 ? 1 : 0, (int)n_q_heads, (int)n_kv_heads, (int)head_dim, (int)nonrot_dim,
            g == TRIA_OK ? "eligible" : "ineligible", why);
   return g;
 }
@@ -531,7 +543,7 @@ extern "C" tria_status tria_evict(const tria_stats* stats, int32_t layer, const 
   const Layout L = make_layout(cache, stats->group);
   if ((r = check_ws(ws, ws_bytes, L)) != TRIA_OK) return r;
   cudaStream_t st = (cudaStream_t)stream;
-  if (fused_preferred(cache, stats->group, 1))
+  if (fused_preferred(stats, cache, 1))
     return launch_fused(stats, &layer, 1, cache, policy, budget, L, ws, nullptr, st);
   return evict_staged(stats, layer, cache, policy, budget, L, ws, st);
 }
@@ -596,7 +608,7 @@ extern "C" tria_status tria_evict_model(const tria_stats* stats, const int32_t* 
   if ((r = check_policy(caches, policy, true, budget)) != TRIA_OK) return r;
   if (score_out && ((uintptr_t)score_out % 4) != 0) return TRIA_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
-  if (fused_ok(caches, stats->group, n_layers) && (score_out || fused_preferred(caches, stats->group, n_layers))) {
+  if (fused_ok(stats, caches, n_layers) && (score_out || fused_preferred(stats, caches, n_layers))) {
     const Layout L = make_model_layout(caches, stats->group, n_layers);
     if ((r = check_ws(ws, ws_bytes, L)) != TRIA_OK) return r;
     return launch_fused(stats, layers, n_layers, caches, policy, budget, L, ws, score_out, st);

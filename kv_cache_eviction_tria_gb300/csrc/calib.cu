@@ -5,6 +5,10 @@
 // calibration text: the average query direction and a weight per frequency) and
 // §5 Phase C (the q_mean / q_abs arrays, [layers][heads][frequency pairs]).
 // With NEOX pairs z = q[f] + i q[f + hd/2]: q_mean = mean z, q_abs = mean |z|.
+// Heads whose last nonrot dims are not rotary: the fcr = (hd - nonrot) / 2
+// rotary pairs are (f, f + fcr) and the nonrot / 2 content pairs that follow
+// are (f + fcr, f + hd/2), whose mean is the mean non-rotary query (the
+// content term of [Doc] §6 "Non-rotary models"); the finish step splits them.
 //
 // One streaming read of the queries: a block takes a range of tokens and a
 // block of 64 (head, 16-byte vector of pairs) slots, reads contiguous spans
@@ -43,7 +47,8 @@ constexpr int kCalibVecThreads = kCalibSlots * kCalibStreams;
 
 template <typename T>
 __global__ void __launch_bounds__(kCalibVecThreads) k_calib_acc(const T* __restrict__ q, int n_tokens, int n_heads,
-                                                                 int hd, int tok_per_block, double* __restrict__ acc) {
+                                                                 int hd, int fcr, int tok_per_block,
+                                                                 double* __restrict__ acc) {
   constexpr int P = 16 / sizeof(T);
   __shared__ float red[kCalibSlots][3 * P];
   const int fc = hd / 2;
@@ -56,7 +61,11 @@ __global__ void __launch_bounds__(kCalibVecThreads) k_calib_acc(const T* __restr
   const int t0 = blockIdx.x * tok_per_block, t1 = min(n_tokens, t0 + tok_per_block);
   if (sl < slots) {
     const int h = sl / vpr, f0 = (sl - h * vpr) * P;
-    const T* base = q + (size_t)h * hd + f0;
+    // first dims of the pairs' two halves (fcr % P == 0: a vector is all
+    // rotary or all content)
+    const int d_re = f0 < fcr ? f0 : f0 + fcr, d_im = f0 < fcr ? f0 + fcr : f0 + fc;
+    const T* base = q + (size_t)h * hd + d_re;
+    const int im_off = d_im - d_re;
     const size_t stride = (size_t)n_heads * hd;
     float sr[P], si[P], sa[P];
 #pragma unroll
@@ -81,14 +90,14 @@ __global__ void __launch_bounds__(kCalibVecThreads) k_calib_acc(const T* __restr
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         a[u] = __ldcs(reinterpret_cast<const uint4*>(r + u * step));
-        b[u] = __ldcs(reinterpret_cast<const uint4*>(r + u * step + fc));
+        b[u] = __ldcs(reinterpret_cast<const uint4*>(r + u * step + im_off));
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) add(a[u], b[u]);
     }
     for (; t < t1; t += kCalibStreams) {
       const T* r0 = base + (size_t)t * stride;
-      add(__ldcs(reinterpret_cast<const uint4*>(r0)), __ldcs(reinterpret_cast<const uint4*>(r0 + fc)));
+      add(__ldcs(reinterpret_cast<const uint4*>(r0)), __ldcs(reinterpret_cast<const uint4*>(r0 + im_off)));
     }
     float* mine = red[threadIdx.x % kCalibSlots];
 #pragma unroll
@@ -111,7 +120,7 @@ __global__ void __launch_bounds__(kCalibVecThreads) k_calib_acc(const T* __restr
 // Scalar body for head_dim not a multiple of 4: lane l owns pairs l, l + 32, ...
 template <typename T>
 __global__ void __launch_bounds__(kCalibWarps * 32) k_calib_acc_scalar(const T* __restrict__ q, int n_tokens,
-                                                                        int n_heads, int hd,
+                                                                        int n_heads, int hd, int fcr,
                                                                         double* __restrict__ acc) {
   __shared__ float part[kCalibWarps][3][kCalibMaxPairs];
   const int h = blockIdx.y;
@@ -127,7 +136,8 @@ __global__ void __launch_bounds__(kCalibWarps * 32) k_calib_acc_scalar(const T* 
     for (int j = 0; j < kCalibPerLane; ++j) {
       const int f = lane + 32 * j;
       if (f < fc) {
-        const float re = as_f32(row[f]), im = as_f32(row[f + fc]);
+        const bool rot = f < fcr;
+        const float re = as_f32(row[rot ? f : f + fcr]), im = as_f32(row[rot ? f + fcr : f + fc]);
         sr[j] += re;
         si[j] += im;
         sa[j] += sqrtf(fmaf(re, re, im * im));
@@ -152,13 +162,23 @@ __global__ void __launch_bounds__(kCalibWarps * 32) k_calib_acc_scalar(const T* 
   }
 }
 
-__global__ void k_calib_finish(const double* __restrict__ acc, double inv_n, int n, float* __restrict__ q_mean,
-                               float* __restrict__ q_abs) {
+// acc [heads][fc][3] -> q_mean [heads][fcr][2], q_abs [heads][fcr] and
+// q_nonrot [heads][2 (fc - fcr)] (content pair e: dims e and e + nonrot/2)
+__global__ void k_calib_finish(const double* __restrict__ acc, double inv_n, int n_heads, int fc, int fcr,
+                               float* __restrict__ q_mean, float* __restrict__ q_abs, float* __restrict__ q_nonrot) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;   // (head, pair)
-  if (i >= n) return;
-  q_mean[2 * i] = (float)(acc[3 * i] * inv_n);
-  q_mean[2 * i + 1] = (float)(acc[3 * i + 1] * inv_n);
-  q_abs[i] = (float)(acc[3 * i + 2] * inv_n);
+  if (i >= n_heads * fc) return;
+  const int h = i / fc, f = i - h * fc;
+  if (f < fcr) {
+    const int o = h * fcr + f;
+    q_mean[2 * o] = (float)(acc[3 * i] * inv_n);
+    q_mean[2 * o + 1] = (float)(acc[3 * i + 1] * inv_n);
+    q_abs[o] = (float)(acc[3 * i + 2] * inv_n);
+  } else {
+    const int nr = 2 * (fc - fcr), e = f - fcr;
+    q_nonrot[h * nr + e] = (float)(acc[3 * i] * inv_n);
+    q_nonrot[h * nr + e + nr / 2] = (float)(acc[3 * i + 1] * inv_n);
+  }
 }
 
 bool aligned4(const void* p) { return ((uintptr_t)p & 3u) == 0; }
@@ -169,11 +189,13 @@ bool aligned4(const void* p) { return ((uintptr_t)p & 3u) == 0; }
 using namespace tria;
 
 extern "C" tria_status tria_calib_accumulate(const void* q, tria_dtype q_type, int32_t n_tokens, int32_t n_q_heads,
-                                             int32_t head_dim, double* acc, void* stream) {
+                                             int32_t head_dim, int32_t nonrot_dim, double* acc, void* stream) {
   if ((!q && n_tokens > 0) || !acc || n_tokens < 0 || n_q_heads < 1) return TRIA_ERR_INVALID_ARG;
   if (!aligned4(q) || ((uintptr_t)acc & 7u) != 0) return TRIA_ERR_INVALID_ARG;
   if (q_type != TRIA_F32 && q_type != TRIA_F16) return TRIA_ERR_UNSUPPORTED;
   if (head_dim < 2 || head_dim % 2 != 0 || head_dim > 2 * kCalibMaxPairs) return TRIA_ERR_UNSUPPORTED;
+  if (nonrot_dim < 0 || nonrot_dim % 2 != 0 || nonrot_dim >= head_dim) return TRIA_ERR_INVALID_ARG;
+  const int fcr = (head_dim - nonrot_dim) / 2;
   if (n_tokens == 0) return TRIA_OK;
   const dim3 grid((n_tokens + kCalibTokens - 1) / kCalibTokens, n_q_heads);
   if (grid.y > 65535) return TRIA_ERR_UNSUPPORTED;
@@ -181,7 +203,7 @@ extern "C" tria_status tria_calib_accumulate(const void* q, tria_dtype q_type, i
   // the vector body needs every half-row to be whole 16-byte vectors, and a
   // 16-byte aligned base
   const int esz = q_type == TRIA_F32 ? 4 : 2;
-  const bool vec = ((head_dim / 2) * esz) % 16 == 0 && ((uintptr_t)q % 16) == 0;
+  const bool vec = ((head_dim / 2) * esz) % 16 == 0 && (fcr * esz) % 16 == 0 && ((uintptr_t)q % 16) == 0;
   if (vec) {
     // about one block per SM in all: slot blocks x token ranges
     int dev = 0, sms = 0;
@@ -193,23 +215,31 @@ extern "C" tria_status tria_calib_accumulate(const void* q, tria_dtype q_type, i
     const int tpb = max(2 * kCalibStreams, (n_tokens + ranges - 1) / ranges);
     const dim3 vgrid((n_tokens + tpb - 1) / tpb, slot_blocks);
     if (q_type == TRIA_F32)
-      k_calib_acc<float><<<vgrid, kCalibVecThreads, 0, st>>>((const float*)q, n_tokens, n_q_heads, head_dim, tpb, acc);
+      k_calib_acc<float><<<vgrid, kCalibVecThreads, 0, st>>>((const float*)q, n_tokens, n_q_heads, head_dim, fcr,
+                                                             tpb, acc);
     else
-      k_calib_acc<__half><<<vgrid, kCalibVecThreads, 0, st>>>((const __half*)q, n_tokens, n_q_heads, head_dim, tpb, acc);
+      k_calib_acc<__half><<<vgrid, kCalibVecThreads, 0, st>>>((const __half*)q, n_tokens, n_q_heads, head_dim, fcr,
+                                                              tpb, acc);
   } else if (q_type == TRIA_F32) {
-    k_calib_acc_scalar<float><<<grid, kCalibWarps * 32, 0, st>>>((const float*)q, n_tokens, n_q_heads, head_dim, acc);
+    k_calib_acc_scalar<float><<<grid, kCalibWarps * 32, 0, st>>>((const float*)q, n_tokens, n_q_heads, head_dim,
+                                                                 fcr, acc);
   } else {
-    k_calib_acc_scalar<__half><<<grid, kCalibWarps * 32, 0, st>>>((const __half*)q, n_tokens, n_q_heads, head_dim, acc);
+    k_calib_acc_scalar<__half><<<grid, kCalibWarps * 32, 0, st>>>((const __half*)q, n_tokens, n_q_heads, head_dim,
+                                                                  fcr, acc);
   }
   return cudaGetLastError() == cudaSuccess ? TRIA_OK : TRIA_ERR_CUDA;
 }
 
 extern "C" tria_status tria_calib_finish(const double* acc, int64_t n_tokens, int32_t n_q_heads, int32_t head_dim,
-                                         float* q_mean, float* q_abs, void* stream) {
+                                         int32_t nonrot_dim, float* q_mean, float* q_abs, float* q_nonrot,
+                                         void* stream) {
   if (!acc || !q_mean || !q_abs || n_tokens <= 0 || n_q_heads < 1) return TRIA_ERR_INVALID_ARG;
   if (((uintptr_t)acc & 7u) != 0 || !aligned4(q_mean) || !aligned4(q_abs)) return TRIA_ERR_INVALID_ARG;
   if (head_dim < 2 || head_dim % 2 != 0 || head_dim > 2 * kCalibMaxPairs) return TRIA_ERR_UNSUPPORTED;
+  if (nonrot_dim < 0 || nonrot_dim % 2 != 0 || nonrot_dim >= head_dim) return TRIA_ERR_INVALID_ARG;
+  if (nonrot_dim > 0 && (!q_nonrot || !aligned4(q_nonrot))) return TRIA_ERR_INVALID_ARG;
   const int n = n_q_heads * (head_dim / 2);
-  k_calib_finish<<<(n + 255) / 256, 256, 0, (cudaStream_t)stream>>>(acc, 1.0 / (double)n_tokens, n, q_mean, q_abs);
+  k_calib_finish<<<(n + 255) / 256, 256, 0, (cudaStream_t)stream>>>(
+      acc, 1.0 / (double)n_tokens, n_q_heads, head_dim / 2, (head_dim - nonrot_dim) / 2, q_mean, q_abs, q_nonrot);
   return cudaGetLastError() == cudaSuccess ? TRIA_OK : TRIA_ERR_CUDA;
 }

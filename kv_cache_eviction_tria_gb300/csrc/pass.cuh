@@ -740,7 +740,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
     };
     if (p_beg < p_end) {
       Body body;
-      body.init(lane);
+      body.init(lane, FC);
       int seg = seg_of(p_beg, 0);
       PSeg sv = pass_seg(P, seg);
       issue(p_beg, seg, sv, 0);
@@ -809,7 +809,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
           cp_async_wait<1>();   // this piece's scales (the next piece's may still be in flight)
           __syncwarp();
         }
-        body.piece(ring + st * kPassPieceBytes, sc_ring + st * kPassScaleStage, rows, P.k_rb, P.ks_rb,
+        body.template piece_t<S / 2>(ring + st * kPassPieceBytes, sc_ring + st * kPassScaleStage, rows, P.k_rb, P.ks_rb,
                    P.raw + (size_t)(sv.wrow0 + r0) * G);
         __syncwarp();
         if (p + 1 == p_end) finish_run(p_end);

@@ -9,7 +9,11 @@
 //
 // Per row r and query head h of the segment's group:
 //   raw_h(r) = sum_f  Wr_{h,f} K[r][f] + Wi_{h,f} K[r][f+fc] + M_{h,f} |k_f|
-// with W = qbar E_f e^{i w_f p} and M = q_abs - |qbar|.
+// with W = qbar E_f e^{i w_f p} and M = q_abs - |qbar|. Heads whose last
+// nonrot dims are not rotary pair the fcr = (hd - nonrot) / 2 rotary pairs as
+// (f, f + fcr) and add nonrot / 2 content pairs (f + fcr, f + fc) of
+// frequency 0 and M = 0: their phase term is the mean non-rotary query's dot
+// product with those dims ([Doc] §4 gate field nonrot=, §6 non-rotary models).
 //
 // Work layout (persistent, one CTA per SM): the live rows of all segments are
 // cut into pieces of at most 8 KB of keys; the pieces, in segment order, are
@@ -298,6 +302,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1) k_score(const __grid_constan
   const int f0 = q * PPT;
   const int fc = P.fc;
   const bool lane_on = f0 < fc;
+  // pairs f < fcr are rotary, (f, f + fcr); the rest are the content pairs of
+  // the non-rotary dims, (f + fcr, f + fc), with no norm term (fcr % PPT == 0)
+  const bool lane_rot = f0 < P.fcr;
+  const int e_re = lane_rot ? f0 : f0 + P.fcr, e_im = lane_rot ? f0 + P.fcr : f0 + fc;
 
   // this lane's slice of W (real / imaginary) and M for the current segment,
   // on pairs of consecutive frequencies
@@ -415,12 +423,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1) k_score(const __grid_constan
         float2 kr[PPT / 2], ki[PPT / 2];
         if (rr < rows && lane_on) {
           const uint8_t* row = buf + (size_t)rr * P.k_rb;
-          Loader<KT, PPT>::half(row, f0, kr);
-          Loader<KT, PPT>::half(row, fc + f0, ki);
+          Loader<KT, PPT>::half(row, e_re, kr);
+          Loader<KT, PPT>::half(row, e_im, ki);
           if constexpr (KT == TRIA_Q8_0) {
             const __half* sc = reinterpret_cast<const __half*>(P.ks + (size_t)(grow + rr) * P.ks_rb);
-            const float d1 = __half2float(sc[f0 >> 5]);
-            const float d2 = __half2float(sc[(fc + f0) >> 5]);
+            const float d1 = __half2float(sc[e_re >> 5]);
+            const float d2 = __half2float(sc[e_im >> 5]);
 #pragma unroll
             for (int j = 0; j < PPT / 2; ++j) {
               kr[j] = __fmul2_rn(kr[j], make_float2(d1, d1));
@@ -435,7 +443,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) k_score(const __grid_constan
 #pragma unroll
         for (int j = 0; j < PPT / 2; ++j) {
           const float2 sq = __ffma2_rn(ki[j], ki[j], __fmul2_rn(kr[j], kr[j]));
-          mag[j] = make_float2(sqrt_approx(sq.x), sqrt_approx(sq.y));
+          mag[j] = lane_rot ? make_float2(sqrt_approx(sq.x), sqrt_approx(sq.y)) : make_float2(0.f, 0.f);
         }
 #pragma unroll
         for (int h = 0; h < G; ++h) {
@@ -578,7 +586,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) k_score_tc(const __grid_cons
   };
 
   Body body;
-  body.init(lane);
+  body.init(lane, P.fcr);
   auto load_consts = [&](const SegView& v) {
     body.load_consts(P.qe + P.seq[v.s].qe_off + (size_t)v.g * G * FC, P.mw + P.seq[v.s].qe_off + (size_t)v.g * G * FC,
                      s_turns, (unsigned long long)P.seq[v.s].cur_pos);
@@ -741,6 +749,7 @@ bool launch_score_tc_k(const Pass& P, cudaStream_t st, cudaError_t* err) {
 }
 
 bool launch_score_tc(const Pass& P, cudaStream_t st, cudaError_t* err) {
+  if (P.fcr % 32 != 0) return false;   // rotary pairs in whole 32-pair steps
   if (P.k_type == TRIA_F16) return launch_score_tc_k<TRIA_F16>(P, st, err);
   if (P.k_type == TRIA_Q8_0) return launch_score_tc_k<TRIA_Q8_0>(P, st, err);
   return false;

@@ -26,6 +26,16 @@
 // B, which a contraction is free to permute), so no transposing load is
 // needed. Real and imaginary parts of a frequency sit in steps s and
 // s + S/2 at the same lane and register position.
+//
+// Heads with non-rotary dims (the last nonrot of head_dim are never rotated;
+// the first rot = head_dim - nonrot are NEOX pairs (f, f + rot/2)): the
+// statistics loader extends the rot/2 rotary pairs with nonrot/2 "content
+// pairs" (rot + e, rot + nonrot/2 + e) of frequency 0 and norm weight 0, whose
+// phase term is exactly the mean non-rotary query's dot product with those
+// dims. With rot a multiple of 64, pair step s (32 pairs) is all rotary for
+// s < hr = rot/64 (real parts in step s, imaginary in step s + hr) and all
+// content otherwise (steps s + hr and s + S/2); the norm term runs on the
+// rotary pair steps only.
 #pragma once
 
 #include "tria_internal.cuh"
@@ -126,13 +136,16 @@ struct TcBody {
   static_assert(SH::kOk, "tensor-core body shape");
 
   int g, q, oh, hl;
+  int hr;                           // rotary pair steps (S / 2 when every dim is rotary)
   bool owriter;
   uint32_t bp[S][NT][4];            // phase weights, fp16 pairs
   uint32_t bm[S / 2][NT][4][2];     // magnitude weights, tf32
   float unscale[kHeads];
   Mom run[kHeads];
 
-  __device__ __forceinline__ void init(int lane) {
+  // fcr: rotary frequency pairs of the head (a multiple of 32)
+  __device__ __forceinline__ void init(int lane, int fcr) {
+    hr = fcr / 32;
     g = lane >> 2;
     q = lane & 3;
     oh = G == 8 ? 2 * q : (G == 4 ? 2 * (q & 1) : 0);
@@ -227,6 +240,16 @@ struct TcBody {
   // to out[row * G + head] and adds the rows to the running moments.
   __device__ __forceinline__ void piece(const uint8_t* buf, const uint8_t* scb, int rows, int k_rb, int ks_rb,
                                         float* out) {
+    if (hr == S / 2) piece_t<S / 2>(buf, scb, rows, k_rb, ks_rb, out);
+    else piece_t<-1>(buf, scb, rows, k_rb, ks_rb, out);
+  }
+
+  // The body for HR rotary pair steps (-1: the runtime hr); HR = S / 2 is the
+  // all-rotary head with every step offset a constant.
+  template <int HR>
+  __device__ __forceinline__ void piece_t(const uint8_t* buf, const uint8_t* scb, int rows, int k_rb, int ks_rb,
+                                          float* out) {
+    const int hr_ = HR >= 0 ? HR : hr;
     // shifted sums of this piece for my output heads
     float shift[kHeads], m1[kHeads], m2[kHeads], cnt[kHeads];
 #pragma unroll
@@ -263,10 +286,12 @@ struct TcBody {
         const uint8_t* rg8 = rg + (size_t)8 * k_rb;
 #pragma unroll
         for (int s2 = 0; s2 < S / 2; ++s2) {
-          const uint4 kr0 = *reinterpret_cast<const uint4*>(rg + 64 * s2);
-          const uint4 kr8 = *reinterpret_cast<const uint4*>(rg8 + 64 * s2);
-          const uint4 ki0 = *reinterpret_cast<const uint4*>(rg + 64 * (s2 + S / 2));
-          const uint4 ki8 = *reinterpret_cast<const uint4*>(rg8 + 64 * (s2 + S / 2));
+          const bool rotary = s2 < hr_;
+          const int sr = rotary ? s2 : s2 + hr_, si = rotary ? s2 + hr_ : s2 + S / 2;   // real / imaginary steps
+          const uint4 kr0 = *reinterpret_cast<const uint4*>(rg + 64 * sr);
+          const uint4 kr8 = *reinterpret_cast<const uint4*>(rg8 + 64 * sr);
+          const uint4 ki0 = *reinterpret_cast<const uint4*>(rg + 64 * si);
+          const uint4 ki8 = *reinterpret_cast<const uint4*>(rg8 + 64 * si);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             mma_f16(acc[nt], kr0.x, kr8.x, kr0.y, kr8.y, bp[s2][nt][0], bp[s2][nt][1]);
@@ -275,6 +300,7 @@ struct TcBody {
             mma_f16(acc[nt], kr0.z, kr8.z, kr0.w, kr8.w, bp[s2][nt][2], bp[s2][nt][3]);
             mma_f16(di, ki0.z, ki8.z, ki0.w, ki8.w, bp[s2 + S / 2][nt][2], bp[s2 + S / 2][nt][3]);
           }
+          if (!rotary) continue;   // content pairs: no norm term
           float mg0[8], mg8[8];
           granule_mag(kr0, ki0, mg0);
           granule_mag(kr8, ki8, mg8);
@@ -304,12 +330,14 @@ struct TcBody {
         const __half* sg8 = reinterpret_cast<const __half*>(scb + (size_t)(16 * mt + g + 8) * ks_rb);
 #pragma unroll
         for (int s2 = 0; s2 < S / 2; ++s2) {
-          const uint2 wr0 = *reinterpret_cast<const uint2*>(rg + 32 * s2);
-          const uint2 wr8 = *reinterpret_cast<const uint2*>(rg8 + 32 * s2);
-          const uint2 wi0 = *reinterpret_cast<const uint2*>(rg + 32 * (s2 + S / 2));
-          const uint2 wi8 = *reinterpret_cast<const uint2*>(rg8 + 32 * (s2 + S / 2));
-          const float dr0 = __half2float(sg0[s2]), dr8 = __half2float(sg8[s2]);
-          const float di0 = __half2float(sg0[s2 + S / 2]), di8 = __half2float(sg8[s2 + S / 2]);
+          const bool rotary = s2 < hr_;
+          const int sr = rotary ? s2 : s2 + hr_, si = rotary ? s2 + hr_ : s2 + S / 2;   // real / imaginary blocks
+          const uint2 wr0 = *reinterpret_cast<const uint2*>(rg + 32 * sr);
+          const uint2 wr8 = *reinterpret_cast<const uint2*>(rg8 + 32 * sr);
+          const uint2 wi0 = *reinterpret_cast<const uint2*>(rg + 32 * si);
+          const uint2 wi8 = *reinterpret_cast<const uint2*>(rg8 + 32 * si);
+          const float dr0 = __half2float(sg0[sr]), dr8 = __half2float(sg8[sr]);
+          const float di0 = __half2float(sg0[si]), di8 = __half2float(sg8[si]);
           uint32_t ar0[4], ar8[4], ai0[4], ai8[4];
           i8x4_to_h2x2(wr0.x, ar0[0], ar0[1]);
           i8x4_to_h2x2(wr0.y, ar0[2], ar0[3]);
@@ -331,6 +359,7 @@ struct TcBody {
             acc[nt][2] = fmaf(tr[2], dr8, fmaf(ti[2], di8, acc[nt][2]));
             acc[nt][3] = fmaf(tr[3], dr8, fmaf(ti[3], di8, acc[nt][3]));
           }
+          if (!rotary) continue;   // content pairs: no norm term
           float mg0[8], mg8[8];
           q8_mag(ar0, ai0, dr0, di0, mg0);
           q8_mag(ar8, ai8, dr8, di8, mg8);

@@ -94,6 +94,7 @@ struct SeqInfo {
 // Everything a kernel of the pass needs, passed by value.
 struct Pass {
   int32_t n_seqs, n_kv, n_seg, G, hd, fc;
+  int32_t fcr;                        // rotary pairs of fc (fc when every dim is rotary)
   int32_t window;
   int32_t k_type, v_type;
   int32_t k_rb, ks_rb, v_rb, vs_rb;   // bytes per row of each plane (0: absent)
@@ -561,7 +562,9 @@ tria_status check_policy(const tria_layer_cache* c, const tria_policy* p, bool n
 // Opaque stats handle of the C ABI.
 struct tria_stats {
   int32_t n_layers, n_q_heads, n_kv_heads, group;
-  float2* qe;                  // per loaded layer l: [n_kv][G][fc_l] from qe_off[l]
+  int32_t nonrot_dim;          // non-rotary dims of every head (the last ones)
+  float2* qe;                  // per loaded layer l: [n_kv][G][fc_l] from qe_off[l]; fc_l = head_dim_l / 2
+                               // pairs: the rotary ones, then the content pairs of the non-rotary dims
   float* mw;                   // same layout as qe
   unsigned long long* turns;   // per loaded layer l: [fc_l] from turns_off[l]
   std::vector<int32_t> head_dim;     // [L]

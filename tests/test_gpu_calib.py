@@ -70,3 +70,42 @@ def test_calibrated_stats_load(lib):
     np.testing.assert_allclose(qm[0], ref_mean, rtol=1e-5, atol=1e-6)
     np.testing.assert_allclose(qa[0], ref_abs, rtol=1e-5, atol=1e-6)
     st.close()
+
+
+NONROT_CASES = [
+    # tokens, heads, head_dim, nonrot, dtype
+    (1000, 8, 128, 64, "f16"),    # vector body, content vectors after the rotary ones
+    (513, 4, 256, 192, "f32"),
+    (300, 2, 96, 32, "f16"),
+    (77, 3, 128, 8, "f32"),       # 60 rotary pairs: not whole fp32 vectors -> scalar body
+    (50, 2, 6, 2, "f32"),         # scalar body, one content pair
+]
+
+
+@pytest.mark.parametrize("t,h,hd,nonrot,dtype", NONROT_CASES)
+def test_calibration_non_rotary_dims(lib, t, h, hd, nonrot, dtype):
+    """Heads whose last nonrot dims are not rotary: rotary pairs (f, f + rot/2)
+    and the mean non-rotary query, against calibrate / calibrate_nonrot."""
+    import torch
+    q = _queries(t, h, hd, dtype, seed=3 * t + hd + nonrot)
+    acc = torch.zeros((h, hd // 2, 3), dtype=torch.float64, device="cuda")
+    lib.calib_accumulate(torch.from_numpy(q).cuda(), acc, nonrot_dim=nonrot)
+    q_mean, q_abs, q_nonrot = lib.calib_finish(acc, t, nonrot_dim=nonrot)
+    torch.cuda.synchronize()
+    q64 = q.astype(np.float64)
+    ref_mean, ref_abs = O.calibrate(q64, nonrot)
+    ref_nonrot = O.calibrate_nonrot(q64, nonrot)
+    scale = np.abs(q64).mean()
+    np.testing.assert_allclose(q_mean.cpu().numpy(), ref_mean, rtol=1e-5, atol=1e-5 * scale)
+    np.testing.assert_allclose(q_abs.cpu().numpy(), ref_abs, rtol=1e-5, atol=1e-5 * scale)
+    np.testing.assert_allclose(q_nonrot.cpu().numpy(), ref_nonrot, rtol=1e-5, atol=1e-5 * scale)
+
+
+def test_calibration_non_rotary_host_checks(lib):
+    import torch
+    acc = torch.zeros((2, 32, 3), dtype=torch.float64, device="cuda")
+    q = torch.zeros((4, 2, 64), dtype=torch.float32, device="cuda")
+    for bad in (-2, 3, 64):
+        with pytest.raises(lib.TriaError) as err:
+            lib.calib_accumulate(q, acc, nonrot_dim=bad)
+        assert err.value.status == lib.ERR_INVALID_ARG

@@ -59,7 +59,7 @@ def test_library_exports_every_declared_function(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert tria.version() == 1
+    assert tria.version() == 2
     for code in range(9):
         assert tria.status_string(code) not in ("", "unknown status")
     assert tria.status_string(99) == "unknown status"
@@ -85,6 +85,19 @@ def test_gate_log_line_matches_the_documented_line(lib):
     assert st == tria.ERR_UNSUPPORTED and line.endswith("-> ineligible (head_dim > 256)") and "is_q8_0=0" in line
     st, line = tria.gate_describe(30, 8, 128, "q8_0")
     assert st == tria.ERR_UNSUPPORTED and "(nh % nkv != 0)" in line
+
+
+def test_gate_non_rotary_dims(lib):
+    """Heads with non-rotary dims: the gate line carries nonrot=; eligible
+    when the rotary dims are a multiple of 16, invalid outside [0, head_dim)."""
+    st, line = tria.gate_describe(32, 8, 128, "f16", nonrot_dim=64)
+    assert st == tria.OK and "hd=128 nonrot=64 -> eligible" in line
+    assert tria.gate_check(32, 8, 256, 192) == tria.OK
+    assert tria.gate_check(32, 8, 128, 16) == tria.OK          # 112 rotary dims
+    st, line = tria.gate_describe(32, 8, 128, "q8_0", nonrot_dim=8)
+    assert st == tria.ERR_UNSUPPORTED and line.endswith("(rotary dims % 16 != 0)")
+    assert tria.gate_check(32, 8, 128, 128) == tria.ERR_INVALID_ARG
+    assert tria.gate_check(32, 8, 128, -2) == tria.ERR_INVALID_ARG
 
 
 def test_budget_rows_and_trigger(lib):
@@ -218,22 +231,27 @@ def test_calibration_argument_checks(lib):
     # rejected on the host before any launch (fake, aligned pointers are never touched)
     q, acc = ctypes.c_void_p(0x100000), ctypes.c_void_p(0x200000)
     call = lambda *a: tria.raw_call("tria_calib_accumulate", *a)
-    assert call(None, tria.F16, 8, 4, 128, acc, None) == tria.ERR_INVALID_ARG
-    assert call(q, tria.F16, 8, 4, 128, None, None) == tria.ERR_INVALID_ARG
-    assert call(q, tria.F16, -1, 4, 128, acc, None) == tria.ERR_INVALID_ARG
-    assert call(q, tria.F16, 8, 0, 128, acc, None) == tria.ERR_INVALID_ARG
-    assert call(ctypes.c_void_p(0x100002), tria.F16, 8, 4, 128, acc, None) == tria.ERR_INVALID_ARG
-    assert call(q, tria.F16, 8, 4, 128, ctypes.c_void_p(0x200004), None) == tria.ERR_INVALID_ARG
-    assert call(q, tria.Q8_0, 8, 4, 128, acc, None) == tria.ERR_UNSUPPORTED
-    assert call(q, tria.F32, 8, 4, 127, acc, None) == tria.ERR_UNSUPPORTED
-    assert call(q, tria.F32, 8, 4, 1024, acc, None) == tria.ERR_UNSUPPORTED
-    assert call(q, tria.F32, 0, 4, 128, acc, None) == tria.OK   # nothing to add, no launch
-    assert call(None, tria.F32, 0, 4, 128, acc, None) == tria.OK
+    assert call(None, tria.F16, 8, 4, 128, 0, acc, None) == tria.ERR_INVALID_ARG
+    assert call(q, tria.F16, 8, 4, 128, 0, None, None) == tria.ERR_INVALID_ARG
+    assert call(q, tria.F16, -1, 4, 128, 0, acc, None) == tria.ERR_INVALID_ARG
+    assert call(q, tria.F16, 8, 0, 128, 0, acc, None) == tria.ERR_INVALID_ARG
+    assert call(ctypes.c_void_p(0x100002), tria.F16, 8, 4, 128, 0, acc, None) == tria.ERR_INVALID_ARG
+    assert call(q, tria.F16, 8, 4, 128, 0, ctypes.c_void_p(0x200004), None) == tria.ERR_INVALID_ARG
+    assert call(q, tria.Q8_0, 8, 4, 128, 0, acc, None) == tria.ERR_UNSUPPORTED
+    assert call(q, tria.F32, 8, 4, 127, 0, acc, None) == tria.ERR_UNSUPPORTED
+    assert call(q, tria.F32, 8, 4, 1024, 0, acc, None) == tria.ERR_UNSUPPORTED
+    assert call(q, tria.F32, 0, 4, 128, 0, acc, None) == tria.OK   # nothing to add, no launch
+    assert call(None, tria.F32, 0, 4, 128, 0, acc, None) == tria.OK
     fin = lambda *a: tria.raw_call("tria_calib_finish", *a)
     qm, qa = ctypes.c_void_p(0x300000), ctypes.c_void_p(0x400000)
-    assert fin(acc, 0, 4, 128, qm, qa, None) == tria.ERR_INVALID_ARG
-    assert fin(acc, 10, 4, 128, None, qa, None) == tria.ERR_INVALID_ARG
-    assert fin(acc, 10, 4, 130000, qm, qa, None) == tria.ERR_UNSUPPORTED
+    assert fin(acc, 0, 4, 128, 0, qm, qa, None, None) == tria.ERR_INVALID_ARG
+    assert fin(acc, 10, 4, 128, 0, None, qa, None, None) == tria.ERR_INVALID_ARG
+    assert fin(acc, 10, 4, 130000, 0, qm, qa, None, None) == tria.ERR_UNSUPPORTED
+    # non-rotary dims: even, in [0, head_dim); the finish needs q_nonrot then
+    assert call(q, tria.F16, 8, 4, 128, 3, acc, None) == tria.ERR_INVALID_ARG
+    assert call(q, tria.F16, 8, 4, 128, 128, acc, None) == tria.ERR_INVALID_ARG
+    assert fin(acc, 10, 4, 128, 64, qm, qa, None, None) == tria.ERR_INVALID_ARG
+    assert fin(acc, 10, 4, 128, -2, qm, qa, ctypes.c_void_p(0x500000), None) == tria.ERR_INVALID_ARG
 
 
 def test_select_noalloc_host_checks_match_select(lib):
