@@ -30,6 +30,9 @@
 //    warp's stage, publish "read", wait (bounded) for the lower blocks that
 //    read its destination rows, store. The next block's claim and keep
 //    entries load while the current block's rows load.
+//  * Final moves: once every segment is selected (a grid barrier), the
+//    blocks left move in k_move's block-major order, with the whole dynamic
+//    shared memory as move stages (224 KB).
 //  * The last CTA to finish sets n_live and resets the call's counters.
 // The scored / ready lists and the per-segment counters live at a fixed
 // place of the workspace (PassCtl). Every wait is bounded
@@ -72,6 +75,7 @@ struct FPass {
   int32_t spin_limit;
   int32_t piece_rows;   // key rows per piece
   int32_t cs_max;       // columns of a segment's run-partial table (>= its score runs)
+  int32_t dyn_bytes;    // dynamic shared memory of the launch (set by the launcher)
   int32_t c_max;        // chunks per segment (max)
   int64_t rows_per_layer;   // workspace rows of one layer
   const float2* qe;
@@ -127,6 +131,9 @@ struct PassSmem {
   static constexpr int kTurns = kFirst + ((kPassMaxSegs + 1) * 4 + 15) / 16 * 16;
   static constexpr int kBytes = kTurns + 128 * 8;
 };
+// The final move phase reuses all of it (and a little more) as move stages:
+// k_move's 224 KB, seven 32 KB stages of head_dim-256 fp16 key + value rows.
+constexpr int kPassDynBytes = PassSmem::kBytes > kMoveSmemLimit ? PassSmem::kBytes : kMoveSmemLimit;
 
 template <int G>
 __device__ __forceinline__ void load_raw_g(const float* rp, float* x) {
@@ -179,7 +186,10 @@ __device__ __noinline__ void pass_select(const FPass& P, int sg, int nr, uint32_
   constexpr int UB = kSmem ? 1 : 16;   // key loads in flight per thread (global keys)
 
   float mu[G], inv[G];
-  block_moments_of_runs<G>(P.parts + (size_t)sg * kRunCols * P.cs_max, P.cs_max, nr, mu, inv);
+  // the histogram's words serve as the merge's scratch first
+  block_moments_of_runs<G>(P.parts + (size_t)sg * kRunCols * P.cs_max, P.cs_max, nr, mu, inv,
+                           reinterpret_cast<float*>(hist));
+  __syncthreads();
   for (int i = tid; i < kHistBins; i += blockDim.x) hist[i] = 0u;
   __syncthreads();
 
@@ -891,6 +901,11 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
       }
     }
     if (mover && lane == 0) bulk_wait_all();   // the stores of the service loop
+    // the ring barriers are done with: their words become move stages
+    if (lane == 0) {
+      mbar_inval(&bars[0]);
+      mbar_inval(&bars[1]);
+    }
     // every segment is selected (each CTA finished its selects before here):
     // the moves left, in k_move's order
     __shared__ int s_span;
@@ -903,7 +918,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
       atomicMax(&s_span, nb - min(nb, __ldcg(P.ctl->move_next + sg)));
     }
     __syncthreads();
-    pass_moves_final(P, stg, s_src[warp], tag, n_active, min(kPassWarps, kPassRing / L.bytes), s_span);
+    pass_moves_final(P, stg, s_src[warp], tag, n_active, min(kPassWarps, P.dyn_bytes / L.bytes), s_span);
   }
 
   // ---- the last CTA: n_live of the active sequences, counters reset
@@ -961,31 +976,41 @@ inline bool pass_supported(int k_type, int hd, int G) {
   return hd == 256 && G <= 4;
 }
 
-cudaError_t launch_pass_f16(const FPass& P, cudaStream_t st);   // pass_f16.cu
-cudaError_t launch_pass_q8(const FPass& P, cudaStream_t st);    // pass_q8.cu
+cudaError_t launch_pass_f16(FPass& P, cudaStream_t st);   // pass_f16.cu
+cudaError_t launch_pass_q8(FPass& P, cudaStream_t st);    // pass_q8.cu
 
+// Sets P.dyn_bytes: the dynamic shared memory of the launch, kPassDynBytes
+// or what the kernel's static shared memory leaves of the per-block limit
+// (at least the scoring layout's).
 template <int KT, int G, int S>
-cudaError_t launch_pass_t(const FPass& P, cudaStream_t st) {
+cudaError_t launch_pass_t(FPass& P, cudaStream_t st) {
   auto kern = k_pass<KT, G, S>;
-  static const cudaError_t attr = set_smem_attrs(kern, PassSmem::kBytes);
-  if (attr != cudaSuccess) return attr;
-  static int grid = 0;
+  static int grid = 0, dyn = 0;
   if (grid == 0) {
-    int dev = 0, sms = 0, per_sm = 0;
+    int dev = 0, sms = 0, per_sm = 0, optin = 0;
+    cudaFuncAttributes fa{};
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kPassThreads, PassSmem::kBytes);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    int d = optin - (int)fa.sharedSizeBytes;
+    d = (d < kPassDynBytes ? d : kPassDynBytes) & ~127;
+    if (d < PassSmem::kBytes) return cudaErrorInvalidConfiguration;
+    e = set_smem_attrs(kern, d);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kPassThreads, d);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    dyn = d;
     grid = sms;   // one CTA per SM
   }
-  void* args[] = {const_cast<FPass*>(&P)};
-  return cudaLaunchCooperativeKernel((const void*)kern, dim3(grid), dim3(kPassThreads), args,
-                                     (size_t)PassSmem::kBytes, st);
+  P.dyn_bytes = dyn;
+  void* args[] = {&P};
+  return cudaLaunchCooperativeKernel((const void*)kern, dim3(grid), dim3(kPassThreads), args, (size_t)dyn, st);
 }
 
 template <int KT>
-cudaError_t launch_pass_k(const FPass& P, cudaStream_t st) {
+cudaError_t launch_pass_k(FPass& P, cudaStream_t st) {
   switch (P.hd) {
     case 64:
       switch (P.G) {

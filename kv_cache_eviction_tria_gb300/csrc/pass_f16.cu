@@ -3,6 +3,6 @@
 
 namespace tria {
 
-cudaError_t launch_pass_f16(const FPass& P, cudaStream_t st) { return launch_pass_k<TRIA_F16>(P, st); }
+cudaError_t launch_pass_f16(FPass& P, cudaStream_t st) { return launch_pass_k<TRIA_F16>(P, st); }
 
 }  // namespace tria

@@ -3,6 +3,6 @@
 
 namespace tria {
 
-cudaError_t launch_pass_q8(const FPass& P, cudaStream_t st) { return launch_pass_k<TRIA_Q8_0>(P, st); }
+cudaError_t launch_pass_q8(FPass& P, cudaStream_t st) { return launch_pass_k<TRIA_Q8_0>(P, st); }
 
 }  // namespace tria

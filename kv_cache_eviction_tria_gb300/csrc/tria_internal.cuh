@@ -228,6 +228,10 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
 
+__device__ __forceinline__ void mbar_inval(uint64_t* bar) {
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -414,10 +418,12 @@ __device__ __forceinline__ void moments_from_sums(const float* c, const float* s
 
 // Moments of one segment from its run partials (tab: kRunCols columns of cs
 // floats, runs 0 .. nr-1), merged by one block; see block_segment_moments.
+// scratch: shared memory for 33 x (1 + 2G) floats; the block may reuse it
+// once it has passed a __syncthreads after the call.
 template <int G>
-__device__ void block_moments_of_runs(const float* tab, int cs, int nr, float* mu, float* inv) {
-  __shared__ float red[32][1 + 2 * G];
-  __shared__ float sums[1 + 2 * G];
+__device__ void block_moments_of_runs(const float* tab, int cs, int nr, float* mu, float* inv, float* scratch) {
+  float (*red)[1 + 2 * G] = reinterpret_cast<float (*)[1 + 2 * G]>(scratch);
+  float* sums = scratch + 32 * (1 + 2 * G);
   float c[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) c[h] = __ldcg(&tab[(1 + h) * cs]);
@@ -466,6 +472,12 @@ __device__ void block_moments_of_runs(const float* tab, int cs, int nr, float* m
   }
   __syncthreads();
   moments_from_sums<G>(c, sums, mu, inv);
+}
+
+template <int G>
+__device__ void block_moments_of_runs(const float* tab, int cs, int nr, float* mu, float* inv) {
+  __shared__ float scratch[33 * (1 + 2 * G)];
+  block_moments_of_runs<G>(tab, cs, nr, mu, inv, scratch);
 }
 
 // Mean and 1 / (std + 1e-6) of the segment's heads, merged by one block
