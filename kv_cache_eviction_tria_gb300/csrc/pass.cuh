@@ -183,7 +183,7 @@ __device__ __noinline__ void pass_select(const FPass& P, int sg, int nr, uint32_
   const int n = v.n, lo = v.sink, hi = n - P.window;
   const int k = v.B - v.sink - P.window;
   const KeyStore<kSmem> keys{kSmem ? smem_keys : P.keys + v.wrow0};
-  constexpr int UB = kSmem ? 1 : 16;   // key loads in flight per thread (global keys)
+  constexpr int UB = kSmem ? 1 : 32;   // key loads in flight per thread (global keys)
 
   float mu[G], inv[G];
   // the histogram's words serve as the merge's scratch first
@@ -194,17 +194,28 @@ __device__ __noinline__ void pass_select(const FPass& P, int sg, int nr, uint32_
   __syncthreads();
 
   // z-max keys of every live row and the first radix histogram of the
-  // candidates [lo, hi); loads of U rows per thread are in flight together
+  // candidates [lo, hi); loads of U rows per thread are in flight together,
+  // and the next batch's lines are asked for in L2 meanwhile (one prefetch
+  // per 128-byte line, by the thread whose row starts it)
   {
     constexpr int U = G > 4 ? 4 : (G == 4 ? 8 : 16);   // raw rows in flight per thread
+    constexpr int kRowsPerLine = 128 / (4 * G);
     const float* raw = P.raw + (size_t)v.wrow0 * G;
     float* so = P.score_out ? P.score_out + v.wrow0 : nullptr;
+    const bool line_head = (v.wrow0 + tid) % kRowsPerLine == 0;   // rows of this thread start lines
     for (int base = tid; base < n; base += U * kPassThreads) {
       float x[U][G];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int r = base + u * kPassThreads;
         if (r < n) load_raw_g<G>(raw + (size_t)r * G, x[u]);
+      }
+      if (line_head) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int r = base + (U + u) * kPassThreads;
+          if (r < n) asm volatile("prefetch.global.L2 [%0];" ::"l"(raw + (size_t)r * G));
+        }
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
