@@ -263,6 +263,14 @@ tria_status tria_evict(const tria_stats* stats, int32_t layer, const tria_layer_
 tria_status tria_evict_staged(const tria_stats* stats, int32_t layer, const tria_layer_cache* cache,
                               const tria_policy* policy, void* ws, size_t ws_bytes, void* stream);
 
+/* Byte offset, in a workspace laid out for `cache` (tria_workspace_size), of
+ * the float array [rows] where the staged evict path keeps the z-max score it
+ * selected with ([Doc] §5 Phase C): after tria_evict_staged, element r holds
+ * s(r) for every live row r (before compaction) of each segment above its
+ * budget; other rows are not written. The fused kernel keeps its scores
+ * elsewhere (tria_evict_model's score_out). 0 on invalid input. No GPU use. */
+size_t tria_workspace_score_offset(const tria_layer_cache* cache);
+
 /* Workspace bytes for tria_evict_model over n_layers layers of caches shaped
  * like `cache` (also enough for every single-layer call on one of them). 0 on
  * invalid input (n_layers outside 1 .. 128). */

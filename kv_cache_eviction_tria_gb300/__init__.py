@@ -40,7 +40,7 @@ EXPORTS = (
     "tria_calib_accumulate", "tria_calib_finish", "tria_append", "tria_schedule_check", "tria_seq_init",
     "tria_seq_prefill", "tria_seq_decode", "tria_schedule_plan", "tria_schedule_passed",
     "tria_shared_combine", "tria_shared_select",
-    "tria_status_string", "tria_version",
+    "tria_status_string", "tria_version", "tria_workspace_score_offset",
 )
 
 
@@ -184,6 +184,8 @@ def load_library(path: str | None = None):
     lib.tria_schedule_passed.restype = i32
     lib.tria_status_string.argtypes = [i32]
     lib.tria_status_string.restype = ctypes.c_char_p
+    lib.tria_workspace_score_offset.argtypes = [ctypes.POINTER(_LayerCache)]
+    lib.tria_workspace_score_offset.restype = sz
     lib.tria_version.argtypes = []
     lib.tria_version.restype = i32
     _lib = lib
@@ -359,6 +361,18 @@ def workspace_size(cache: LayerCache, group: int) -> int:
     if n == 0:
         raise TriaError(ERR_INVALID_ARG, "tria_workspace_size")
     return n
+
+
+def workspace_scores(ws, cache: LayerCache):
+    """tria_workspace_score_offset: the workspace's float view of the z-max
+    scores the staged evict path selected with (valid after evict_staged for
+    the live rows of segments above their budget)."""
+    c = cache.c_struct()
+    off = load_library().tria_workspace_score_offset(ctypes.byref(c))
+    if off == 0:
+        raise TriaError(ERR_INVALID_ARG, "tria_workspace_score_offset")
+    rows = int(max(r0 + cache.n_kv_heads * cp for r0, cp in zip(cache.seq_row0, cache.capacity)))
+    return ws[off:off + 4 * rows].view(__import__("torch").float32)
 
 
 def workspace_init(ws, stream=None):

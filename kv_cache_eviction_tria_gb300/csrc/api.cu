@@ -778,4 +778,9 @@ extern "C" const char* tria_status_string(tria_status s) {
   return "unknown status";
 }
 
+extern "C" size_t tria_workspace_score_offset(const tria_layer_cache* cache) {
+  if (check_cache(cache) != TRIA_OK) return 0;
+  return make_layout(cache, 0).score;
+}
+
 extern "C" int32_t tria_version(void) { return TRIA_VERSION; }

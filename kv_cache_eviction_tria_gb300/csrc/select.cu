@@ -463,6 +463,7 @@ __global__ void __launch_bounds__(kClThreads) k_select_cl(const __grid_constant_
             s = (x[u][0] - mu[0]) * inv[0];
 #pragma unroll
             for (int h = 1; h < G; ++h) s = fmaxf(s, (x[u][h] - mu[h]) * inv[h]);
+            P.score[sv.row0 + r] = s;   // the evict path's z-max, kept in the workspace
           }
           keys[r - r0] = score_key(s);
         }

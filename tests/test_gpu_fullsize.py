@@ -1,7 +1,8 @@
 """Element-wise parity at full workload size, where the persistent scorer's
 every warp streams several pieces through its two-stage ring (so the second
 stage, the ring's phase flips and moment partials spanning several pieces are
-all exercised), and the cooperative grid select that takes segments over
+all exercised), the z-max score the staged evict path selects with (kept in
+the workspace), and the cooperative grid select that takes segments over
 262144 rows.
 
 Every row of each sampled segment is compared with the oracle at the stated
@@ -74,6 +75,48 @@ def test_full_size_scores_every_row(lib, name, layer, segs):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("name,layer,segs", [
+    ("qwen3_8b_layer", 0, [(0, 1), (0, 6)]),
+    ("q8_0", 2, [(0, 4)]),
+    ("batched_long", 0, None),      # the longest sequence's head 1
+])
+def test_staged_evict_zmax_every_row(lib, name, layer, segs):
+    """The z-max score the staged evict path selects with (computed inside the
+    cluster select and kept in the workspace) against the oracle, every live
+    row of sampled full-size segments, then the keep-set rule on the same rows."""
+    from synth import device as D
+    D.build()
+    w = W.get_workload(name)
+    qm, qa = W.make_stats(w)
+    st = lib.Stats(qm, qa, n_kv_heads=w.n_kv_heads, head_dim=w.head_dim, rope_theta=w.rope_theta)
+    t = D.alloc_layer(w)
+    D.fill_layer(w, layer, t)
+    pos0 = t["pos"].clone()
+    cache, pol = U.workload_cache(lib, w, t), U.workload_policy(lib, w)
+    ws = U.new_workspace(lib, cache, w.group)
+    lib.evict_staged(st, layer, cache, pol, ws=ws)
+    assert lib.device_status(ws) == lib.OK
+    zs = lib.workspace_scores(ws, cache)
+    if segs is None:
+        segs = [(int(np.argmax(w.n_live)), 1)]
+    r0s = w.seq_row0()
+    for s, g in segs:
+        n = w.n_live[s]
+        r0 = int(r0s[s] + g * w.capacity[s])
+        raw, sc = _oracle_scores(w, layer, s, g, qm, qa)
+        got = zs[r0:r0 + n].cpu().numpy()
+        err = np.abs(got - sc) / np.maximum(np.abs(sc), 1.0)
+        assert err.max() <= U.RTOL, f"{name} s{s} g{g}: z-max rel err {err.max():.3e}"
+        b = lib.budget_rows(w.budget_frac, w.n_ctx[s])
+        want = O.select_keep(sc, n, b, w.sink, w.window)
+        kept_pos = t["pos"][r0:r0 + b].cpu().numpy()
+        gk = np.searchsorted(pos0[r0:r0 + n].cpu().numpy(), kept_pos)
+        U.assert_keep_sets_match(gk, want, sc, n, b, w.sink, w.window, f"{name} s{s} g{g}")
+    st.close()
+    del t
+    torch.cuda.empty_cache()
+
+
 def _dummy_cache(lib, case):
     """A layer cache for select-only calls: key / value / position planes are
     never read by the select, so small placeholder tensors stand in for them."""
@@ -131,6 +174,10 @@ def test_evict_end_to_end_over_262144_rows(lib):
     raw, sc = O.segment_scores(kf, O.as_complex(host["q_mean"][0][hs]),
                                O.mlr_weight(host["q_mean"][0][hs], host["q_abs"][0][hs]),
                                O.rope_omega(case.hd, case.theta), case.cur_pos[0], O.default_future_offsets())
+    # the cooperative path's z-max, every row
+    got = lib.workspace_scores(ws, cache)[:n].cpu().numpy()
+    err = np.abs(got - sc) / np.maximum(np.abs(sc), 1.0)
+    assert err.max() <= U.RTOL, f"z-max rel err {err.max():.3e}"
     want = O.select_keep(sc, n, b, case.sink, case.window)
     pos_after = dev["pos"][:b].cpu().numpy()
     gk = np.searchsorted(host["pos"][:n], pos_after)

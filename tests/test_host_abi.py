@@ -254,6 +254,17 @@ def test_calibration_argument_checks(lib):
     assert fin(acc, 10, 4, 128, -2, qm, qa, ctypes.c_void_p(0x500000), None) == tria.ERR_INVALID_ARG
 
 
+def test_workspace_score_offset(lib):
+    """The staged evict path's z-max array sits inside the workspace, at the same
+    place whatever the group; invalid caches give 0."""
+    c = _fake_cache()
+    off = tria.raw_call("tria_workspace_score_offset", ctypes.byref(c.c_struct()))
+    assert 0 < off < tria.workspace_size(c, 0) <= tria.workspace_size(c, 4)
+    assert off % 256 == 0
+    bad = _fake_cache(n_kv=0)
+    assert tria.raw_call("tria_workspace_score_offset", ctypes.byref(bad.c_struct())) == 0
+
+
 def test_select_noalloc_host_checks_match_select(lib):
     """tria_select_noalloc rejects on the host exactly what tria_select rejects
     (checks that need no workspace): overlapping sequences, a negative n_ctx,
