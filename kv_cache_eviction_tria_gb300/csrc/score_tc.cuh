@@ -62,6 +62,11 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// The high part of x for a tf32 hi / remainder split: x with its low 13
+// mantissa bits cleared (one logic op). x - hi is exact in fp32 and below
+// 2^-10 |x|, so the remainder's own truncation to tf32 costs < 2^-20 |x|.
+__device__ __forceinline__ uint32_t tf32_hi(float x) { return __float_as_uint(x) & 0xFFFFE000u; }
+
 __device__ __forceinline__ uint32_t to_tf32(float x) {
   uint32_t y;
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
@@ -306,8 +311,8 @@ struct TcBody {
           granule_mag(kr8, ki8, mg8);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const uint32_t h0 = to_tf32(mg0[2 * u]), h1 = to_tf32(mg8[2 * u]);
-            const uint32_t h2 = to_tf32(mg0[2 * u + 1]), h3 = to_tf32(mg8[2 * u + 1]);
+            const uint32_t h0 = tf32_hi(mg0[2 * u]), h1 = tf32_hi(mg8[2 * u]);
+            const uint32_t h2 = tf32_hi(mg0[2 * u + 1]), h3 = tf32_hi(mg8[2 * u + 1]);
             const uint32_t l0 = __float_as_uint(mg0[2 * u] - __uint_as_float(h0));
             const uint32_t l1 = __float_as_uint(mg8[2 * u] - __uint_as_float(h1));
             const uint32_t l2 = __float_as_uint(mg0[2 * u + 1] - __uint_as_float(h2));
@@ -365,8 +370,8 @@ struct TcBody {
           q8_mag(ar8, ai8, dr8, di8, mg8);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const uint32_t h0 = to_tf32(mg0[2 * u]), h1 = to_tf32(mg8[2 * u]);
-            const uint32_t h2 = to_tf32(mg0[2 * u + 1]), h3 = to_tf32(mg8[2 * u + 1]);
+            const uint32_t h0 = tf32_hi(mg0[2 * u]), h1 = tf32_hi(mg8[2 * u]);
+            const uint32_t h2 = tf32_hi(mg0[2 * u + 1]), h3 = tf32_hi(mg8[2 * u + 1]);
             const uint32_t l0 = __float_as_uint(mg0[2 * u] - __uint_as_float(h0));
             const uint32_t l1 = __float_as_uint(mg8[2 * u] - __uint_as_float(h1));
             const uint32_t l2 = __float_as_uint(mg0[2 * u + 1] - __uint_as_float(h2));
