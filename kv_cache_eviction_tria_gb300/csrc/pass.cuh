@@ -173,6 +173,8 @@ struct KeyStore {
 // score-run partials, z-max keys and the first radix histogram in one sweep,
 // up to two more radix passes, then the keep list (B entries) and the
 // kept-row prefix of every chunk; publishes the segment in the ready list.
+// smem_keys: the keys (kSmem) or, with the keys in the workspace, scratch
+// for the chunks' ballots (both in the ring area, below the histogram).
 template <int G, bool kSmem>
 __device__ __noinline__ void pass_select(const FPass& P, int sg, int nr, uint32_t* smem_keys, uint32_t* hist) {
   __shared__ int s_info[4];
@@ -317,11 +319,15 @@ __device__ __noinline__ void pass_select(const FPass& P, int sg, int nr, uint32_
   }
 
   // keep list: warps take contiguous chunk ranges; sweep 1 counts each warp's
-  // ties and strict keeps, sweep 2 writes the kept rows and chunk prefixes
+  // ties and strict keeps, sweep 2 writes the kept rows and chunk prefixes.
+  // With the keys in the workspace, sweep 1 also leaves each chunk's tie and
+  // strict-keep ballots in shared memory (the ring area is free then; 8 bytes
+  // a chunk), so that sweep 2 reads no key again.
   const int nch = (n + kChunk - 1) / kChunk;
   const int cpw = (nch + kPassWarps - 1) / kPassWarps;
   const int c0 = min(nch, warp * cpw), c1 = min(nch, c0 + cpw);
   constexpr int CB = kSmem ? 1 : 16;   // chunks whose keys load together (global keys)
+  uint2* masks = !kSmem && nch * 8 <= kPassHistOff ? reinterpret_cast<uint2*>(smem_keys) : nullptr;
   {
     int wt = 0, wk = 0;
     for (int cb = c0; cb < c1; cb += CB) {
@@ -338,8 +344,11 @@ __device__ __noinline__ void pass_select(const FPass& P, int sg, int nr, uint32_
         const bool in = r < n;
         const bool pr = in && (r < lo || r >= hi);
         const bool cand = in && !pr && k > 0;
-        wt += __popc(__ballot_sync(0xffffffffu, cand && kk[u] == T));
-        wk += __popc(__ballot_sync(0xffffffffu, pr || (cand && kk[u] > T)));
+        const uint32_t bt = __ballot_sync(0xffffffffu, cand && kk[u] == T);
+        const uint32_t bs = __ballot_sync(0xffffffffu, pr || (cand && kk[u] > T));
+        if (masks && lane == 0) masks[cb + u] = make_uint2(bt, bs);
+        wt += __popc(bt);
+        wk += __popc(bs);
       }
     }
     if (lane == 0) {
@@ -355,30 +364,44 @@ __device__ __noinline__ void pass_select(const FPass& P, int sg, int nr, uint32_
   }
   int32_t* keep = P.keep + v.wrow0;
   int* pre = P.prefix + (size_t)sg * (P.c_max + 1);
-  for (int cb = c0; cb < c1; cb += CB) {
-    uint32_t kk[CB];
-#pragma unroll
-    for (int u = 0; u < CB; ++u) {
-      const int r = (cb + u) * kChunk + lane;
-      kk[u] = (cb + u < c1 && r < n && r >= lo && r < hi && k > 0) ? keys.get(r) : 0u;
+  const uint32_t lt = (1u << lane) - 1u;
+  // one chunk: its tie and strict-keep ballots -> its kept rows (the ties by
+  // rank), written at the run's position
+  auto emit_chunk = [&](int ci, uint32_t bt, uint32_t bs) {
+    const int r = ci * kChunk + lane;
+    const bool is_tie = (bt >> lane) & 1u;
+    const int trank = tie_run + __popc(bt & lt);
+    const bool kp = ((bs >> lane) & 1u) || (is_tie && trank < kr);
+    const uint32_t bk = __ballot_sync(0xffffffffu, kp);
+    if (lane == 0) pre[ci] = keep_run;
+    if (kp) keep[keep_run + __popc(bk & lt)] = r;
+    tie_run += __popc(bt);
+    keep_run += __popc(bk);
+  };
+  if (masks) {
+    for (int ci = c0; ci < c1; ++ci) {
+      const uint2 m = masks[ci];
+      emit_chunk(ci, m.x, m.y);
     }
+  } else {
+    for (int cb = c0; cb < c1; cb += CB) {
+      uint32_t kk[CB];
 #pragma unroll
-    for (int u = 0; u < CB; ++u) {
-      const int ci = cb + u;
-      if (ci >= c1) break;
-      const int r = ci * kChunk + lane;
-      const bool in = r < n;
-      const bool pr = in && (r < lo || r >= hi);
-      const bool cand = in && !pr && k > 0;
-      const bool is_tie = cand && kk[u] == T;
-      const uint32_t bt = __ballot_sync(0xffffffffu, is_tie);
-      const int trank = tie_run + __popc(bt & ((1u << lane) - 1u));
-      const bool kp = pr || (cand && kk[u] > T) || (is_tie && trank < kr);
-      const uint32_t bk = __ballot_sync(0xffffffffu, kp);
-      if (lane == 0) pre[ci] = keep_run;
-      if (kp) keep[keep_run + __popc(bk & ((1u << lane) - 1u))] = r;
-      tie_run += __popc(bt);
-      keep_run += __popc(bk);
+      for (int u = 0; u < CB; ++u) {
+        const int r = (cb + u) * kChunk + lane;
+        kk[u] = (cb + u < c1 && r < n && r >= lo && r < hi && k > 0) ? keys.get(r) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < CB; ++u) {
+        const int ci = cb + u;
+        if (ci >= c1) break;
+        const int r = ci * kChunk + lane;
+        const bool in = r < n;
+        const bool pr = in && (r < lo || r >= hi);
+        const bool cand = in && !pr && k > 0;
+        emit_chunk(ci, __ballot_sync(0xffffffffu, cand && kk[u] == T),
+                   __ballot_sync(0xffffffffu, pr || (cand && kk[u] > T)));
+      }
     }
   }
   if (warp == kPassWarps - 1 && lane == 0) {
@@ -879,7 +902,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) k_pass(const __grid_constant_
         if (pass_seg(P, sel).n <= kPassSmemKeys)
           pass_select<G, true>(P, sel, nr, reinterpret_cast<uint32_t*>(smem + PassSmem::kRing), hist);
         else
-          pass_select<G, false>(P, sel, nr, nullptr, hist);
+          pass_select<G, false>(P, sel, nr, reinterpret_cast<uint32_t*>(smem + PassSmem::kRing), hist);
         continue;
       }
       if (sel == -2) break;
