@@ -87,13 +87,17 @@ FUSED_CASES = [
          cur_pos=[2500, 37], budget_frac=0.3, window=8, sink=2),
     dict(n_kv=3, group=1, hd=64, k_type="q8_0", v_type="q8_0", n_live=[1200], capacity=[1280], cur_pos=[1200],
          budget_frac=0.4, window=32, sink=0),
-    # segments longer than the shared-memory keys (32768 rows): keys through
-    # the workspace; odd capacities put every segment's rows (and keys) off
-    # the 16-byte boundary; G 1 and 2 make raw-score rows of 4 and 8 bytes
-    dict(n_kv=2, group=1, hd=128, k_type="f16", v_type="f16", n_live=[40001, 33000], capacity=[40003, 33001],
+    # segments near the shared-memory key limit (47104 rows) on either side:
+    # keys in shared memory or through the workspace (with the cut bin's keys
+    # gathered for the last radix pass and the chunk ballots kept for the keep
+    # list); odd capacities put every segment's rows (and keys) off the
+    # 16-byte boundary; G 1, 2 and 4 make raw-score rows of 4, 8 and 16 bytes
+    dict(n_kv=2, group=1, hd=128, k_type="f16", v_type="f16", n_live=[47105, 33000], capacity=[47107, 33001],
          cur_pos=[50000, 33000], budget_frac=0.3, window=100, sink=3),
-    dict(n_kv=3, group=2, hd=64, k_type="q8_0", v_type="f16", n_live=[35555], capacity=[35557], cur_pos=[35555],
+    dict(n_kv=3, group=2, hd=64, k_type="q8_0", v_type="f16", n_live=[60001], capacity=[60003], cur_pos=[60001],
          budget_frac=0.45, window=64, sink=1),
+    dict(n_kv=1, group=4, hd=64, k_type="f16", v_type="f16", n_live=[100003, 47104], capacity=[100005, 47104],
+         cur_pos=[100003, 47104], budget_frac=0.25, window=1024, sink=4),
     # k = 0: the budget is exactly sink + window (only protected rows survive)
     dict(n_kv=2, group=4, hd=128, k_type="f16", v_type="f16", n_live=[900], capacity=[1024], cur_pos=[900],
          budget_rows=[132], window=128, sink=4),
