@@ -250,11 +250,12 @@ tria_status tria_compact(const tria_layer_cache* cache, const tria_policy* polic
                          const int32_t* keep, void* ws, size_t ws_bytes, void* stream);
 
 /* The whole pass (steps 1-3) for one layer and all sequences of the call.
- * Calls of at least 128 segments (n_seqs x n_kv_heads) with fp16 or q8_0
- * keys, head_dim 64 or 128 (any group) or 256 (group <= 4) and every dim
- * rotary (statistics with nonrot_dim 0) run as one fused persistent kernel
- * (see tria_evict_model); the others run the three staged kernels of
- * tria_evict_staged. Same results either way. */
+ * Calls with fp16 or q8_0 keys, head_dim 64 or 128 (any group) or 256
+ * (group <= 4) and every dim rotary (statistics with nonrot_dim 0) run as one
+ * fused persistent kernel (see tria_evict_model) when they have at least 128
+ * segments (n_seqs x n_kv_heads), or at least 32 with no capacity above 65536
+ * rows; the others run the three staged kernels of tria_evict_staged. Same
+ * results either way. */
 tria_status tria_evict(const tria_stats* stats, int32_t layer, const tria_layer_cache* cache,
                        const tria_policy* policy, void* ws, size_t ws_bytes, void* stream);
 
@@ -284,9 +285,10 @@ size_t tria_model_workspace_size(const tria_layer_cache* cache, int32_t n_layers
  * with its own planes and its own n_live array (device, updated in place).
  * Every layer must be loaded with the first layer's RoPE frequencies
  * (TRIA_ERR_UNSUPPORTED otherwise) and appear once. One policy for all
- * layers. Shapes of the fused kernel (see tria_evict) with 128 to 2048
- * segments (n_layers x n_seqs x n_kv_heads; any count from 1 when score_out is
- * given) run as ONE persistent kernel for all layers: every warp streams a
+ * layers. Shapes of the fused kernel (see tria_evict) with up to 2048
+ * segments (n_layers x n_seqs x n_kv_heads; at least 128, or 32 with no
+ * capacity above 65536 rows, or any count from 1 when score_out is given)
+ * run as ONE persistent kernel for all layers: every warp streams a
  * run of the keys, each scored segment is selected by one CTA as soon as its
  * warps finish, and the rows move once segments are selected; other calls run
  * tria_evict_staged per layer.

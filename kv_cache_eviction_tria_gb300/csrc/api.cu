@@ -259,13 +259,24 @@ bool fused_ok(const tria_stats* st, const tria_layer_cache* c, int n_layers) {
 }
 
 // The fused kernel pays the staged path's ramps and launch gaps once, but
-// selects each segment on one CTA; measured on GB300 it is ahead once a call
-// has enough segments to spread the selections over the grid (36 Qwen3-8B
-// layers: 0.47 ms against 1.44 ms), and behind for a few long segments (one
-// Qwen3-8B layer of 8 x 32768 rows: 111 us against 62 us).
+// selects each segment on one CTA (the staged select uses an 8-CTA cluster)
+// and moves the rows only once every segment is selected. Measured on GB300
+// (whole-model steps): it is ahead from 128 segments on whatever their
+// length (4 long-context layers of 32 segments of 35K-112K rows: 2.03 against
+// 2.14 ms; 16 q8_0 layers: 1.15 against 1.55 ms), and from 32 segments on
+// when no segment holds more than 65536 rows (4 Qwen3-8B steady-state layers:
+// 0.10 against 0.16 ms; 4 q8_0 layers of 65536 rows: even); with a few long
+// segments the staged kernels are faster (one Qwen3-8B layer of 8 x 32768
+// rows: 61 against 111 us; one long-context layer: 0.53 against 0.68 ms).
 constexpr int kFusedMinSegs = 128;
+constexpr int kFusedMinShortSegs = 32;
+constexpr int kFusedShortRows = 65536;
 bool fused_preferred(const tria_stats* st, const tria_layer_cache* c, int n_layers) {
-  return fused_ok(st, c, n_layers) && (int64_t)n_layers * c->n_seqs * c->n_kv_heads >= kFusedMinSegs;
+  if (!fused_ok(st, c, n_layers)) return false;
+  const int64_t segs = (int64_t)n_layers * c->n_seqs * c->n_kv_heads;
+  int cap_max = 0;
+  for (int s = 0; s < c->n_seqs; ++s) cap_max = std::max(cap_max, c->capacity[s]);
+  return segs >= kFusedMinSegs || (segs >= kFusedMinShortSegs && cap_max <= kFusedShortRows);
 }
 
 }  // namespace
