@@ -92,13 +92,44 @@ __device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t&
   hi = *reinterpret_cast<const uint32_t*>(&hb);
 }
 
-// |k| of 8 frequencies from fp16 pairs of block values times their scales:
-// real parts r * dr, imaginary parts i * di
-__device__ __forceinline__ void q8_mag(const uint32_t* r, const uint32_t* i, float dr, float di, float* m) {
+// Products of fp16 values in fp32 without converting them first: the
+// mixed-precision fma (fp16 sources, fp32 addend and result) forms the
+// product exactly and rounds once after the add.
+__device__ __forceinline__ float2 mul_h2_h(uint32_t pair, unsigned short s) {   // (pair.lo * s, pair.hi * s)
+  float lo, hi;
+  asm("{.reg .f16 a, b, c;\n"
+      " mov.b32 {a, b}, %2;\n"
+      " mov.b16 c, %3;\n"
+      " fma.rn.f32.f16 %0, a, c, 0f00000000;\n"
+      " fma.rn.f32.f16 %1, b, c, 0f00000000;\n}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(pair), "h"(s));
+  return make_float2(lo, hi);
+}
+
+__device__ __forceinline__ float2 sumsq_h2(uint32_t re, uint32_t im) {   // re^2 + im^2 per half, in fp32
+  float lo, hi;
+  asm("{.reg .f16 a, b, c, d;\n"
+      " .reg .f32 t, u;\n"
+      " mov.b32 {a, b}, %2;\n"
+      " mov.b32 {c, d}, %3;\n"
+      " fma.rn.f32.f16 t, a, a, 0f00000000;\n"
+      " fma.rn.f32.f16 u, b, b, 0f00000000;\n"
+      " fma.rn.f32.f16 %0, c, c, t;\n"
+      " fma.rn.f32.f16 %1, d, d, u;\n}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(re), "r"(im));
+  return make_float2(lo, hi);
+}
+
+// |k| of 8 frequencies from fp16 pairs of block values times their fp16
+// scales: real parts r * dr, imaginary parts i * di (products exact in fp32)
+__device__ __forceinline__ void q8_mag(const uint32_t* r, const uint32_t* i, unsigned short dr, unsigned short di,
+                                       float* m) {
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
-    const float2 a = __fmul2_rn(__half22float2(*reinterpret_cast<const __half2*>(&r[t])), make_float2(dr, dr));
-    const float2 b = __fmul2_rn(__half22float2(*reinterpret_cast<const __half2*>(&i[t])), make_float2(di, di));
+    const float2 a = mul_h2_h(r[t], dr);
+    const float2 b = mul_h2_h(i[t], di);
     const float2 sq = __ffma2_rn(b, b, __fmul2_rn(a, a));
     m[2 * t] = sqrt_approx(sq.x);
     m[2 * t + 1] = sqrt_approx(sq.y);
@@ -106,13 +137,12 @@ __device__ __forceinline__ void q8_mag(const uint32_t* r, const uint32_t* i, flo
 }
 
 // |k| of the 8 frequencies of one granule: real parts r, imaginary parts i
+// (the squares exact in fp32, one rounding for their sum)
 __device__ __forceinline__ void granule_mag(const uint4& r, const uint4& i, float* m) {
   const uint32_t rr[4] = {r.x, r.y, r.z, r.w}, ii[4] = {i.x, i.y, i.z, i.w};
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
-    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&rr[t]));
-    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&ii[t]));
-    const float2 sq = __ffma2_rn(b, b, __fmul2_rn(a, a));
+    const float2 sq = sumsq_h2(rr[t], ii[t]);
     m[2 * t] = sqrt_approx(sq.x);
     m[2 * t + 1] = sqrt_approx(sq.y);
   }
@@ -366,8 +396,8 @@ struct TcBody {
           }
           if (!rotary) continue;   // content pairs: no norm term
           float mg0[8], mg8[8];
-          q8_mag(ar0, ai0, dr0, di0, mg0);
-          q8_mag(ar8, ai8, dr8, di8, mg8);
+          q8_mag(ar0, ai0, __half_as_ushort(sg0[sr]), __half_as_ushort(sg0[si]), mg0);
+          q8_mag(ar8, ai8, __half_as_ushort(sg8[sr]), __half_as_ushort(sg8[si]), mg8);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const uint32_t h0 = tf32_hi(mg0[2 * u]), h1 = tf32_hi(mg8[2 * u]);
