@@ -302,6 +302,15 @@ tria_status tria_evict_model(const tria_stats* stats, const int32_t* layers, int
                              const tria_layer_cache* caches, const tria_policy* policy, float* score_out,
                              void* ws, size_t ws_bytes, void* stream);
 
+/* Which kernels tria_evict_model runs for these arguments without score_out:
+ * 1 = the fused kernel (one launch for all layers), 0 = tria_evict_staged per
+ * layer (three launches each), -1 = arguments that tria_evict_model rejects.
+ * Same arguments and meaning as there. Host only: reads the stats handle's
+ * host metadata and the caches' host arrays, launches nothing, needs no GPU
+ * work (a stats handle still comes from tria_load_stats). */
+int32_t tria_evict_model_fused(const tria_stats* stats, const int32_t* layers, int32_t n_layers,
+                               const tria_layer_cache* caches);
+
 /* tria_evict over sequences of different layers in one call (the pass is
  * per segment, so layers only change which statistics a segment uses): the
  * caller lays several layers' caches out as the sequences of one

@@ -35,7 +35,8 @@ NO_PASS = 2 ** 31 - 1
 EXPORTS = (
     "tria_gate_check", "tria_gate_describe", "tria_budget_rows", "tria_should_evict", "tria_load_stats", "tria_free_stats",
     "tria_workspace_size", "tria_workspace_init", "tria_score", "tria_select", "tria_compact",
-    "tria_evict", "tria_evict_staged", "tria_evict_model", "tria_model_workspace_size", "tria_evict_layers",
+    "tria_evict", "tria_evict_staged", "tria_evict_model", "tria_evict_model_fused", "tria_model_workspace_size",
+    "tria_evict_layers",
     "tria_evict_profiled", "tria_evict_marked", "tria_select_noalloc", "tria_device_status", "tria_selftest_bounded_wait",
     "tria_calib_accumulate", "tria_calib_finish", "tria_append", "tria_schedule_check", "tria_seq_init",
     "tria_seq_prefill", "tria_seq_decode", "tria_schedule_plan", "tria_schedule_passed",
@@ -146,6 +147,8 @@ def load_library(path: str | None = None):
     lib.tria_evict_model.argtypes = [vp, ctypes.POINTER(i32), i32, ctypes.POINTER(_LayerCache),
                                      ctypes.POINTER(_Policy), vp, vp, sz, vp]
     lib.tria_evict_model.restype = i32
+    lib.tria_evict_model_fused.argtypes = [vp, ctypes.POINTER(i32), i32, ctypes.POINTER(_LayerCache)]
+    lib.tria_evict_model_fused.restype = i32
     lib.tria_evict_layers.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(_LayerCache), ctypes.POINTER(_Policy),
                                       vp, sz, vp]
     lib.tria_evict_layers.restype = i32
@@ -451,6 +454,20 @@ def evict_model(stats: Stats, layers, caches, policy: Policy, *, ws, score_out=N
     _check(load_library().tria_evict_model(stats.handle, ptr, len(layers), structs, ctypes.byref(p),
                                            _ptr(score_out) if score_out is not None else None, wp, wb,
                                            _stream_handle(stream)), "tria_evict_model")
+
+
+def evict_model_fused(stats: Stats, layers, caches) -> bool:
+    """tria_evict_model_fused: whether tria_evict_model (without score_out)
+    runs these layers as one fused kernel (True) or as the staged kernels per
+    layer (False). Host only."""
+    if len(caches) != len(layers) or not caches:
+        raise ValueError("one cache per layer")
+    structs = (_LayerCache * len(caches))(*[c.c_struct() for c in caches])
+    arr, ptr = _host_array(layers, np.int32, ctypes.c_int32)
+    r = load_library().tria_evict_model_fused(stats.handle, ptr, len(layers), structs)
+    if r < 0:
+        raise TriaError(ERR_INVALID_ARG, "tria_evict_model_fused")
+    return r == 1
 
 
 def evict_layers(stats: Stats, layer_of_seq, cache: LayerCache, policy: Policy, *, ws, stream=None):

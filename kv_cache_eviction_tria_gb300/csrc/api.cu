@@ -610,6 +610,12 @@ extern "C" size_t tria_model_workspace_size(const tria_layer_cache* cache, int32
   return make_model_layout(cache, group, n_layers).total;
 }
 
+extern "C" int32_t tria_evict_model_fused(const tria_stats* stats, const int32_t* layers, int32_t n_layers,
+                                          const tria_layer_cache* caches) {
+  if (check_model(stats, layers, n_layers, caches) != TRIA_OK) return -1;
+  return fused_preferred(stats, caches, n_layers) ? 1 : 0;
+}
+
 extern "C" tria_status tria_evict_model(const tria_stats* stats, const int32_t* layers, int32_t n_layers,
                                         const tria_layer_cache* caches, const tria_policy* policy,
                                         float* score_out, void* ws, size_t ws_bytes, void* stream) {

@@ -202,6 +202,31 @@ def test_model_pass_q8_and_bad_n_live(lib):
     st.close()
 
 
+def test_model_dispatch_query_follows_the_documented_rule(lib):
+    """tria_evict_model_fused: the fused kernel from 128 segments whatever
+    their length, or from 32 with no capacity above 65536 rows; the staged
+    kernels below that (the query reads host metadata only: the cache
+    addresses are fake and never touched)."""
+    w = W.get_workload("qwen3_8b_full")
+    qm, qa = W.make_stats(w)
+    st = lib.Stats(qm, qa, n_kv_heads=w.n_kv_heads, head_dim=w.head_dim, rope_theta=w.rope_theta)
+
+    def caches(n, cap):
+        return [lib.LayerCache(k=0x1000000 * (l + 1), v=0x1000000 * (l + 1) + 0x800000, pos=0x10000 * (l + 1),
+                               n_live=0x100 * (l + 1), seq_row0=[0], capacity=[cap], head_dim=w.head_dim,
+                               n_kv_heads=w.n_kv_heads) for l in range(n)]
+
+    # 8 segments per layer
+    for n_layers, cap, fused in [(36, 12288, True), (4, 12288, True), (3, 12288, False), (1, 32768, False),
+                                 (4, 100000, False), (15, 100000, False), (16, 100000, True)]:
+        got = lib.evict_model_fused(st, list(range(n_layers)), caches(n_layers, cap))
+        assert got is fused, (n_layers, cap)
+    one = caches(1, 12288)
+    with pytest.raises(lib.TriaError):   # the same cache twice: the model call rejects it
+        lib.evict_model_fused(st, [0, 1], one + one)
+    st.close()
+
+
 def test_whole_model_qwen3_steady_state(lib):
     """All 36 layers of the Qwen3-8B steady state (6272 live rows -> 6144 per
     segment) in one tria_evict_model call, in the launch configuration the

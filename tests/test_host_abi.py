@@ -160,6 +160,15 @@ def test_host_validation_rejects_before_any_launch(lib):
         == tria.ERR_WORKSPACE
 
 
+def test_model_dispatch_query_host_checks(lib):
+    # no stats handle, or no layers: the model call would reject them (-1)
+    c = _fake_cache()
+    structs = (tria._LayerCache * 1)(c.c_struct())
+    layers = (ctypes.c_int32 * 1)(0)
+    assert tria.raw_call("tria_evict_model_fused", None, layers, 1, structs) == -1
+    assert tria.raw_call("tria_evict_model_fused", None, None, 0, structs) == -1
+
+
 def test_shared_slot_and_append_argument_checks(lib):
     # rejected on the host before any launch (fake, aligned pointers are never touched)
     c = _fake_cache()
