@@ -177,7 +177,10 @@ def raw_scores(k_rot: np.ndarray, q_mean_c: np.ndarray, m_weight: np.ndarray,
 
 
 def znorm(raw: np.ndarray) -> np.ndarray:
-    """Per-query-head z-score over all live rows ([Doc] Phase C)."""
+    """Per-query-head z-score over all live rows ([Doc] Phase C). A segment
+    without live rows has no rows to normalise (and no moments)."""
+    if raw.shape[0] == 0:
+        return np.array(raw, dtype=np.float64)
     mu = raw.mean(axis=0)
     sd = raw.std(axis=0)  # population
     return (raw - mu[None, :]) / (sd[None, :] + Z_EPS)
