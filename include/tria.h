@@ -162,7 +162,7 @@ typedef struct tria_policy {
 } tria_policy;
 
 /* Host-only gate of [Doc] §4 "GPU scoring requirements" (n_q % n_kv == 0,
- * head_dim <= 256 and % 32 == 0) plus this build's group <= 8. The page's gate
+ * head_dim <= 256 and % 32 == 0) plus this library's limit of group <= 8. The page's gate
  * also wants no non-rotary dims ([Doc] §6 "Non-rotary models" are scored on the
  * CPU there); here heads with nonrot_dim non-rotary dims are eligible when the
  * rotary dims head_dim - nonrot_dim are a multiple of 16 (UNSUPPORTED
