@@ -194,6 +194,13 @@ def test_znorm_closed_form():
     np.testing.assert_allclose(O.znorm(raw)[:, 0], (raw[:, 0] - 2.5) / (sd + 1e-6), rtol=1e-15)
     const = np.full((7, 2), 3.25)
     assert np.all(O.znorm(const) == 0.0)
+    # a segment without live rows: nothing to normalise, and no moments are taken
+    import warnings
+    with warnings.catch_warnings():
+        warnings.simplefilter("error")
+        empty = O.znorm(np.zeros((0, 4)))
+    assert empty.shape == (0, 4)
+    assert O.gqa_max(empty).shape == (0,)
 
 
 def test_znorm_moments_and_gqa_max():
